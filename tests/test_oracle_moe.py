@@ -1,0 +1,196 @@
+"""Pins for the oracle's MoE layer: route sort by brute force, GEMM closed forms
+and operand orientation, SwiGLU and combine hand values, the dense-MLP special
+case, and permutation / batch invariants.  CPU only."""
+
+import os
+
+import numpy as np
+import pytest
+
+import moe_synth as S
+from oracle import formats as F
+from oracle import moe as M
+from oracle import quant as Q
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                lhs, rhs = [p.strip() for p in line.split("|")]
+                yield [float(v) for v in lhs.split()], int(rhs, 16)
+
+
+# ---------------------------------------------------------------- route sort
+def test_route_sort_bruteforce():
+    rng = np.random.default_rng(0)
+    for T, k, E in ((1, 1, 1), (5, 2, 3), (17, 4, 8), (64, 8, 16)):
+        ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+        counts, offsets, order = M.route_sort(ids, E)
+        for e in range(E):
+            want = [t * k + s for t in range(T) for s in range(k) if ids[t, s] == e]
+            got = list(order[offsets[e]:offsets[e + 1]])
+            assert got == want
+            assert counts[e] == len(want)
+        assert offsets[-1] == T * k
+
+
+def test_route_sort_rejects_bad_ids():
+    with pytest.raises(ValueError):
+        M.route_sort(np.array([[0, 4]]), 4)
+
+
+# ---------------------------------------------------------------- GEMM
+def _const_operand(rows, cols, nib, sc):
+    return np.full((rows, cols), nib, np.uint8), np.full((rows, cols // 16), sc, np.uint8)
+
+
+def test_qgemm_closed_forms():
+    for K in (32, 64, 256):
+        a = _const_operand(3, K, 0x2, 0x38)        # all 1.0, scale 1
+        w = _const_operand(5, K, 0x2, 0x38)
+        assert np.all(M.qgemm_f64(*a, *w) == K)
+        a = _const_operand(2, K, 0x7, 0x7E)        # 6 * 448
+        w = _const_operand(4, K, 0x9, 0x01)        # -0.5 * 2^-9
+        assert np.all(M.qgemm_f64(*a, *w) == K * 6 * 448 * -0.5 * 2.0 ** -9)
+
+
+def test_qgemm_orientation_one_hot():
+    # A row i is 1.0 at column c_i only: acc[i, n] must be W's dequantised (n, c_i)
+    rng = np.random.default_rng(1)
+    K, N = 64, 24
+    w_codes = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    w_sc = rng.integers(0x20, 0x50, (N, K // 16)).astype(np.uint8)
+    cols = [0, 17, 33, 63, 40]
+    a_codes = np.zeros((len(cols), K), np.uint8)
+    for i, c in enumerate(cols):
+        a_codes[i, c] = 0x2
+    a_sc = np.full((len(cols), K // 16), 0x38, np.uint8)
+    acc = M.qgemm_f64(a_codes, a_sc, w_codes, w_sc)
+    wd = Q.dequantize_rows(w_codes, w_sc)
+    for i, c in enumerate(cols):
+        assert np.array_equal(acc[i], wd[:, c])
+
+
+def test_qgemm_vs_triple_loop():
+    rng = np.random.default_rng(2)
+    for M_, N, K in ((1, 1, 32), (7, 32, 64), (3, 5, 32)):
+        a = (rng.integers(0, 16, (M_, K)).astype(np.uint8), rng.integers(0, 0x7F, (M_, K // 16)).astype(np.uint8))
+        w = (rng.integers(0, 16, (N, K)).astype(np.uint8), rng.integers(0, 0x7F, (N, K // 16)).astype(np.uint8))
+        acc = M.qgemm_f64(*a, *w)
+        for m in range(M_):
+            for n in range(N):
+                s = 0.0
+                for kk in range(K):
+                    qa = F.E2M1_VALUES[a[0][m, kk] & 7] * (-1 if a[0][m, kk] & 8 else 1)
+                    qw = F.E2M1_VALUES[w[0][n, kk] & 7] * (-1 if w[0][n, kk] & 8 else 1)
+                    s += qa * F.E4M3_VALUES[a[1][m, kk // 16]] * qw * F.E4M3_VALUES[w[1][n, kk // 16]]
+                assert acc[m, n] == s
+
+
+def test_epilogue_order():
+    acc = np.array([[3.0]])
+    v = M.epilogue_f64(acc, np.array([0.5], np.float32), np.array([0.25], np.float32))
+    assert v[0, 0] == 3.0 * 0.5 * 0.25
+
+
+# ---------------------------------------------------------------- SwiGLU / combine
+def test_swiglu_golden():
+    for (gate, up, p), want in _golden("swiglu_prob.txt"):
+        gb = F.round_to_bf16_bits(np.array([[gate]]))
+        ub = F.round_to_bf16_bits(np.array([[up]]))
+        h = M.swiglu_prob(gb, ub, np.array([p], np.float32))
+        assert int(h[0, 0]) == want, (gate, up, p, hex(int(h[0, 0])))
+
+
+def test_swiglu_limits():
+    big = F.round_to_bf16_bits(np.array([[30.0, -30.0, -3.0e38, 3.0e38]]))
+    one = F.round_to_bf16_bits(np.ones((1, 4)))
+    h = F.bf16_bits_to_f32(M.swiglu_prob(big, one, np.array([1.0], np.float32)))
+    assert h[0, 0] == 30.0                      # sigmoid(30) rounds to 1
+    assert abs(h[0, 1]) < 1e-11                 # -30 * e^-30
+    assert h[0, 2] == 0                         # -3e38 * sigmoid(-3e38) = -0
+    assert h[0, 3] == F.bf16_bits_to_f32(big)[0, 3]   # sigmoid(3e38) = 1
+
+
+def test_combine_golden_order():
+    for vals, want in _golden("combine_order.txt"):
+        y = F.round_to_bf16_bits(np.array(vals)).reshape(1, len(vals), 1)
+        assert int(M.combine_slots(y)[0, 0]) == want
+
+
+def test_combine_k1_identity_and_permutation():
+    rng = np.random.default_rng(3)
+    y = F.round_to_bf16_bits(rng.standard_normal((6, 1, 16)))
+    assert np.array_equal(M.combine_slots(y), y[:, 0, :])
+    y = F.round_to_bf16_bits(rng.standard_normal((6, 3, 16)))
+    perm = rng.permutation(6)
+    assert np.array_equal(M.combine_slots(y[perm]), M.combine_slots(y)[perm])
+
+
+# ---------------------------------------------------------------- whole layer
+def _tiny(T=32, E=4, k=2, H=64, I=32, seed=0):
+    cfg = S.LayerConfig("t", H=H, I=I, E=E, k=k, T=T, seed=seed)
+    return cfg, S.make_layer(cfg)
+
+
+def test_dense_special_case():
+    # E=1, k=1, p=1: the quantised layer approximates the unquantised FP64 SwiGLU MLP.
+    cfg = S.LayerConfig("dense", H=256, I=128, E=1, k=1, T=64)
+    L = S.make_layer(cfg)
+    assert np.all(L["topk_w"] == 1.0) and np.all(L["topk_ids"] == 0)
+    wq = M.quantize_weights(L["w1"], L["w2"])
+    out = F.bf16_bits_to_f32(M.moe_forward(L["x"], L["topk_ids"], L["topk_w"], wq)).astype(np.float64)
+    ref = M.dense_swiglu_mlp_f64(F.bf16_bits_to_f32(L["x"]), F.bf16_bits_to_f32(L["w1"][0]),
+                                 F.bf16_bits_to_f32(L["w2"][0]))
+    rel = np.linalg.norm(out - ref) / np.linalg.norm(ref)
+    assert rel < 0.25, rel
+    # and the exact FP64 chain on the quantised operands (no NVFP4 error in the
+    # reference) is reproduced to BF16 precision
+    xq = Q.quantize_rows(F.bf16_bits_to_f32(L["x"]))
+    (c1, s1, g1), (c2, s2, g2) = wq.expert(0)
+    xd, w1d, w2d = Q.dequantize_rows(*xq), Q.dequantize_rows(c1, s1, g1), Q.dequantize_rows(c2, s2, g2)
+    gate, up = xd @ w1d[:128].T, xd @ w1d[128:].T
+    h = gate / (1 + np.exp(-gate)) * up
+    hq = Q.quantize_rows(F.bf16_bits_to_f32(F.round_to_bf16_bits(h)))
+    ref_q = Q.dequantize_rows(*hq) @ w2d.T
+    rel_q = np.linalg.norm(out - ref_q) / np.linalg.norm(ref_q)
+    assert rel_q < 0.05, rel_q
+
+
+def test_layer_batch_invariance_and_permutation():
+    cfg, L = _tiny(T=24, E=4, k=2)
+    wq = M.quantize_weights(L["w1"], L["w2"])
+    full = M.moe_forward(L["x"], L["topk_ids"], L["topk_w"], wq)
+    # any split into sub-batches gives the same rows
+    parts = [M.moe_forward(L["x"][a:b], L["topk_ids"][a:b], L["topk_w"][a:b], wq)
+             for a, b in ((0, 1), (1, 8), (8, 24))]
+    assert np.array_equal(np.concatenate(parts), full)
+    perm = np.random.default_rng(5).permutation(24)
+    out_p = M.moe_forward(L["x"][perm], L["topk_ids"][perm], L["topk_w"][perm], wq)
+    assert np.array_equal(out_p, full[perm])
+
+
+def test_layer_linear_in_prob_sign():
+    # with k=1 the output is y of the single slot; p scales h before quantisation,
+    # and quantisation commutes with power-of-two scaling, so p = 2^-n gives
+    # exactly the p = 1 output times 2^-n (no subnormals at these sizes)
+    cfg, L = _tiny(T=8, E=2, k=1)
+    wq = M.quantize_weights(L["w1"], L["w2"])
+    ids = L["topk_ids"]
+    o1 = F.bf16_bits_to_f32(M.moe_forward(L["x"], ids, np.ones((8, 1), np.float32), wq))
+    o4 = F.bf16_bits_to_f32(M.moe_forward(L["x"], ids, np.full((8, 1), 0.25, np.float32), wq))
+    assert np.array_equal(o4, o1 * np.float32(0.25))
+
+
+def test_layer_intermediates_consistent():
+    cfg, L = _tiny(T=16, E=4, k=2)
+    wq = M.quantize_weights(L["w1"], L["w2"])
+    out, inter = M.moe_forward(L["x"], L["topk_ids"], L["topk_w"], wq, keep=True)
+    assert np.array_equal(M.combine_slots(inter["y"]), out)
+    assert np.array_equal(inter["gu"], F.round_to_bf16_bits(inter["v1"]))
+    # every routed pair was computed
+    assert np.count_nonzero(np.abs(inter["v1"]).sum(1)) == 16 * 2
