@@ -1,0 +1,228 @@
+/*
+ * nvfp4_moe.h -- C ABI of the batch-invariant NVFP4 W4A4 MoE expert forward
+ * for GB300 (sm_103a).
+ *
+ * What is computed (sources; the pages are cited by title and section):
+ *
+ *  [miniTE/differs]  "miniTE diagnoses and narrows the cross-engine execution
+ *      gap of NVFP4 RL" (onedev.kr/papers/1404), section "How it differs":
+ *      two-level NVFP4 -- E2M1 codes, one E4M3 scale per 16 elements, an FP32
+ *      outer scale per row g = max|row| / (6*448), round-to-nearest-even, no
+ *      Hadamard transform, no stochastic rounding; g^x*g^w applied in an FP32
+ *      epilogue before the BF16 cast; the router probability multiplies the
+ *      SwiGLU activation before FC2; the expert combine order is preserved.
+ *  [miniTE/use]  same page, section "How to use it": the quantiser writes the
+ *      packed FP4 codes, block scales and outer scales into contiguous buffers
+ *      the grouped GEMM consumes directly; expert boundaries are device
+ *      offsets; sort+amax then pad(X, amax) then quantise (no separate
+ *      activation scan); FC2 maxima come from the producer of the
+ *      router-weighted activation; FC1 and FC2 have their own GEMM settings.
+ *  [RL/4.4]  "Finishing RL training faster: bitwise consistency, high
+ *      performance, agent-driven" (spke.com/ko/ai/article/3192), section 4.4
+ *      "Expert GEMM: two layouts, same row result": per-token quantisation,
+ *      a fixed per-row accumulation order, SiLU(gate)*up in FP32 rounded once.
+ *  [RL/4.5]  same article, section 4.5 "Cross-GPU reduction": expert outputs
+ *      summed in FP32 in top-k slot order.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev are device pointers; the caller allocates and owns
+ *    every buffer.  The library never allocates or frees memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All GPU work is enqueued on it; no entry point synchronises
+ *    except nvfp4_get_device_error.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns an error and enqueues nothing.  A failed launch
+ *    returns NVFP4_ERR_CUDA.  Conditions only the GPU can see (an expert id
+ *    out of range, a non-finite row maximum, a bounded wait that ran out) are
+ *    recorded in a per-device error word read by nvfp4_get_device_error.
+ *  - BF16 tensors are raw IEEE bfloat16 bit patterns (uint16).
+ *
+ * NVFP4 storage used by every entry point ("NVFP4 rows"):
+ *  - codes  uint8 [rows_pad][cols/2]: element 2j of a row is the low nibble
+ *           of byte j, element 2j+1 the high nibble; nibble = sign<<3 | E2M1
+ *           magnitude index (0,0.5,1,1.5,2,3,4,6).
+ *  - sf     uint8, nvfp4_sf_bytes(rows, cols) bytes: the E4M3 block scale of
+ *           row r, block b (elements 16b..16b+15) is at byte
+ *             ((r/128) * (cols/64) + b/4) * 512 + (r%32)*16 + ((r%128)/32)*4 + b%4
+ *           i.e. 512-byte tiles of 128 rows x 64 columns laid out so one tile
+ *           is what the tensor core's scale-factor copy takes for one MMA step.
+ *  - g      float32 [rows]: the outer scale.
+ *  - rows_pad = nvfp4_rows_padded(rows) = rows rounded up to 128.
+ */
+#ifndef NVFP4_MOE_H
+#define NVFP4_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,          /* null pointer, negative size, misaligned pointer */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 2,    /* shape outside the supported set (see each call) */
+    NVFP4_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below moe_workspace_bytes(...) */
+    NVFP4_ERR_CUDA = 4,                 /* a CUDA runtime/driver call or launch failed */
+    NVFP4_ERR_BAD_EXPERT_ID = 5,        /* device: a top-k id outside [0, E) */
+    NVFP4_ERR_NONFINITE = 6,            /* device: a row maximum was Inf or NaN */
+    NVFP4_ERR_DEVICE_TIMEOUT = 7        /* device: a bounded pipeline wait ran out */
+} nvfp4_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvfp4_status_string(int status);
+
+/* rows rounded up to a multiple of 128 (the GEMM M tile). */
+int64_t nvfp4_rows_padded(int64_t rows);
+
+/* Bytes of the block-scale array of an NVFP4 matrix of rows x cols
+ * (cols % 64 == 0): nvfp4_rows_padded(rows) * cols / 16.  0 on bad input. */
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
+
+/*
+ * nvfp4_quantize_rows -- two-level NVFP4 quantisation of each row of a BF16
+ * matrix [miniTE/differs]: g = max|row| / 2688 (FP32 divide);
+ * s_b = E4M3_rne(bmax_b / (g*6)) for each 16-element block; code =
+ * E2M1_rne(x / (g*s_b)) with the sign of x; a zero row, or a block whose
+ * divisor g*s_b is 0, gets zero codes.  Used for weight rows (one row per
+ * output channel, along the reduction dimension) and for any activation rows.
+ *
+ *  x_dev      BF16 [rows][ld], 16-byte aligned, ld % 8 == 0, ld >= cols
+ *  rows       >= 0;  cols % 64 == 0, 64 <= cols <= 8192
+ *  codes_dev  uint8 [nvfp4_rows_padded(rows)][cols/2], 16-byte aligned
+ *  sf_dev     nvfp4_sf_bytes(rows, cols) bytes, 16-byte aligned
+ *  g_dev      float [rows]
+ * The rows between rows and rows_pad get zero codes and zero scales.
+ * Device error: NVFP4_ERR_NONFINITE if a row holds Inf/NaN.
+ */
+nvfp4_status nvfp4_quantize_rows(const void* x_dev, int64_t rows, int64_t cols, int64_t ld,
+                                 void* codes_dev, void* sf_dev, float* g_dev, void* stream);
+
+/* ------------------------------------------------------------------------
+ * MoE layer.  Shapes: T tokens, H hidden, I expert intermediate (FC1 has 2I
+ * outputs: gate rows 0..I-1 then up rows I..2I-1), E experts, top-k.
+ * Supported: H % 256 == 0, 256 <= H <= 8192; I % 128 == 0, 128 <= I <= 8192;
+ * 1 <= E <= 1024; 1 <= k <= min(E, 32); 0 <= T, T*k < 2^30.
+ * --------------------------------------------------------------------- */
+
+/* Quantised expert weights, as written by nvfp4_quantize_rows over the
+ * [E*2I, H] view of W1 and the [E*H, I] view of W2. */
+typedef struct {
+    const void*  w1_codes;  /* uint8 [E*2I][H/2]            */
+    const void*  w1_sf;     /* nvfp4_sf_bytes(E*2I, H) bytes */
+    const float* w1_g;      /* [E*2I]                        */
+    const void*  w2_codes;  /* uint8 [E*H][I/2]             */
+    const void*  w2_sf;     /* nvfp4_sf_bytes(E*H, I) bytes  */
+    const float* w2_g;      /* [E*H]                         */
+    int32_t E, H, I;
+} moe_nvfp4_weights;
+
+/* Byte offsets of the sub-buffers of a MoE workspace (all 256-byte aligned).
+ * The routed rows are expert-contiguous; expert e owns rows
+ * [expert_offsets[e], expert_offsets[e+1]), a multiple of 128 rows whose
+ * first count_e rows are its (token, slot) pairs in token-then-slot order
+ * and the rest padding. */
+typedef struct {
+    int64_t T; int32_t H, I, E, k;
+    int64_t rows_cap;     /* capacity of routed rows: every buffer below has this many */
+    int64_t n_chunks;     /* 256-token chunks of the route sort */
+    size_t a_codes;       /* uint8 [rows_cap][H/2]   quantised X rows (FC1 A operand) */
+    size_t a_sf;          /* nvfp4_sf_bytes(rows_cap, H) */
+    size_t a_g;           /* float [rows_cap]        g^x of each routed row */
+    size_t row_pair;      /* int32 [rows_cap]        token*k + slot, -1 for a pad row */
+    size_t row_prob;      /* float [rows_cap]        router probability of the row */
+    size_t amax2;         /* uint32 [rows_cap]       bits of max|h| of the row (FC2 maxima) */
+    size_t chunk_count;   /* int32 [E][n_chunks]     route-sort scratch */
+    size_t chunk_base;    /* int32 [E][n_chunks]     route-sort scratch */
+    size_t pair_rank;     /* int32 [T*k]             route-sort scratch */
+    size_t expert_count;  /* int32 [E]               unpadded rows per expert */
+    size_t route_end;     /* bytes used by moe_route_sort_amax (prefix of the workspace) */
+    size_t h;             /* bf16 [rows_cap][I]      SwiGLU x prob (FC2 input before requant) */
+    size_t a2_codes;      /* uint8 [rows_cap][I/2]   requantised h (FC2 A operand) */
+    size_t a2_sf;         /* nvfp4_sf_bytes(rows_cap, I) */
+    size_t a2_g;          /* float [rows_cap] */
+    size_t y;             /* bf16 [T][k][H]          FC2 output per (token, slot) */
+    size_t total;         /* == moe_workspace_bytes(T, H, I, E, k) */
+} moe_workspace_layout;
+
+/* Fill *out with the workspace layout for this shape.  Host only. */
+nvfp4_status moe_workspace_layout_query(int64_t T, int H, int I, int E, int k,
+                                        moe_workspace_layout* out);
+
+/* Workspace bytes a forward of this shape needs (0 on unsupported shape).
+ * The size is a static capacity: it depends on the shape only, never on the
+ * routing, so no host synchronisation is needed to size it. */
+size_t moe_workspace_bytes(int64_t T, int H, int I, int E, int k);
+
+/*
+ * moe_route_sort_amax -- route sort + per-token amax + pad + NVFP4 quantise
+ * of the FC1 input [miniTE/use].  Counting sort of the (token, slot) pairs by
+ * expert, stable in token-then-slot order; each expert's rows padded to a
+ * multiple of 128; each token row read once, its max|x| taken in the same
+ * pass, quantised once (as nvfp4_quantize_rows) and written to its k routed
+ * rows.  Also records each row's (token, slot) and router probability, and
+ * zeroes the FC2 maxima.  Pad rows get zero scales and g = 0.
+ *
+ *  x_dev           BF16 [T][H], 16-byte aligned
+ *  topk_ids_dev    int32 [T][k], slot order = top-k order
+ *  topk_w_dev      float [T][k], the router probability of each slot
+ *  expert_offsets_dev  int32 [E+1], written: padded row starts, [E] = total rows
+ *  ws_dev, ws_bytes    workspace of at least moe_workspace_bytes(T,H,I,E,k)
+ *                  bytes (any I: only the prefix layout.route_end is touched),
+ *                  256-byte aligned
+ * Device errors: NVFP4_ERR_BAD_EXPERT_ID, NVFP4_ERR_NONFINITE.
+ */
+nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int k,
+                                 const int32_t* topk_ids_dev, const float* topk_w_dev,
+                                 int32_t* expert_offsets_dev,
+                                 void* ws_dev, size_t ws_bytes, void* stream);
+
+/*
+ * moe_expert_forward_nvfp4 -- the expert forward after the route sort:
+ * FC1 grouped GEMM (tcgen05 block-scaled FP4, FP32 accumulate) with the
+ * epilogue v = (acc*g^x)*g^w, BF16 gate/up, h = bf16(f32(silu(gate)*up)*p)
+ * and the row maxima of h; requantisation of h with those maxima; FC2
+ * grouped GEMM with the same epilogue, BF16 y per (token, slot); and the
+ * combine out[t] = bf16(sum over slots 0..k-1 in order, FP32)
+ * [miniTE/differs, miniTE/use, RL/4.4, RL/4.5].  Equivalent to
+ * moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16.
+ *
+ *  w                   quantised weights (host struct, device pointers)
+ *  T, k                as given to moe_route_sort_amax
+ *  expert_offsets_dev  as written by moe_route_sort_amax
+ *  out_dev             BF16 [T][H], 16-byte aligned
+ *  ws_dev, ws_bytes    the workspace moe_route_sort_amax filled
+ * Device error: NVFP4_ERR_DEVICE_TIMEOUT (a pipeline wait ran out).
+ */
+nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
+                                      const int32_t* expert_offsets_dev, void* out_dev,
+                                      void* ws_dev, size_t ws_bytes, void* stream);
+
+/* The four stages of moe_expert_forward_nvfp4, callable one by one (the
+ * "unfused API").  fc1_debug_dev / fc2_debug_dev may be NULL; if given they
+ * receive the FP32 pre-cast epilogue values v of every real routed row:
+ * float [rows_cap][2I] (gate columns then up columns) and float
+ * [rows_cap][H]; pad rows are not written. */
+nvfp4_status moe_fc1_swiglu_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
+                                  const int32_t* expert_offsets_dev, void* ws_dev,
+                                  size_t ws_bytes, float* fc1_debug_dev, void* stream);
+nvfp4_status moe_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
+                               const int32_t* expert_offsets_dev, void* ws_dev,
+                               size_t ws_bytes, void* stream);
+nvfp4_status moe_fc2_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
+                           const int32_t* expert_offsets_dev, void* ws_dev,
+                           size_t ws_bytes, float* fc2_debug_dev, void* stream);
+nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev,
+                              void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, then report and clear this device's error word:
+ * *device_status receives NVFP4_OK or the first device error recorded since
+ * the last call.  Returns NVFP4_ERR_CUDA if the synchronisation failed. */
+nvfp4_status nvfp4_get_device_error(void* stream, int* device_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_MOE_H */

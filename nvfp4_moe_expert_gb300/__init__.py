@@ -1,0 +1,284 @@
+"""Python binding of libnvfp4moe.so, the GB300 (sm_103a) NVFP4 W4A4 MoE expert forward.
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels; PyTorch provides device memory and the current stream.  The
+entry points have the names of the C ABI in ``include/nvfp4_moe.h``:
+
+    nvfp4_quantize_rows, moe_route_sort_amax, moe_expert_forward_nvfp4,
+    moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16,
+    moe_workspace_bytes, moe_workspace_layout_query, nvfp4_sf_bytes,
+    nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string
+
+There is no CPU fallback: if the library is missing or a call fails, an
+exception is raised.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4moe.so")
+
+NVFP4_OK = 0
+STATUS_NAMES = {
+    0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED_SHAPE",
+    3: "NVFP4_ERR_WORKSPACE_TOO_SMALL", 4: "NVFP4_ERR_CUDA", 5: "NVFP4_ERR_BAD_EXPERT_ID",
+    6: "NVFP4_ERR_NONFINITE", 7: "NVFP4_ERR_DEVICE_TIMEOUT",
+}
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+
+
+class moe_nvfp4_weights(ctypes.Structure):
+    _fields_ = [
+        ("w1_codes", ctypes.c_void_p), ("w1_sf", ctypes.c_void_p), ("w1_g", ctypes.c_void_p),
+        ("w2_codes", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("w2_g", ctypes.c_void_p),
+        ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+    ]
+
+
+class moe_workspace_layout(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+        ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+        ("rows_cap", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
+    ] + [(n, ctypes.c_size_t) for n in (
+        "a_codes", "a_sf", "a_g", "row_pair", "row_prob", "amax2", "chunk_count", "chunk_base",
+        "pair_rank", "expert_count", "route_end", "h", "a2_codes", "a2_sf", "a2_g", "y", "total")]
+
+
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+_SIGNATURES = {
+    "nvfp4_status_string": (ctypes.c_char_p, [_I32]),
+    "nvfp4_rows_padded": (_I64, [_I64]),
+    "nvfp4_sf_bytes": (_SZ, [_I64, _I64]),
+    "nvfp4_quantize_rows": (_I32, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "moe_workspace_layout_query": (_I32, [_I64, _I32, _I32, _I32, _I32, ctypes.POINTER(moe_workspace_layout)]),
+    "moe_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
+    "moe_route_sort_amax": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_forward_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "moe_fc1_swiglu_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
+    "moe_requant_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
+    "moe_fc2_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
+    "moe_combine_bf16": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
+    "nvfp4_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_int)]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded library (loaded on first use; raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m nvfp4_moe_expert_gb300.build` "
+                "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(fn, status):
+    if status != NVFP4_OK:
+        raise NVFP4Error(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# ---------------------------------------------------------------- host queries
+def nvfp4_status_string(status):
+    return lib().nvfp4_status_string(status).decode()
+
+
+def nvfp4_rows_padded(rows):
+    return lib().nvfp4_rows_padded(rows)
+
+
+def nvfp4_sf_bytes(rows, cols):
+    return lib().nvfp4_sf_bytes(rows, cols)
+
+
+def moe_workspace_bytes(T, H, I, E, k):
+    return lib().moe_workspace_bytes(T, H, I, E, k)
+
+
+def moe_workspace_layout_query(T, H, I, E, k):
+    L = moe_workspace_layout()
+    _check("moe_workspace_layout_query", lib().moe_workspace_layout_query(T, H, I, E, k, ctypes.byref(L)))
+    return L
+
+
+# ---------------------------------------------------------------- quantiser
+def nvfp4_quantize_rows(x, codes=None, sf=None, g=None, stream=None):
+    """NVFP4-quantise each row of a BF16 CUDA matrix [rows, cols]; returns (codes, sf, g)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bfloat16 tensor")
+    _need_cuda(x)
+    rows, cols = x.shape
+    rp = nvfp4_rows_padded(rows)
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rp, cols // 2), dtype=torch.uint8, device=dev)
+    if sf is None:
+        sf = torch.empty(max(nvfp4_sf_bytes(rows, cols), 1), dtype=torch.uint8, device=dev)
+    if g is None:
+        g = torch.empty(rows, dtype=torch.float32, device=dev)
+    _check("nvfp4_quantize_rows", lib().nvfp4_quantize_rows(
+        _ptr(x), rows, cols, x.stride(0), _ptr(codes), _ptr(sf), _ptr(g), _stream(stream)))
+    return codes, sf, g
+
+
+def nvfp4_get_device_error(stream=None):
+    st = ctypes.c_int(0)
+    _check("nvfp4_get_device_error", lib().nvfp4_get_device_error(_stream(stream), ctypes.byref(st)))
+    return st.value
+
+
+# ---------------------------------------------------------------- MoE
+class MoEWeights:
+    """Quantised expert weights (device tensors) and the C struct pointing at them."""
+
+    def __init__(self, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, E, H, I):
+        self.tensors = (w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g)
+        self.E, self.H, self.I = E, H, I
+        self.struct = moe_nvfp4_weights(*[t.data_ptr() for t in self.tensors], E, H, I)
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+def quantize_moe_weights(w1, w2, stream=None):
+    """w1 bf16 [E, 2I, H] (gate rows then up rows), w2 bf16 [E, H, I] -> MoEWeights."""
+    E, two_i, H = w1.shape
+    I = two_i // 2
+    if tuple(w2.shape) != (E, H, I):
+        raise ValueError("w2 must be [E, H, I]")
+    c1, s1, g1 = nvfp4_quantize_rows(w1.reshape(E * two_i, H), stream=stream)
+    c2, s2, g2 = nvfp4_quantize_rows(w2.reshape(E * H, I), stream=stream)
+    return MoEWeights(c1, s1, g1, c2, s2, g2, E, H, I)
+
+
+def alloc_workspace(T, H, I, E, k, device="cuda"):
+    n = moe_workspace_bytes(T, H, I, E, k)
+    if n == 0:
+        raise NVFP4Error("moe_workspace_bytes", 2)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_route_sort_amax(x, topk_ids, topk_w, E, expert_offsets, ws, stream=None):
+    """Route sort + per-token amax + pad + NVFP4 quantise of x [T, H] into ws."""
+    _need_cuda(x, topk_ids, topk_w, expert_offsets, ws)
+    if x.dtype != torch.bfloat16 or topk_ids.dtype != torch.int32 or topk_w.dtype != torch.float32:
+        raise ValueError("x bf16, topk_ids int32, topk_w float32 expected")
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    _check("moe_route_sort_amax", lib().moe_route_sort_amax(
+        _ptr(x), T, H, E, k, _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_expert_forward_nvfp4(weights, T, k, expert_offsets, out, ws, stream=None):
+    _need_cuda(expert_offsets, out, ws)
+    _check("moe_expert_forward_nvfp4", lib().moe_expert_forward_nvfp4(
+        weights.ref(), T, k, _ptr(expert_offsets), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_fc1_swiglu_nvfp4(weights, T, k, expert_offsets, ws, debug=None, stream=None):
+    _need_cuda(expert_offsets, ws, debug)
+    _check("moe_fc1_swiglu_nvfp4", lib().moe_fc1_swiglu_nvfp4(
+        weights.ref(), T, k, _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(debug), _stream(stream)))
+
+
+def moe_requant_nvfp4(weights, T, k, expert_offsets, ws, stream=None):
+    _need_cuda(expert_offsets, ws)
+    _check("moe_requant_nvfp4", lib().moe_requant_nvfp4(
+        weights.ref(), T, k, _ptr(expert_offsets), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_fc2_nvfp4(weights, T, k, expert_offsets, ws, debug=None, stream=None):
+    _need_cuda(expert_offsets, ws, debug)
+    _check("moe_fc2_nvfp4", lib().moe_fc2_nvfp4(
+        weights.ref(), T, k, _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(debug), _stream(stream)))
+
+
+def moe_combine_bf16(weights, T, k, out, ws, stream=None):
+    _need_cuda(out, ws)
+    _check("moe_combine_bf16", lib().moe_combine_bf16(
+        weights.ref(), T, k, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+class MoELayer:
+    """Convenience wrapper: owns quantised weights and a workspace sized per call."""
+
+    def __init__(self, w1, w2, stream=None):
+        self.weights = quantize_moe_weights(w1, w2, stream=stream)
+        self.E, self.H, self.I = self.weights.E, self.weights.H, self.weights.I
+        self._ws = {}
+
+    def workspace(self, T, k, device):
+        key = (T, k)
+        if key not in self._ws:
+            self._ws.clear()
+            self._ws[key] = alloc_workspace(T, self.H, self.I, self.E, k, device)
+        return self._ws[key]
+
+    def forward(self, x, topk_ids, topk_w, out=None, stream=None):
+        T, H = x.shape
+        k = topk_ids.shape[1]
+        ws = self.workspace(T, k, x.device)
+        offs = torch.empty(self.E + 1, dtype=torch.int32, device=x.device)
+        if out is None:
+            out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+        moe_route_sort_amax(x, topk_ids, topk_w, self.E, offs, ws, stream=stream)
+        moe_expert_forward_nvfp4(self.weights, T, k, offs, out, ws, stream=stream)
+        return out
+
+
+# ---------------------------------------------------------------- layout helpers
+def sf_byte_index(rows, cols):
+    """numpy int64 [rows, cols/16]: byte offset of each block scale in the library's
+    scale-factor layout (512-byte tiles of 128 rows x 64 columns)."""
+    import numpy as np
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    b = np.arange(cols // 16, dtype=np.int64)[None, :]
+    return ((r >> 7) * (cols >> 6) + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3)
+
+
+def sf_to_rows(sf, rows, cols):
+    """Library scale-factor bytes (numpy uint8) -> plain [rows, cols/16] E4M3 codes."""
+    return sf[sf_byte_index(rows, cols)]
+
+
+def sf_from_rows(scales, cols, rows_pad=None):
+    """Plain [rows, cols/16] E4M3 codes -> library scale-factor bytes (numpy uint8)."""
+    import numpy as np
+    rows = scales.shape[0]
+    rows_pad = nvfp4_rows_padded(rows) if rows_pad is None else rows_pad
+    out = np.zeros(rows_pad * cols // 16, dtype=np.uint8)
+    out[sf_byte_index(rows, cols)] = scales
+    return out

@@ -1,0 +1,346 @@
+// C ABI of the NVFP4 MoE expert forward: argument validation, workspace
+// layout, per-device state (error word, SM count) and the launch sequences.
+// The operations themselves are documented in include/nvfp4_moe.h.
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+// First device-side error since the last nvfp4_get_device_error (0 = none).
+__device__ int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int* g_err_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return (d >= 0 && d < kMaxDevices) ? d : -1;
+}
+
+// Device address of this device's error word (looked up once per device).
+int* device_error_ptr() {
+    const int d = current_device();
+    if (d < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_err_ptr[d]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_err_ptr[d] = static_cast<int*>(p);
+    }
+    return g_err_ptr[d];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool moe_shape_ok(int64_t T, int H, int I, int E, int k) {
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return false;
+    if (H < 256 || H > 8192 || H % 256) return false;
+    if (I < 128 || I > 8192 || I % 128) return false;
+    if (T * static_cast<int64_t>(k) >= (int64_t(1) << 30)) return false;
+    return true;
+}
+
+void compute_layout(int64_t T, int H, int I, int E, int k, moe_workspace_layout* L) {
+    std::memset(L, 0, sizeof(*L));
+    L->T = T;
+    L->H = H;
+    L->I = I;
+    L->E = E;
+    L->k = k;
+    const int64_t R = T * k;
+    const int64_t live_experts = R < E ? R : E;
+    L->rows_cap = (R + live_experts * (kTileM - 1) + kTileM - 1) / kTileM * kTileM;
+    L->n_chunks = (T + 255) / 256;
+    const int64_t rc = L->rows_cap;
+    size_t o = 0;
+    auto take = [&o](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L->a_codes = take(rc * H / 2);
+    L->a_sf = take(rc * H / 16);
+    L->a_g = take(rc * 4);
+    L->row_pair = take(rc * 4);
+    L->row_prob = take(rc * 4);
+    L->amax2 = take(rc * 4);
+    L->chunk_count = take(static_cast<size_t>(E) * L->n_chunks * 4);
+    L->chunk_base = take(static_cast<size_t>(E) * L->n_chunks * 4);
+    L->pair_rank = take(R * 4);
+    L->expert_count = take(static_cast<size_t>(E) * 4);
+    L->route_end = o;
+    L->h = take(rc * I * 2);
+    L->a2_codes = take(rc * I / 2);
+    L->a2_sf = take(rc * I / 16);
+    L->a2_g = take(rc * 4);
+    L->y = take(R * H * 2);
+    L->total = o;
+}
+
+nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// Shared validation of the calls that run on a filled workspace.
+nvfp4_status check_forward_args(const moe_nvfp4_weights* w, int64_t T, int k, const void* ws, size_t ws_bytes,
+                                moe_workspace_layout* L) {
+    if (!w || !ws) return NVFP4_ERR_INVALID_ARG;
+    if (!w->w1_codes || !w->w1_sf || !w->w1_g || !w->w2_codes || !w->w2_sf || !w->w2_g) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(w->w1_codes, 16) || !aligned(w->w1_sf, 16) || !aligned(w->w2_codes, 16) || !aligned(w->w2_sf, 16) ||
+        !aligned(ws, 256))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!moe_shape_ok(T, w->H, w->I, w->E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    compute_layout(T, w->H, w->I, w->E, k, L);
+    if (ws_bytes < L->total) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+    return NVFP4_OK;
+}
+
+GemmArgs fc1_args(const moe_nvfp4_weights* w, const int32_t* offsets, void* ws, const moe_workspace_layout& L,
+                  float* debug, int* err) {
+    GemmArgs a{};
+    a.a_codes = at<uint8_t>(ws, L.a_codes);
+    a.a_sf = at<uint8_t>(ws, L.a_sf);
+    a.a_g = at<float>(ws, L.a_g);
+    a.b_codes = static_cast<const uint8_t*>(w->w1_codes);
+    a.b_sf = static_cast<const uint8_t*>(w->w1_sf);
+    a.b_g = w->w1_g;
+    a.rows_cap = L.rows_cap;
+    a.K = w->H;
+    a.Nw = 2 * w->I;
+    a.E = w->E;
+    a.offsets = offsets;
+    a.row_pair = at<int32_t>(ws, L.row_pair);
+    a.row_prob = at<float>(ws, L.row_prob);
+    a.I = w->I;
+    a.h = at<uint16_t>(ws, L.h);
+    a.amax2 = at<uint32_t>(ws, L.amax2);
+    a.H = w->H;
+    a.y = nullptr;
+    a.debug = debug;
+    a.err = err;
+    return a;
+}
+
+GemmArgs fc2_args(const moe_nvfp4_weights* w, const int32_t* offsets, void* ws, const moe_workspace_layout& L,
+                  float* debug, int* err) {
+    GemmArgs a{};
+    a.a_codes = at<uint8_t>(ws, L.a2_codes);
+    a.a_sf = at<uint8_t>(ws, L.a2_sf);
+    a.a_g = at<float>(ws, L.a2_g);
+    a.b_codes = static_cast<const uint8_t*>(w->w2_codes);
+    a.b_sf = static_cast<const uint8_t*>(w->w2_sf);
+    a.b_g = w->w2_g;
+    a.rows_cap = L.rows_cap;
+    a.K = w->I;
+    a.Nw = w->H;
+    a.E = w->E;
+    a.offsets = offsets;
+    a.row_pair = at<int32_t>(ws, L.row_pair);
+    a.row_prob = at<float>(ws, L.row_prob);
+    a.I = w->I;
+    a.h = nullptr;
+    a.amax2 = nullptr;
+    a.H = w->H;
+    a.y = at<uint16_t>(ws, L.y);
+    a.debug = debug;
+    a.err = err;
+    return a;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    const int d = current_device();
+    if (d < 0) return 1;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_sm_count[d]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n < 1) n = 1;
+        g_sm_count[d] = n;
+    }
+    return g_sm_count[d];
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+const char* nvfp4_status_string(int status) {
+    switch (status) {
+        case NVFP4_OK: return "NVFP4_OK";
+        case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
+        case NVFP4_ERR_UNSUPPORTED_SHAPE: return "NVFP4_ERR_UNSUPPORTED_SHAPE";
+        case NVFP4_ERR_WORKSPACE_TOO_SMALL: return "NVFP4_ERR_WORKSPACE_TOO_SMALL";
+        case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+        case NVFP4_ERR_BAD_EXPERT_ID: return "NVFP4_ERR_BAD_EXPERT_ID";
+        case NVFP4_ERR_NONFINITE: return "NVFP4_ERR_NONFINITE";
+        case NVFP4_ERR_DEVICE_TIMEOUT: return "NVFP4_ERR_DEVICE_TIMEOUT";
+        default: return "NVFP4_UNKNOWN_STATUS";
+    }
+}
+
+int64_t nvfp4_rows_padded(int64_t rows) {
+    if (rows < 0) return 0;
+    return (rows + kTileM - 1) / kTileM * kTileM;
+}
+
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols <= 0 || cols % 64) return 0;
+    return static_cast<size_t>(nvfp4_rows_padded(rows)) * static_cast<size_t>(cols / 16);
+}
+
+nvfp4_status nvfp4_quantize_rows(const void* x_dev, int64_t rows, int64_t cols, int64_t ld, void* codes_dev,
+                                 void* sf_dev, float* g_dev, void* stream) {
+    if (rows < 0 || cols < 64 || cols > 8192 || cols % 64 || ld < cols || ld % 8) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return NVFP4_OK;
+    if (!x_dev || !codes_dev || !sf_dev || !g_dev) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x_dev, 16) || !aligned(codes_dev, 16) || !aligned(sf_dev, 16) || !aligned(g_dev, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    int* err = device_error_ptr();
+    if (!err) return NVFP4_ERR_CUDA;
+    return from_cuda(launch_quantize_rows(static_cast<const uint16_t*>(x_dev), rows, cols, ld,
+                                          static_cast<uint8_t*>(codes_dev), static_cast<uint8_t*>(sf_dev), g_dev, err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_workspace_layout_query(int64_t T, int H, int I, int E, int k, moe_workspace_layout* out) {
+    if (!out) return NVFP4_ERR_INVALID_ARG;
+    if (!moe_shape_ok(T, H, I, E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    compute_layout(T, H, I, E, k, out);
+    return NVFP4_OK;
+}
+
+size_t moe_workspace_bytes(int64_t T, int H, int I, int E, int k) {
+    if (!moe_shape_ok(T, H, I, E, k)) return 0;
+    moe_workspace_layout L;
+    compute_layout(T, H, I, E, k, &L);
+    return L.total;
+}
+
+nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int k, const int32_t* topk_ids_dev,
+                                 const float* topk_w_dev, int32_t* expert_offsets_dev, void* ws_dev, size_t ws_bytes,
+                                 void* stream) {
+    if (!moe_shape_ok(T, H, 128, E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!expert_offsets_dev || !ws_dev) return NVFP4_ERR_INVALID_ARG;
+    if (T > 0 && (!x_dev || !topk_ids_dev || !topk_w_dev)) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x_dev, 16) || !aligned(ws_dev, 256) || !aligned(topk_ids_dev, 4) || !aligned(topk_w_dev, 4) ||
+        !aligned(expert_offsets_dev, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    moe_workspace_layout L;
+    compute_layout(T, H, 128, E, k, &L);
+    if (ws_bytes < L.route_end) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+    int* err = device_error_ptr();
+    if (!err) return NVFP4_ERR_CUDA;
+    RouteBufs b;
+    b.a_codes = at<uint8_t>(ws_dev, L.a_codes);
+    b.a_sf = at<uint8_t>(ws_dev, L.a_sf);
+    b.a_g = at<float>(ws_dev, L.a_g);
+    b.row_pair = at<int32_t>(ws_dev, L.row_pair);
+    b.row_prob = at<float>(ws_dev, L.row_prob);
+    b.amax2 = at<uint32_t>(ws_dev, L.amax2);
+    b.chunk_count = at<int32_t>(ws_dev, L.chunk_count);
+    b.chunk_base = at<int32_t>(ws_dev, L.chunk_base);
+    b.pair_rank = at<int32_t>(ws_dev, L.pair_rank);
+    b.expert_count = at<int32_t>(ws_dev, L.expert_count);
+    b.n_chunks = L.n_chunks;
+    return from_cuda(launch_route_sort_quant(static_cast<const uint16_t*>(x_dev), T, H, E, k, topk_ids_dev, topk_w_dev,
+                                             expert_offsets_dev, b, err, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_fc1_swiglu_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                                  void* ws_dev, size_t ws_bytes, float* fc1_debug_dev, void* stream) {
+    moe_workspace_layout L;
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    if (s != NVFP4_OK) return s;
+    if (!expert_offsets_dev) return NVFP4_ERR_INVALID_ARG;
+    if (T == 0) return NVFP4_OK;
+    int* err = device_error_ptr();
+    if (!err) return NVFP4_ERR_CUDA;
+    return from_cuda(launch_fc1(fc1_args(w, expert_offsets_dev, ws_dev, L, fc1_debug_dev, err),
+                                static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                               void* ws_dev, size_t ws_bytes, void* stream) {
+    moe_workspace_layout L;
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    if (s != NVFP4_OK) return s;
+    if (!expert_offsets_dev) return NVFP4_ERR_INVALID_ARG;
+    if (T == 0) return NVFP4_OK;
+    int* err = device_error_ptr();
+    if (!err) return NVFP4_ERR_CUDA;
+    return from_cuda(launch_requant(at<uint16_t>(ws_dev, L.h), at<uint32_t>(ws_dev, L.amax2),
+                                    at<int32_t>(ws_dev, L.row_pair), expert_offsets_dev, w->E, L.rows_cap, w->I,
+                                    at<uint8_t>(ws_dev, L.a2_codes), at<uint8_t>(ws_dev, L.a2_sf),
+                                    at<float>(ws_dev, L.a2_g), err, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_fc2_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                           void* ws_dev, size_t ws_bytes, float* fc2_debug_dev, void* stream) {
+    moe_workspace_layout L;
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    if (s != NVFP4_OK) return s;
+    if (!expert_offsets_dev) return NVFP4_ERR_INVALID_ARG;
+    if (T == 0) return NVFP4_OK;
+    int* err = device_error_ptr();
+    if (!err) return NVFP4_ERR_CUDA;
+    return from_cuda(launch_fc2(fc2_args(w, expert_offsets_dev, ws_dev, L, fc2_debug_dev, err),
+                                static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev, void* ws_dev,
+                              size_t ws_bytes, void* stream) {
+    moe_workspace_layout L;
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    if (s != NVFP4_OK) return s;
+    if (T == 0) return NVFP4_OK;
+    if (!out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(launch_combine(at<uint16_t>(ws_dev, L.y), T, k, w->H, static_cast<uint16_t*>(out_dev),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                                      void* out_dev, void* ws_dev, size_t ws_bytes, void* stream) {
+    moe_workspace_layout L;
+    nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    if (s != NVFP4_OK) return s;
+    if (T == 0) return NVFP4_OK;
+    if (!expert_offsets_dev || !out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
+    s = moe_fc1_swiglu_nvfp4(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream);
+    if (s != NVFP4_OK) return s;
+    s = moe_requant_nvfp4(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, stream);
+    if (s != NVFP4_OK) return s;
+    s = moe_fc2_nvfp4(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream);
+    if (s != NVFP4_OK) return s;
+    return moe_combine_bf16(w, T, k, out_dev, ws_dev, ws_bytes, stream);
+}
+
+nvfp4_status nvfp4_get_device_error(void* stream, int* device_status) {
+    if (!device_status) return NVFP4_ERR_INVALID_ARG;
+    *device_status = NVFP4_OK;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    *device_status = v;
+    return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// Fixed-order top-k combine: out[t, :] = bf16( ((0 + y[t,0,:]) + y[t,1,:]) + ... + y[t,k-1,:] )
+// with FP32 additions in top-k slot order.
+//
+// "Finishing RL training faster: bitwise consistency, high performance,
+// agent-driven" (spke.com/ko/ai/article/3192), section 4.5 "Cross-GPU
+// reduction": expert outputs are accumulated in FP32 in top-k slot order on
+// the token's owner; "miniTE diagnoses and narrows the cross-engine execution
+// gap of NVFP4 RL", section "How it differs": the combine order survives
+// padding, quantisation and cast.  The router probability was already
+// applied before FC2, so the combine is a plain sum.
+//
+// HBM-bound: each thread owns 8 consecutive columns of one token (16-byte
+// loads of the k slot rows, one 16-byte store); a grid-stride loop over
+// T*H/8 such vectors keeps every load and store coalesced.
+#include "common.cuh"
+
+namespace nvfp4 {
+namespace {
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, int64_t T, int k, int H,
+                                                      uint16_t* __restrict__ out) {
+    const int vec_per_row = H / 8;
+    const int64_t nvec = T * vec_per_row;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        const int64_t t = i / vec_per_row;
+        const int v = static_cast<int>(i - t * vec_per_row);
+        const uint4* src = reinterpret_cast<const uint4*>(y + t * k * H) + v;
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        for (int s = 0; s < k; ++s) {
+            const uint4 w = __ldcs(src + static_cast<int64_t>(s) * vec_per_row);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(ws[j] << 16));
+                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __uint_as_float(ws[j] & 0xFFFF0000u));
+            }
+        }
+        uint4 o;
+        o.x = bf16x2_rn(acc[0], acc[1]);
+        o.y = bf16x2_rn(acc[2], acc[3]);
+        o.z = bf16x2_rn(acc[4], acc[5]);
+        o.w = bf16x2_rn(acc[6], acc[7]);
+        reinterpret_cast<uint4*>(out + t * H)[v] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st) {
+    const int64_t nvec = T * (H / 8);
+    if (nvec == 0) return cudaSuccess;
+    int64_t blocks = (nvec + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(y, T, k, H, out);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

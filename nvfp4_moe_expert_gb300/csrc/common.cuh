@@ -1,0 +1,92 @@
+// Shared definitions of the CUDA path: constants of the NVFP4 layout, the
+// device error word protocol and the host-side launchers each .cu provides.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4_moe.h"
+
+namespace nvfp4 {
+
+constexpr int kBlock = 16;          // elements per E4M3 block scale
+constexpr int kTileM = 128;         // GEMM M tile = row padding of each expert
+constexpr int kSfAtomBytes = 512;   // one 128-row x 64-column scale tile
+constexpr float kOuterDivisor = 2688.0f;   // 6 * 448
+
+// Byte offset of the E4M3 scale of (row r, block b) in a matrix with `cols` columns.
+__host__ __device__ inline size_t sf_offset(int64_t r, int64_t b, int64_t cols) {
+    return static_cast<size_t>(((r >> 7) * (cols >> 6) + (b >> 2)) * kSfAtomBytes + (r & 31) * 16 +
+                               ((r & 127) >> 5) * 4 + (b & 3));
+}
+
+// Record a device-side error (first one wins).
+__device__ __forceinline__ void set_device_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Cycles a pipeline wait may spin before it reports NVFP4_ERR_DEVICE_TIMEOUT (~2 s).
+constexpr long long kWaitBudgetCycles = 4000000000LL;
+
+// ---- host launchers (each defined in the .cu that holds the kernel) ----
+struct RouteBufs {
+    uint8_t* a_codes;
+    uint8_t* a_sf;
+    float* a_g;
+    int32_t* row_pair;
+    float* row_prob;
+    uint32_t* amax2;
+    int32_t* chunk_count;
+    int32_t* chunk_base;
+    int32_t* pair_rank;
+    int32_t* expert_count;
+    int64_t n_chunks;
+};
+
+cudaError_t launch_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
+                                 uint8_t* sf, float* g, int* err, cudaStream_t st);
+
+cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, int k, const int32_t* ids,
+                                    const float* probs, int32_t* offsets, const RouteBufs& b, int* err,
+                                    cudaStream_t st);
+
+cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32_t* row_pair,
+                           const int32_t* offsets, int E, int64_t rows_cap, int I, uint8_t* codes, uint8_t* sf,
+                           float* g, int* err, cudaStream_t st);
+
+struct GemmArgs {
+    // operands
+    const uint8_t* a_codes;   // [rows_cap][K/2]
+    const uint8_t* a_sf;
+    const float* a_g;         // per routed row
+    const uint8_t* b_codes;   // [E*Nw][K/2]
+    const uint8_t* b_sf;
+    const float* b_g;         // [E*Nw]
+    int64_t rows_cap;
+    int K;                    // reduction length (H for FC1, I for FC2)
+    int Nw;                   // weight rows per expert (2I for FC1, H for FC2)
+    int E;
+    const int32_t* offsets;   // [E+1] padded expert row starts
+    const int32_t* row_pair;  // token*k + slot or -1
+    const float* row_prob;
+    // FC1 outputs
+    int I;
+    uint16_t* h;              // [rows_cap][I]
+    uint32_t* amax2;          // [rows_cap]
+    // FC2 outputs
+    int H;
+    uint16_t* y;              // [T*k][H]
+    float* debug;             // optional pre-cast FP32 values
+    int* err;
+};
+
+cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st);
+
+cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace nvfp4

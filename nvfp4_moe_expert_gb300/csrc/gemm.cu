@@ -1,0 +1,447 @@
+// Grouped block-scaled FP4 GEMMs of the expert forward on tcgen05.
+//
+//   FC1:  acc[r, n] = sum_k (qa*sa)[r,k] (qw*sw)[e*2I+n, k]      (gate n < I, up n >= I)
+//         v = (acc*g^x[r])*g^w[n] in FP32, gate/up = bf16(v),
+//         h = bf16( f32( silu(gate)*up ) * p[r] ),  amax2[r] = max|h[r,:]|
+//   FC2:  y[pair(r), :] = bf16( (acc*g2[r])*g^w2[:] )
+//
+// What is computed follows "miniTE diagnoses and narrows the cross-engine
+// execution gap of NVFP4 RL" (onedev.kr/papers/1404), sections "How it
+// differs" (FP32 epilogue with g^x g^w before the BF16 cast; router
+// probability on the SwiGLU activation before FC2) and "How to use it"
+// (expert boundaries as device offsets; FC2 maxima from the producer of the
+// router-weighted activation; separate FC1/FC2 settings), and "Finishing RL
+// training faster...", section 4.4 "Expert GEMM: two layouts, same row
+// result" (SiLU(gate)*up in FP32, one rounding; each row accumulated in a
+// fixed order, independent of its neighbours).
+//
+// Kernel design (sm_103a):
+//  * persistent: one 192-thread CTA per SM walks the (m-tile, n-tile) list;
+//    the list length comes from the device-side expert offsets, so nothing
+//    is read back to the host;
+//  * warp 0 = TMA producer: A tile 128 rows x 256 K (16 KB, 128B swizzle),
+//    B tile 256 rows x 256 K as two 128-row boxes (FC1: the gate rows and
+//    the matching up rows, so one tile holds both halves of SwiGLU), and the
+//    scale-factor tiles by plain bulk copies; 4-stage mbarrier ring;
+//  * warp 1 = MMA issuer: tcgen05.cp moves the stage's scale factors into
+//    TMEM, then 4 x tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//    (M=128, N=256, K=64) accumulate in a 256-column FP32 TMEM tile;
+//  * warps 2-5 = epilogue: tcgen05.ld of their 32-lane quarter, FP32 scales,
+//    BF16 casts and the fused SwiGLU x prob; direct 32-byte row stores.
+//  Every row's arithmetic is the same whatever tile, expert or batch it is
+//  in: one tile shape, no split-K, K always walked 0..K-1 in 64-wide steps.
+//  All waits are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+// SiLU of every BF16 value, each computed in FP64 and rounded once to FP32.
+__device__ float g_silu_table[65536];
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBKBytes = 128;                         // 256 FP4 values of K
+constexpr int kABytes = kBM * kBKBytes;               // 16 KB
+constexpr int kBBoxBytes = 128 * kBKBytes;            // one 128-row B box
+constexpr int kBBytes = kBN * kBKBytes;               // 32 KB
+constexpr int kSfaOff = kABytes + kBBytes;            // 4 scale tiles of A
+constexpr int kSfbOff = kSfaOff + 4 * kSfAtomBytes;   // 2 x 4 scale tiles of B
+constexpr int kStageBytes = kSfbOff + 8 * kSfAtomBytes;
+static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+constexpr int kBarrierBytes = 256;
+constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 256;                     // per stage: SFA 16 cols, SFB 32 cols
+constexpr uint32_t kSfColsPerStage = 48;
+static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+
+__global__ void init_silu_table_kernel() {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < 65536) {
+        const double a = static_cast<double>(__uint_as_float(static_cast<uint32_t>(i) << 16));
+        g_silu_table[i] = __double2float_rn(a / (1.0 + exp(-a)));
+    }
+}
+
+__device__ __forceinline__ int expert_of_row(const int32_t* __restrict__ off, int E, int row) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(off + mid) <= row) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return a | (b << 16);
+}
+
+template <bool kFC1>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* tmem_full = empty + kStages;
+    uint64_t* tmem_empty = tmem_full + 1;
+    uint64_t* drain = tmem_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int E = args.E;
+    const int num_m_tiles = __ldg(args.offsets + E) / kBM;
+    const int n_tiles = kFC1 ? args.I / 128 : args.H / kBN;
+    const int num_tiles = num_m_tiles * n_tiles;
+    const int num_k64 = args.K / 64;
+    const int num_ks = (num_k64 + 3) / 4;
+
+    bool failed = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_a = policy_evict_last();
+            const uint64_t pol_b = policy_evict_normal();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_parity = 0;
+            for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
+                const int mt = t / n_tiles, nt = t % n_tiles;
+                const int e = expert_of_row(args.offsets, E, mt * kBM);
+                int row0, row1;
+                if (kFC1) {
+                    row0 = e * args.Nw + nt * 128;
+                    row1 = row0 + args.I;
+                } else {
+                    row0 = e * args.Nw + nt * kBN;
+                    row1 = row0 + 128;
+                }
+                for (int ks = 0; ks < num_ks; ++ks) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetCycles)) {
+                        failed = true;
+                        break;
+                    }
+                    const int nk = min(4, num_k64 - 4 * ks);
+                    const uint32_t sf_bytes = static_cast<uint32_t>(nk) * kSfAtomBytes;
+                    mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + 3 * sf_bytes);
+                    uint8_t* st = smem + stage * kStageBytes;
+                    tma_load_2d(st, &tmA, &full[stage], ks * kBKBytes, mt * kBM, pol_a);
+                    tma_load_2d(st + kABytes, &tmB, &full[stage], ks * kBKBytes, row0, pol_b);
+                    tma_load_2d(st + kABytes + kBBoxBytes, &tmB, &full[stage], ks * kBKBytes, row1, pol_b);
+                    bulk_load(st + kSfaOff,
+                              args.a_sf + (static_cast<int64_t>(mt) * num_k64 + 4 * ks) * kSfAtomBytes, sf_bytes,
+                              &full[stage], pol_a);
+                    bulk_load(st + kSfbOff,
+                              args.b_sf + (static_cast<int64_t>(row0 / 128) * num_k64 + 4 * ks) * kSfAtomBytes,
+                              sf_bytes, &full[stage], pol_b);
+                    bulk_load(st + kSfbOff + 4 * kSfAtomBytes,
+                              args.b_sf + (static_cast<int64_t>(row1 / 128) * num_k64 + 4 * ks) * kSfAtomBytes,
+                              sf_bytes, &full[stage], pol_b);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (failed) {
+                set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                // let every copy still in flight land before the CTA's shared memory goes away
+                for (int s = 0; s < kStages; ++s) {
+                    if (issued & (1u << s)) {
+                        mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, kWaitBudgetCycles);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_nvf4(kBM, kBN);
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool issued_any = false;
+            for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
+                if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, kWaitBudgetCycles)) {
+                    failed = true;
+                    break;
+                }
+                acc_phase ^= 1u;
+                tc_fence_after();
+                for (int ks = 0; ks < num_ks; ++ks) {
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetCycles)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(4, num_k64 - 4 * ks);
+                    const uint32_t st = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sf_col = tmem + kSfCol0 + kSfColsPerStage * stage;
+                    for (int j = 0; j < nk; ++j) {
+                        tc_cp_32x128b_warpx4(sf_col + 4 * j, sdesc_sf(st + kSfaOff + kSfAtomBytes * j));
+                        tc_cp_32x128b_warpx4(sf_col + 16 + 8 * j, sdesc_sf(st + kSfbOff + kSfAtomBytes * j));
+                        tc_cp_32x128b_warpx4(sf_col + 16 + 8 * j + 4,
+                                             sdesc_sf(st + kSfbOff + 4 * kSfAtomBytes + kSfAtomBytes * j));
+                    }
+                    const uint64_t adesc = sdesc_k_sw128(st);
+                    const uint64_t bdesc = sdesc_k_sw128(st + kABytes);
+                    for (int j = 0; j < nk; ++j) {
+                        // +32 bytes of K per step = +2 in the descriptor's address field
+                        tc_mma_nvf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                                    (ks | j) != 0 ? 1u : 0u);
+                    }
+                    issued_any = true;
+                    tc_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (failed) break;
+                tc_commit(tmem_full);
+            }
+            if (failed) {
+                set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                if (issued_any) {   // wait for the MMAs already issued before TMEM is released
+                    tc_commit(drain);
+                    mbar_wait_bounded(drain, 0, nullptr, kWaitBudgetCycles);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                              // TMEM lane quarter of this warp
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
+                if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            acc_phase ^= 1u;
+            tc_fence_after();
+            const int mt = t / n_tiles, nt = t % n_tiles;
+            const int e = expert_of_row(args.offsets, E, mt * kBM);
+            const int64_t row = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
+            const int pair = __ldg(args.row_pair + row);
+            const bool live = pair >= 0;
+            const float gr = live ? __ldg(args.a_g + row) : 0.0f;
+            if (kFC1) {
+                const int I = args.I;
+                const float p = live ? __ldg(args.row_prob + row) : 0.0f;
+                const float* gw_gate = args.b_g + static_cast<int64_t>(e) * args.Nw + nt * 128;
+                const float* gw_up = gw_gate + I;
+                uint16_t* hrow = args.h + row * I + nt * 128;
+                float* dbg = args.debug ? args.debug + row * (2 * I) + nt * 128 : nullptr;
+                float hmax = 0.0f;
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t rg[16], ru[16];
+                    tmem_ld_32x32b_x16(taddr + c, rg);
+                    tmem_ld_32x32b_x16(taddr + 128 + c, ru);
+                    tmem_ld_wait();
+                    if (live) {
+                        uint32_t packed[8];
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            float hv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const float vg = __fmul_rn(__fmul_rn(__uint_as_float(rg[i + u]), gr),
+                                                           __ldg(gw_gate + c + i + u));
+                                const float vu = __fmul_rn(__fmul_rn(__uint_as_float(ru[i + u]), gr),
+                                                           __ldg(gw_up + c + i + u));
+                                if (dbg) {
+                                    dbg[c + i + u] = vg;
+                                    dbg[I + c + i + u] = vu;
+                                }
+                                const __nv_bfloat16 gb = __float2bfloat16_rn(vg);
+                                const __nv_bfloat16 ub = __float2bfloat16_rn(vu);
+                                const float s = g_silu_table[__bfloat16_as_ushort(gb)];
+                                const float t1 = __fmul_rn(s, __bfloat162float(ub));
+                                const float t2 = __fmul_rn(t1, p);
+                                hv[u] = __bfloat162float(__float2bfloat16_rn(t2));
+                                hmax = fmaxf(hmax, fabsf(hv[u]));
+                            }
+                            packed[i / 2] = pack_bf16x2(hv[0], hv[1]);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(hrow + c);
+                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    }
+                }
+                if (live) atomicMax(args.amax2 + row, __float_as_uint(hmax));
+            } else {
+                const int H = args.H;
+                const float* gw = args.b_g + static_cast<int64_t>(e) * args.Nw + nt * kBN;
+                uint16_t* yrow = live ? args.y + static_cast<int64_t>(pair) * H + nt * kBN : nullptr;
+                float* dbg = args.debug ? args.debug + row * H + nt * kBN : nullptr;
+#pragma unroll 1
+                for (int c = 0; c < kBN; c += 16) {
+                    uint32_t ra[16];
+                    tmem_ld_32x32b_x16(taddr + c, ra);
+                    tmem_ld_wait();
+                    if (live) {
+                        uint32_t packed[8];
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(ra[i]), gr), __ldg(gw + c + i));
+                            const float v1 =
+                                __fmul_rn(__fmul_rn(__uint_as_float(ra[i + 1]), gr), __ldg(gw + c + i + 1));
+                            if (dbg) {
+                                dbg[c + i] = v0;
+                                dbg[c + i + 1] = v1;
+                            }
+                            packed[i / 2] = pack_bf16x2(v0, v1);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tmem_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        }
+    });
+    return fn;
+}
+
+// 2D map over an NVFP4 code matrix [rows][row_bytes], 128 x 128-byte boxes, 128B swizzle.
+bool make_code_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_init_mutex;
+bool g_silu_ready[kMaxDevices];
+bool g_attr_ready[kMaxDevices][2];
+
+cudaError_t prepare_device(bool fc1, cudaStream_t st) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_init_mutex);
+    const int which = fc1 ? 0 : 1;
+    if (!g_attr_ready[dev][which]) {
+        e = fc1 ? cudaFuncSetAttribute(grouped_gemm_nvf4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes)
+                : cudaFuncSetAttribute(grouped_gemm_nvf4_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        g_attr_ready[dev][which] = true;
+    }
+    if (fc1 && !g_silu_ready[dev]) {
+        // The table is filled once per device, in stream order before the first
+        // FC1 launch.  Outside stream capture the stream is also synchronised
+        // once, so FC1 launches on other streams see the finished table.
+        init_silu_table_kernel<<<256, 256, 0, st>>>();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(st, &cs);
+        if (e != cudaSuccess) return e;
+        if (cs == cudaStreamCaptureStatusNone) {
+            e = cudaStreamSynchronize(st);
+            if (e != cudaSuccess) return e;
+        }
+        g_silu_ready[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st) {
+    cudaError_t e = prepare_device(fc1, st);
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;
+    if (!make_code_map(&ma, a.a_codes, a.rows_cap, a.K / 2)) return cudaErrorInvalidValue;
+    if (!make_code_map(&mb, a.b_codes, static_cast<int64_t>(a.E) * a.Nw, a.K / 2)) return cudaErrorInvalidValue;
+    const int grid = device_sm_count();
+    if (fc1) grouped_gemm_nvf4_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(ma, mb, a);
+    else grouped_gemm_nvf4_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(ma, mb, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st) { return launch_gemm(true, a, st); }
+cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st) { return launch_gemm(false, a, st); }
+
+}  // namespace nvfp4

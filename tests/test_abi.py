@@ -1,0 +1,145 @@
+"""The C-ABI library loads, exports every symbol include/*.h declares, and its
+host-side queries and argument validation behave as documented.  No kernel is
+launched here: every call below is rejected (or answered) on the host."""
+
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import nvfp4_moe_expert_gb300 as M
+from nvfp4_moe_expert_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return M.lib()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b((?:nvfp4|moe)_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"nvfp4_quantize_rows", "moe_route_sort_amax", "moe_expert_forward_nvfp4"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in M.STATUS_NAMES.items():
+        assert M.nvfp4_status_string(code) == name
+    assert M.nvfp4_status_string(99) == "NVFP4_UNKNOWN_STATUS"
+
+
+def test_sizes(lib):
+    assert M.nvfp4_rows_padded(0) == 0
+    assert M.nvfp4_rows_padded(1) == 128
+    assert M.nvfp4_rows_padded(128) == 128
+    assert M.nvfp4_rows_padded(129) == 256
+    assert M.nvfp4_sf_bytes(1, 64) == 128 * 4
+    assert M.nvfp4_sf_bytes(300, 2048) == 384 * 128
+    assert M.nvfp4_sf_bytes(10, 100) == 0
+
+
+def test_sf_index_is_a_permutation():
+    for rows, cols in ((128, 64), (256, 2048), (384, 768)):
+        idx = M.sf_byte_index(rows, cols)
+        assert np.array_equal(np.sort(idx.ravel()), np.arange(rows * cols // 16))
+        # the first 128-row x 64-column tile is the 32x16-byte block the tensor-core copy takes
+        assert idx[0, 0] == 0 and idx[0, 1] == 1 and idx[32, 0] == 4 and idx[1, 0] == 16
+        if cols > 64:
+            assert idx[0, 4] == 512
+
+
+def test_workspace_layout(lib):
+    L = M.moe_workspace_layout_query(4096, 2048, 768, 128, 8)
+    assert L.rows_cap % 128 == 0 and L.rows_cap >= 4096 * 8
+    assert L.rows_cap <= 4096 * 8 + 128 * 128
+    offs = [L.a_codes, L.a_sf, L.a_g, L.row_pair, L.row_prob, L.amax2, L.chunk_count, L.chunk_base,
+            L.pair_rank, L.expert_count, L.route_end, L.h, L.a2_codes, L.a2_sf, L.a2_g, L.y, L.total]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs)
+    assert L.total == M.moe_workspace_bytes(4096, 2048, 768, 128, 8)
+    assert L.a_sf - L.a_codes >= L.rows_cap * 1024
+    assert L.total - L.y >= 4096 * 8 * 2048 * 2
+    # the capacity only counts experts that can be live
+    small = M.moe_workspace_layout_query(1, 2048, 768, 128, 8)
+    assert small.rows_cap == 1024
+
+
+@pytest.mark.parametrize("shape", [(0, 2048, 768, 0, 8), (4, 2000, 768, 8, 2), (4, 2048, 100, 8, 2),
+                                   (4, 2048, 768, 8, 9), (4, 2048, 768, 2000, 2), (-1, 256, 128, 8, 2)])
+def test_unsupported_shapes(lib, shape):
+    assert M.moe_workspace_bytes(*shape) == 0
+    L = M.moe_workspace_layout()
+    assert lib.moe_workspace_layout_query(*shape, ctypes.byref(L)) == 2
+
+
+def test_quantize_rows_validation(lib):
+    p = ctypes.c_void_p(256)
+    # bad shapes
+    assert lib.nvfp4_quantize_rows(p, 4, 100, 100, p, p, p, None) == 2
+    assert lib.nvfp4_quantize_rows(p, 4, 128, 64, p, p, p, None) == 2
+    assert lib.nvfp4_quantize_rows(p, 4, 16384, 16384, p, p, p, None) == 2
+    # null / misaligned pointers
+    assert lib.nvfp4_quantize_rows(None, 4, 128, 128, p, p, p, None) == 1
+    assert lib.nvfp4_quantize_rows(ctypes.c_void_p(258), 4, 128, 128, p, p, p, None) == 1
+    # zero rows is a no-op
+    assert lib.nvfp4_quantize_rows(None, 0, 128, 128, None, None, None, None) == 0
+
+
+def test_route_validation(lib):
+    p = ctypes.c_void_p(4096)
+    ok_ws = M.moe_workspace_layout_query(16, 256, 128, 8, 2).route_end
+    assert lib.moe_route_sort_amax(p, 16, 256, 8, 2, p, p, p, None, ok_ws, None) == 1
+    assert lib.moe_route_sort_amax(p, 16, 256, 8, 2, p, p, p, p, ok_ws - 1, None) == 3
+    assert lib.moe_route_sort_amax(p, 16, 250, 8, 2, p, p, p, p, ok_ws, None) == 2
+    assert lib.moe_route_sort_amax(p, 16, 256, 8, 2, p, p, p, ctypes.c_void_p(4097), ok_ws, None) == 1
+
+
+def test_forward_validation(lib):
+    p = 4096
+    w = M.moe_nvfp4_weights(p, p, p, p, p, p, 8, 256, 128)
+    need = M.moe_workspace_bytes(16, 256, 128, 8, 2)
+    ws = ctypes.c_void_p(4096)
+    f = lib.moe_expert_forward_nvfp4
+    assert f(None, 16, 2, ws, ws, ws, need, None) == 1
+    assert f(ctypes.byref(w), 16, 2, ws, ws, ws, need - 1, None) == 3
+    assert f(ctypes.byref(w), 16, 9, ws, ws, ws, need, None) == 2
+    bad = M.moe_nvfp4_weights(p, p, 0, p, p, p, 8, 256, 128)
+    assert f(ctypes.byref(bad), 16, 2, ws, ws, ws, need, None) == 1
+    odd = M.moe_nvfp4_weights(p + 8, p, p, p, p, p, 8, 256, 128)
+    assert f(ctypes.byref(odd), 16, 2, ws, ws, ws, need, None) == 1
+    # T = 0 is a valid empty call
+    need0 = M.moe_workspace_bytes(0, 256, 128, 8, 2)
+    assert f(ctypes.byref(w), 0, 2, ws, ws, ws, need0, None) == 0
+    for stage in (lib.moe_fc1_swiglu_nvfp4, lib.moe_fc2_nvfp4):
+        assert stage(ctypes.byref(w), 16, 2, ws, ws, need - 1, None, None) == 3
+    assert lib.moe_requant_nvfp4(ctypes.byref(w), 16, 2, ws, ws, need - 1, None) == 3
+    assert lib.moe_combine_bf16(ctypes.byref(w), 16, 2, ws, ws, need - 1, None) == 3
+
+
+def test_device_error_requires_pointer(lib):
+    assert lib.nvfp4_get_device_error(None, None) == 1
+
+
+def test_product_path_has_no_oracle_import():
+    # the binding and the CUDA sources never reach into the oracle
+    for path in glob.glob(os.path.join(ROOT, "nvfp4_moe_expert_gb300", "**", "*.*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            src = open(path).read()
+            assert "oracle" not in src.replace("the oracle", ""), path

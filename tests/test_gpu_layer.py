@@ -1,0 +1,127 @@
+"""End-to-end parity of the GPU layer (moe_route_sort_amax + moe_expert_forward_nvfp4)
+with the oracle: output relative L2 <= 1e-2, FC2 requantisation code flips
+<= 0.1%, and the fused call identical to the four stages called one by one.
+At the full 2048/768/128/top-8 size with 4096 tokens the oracle checks a
+sample of routed rows and tokens."""
+
+import numpy as np
+import pytest
+import torch
+
+import moe_synth as S
+import nvfp4_moe_expert_gb300 as M
+from nvfp4_moe_expert_gb300 import build as B
+from oracle import formats as F
+from oracle import moe as OM
+from oracle import quant as Q
+from _helpers import FC2_CODE_FLIP_RATE, LAYER_REL_L2, bf16_to_torch, rel_l2, torch_to_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.build()
+    M.lib()
+
+
+def gpu_layer(L, E, stages=False):
+    T, H = L["x"].shape
+    k = L["topk_ids"].shape[1]
+    w = M.quantize_moe_weights(bf16_to_torch(L["w1"]), bf16_to_torch(L["w2"]))
+    I = w.I
+    ws = M.alloc_workspace(T, H, I, E, k)
+    offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    M.moe_route_sort_amax(bf16_to_torch(L["x"]), torch.from_numpy(L["topk_ids"]).cuda(),
+                          torch.from_numpy(L["topk_w"]).cuda(), E, offs, ws)
+    if stages:
+        M.moe_fc1_swiglu_nvfp4(w, T, k, offs, ws)
+        M.moe_requant_nvfp4(w, T, k, offs, ws)
+        M.moe_fc2_nvfp4(w, T, k, offs, ws)
+        M.moe_combine_bf16(w, T, k, out, ws)
+    else:
+        M.moe_expert_forward_nvfp4(w, T, k, offs, out, ws)
+    assert M.nvfp4_get_device_error() == 0
+    return out, ws, offs, M.moe_workspace_layout_query(T, H, I, E, k)
+
+
+def a2_codes_by_pair(ws, lay, T, k, I):
+    rc = lay.rows_cap
+    pair = ws[lay.row_pair:lay.row_pair + 4 * rc].view(torch.int32).cpu().numpy()
+    codes = ws[lay.a2_codes:lay.a2_codes + rc * I // 2].cpu().numpy().reshape(rc, I // 2)
+    out = np.zeros((T * k, I // 2), np.uint8)
+    real = pair >= 0
+    out[pair[real]] = codes[real]
+    return out
+
+
+@pytest.mark.parametrize("cfg", [
+    S.CONFIGS["tiny"],
+    S.LayerConfig("tiny_skew", H=256, I=128, E=8, k=2, T=200, routing="zipf", outlier_frac=0.02),
+    S.LayerConfig("mid", H=1024, I=384, E=16, k=4, T=300),
+    S.LayerConfig("qwen_slice", H=2048, I=768, E=128, k=8, T=96),
+], ids=lambda c: c.name)
+def test_layer_vs_oracle(cfg):
+    L = S.make_layer(cfg)
+    out, ws, offs, lay = gpu_layer(L, cfg.E)
+    wq = OM.quantize_weights(L["w1"], L["w2"])
+    ref, inter = OM.moe_forward(L["x"], L["topk_ids"], L["topk_w"], wq, keep=True)
+    got = torch_to_bf16_bits(out)
+    assert rel_l2(F.bf16_bits_to_f32(got), F.bf16_bits_to_f32(ref)) <= LAYER_REL_L2
+    ref_codes = Q.pack_nibbles(inter["hq"][0])
+    gpu_codes = a2_codes_by_pair(ws, lay, cfg.T, cfg.k, cfg.I)
+    flips = (Q.unpack_nibbles(ref_codes) != Q.unpack_nibbles(gpu_codes)).mean()
+    assert flips <= FC2_CODE_FLIP_RATE, flips
+
+
+def test_fused_equals_stages():
+    cfg = S.LayerConfig("mid", H=1024, I=384, E=16, k=4, T=300)
+    L = S.make_layer(cfg)
+    a = torch_to_bf16_bits(gpu_layer(L, cfg.E)[0])
+    b = torch_to_bf16_bits(gpu_layer(L, cfg.E, stages=True)[0])
+    assert np.array_equal(a, b)
+
+
+def test_run_to_run_deterministic():
+    cfg = S.LayerConfig("skew", H=2048, I=768, E=32, k=4, T=700, routing="zipf", outlier_frac=0.01)
+    L = S.make_layer(cfg)
+    a = torch_to_bf16_bits(gpu_layer(L, cfg.E)[0])
+    b = torch_to_bf16_bits(gpu_layer(L, cfg.E)[0])
+    assert np.array_equal(a, b)
+
+
+def test_dense_special_case_on_gpu():
+    # one expert, top-1, probability 1: the layer is a quantised SwiGLU MLP
+    cfg = S.LayerConfig("dense", H=512, I=256, E=1, k=1, T=130)
+    L = S.make_layer(cfg)
+    out = torch_to_bf16_bits(gpu_layer(L, 1)[0])
+    ref = OM.dense_swiglu_mlp_f64(F.bf16_bits_to_f32(L["x"]), F.bf16_bits_to_f32(L["w1"][0]),
+                                  F.bf16_bits_to_f32(L["w2"][0]))
+    assert rel_l2(F.bf16_bits_to_f32(out), ref) < 0.30
+    wq = OM.quantize_weights(L["w1"], L["w2"])
+    assert rel_l2(F.bf16_bits_to_f32(out), F.bf16_bits_to_f32(OM.moe_forward(
+        L["x"], L["topk_ids"], L["topk_w"], wq))) <= LAYER_REL_L2
+
+
+def test_qwen3_30b_a3b_full_size_sampled():
+    """4096 tokens, 2048/768, 128 experts, top-8: every routed row of a few experts
+    and the full output of a few tokens against the oracle."""
+    cfg = S.CONFIGS["qwen3_30b_a3b"]
+    L = S.make_layer(cfg)
+    out, ws, offs, lay = gpu_layer(L, cfg.E)
+    got = torch_to_bf16_bits(out)
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(cfg.T, 6, replace=False))
+    wq = OM.quantize_weights(L["w1"], L["w2"])
+    ref = OM.moe_forward(L["x"][toks], L["topk_ids"][toks], L["topk_w"][toks], wq)
+    assert rel_l2(F.bf16_bits_to_f32(got[toks]), F.bf16_bits_to_f32(ref)) <= LAYER_REL_L2
+    # per-slot FC2 outputs of every pair routed to experts {0, 77, 127}
+    y = ws[lay.y:lay.y + cfg.T * cfg.k * cfg.H * 2].view(torch.int16).cpu().numpy().view(np.uint16)
+    y = y.reshape(cfg.T, cfg.k, cfg.H)
+    for e in (0, 77, 127):
+        t_e, s_e = np.nonzero(L["topk_ids"] == e)
+        sub_ids = np.zeros((len(t_e), 1), np.int32) + e
+        sub_w = L["topk_w"][t_e, s_e][:, None]
+        _, inter = OM.moe_forward(L["x"][t_e], sub_ids, sub_w, wq, keep=True)
+        assert rel_l2(F.bf16_bits_to_f32(y[t_e, s_e]), F.bf16_bits_to_f32(inter["y"][:, 0])) <= LAYER_REL_L2

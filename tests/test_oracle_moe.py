@@ -147,7 +147,10 @@ def test_dense_special_case():
     ref = M.dense_swiglu_mlp_f64(F.bf16_bits_to_f32(L["x"]), F.bf16_bits_to_f32(L["w1"][0]),
                                  F.bf16_bits_to_f32(L["w2"][0]))
     rel = np.linalg.norm(out - ref) / np.linalg.norm(ref)
-    assert rel < 0.25, rel
+    # one NVFP4 quantisation of Gaussian-like rows costs about 0.095 relative L2;
+    # FC1 carries two (~0.135), the gated product about doubles that in
+    # quadrature, FC2 adds two more: about 0.23 expected, 0.30 is the bound
+    assert rel < 0.30, rel
     # and the exact FP64 chain on the quantised operands (no NVFP4 error in the
     # reference) is reproduced to BF16 precision
     xq = Q.quantize_rows(F.bf16_bits_to_f32(L["x"]))
