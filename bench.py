@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""NVFP4 MoE expert-forward throughput on GB300.
+
+One step = the whole hot path on one batch: moe_route_sort_amax (route sort +
+per-token amax + pad + NVFP4 quantise) and moe_expert_forward_nvfp4 (FC1 +
+SwiGLU x prob, requant, FC2, fixed-order combine), through the C ABI, with the
+quantised weights resident.  Default workload: the Qwen3-30B-A3B-shaped layer
+(hidden 2048, expert intermediate 768, 128 experts, top-8, 4096 tokens,
+balanced routing), seeded synthetic data.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own token
+shard with the same weights (weak scaling, no collective on the data path);
+the timing is the max over ranks.  `--impl reference` times the CPU oracle on
+the host cores instead (bounded sample per step).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth as S  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor ratio on GB300
+FLUSH_BYTES = 512 << 20         # > L2 (129 MB)
+KERNELS_PER_STEP = 7            # hist, scan, quantise-scatter, FC1, requant, FC2, combine
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="qwen3_30b_a3b", choices=sorted(S.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def describe(cfg):
+    return {
+        "workload": f"{cfg.name}: hidden {cfg.H}, expert intermediate {cfg.I} (FC1 out {2 * cfg.I}), "
+                    f"{cfg.E} experts, top-{cfg.k}, {cfg.T} tokens per GPU, {cfg.routing} routing"
+                    + (f", {cfg.outlier_frac:.0%} x20 outlier channels" if cfg.outlier_frac else ""),
+        "tokens": cfg.T, "hidden": cfg.H, "intermediate": cfg.I, "experts": cfg.E, "top_k": cfg.k,
+        "l2": "flushed by a 512 MB write between timed steps",
+        "weights": "pre-quantised NVFP4, resident in HBM (weight quantisation timed separately)",
+    }
+
+
+# ---------------------------------------------------------------- algorithmic work
+def stage_work(cfg):
+    """Algorithmic bytes and FLOPs per launch of each stage (real rows only, no padding)."""
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    R = T * k
+    row_q = lambda C: C // 2 + C // 16 + 4          # codes + block scales + g of one NVFP4 row
+    return {
+        "route_sort_quant": {"bytes": T * (2 * H + k * row_q(H) + 8 * k + 12 * k), "flops": 0},
+        "fc1_swiglu": {"bytes": E * 2 * I * row_q(H) + R * row_q(H) + R * (2 * I + 4 + 8),
+                       "flops": 2 * R * H * 2 * I},
+        "requant": {"bytes": R * (2 * I + 4 + 4) + R * row_q(I), "flops": 0},
+        "fc2": {"bytes": E * H * row_q(I) + R * row_q(I) + R * 2 * H, "flops": 2 * R * I * H},
+        "combine": {"bytes": R * 2 * H + T * 2 * H, "flops": 0},
+    }
+
+
+def roofline_of(name, work, ms, peaks, peak_kind):
+    hbm = float(peaks["hbm_gbs"])
+    fp4 = float(peaks["bf16_tflops"]) * FP4_OVER_BF16
+    b, f = work["bytes"], work["flops"]
+    t_mem = b / (hbm * 1e9)
+    t_cmp = f / (fp4 * 1e12) if f else 0.0
+    if t_cmp > t_mem:
+        ach = f / (ms * 1e-3) / 1e12
+        return {"kernel": name, "bound": "tensor", "achieved": round(ach, 2), "peak": round(fp4, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp4, 4), "traffic": None,
+                "peak_source": f"{peak_kind} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16 ratio)",
+                "algorithmic": f"{f:.4g} FLOP per launch"}
+    ach = b / (ms * 1e-3) / 1e9
+    return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(ach / hbm, 4), "traffic": None, "peak_source": f"{peak_kind} copy bandwidth",
+            "algorithmic": f"{b:.4g} bytes per launch"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [v.strip() for v in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample_rate(cfg, seconds=15.0, n_experts=None):
+    """Time the CPU oracle on a bounded sample of the workload: every (token, slot)
+    pair routed to the first n experts (their weights quantised beforehand,
+    untimed).  Returns (tokens/s, sample description, threads)."""
+    from oracle import moe as OM
+    ids, w = S.make_routing(cfg)
+    x = S.make_x(cfg)
+    if n_experts is None:
+        n_experts = max(1, min(cfg.E, int(round(seconds / 1.0))))
+    w1, w2 = S.make_weights(cfg, experts=n_experts)
+    wq = OM.quantize_weights(w1, w2)
+    for e in range(n_experts):
+        wq.expert(e)
+    groups = []
+    for e in range(n_experts):
+        t_e, s_e = np.nonzero(ids == e)
+        groups.append((x[t_e], np.zeros((len(t_e), 1), np.int32) + e, w[t_e, s_e][:, None]))
+    pairs = sum(len(g[0]) for g in groups)
+    t0 = time.perf_counter()
+    for xe, ie, we in groups:
+        OM.moe_forward(xe, ie, we, wq)
+    dt = time.perf_counter() - t0
+    tokens_per_s = pairs / cfg.k / dt
+    desc = (f"oracle (numpy, FP64 GEMMs) on every routed (token, slot) pair of experts 0..{n_experts - 1} "
+            f"of the {cfg.name} workload: {pairs} pairs in {dt:.2f} s, tokens/s = pairs/s / top-{cfg.k}")
+    return tokens_per_s, desc, os.cpu_count()
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return None
+    from oracle import moe as OM
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    ids, w = S.make_routing(cfg)
+    x = S.make_x(cfg)
+    # experts per step sized from one calibration expert
+    w1, w2 = S.make_weights(cfg, experts=1)
+    wq = OM.quantize_weights(w1, w2)
+    wq.expert(0)
+    t_e, s_e = np.nonzero(ids == 0)
+    t0 = time.perf_counter()
+    OM.moe_forward(x[t_e], np.zeros((len(t_e), 1), np.int32), w[t_e, s_e][:, None], wq)
+    one = time.perf_counter() - t0
+    n_e = int(max(1, min(cfg.E, per_step / max(one, 1e-3))))
+    w1, w2 = S.make_weights(cfg, experts=n_e)
+    wq = OM.quantize_weights(w1, w2)
+    for e in range(n_e):
+        wq.expert(e)
+    groups = []
+    for e in range(n_e):
+        t_e, s_e = np.nonzero(ids == e)
+        groups.append((x[t_e], np.zeros((len(t_e), 1), np.int32) + e, w[t_e, s_e][:, None]))
+    pairs = sum(len(g[0]) for g in groups)
+
+    def step():
+        for xe, ie, we in groups:
+            OM.moe_forward(xe, ie, we, wq)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = pairs * args.steps / cfg.k / dt
+    sample = (f"each step: the CPU oracle on every routed (token, slot) pair of experts 0..{n_e - 1} of the "
+              f"{cfg.name} workload ({pairs} pairs); tokens/s = pairs/s / top-{cfg.k}")
+    return {
+        "impl": "reference", "metric": "nvfp4_moe_expert_forward_tokens_per_s", "value": round(value, 3),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (GEMM) / f32 (quantiser, epilogue)", "data": "synthetic",
+        "config": describe(cfg),
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import nvfp4_moe_expert_gb300 as M
+    from nvfp4_moe_expert_gb300 import build as B
+
+    B.build()
+    M.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x_np = S.make_x(cfg, stream=rank)
+    ids_np, w_np = S.make_routing(cfg, stream=rank)
+    w1_np, w2_np = S.make_weights(cfg)
+    w1, w2 = to_dev(w1_np), to_dev(w2_np)
+    del w1_np, w2_np
+    # S0: weight quantisation, timed on its own
+    M.quantize_moe_weights(w1, w2)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    weights = M.quantize_moe_weights(w1, w2)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wq_ms = ev0.elapsed_time(ev1)
+    del w1, w2
+
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    x = to_dev(x_np)
+    ids = torch.from_numpy(ids_np).to(dev)
+    pw = torch.from_numpy(w_np).to(dev)
+    ws = M.alloc_workspace(T, H, I, E, k, dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+        M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    if M.nvfp4_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- timed region: K steps, L2 flushed between steps (outside the events)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    sampler = ClockSampler(visible.split(",")[local_rank] if visible else local_rank)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if M.nvfp4_get_device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+    value = T * world * K / (total_ms * 1e-3)
+
+    # ---- per-stage attribution (separate pass, same launches, events between stages)
+    names = ["route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"]
+    n_attr = min(K, 100)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n_attr)]
+    for i in range(n_attr):
+        e = evs[i]
+        e[0].record(stream)
+        M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+        e[1].record(stream)
+        M.moe_fc1_swiglu_nvfp4(weights, T, k, offs, ws)
+        e[2].record(stream)
+        M.moe_requant_nvfp4(weights, T, k, offs, ws)
+        e[3].record(stream)
+        M.moe_fc2_nvfp4(weights, T, k, offs, ws)
+        e[4].record(stream)
+        M.moe_combine_bf16(weights, T, k, out, ws)
+        e[5].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_attr))
+                for j, n in enumerate(names)}
+    peaks, peak_kind = load_peaks()
+    work = stage_work(cfg)
+    kernels = {n: roofline_of(n, work[n], stage_ms[n], peaks, peak_kind) | {"ms": round(stage_ms[n], 4)}
+               for n in names}
+    dominant = max(names, key=lambda n: stage_ms[n])
+    roof = dict(kernels[dominant])
+    roof["peak_note"] = "of " + peak_kind
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    x_h = x.cpu().pin_memory()
+    ids_h = ids.cpu().pin_memory()
+    pw_h = pw.cpu().pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_d, ids_d, pw_d = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(pw)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        pw_d.copy_(pw_h, non_blocking=True)
+        M.moe_route_sort_amax(x_d, ids_d, pw_d, E, offs, ws)
+        M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    K2 = min(K, 200)
+    torch.cuda.synchronize()
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_s.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_s.elapsed_time(e_e) / K2
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = x.numel() * 2 + ids.numel() * 4 + pw.numel() * 4
+    d2h = out.numel() * 2
+
+    line = {
+        "metric": "nvfp4_moe_expert_forward_tokens_per_s", "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x ue4m3 block-scaled) MMA, f32 accumulate/epilogue, bf16 in/out",
+        "data": "synthetic (seeded; random-init weights of the layer's shape)",
+        "config": describe(cfg) | {"parallelism": f"token shards x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "kernels": kernels,
+        "weight_quant_ms": round(wq_ms, 3),
+        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "pinned host X/ids/probs copied in, output copied out, every step"},
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": clocks,
+    }
+    return line
+
+
+def main():
+    args = parse()
+    cfg = S.CONFIGS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        line = run_reference(args, cfg, rank, world)
+    else:
+        line = run_ours(args, cfg, rank, world, local_rank)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            v, desc, cores = oracle_sample_rate(cfg)
+            line["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                    "sample": desc}
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -138,7 +138,8 @@ def nvfp4_quantize_rows(x, codes=None, sf=None, g=None, stream=None):
     """NVFP4-quantise each row of a BF16 CUDA matrix [rows, cols]; returns (codes, sf, g)."""
     if x.dtype != torch.bfloat16 or x.dim() != 2:
         raise ValueError("x must be a 2-D bfloat16 tensor")
-    _need_cuda(x)
+    if not x.is_cuda or (x.shape[0] > 0 and x.stride(1) != 1):
+        raise ValueError("x must be a CUDA tensor with contiguous rows")
     rows, cols = x.shape
     rp = nvfp4_rows_padded(rows)
     dev = x.device
