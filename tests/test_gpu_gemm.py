@@ -62,7 +62,8 @@ class Run:
         self.off_np = self.offs.cpu().numpy()
         rc = self.lay.rows_cap
         self.pair = ws_view(self.ws, self.lay.row_pair, rc, torch.int32).cpu().numpy()
-        self.real = np.nonzero(self.pair >= 0)[0]
+        # rows past expert_offsets[E] are capacity the route sort never touched
+        self.real = np.nonzero(self.pair[:self.off_np[-1]] >= 0)[0]
         self.expert = np.searchsorted(self.off_np, self.real, side="right") - 1
         self.wq = OM.quantize_weights(self.L["w1"], self.L["w2"])
 

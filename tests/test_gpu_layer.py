@@ -46,9 +46,11 @@ def gpu_layer(L, E, stages=False):
     return out, ws, offs, M.moe_workspace_layout_query(T, H, I, E, k)
 
 
-def a2_codes_by_pair(ws, lay, T, k, I):
+def a2_codes_by_pair(ws, lay, offs, T, k, I):
     rc = lay.rows_cap
+    used = int(offs.cpu().numpy()[-1])          # rows past expert_offsets[E] were never written
     pair = ws[lay.row_pair:lay.row_pair + 4 * rc].view(torch.int32).cpu().numpy()
+    pair[used:] = -1
     codes = ws[lay.a2_codes:lay.a2_codes + rc * I // 2].cpu().numpy().reshape(rc, I // 2)
     out = np.zeros((T * k, I // 2), np.uint8)
     real = pair >= 0
@@ -70,7 +72,7 @@ def test_layer_vs_oracle(cfg):
     got = torch_to_bf16_bits(out)
     assert rel_l2(F.bf16_bits_to_f32(got), F.bf16_bits_to_f32(ref)) <= LAYER_REL_L2
     ref_codes = Q.pack_nibbles(inter["hq"][0])
-    gpu_codes = a2_codes_by_pair(ws, lay, cfg.T, cfg.k, cfg.I)
+    gpu_codes = a2_codes_by_pair(ws, lay, offs, cfg.T, cfg.k, cfg.I)
     flips = (Q.unpack_nibbles(ref_codes) != Q.unpack_nibbles(gpu_codes)).mean()
     assert flips <= FC2_CODE_FLIP_RATE, flips
 
