@@ -179,6 +179,52 @@ nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int
                                  void* ws_dev, size_t ws_bytes, void* stream);
 
 /*
+ * moe_route_sort_amax_noalloc -- moe_route_sort_amax for callers that cannot
+ * provide scratch memory.  The source pages have no counterpart to this
+ * entry point: it is an interface addition of this library.
+ *
+ * Who needs it: callers whose device memory is planned once at start-up (a
+ * serving engine that assigns every byte up front, an embedded runtime with
+ * no allocator of its own), and hot paths that must not call cudaMalloc
+ * because it can synchronise the device.  Such a caller has its inputs and
+ * its output buffers but no spare scratch to hand over.
+ *
+ * What it does: exactly what moe_route_sort_amax does, with bit-identical
+ * outputs.  Its scratch (per-chunk expert counts, chunk base rows, per-pair
+ * ranks, per-expert counts) lives in a 2 MiB array inside the library, held
+ * on every GPU that loads the library until the process exits.  Nothing is
+ * allocated or freed by this call (no cudaMalloc, cudaFree or allocating
+ * library routine).
+ *
+ *  x_dev, T, H, E, k, topk_ids_dev, topk_w_dev, expert_offsets_dev
+ *                   as for moe_route_sort_amax
+ *  out_dev          the routed-row outputs: the first
+ *                   moe_workspace_layout.chunk_count bytes of a workspace laid
+ *                   out as moe_workspace_layout_query(T, H, I, E, k) describes
+ *                   (codes, scales, g^x, row pair, row probability, FC2 maxima;
+ *                   these offsets do not depend on I), 256-byte aligned.  A full
+ *                   workspace can be passed; its scratch part is not touched.
+ *  out_bytes        size of out_dev; at least layout.chunk_count
+ *
+ * Limits and errors: shapes whose scratch would exceed 2 MiB
+ * (8*E*ceil(T/256) + 4*T*k + 4*E bytes, each part rounded up to 256; e.g.
+ * about 58,000 tokens at E = 128, k = 8) are rejected with
+ * NVFP4_ERR_UNSUPPORTED_SHAPE before anything is launched; other argument
+ * errors as for moe_route_sort_amax.
+ *
+ * Set-up and sharing: the first call on a device looks up the array's device
+ * address (host-side, once per device, with that device current); make that
+ * first call before any stream capture.  Every call on a device shares the
+ * one array and leaves its contents behind; no part of it needs to start at
+ * zero.  Calls that can overlap on the GPU (on different streams without an
+ * ordering between them) race on the array and must not be issued.
+ */
+nvfp4_status moe_route_sort_amax_noalloc(const void* x_dev, int64_t T, int H, int E, int k,
+                                         const int32_t* topk_ids_dev, const float* topk_w_dev,
+                                         int32_t* expert_offsets_dev, void* out_dev,
+                                         size_t out_bytes, void* stream);
+
+/*
  * moe_expert_forward_nvfp4 -- the expert forward after the route sort:
  * FC1 grouped GEMM (tcgen05 block-scaled FP4, FP32 accumulate) with the
  * epilogue v = (acc*g^x)*g^w, BF16 gate/up, h = bf16(f32(silu(gate)*up)*p)

@@ -68,6 +68,7 @@ _SIGNATURES = {
     "moe_fc2_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_combine_bf16": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
     "nvfp4_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_int)]),
+    "moe_route_sort_amax_noalloc": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
 }
 
 _lib = None
@@ -201,6 +202,17 @@ def moe_route_sort_amax(x, topk_ids, topk_w, E, expert_offsets, ws, stream=None)
     _check("moe_route_sort_amax", lib().moe_route_sort_amax(
         _ptr(x), T, H, E, k, _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def moe_route_sort_amax_noalloc(x, topk_ids, topk_w, E, expert_offsets, out, stream=None):
+    """moe_route_sort_amax with its scratch inside the library: `out` only has to hold
+    the routed-row outputs (the first layout.chunk_count bytes of a workspace)."""
+    _need_cuda(x, topk_ids, topk_w, expert_offsets, out)
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    _check("moe_route_sort_amax_noalloc", lib().moe_route_sort_amax_noalloc(
+        _ptr(x), T, H, E, k, _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets), _ptr(out),
+        out.numel(), _stream(stream)))
 
 
 def moe_expert_forward_nvfp4(weights, T, k, expert_offsets, out, ws, stream=None):

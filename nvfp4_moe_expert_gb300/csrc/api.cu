@@ -161,6 +161,8 @@ GemmArgs fc2_args(const moe_nvfp4_weights* w, const int32_t* offsets, void* ws, 
 
 }  // namespace
 
+int* device_error_word() { return device_error_ptr(); }
+
 int device_sm_count() {
     const int d = current_device();
     if (d < 0) return 1;

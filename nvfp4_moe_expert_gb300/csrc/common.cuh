@@ -89,4 +89,7 @@ cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t*
 
 int device_sm_count();
 
+// Device address of this device's error word (nullptr if it cannot be looked up).
+int* device_error_word();
+
 }  // namespace nvfp4
