@@ -16,18 +16,22 @@
 // fixed order, independent of its neighbours).
 //
 // Kernel design (sm_103a):
-//  * persistent: one 192-thread CTA per SM walks the (m-tile, n-tile) list;
+//  * persistent: one 320-thread CTA per SM walks the (m-tile, n-tile) list;
 //    the list length comes from the device-side expert offsets, so nothing
 //    is read back to the host;
 //  * warp 0 = TMA producer: A tile 128 rows x 256 K (16 KB, 128B swizzle),
 //    B tile 256 rows x 256 K as two 128-row boxes (FC1: the gate rows and
 //    the matching up rows, so one tile holds both halves of SwiGLU), and the
-//    scale-factor tiles by plain bulk copies; 4-stage mbarrier ring;
+//    scale-factor tiles by plain bulk copies; 3-stage mbarrier ring;
 //  * warp 1 = MMA issuer: tcgen05.cp moves the stage's scale factors into
 //    TMEM, then 4 x tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //    (M=128, N=256, K=64) accumulate in a 256-column FP32 TMEM tile;
-//  * warps 2-5 = epilogue: tcgen05.ld of their 32-lane quarter, FP32 scales,
-//    BF16 casts and the fused SwiGLU x prob; direct 32-byte row stores.
+//  * warps 2-9 = epilogue, two warps per 32-lane TMEM quarter, each taking
+//    half of the tile's columns.  They copy their accumulator columns to
+//    registers and release TMEM at once, so the next tile's MMAs run while
+//    they apply the FP32 scales (staged in shared memory per tile), BF16
+//    casts and the fused SwiGLU x prob, then write rows through a per-warp
+//    shared-memory transpose as whole 128-byte lines.
 //  Every row's arithmetic is the same whatever tile, expert or batch it is
 //  in: one tile shape, no split-K, K always walked 0..K-1 in 64-wide steps.
 //  All waits are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
@@ -45,8 +49,10 @@ __device__ float g_silu_table[65536];
 
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kStages = 3;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBKBytes = 128;                         // 256 FP4 values of K
@@ -57,8 +63,14 @@ constexpr int kSfaOff = kABytes + kBBytes;            // 4 scale tiles of A
 constexpr int kSfbOff = kSfaOff + 4 * kSfAtomBytes;   // 2 x 4 scale tiles of B
 constexpr int kStageBytes = kSfbOff + 8 * kSfAtomBytes;
 static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+constexpr int kStagePitch = 144;                      // 128 B of BF16 per row + 16 B pad (no bank conflicts)
+constexpr int kStageWarpBytes = 32 * kStagePitch;     // one warp's 32 rows
+constexpr int kEpiStageOff = kStages * kStageBytes;
+constexpr int kScaleOff = kEpiStageOff + kEpiWarps * kStageWarpBytes;   // 128 floats per epilogue warp
+constexpr int kBarOff = kScaleOff + kEpiWarps * 128 * 4;
 constexpr int kBarrierBytes = 256;
-constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;
+constexpr int kSmemBytes = kBarOff + kBarrierBytes + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;                     // per stage: SFA 16 cols, SFB 32 cols
 constexpr uint32_t kSfColsPerStage = 48;
@@ -82,10 +94,33 @@ __device__ __forceinline__ int expert_of_row(const int32_t* __restrict__ off, in
     return lo;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return a | (b << 16);
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The warp's 32 rows x 64 BF16 columns (packed[lane][0..31]) staged through shared
+// memory and written as 4 rows x 128 B per store instruction.  dst_row(r) gives
+// the global address of row r's 64-column chunk, or nullptr to skip the row.
+template <typename RowPtr>
+__device__ __forceinline__ void store_rows_64(uint8_t* stage, const uint32_t (&packed)[32], RowPtr dst_row) {
+    const int lane = threadIdx.x & 31;
+    uint4* mine = reinterpret_cast<uint4*>(stage + lane * kStagePitch);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        mine[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+    }
+    __syncwarp();
+    const int sub = lane & 7;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int r = it * 4 + (lane >> 3);
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * kStagePitch + sub * 16);
+        uint16_t* dst = dst_row(r);
+        if (dst) reinterpret_cast<uint4*>(dst)[sub] = v;
+    }
+    __syncwarp();
 }
 
 template <bool kFC1>
@@ -94,13 +129,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
     uint64_t* empty = full + kStages;
     uint64_t* tmem_full = empty + kStages;
     uint64_t* tmem_empty = tmem_full + 1;
     uint64_t* drain = tmem_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* scale_buf = reinterpret_cast<float*>(smem + kScaleOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -110,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 128);
+        mbar_init(tmem_empty, kEpiThreads);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -252,10 +288,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;                             // 0..7
         const int q = warp & 3;                              // TMEM lane quarter of this warp
+        const int half = ew >> 2;                            // which half of the tile's columns
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        uint8_t* stage_buf = smem + kEpiStageOff + ew * kStageWarpBytes;
+        float* sc = scale_buf + ew * 128;                    // this warp's 128 column scales
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            const int mt = t / n_tiles, nt = t % n_tiles;
+            const int e = expert_of_row(args.offsets, E, mt * kBM);
+            const int64_t row = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
+            const int pair = __ldg(args.row_pair + row);
+            const bool live = pair >= 0;
+            const float gr = live ? __ldg(args.a_g + row) : 0.0f;
+            const float p = (kFC1 && live) ? __ldg(args.row_prob + row) : 0.0f;
+            // the weight scales of this warp's 128 columns (FC1: 64 gate then 64 up), staged per warp
+            {
+                const float* gw = args.b_g + static_cast<int64_t>(e) * args.Nw;
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = lane + 32 * i;
+                    sc[c] = kFC1 ? __ldg(gw + (c < 64 ? nt * 128 + 64 * half + c : args.I + nt * 128 + 64 * half + c - 64))
+                                 : __ldg(gw + nt * kBN + 128 * half + c);
+                }
+                __syncwarp();
+            }
             if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
                 if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
@@ -263,88 +322,82 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             acc_phase ^= 1u;
             tc_fence_after();
-            const int mt = t / n_tiles, nt = t % n_tiles;
-            const int e = expert_of_row(args.offsets, E, mt * kBM);
-            const int64_t row = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
-            const int pair = __ldg(args.row_pair + row);
-            const bool live = pair >= 0;
-            const float gr = live ? __ldg(args.a_g + row) : 0.0f;
+            // copy this warp's 128 accumulator columns to registers, then hand TMEM back
+            uint32_t acc[4][32];
             if (kFC1) {
-                const int I = args.I;
-                const float p = live ? __ldg(args.row_prob + row) : 0.0f;
-                const float* gw_gate = args.b_g + static_cast<int64_t>(e) * args.Nw + nt * 128;
-                const float* gw_up = gw_gate + I;
-                uint16_t* hrow = args.h + row * I + nt * 128;
-                float* dbg = args.debug ? args.debug + row * (2 * I) + nt * 128 : nullptr;
-                float hmax = 0.0f;
-#pragma unroll 1
-                for (int c = 0; c < 128; c += 16) {
-                    uint32_t rg[16], ru[16];
-                    tmem_ld_32x32b_x16(taddr + c, rg);
-                    tmem_ld_32x32b_x16(taddr + 128 + c, ru);
-                    tmem_ld_wait();
-                    if (live) {
-                        uint32_t packed[8];
-#pragma unroll
-                        for (int i = 0; i < 16; i += 2) {
-                            float hv[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const float vg = __fmul_rn(__fmul_rn(__uint_as_float(rg[i + u]), gr),
-                                                           __ldg(gw_gate + c + i + u));
-                                const float vu = __fmul_rn(__fmul_rn(__uint_as_float(ru[i + u]), gr),
-                                                           __ldg(gw_up + c + i + u));
-                                if (dbg) {
-                                    dbg[c + i + u] = vg;
-                                    dbg[I + c + i + u] = vu;
-                                }
-                                const __nv_bfloat16 gb = __float2bfloat16_rn(vg);
-                                const __nv_bfloat16 ub = __float2bfloat16_rn(vu);
-                                const float s = g_silu_table[__bfloat16_as_ushort(gb)];
-                                const float t1 = __fmul_rn(s, __bfloat162float(ub));
-                                const float t2 = __fmul_rn(t1, p);
-                                hv[u] = __bfloat162float(__float2bfloat16_rn(t2));
-                                hmax = fmaxf(hmax, fabsf(hv[u]));
-                            }
-                            packed[i / 2] = pack_bf16x2(hv[0], hv[1]);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(hrow + c);
-                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    }
-                }
-                if (live) atomicMax(args.amax2 + row, __float_as_uint(hmax));
+                tmem_ld_32x32b_x32(taddr + 64 * half, acc[0]);
+                tmem_ld_32x32b_x32(taddr + 64 * half + 32, acc[1]);
+                tmem_ld_32x32b_x32(taddr + 128 + 64 * half, acc[2]);
+                tmem_ld_32x32b_x32(taddr + 128 + 64 * half + 32, acc[3]);
             } else {
-                const int H = args.H;
-                const float* gw = args.b_g + static_cast<int64_t>(e) * args.Nw + nt * kBN;
-                uint16_t* yrow = live ? args.y + static_cast<int64_t>(pair) * H + nt * kBN : nullptr;
-                float* dbg = args.debug ? args.debug + row * H + nt * kBN : nullptr;
-#pragma unroll 1
-                for (int c = 0; c < kBN; c += 16) {
-                    uint32_t ra[16];
-                    tmem_ld_32x32b_x16(taddr + c, ra);
-                    tmem_ld_wait();
-                    if (live) {
-                        uint32_t packed[8];
 #pragma unroll
-                        for (int i = 0; i < 16; i += 2) {
-                            const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(ra[i]), gr), __ldg(gw + c + i));
-                            const float v1 =
-                                __fmul_rn(__fmul_rn(__uint_as_float(ra[i + 1]), gr), __ldg(gw + c + i + 1));
-                            if (dbg) {
-                                dbg[c + i] = v0;
-                                dbg[c + i + 1] = v1;
-                            }
-                            packed[i / 2] = pack_bf16x2(v0, v1);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + c);
-                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    }
-                }
+                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 128 * half + 32 * c, acc[c]);
             }
+            tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(tmem_empty);
+
+            if (kFC1) {
+                const int I = args.I;
+                const float* sg = sc;                        // gate scales of my columns
+                const float* su = sc + 64;                   // up scales
+                float* dbg = args.debug ? args.debug + row * (2 * I) + nt * 128 + 64 * half : nullptr;
+                uint32_t packed[32];
+                float hmax = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 64; j += 2) {
+                    float hv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int c = j + u;
+                        const float vg = __fmul_rn(__fmul_rn(__uint_as_float(acc[c >> 5][c & 31]), gr), sg[c]);
+                        const float vu = __fmul_rn(__fmul_rn(__uint_as_float(acc[2 + (c >> 5)][c & 31]), gr), su[c]);
+                        if (dbg && live) {
+                            dbg[c] = vg;
+                            dbg[I + c] = vu;
+                        }
+                        const __nv_bfloat16 gb = __float2bfloat16_rn(vg);
+                        const __nv_bfloat16 ub = __float2bfloat16_rn(vu);
+                        const float s = __ldg(g_silu_table + __bfloat16_as_ushort(gb));
+                        const float t1 = __fmul_rn(s, __bfloat162float(ub));
+                        hv[u] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(t1, p)));
+                        hmax = fmaxf(hmax, fabsf(hv[u]));
+                    }
+                    packed[j >> 1] = bf16x2_rn(hv[0], hv[1]);
+                }
+                if (live) atomicMax(args.amax2 + row, __float_as_uint(hmax));
+                const int64_t row0 = static_cast<int64_t>(mt) * kBM + q * 32;
+                uint16_t* hbase = args.h + nt * 128 + 64 * half;
+                store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
+                    const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
+                    return pr >= 0 ? hbase + (row0 + r) * I : nullptr;
+                });
+            } else {
+                const int H = args.H;
+                const float* sw = sc;
+                float* dbg = args.debug ? args.debug + row * H + nt * kBN + 128 * half : nullptr;
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {            // two 64-column chunks
+                    uint32_t packed[32];
+#pragma unroll
+                    for (int j = 0; j < 64; j += 2) {
+                        const int c = 64 * c2 + j;
+                        const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(acc[c >> 5][c & 31]), gr), sw[c]);
+                        const float v1 =
+                            __fmul_rn(__fmul_rn(__uint_as_float(acc[(c + 1) >> 5][(c + 1) & 31]), gr), sw[c + 1]);
+                        if (dbg && live) {
+                            dbg[c] = v0;
+                            dbg[c + 1] = v1;
+                        }
+                        packed[j >> 1] = bf16x2_rn(v0, v1);
+                    }
+                    uint16_t* ybase = args.y + nt * kBN + 128 * half + 64 * c2;
+                    store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
+                        const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
+                        return pr >= 0 ? ybase + static_cast<int64_t>(pr) * H : nullptr;
+                    });
+                }
+            }
         }
     }
 
