@@ -6,17 +6,28 @@
 // cross-engine execution gap of NVFP4 RL", section "How it differs":
 // g = max|row| / (6*448) in FP32, an E4M3 scale per 16 elements, E2M1 codes,
 // round-to-nearest-even.  Block scale s_b = e4m3(bmax / (g*6)), code =
-// e2m1(x / (g*s_b)), both divisions IEEE binary32 in that two-step form.
+// e2m1(x / (g*s_b)), both quotients the correctly rounded binary32 quotient.
 // The route sort follows section "How to use it": the tokens are sorted by
 // expert and the row maximum is taken in the same pass that quantises the
 // row, so X is read exactly once.
 //
-// One warp owns one row.  Lane l holds the 16-byte vectors l, l+32, l+64, ...
-// of the row (8 BF16 each); a 16-element block is the vector pair (2b, 2b+1),
-// held by lanes 2j and 2j+1.  Stores are 4 bytes of codes per vector per lane
-// (128 contiguous bytes per warp instruction) and one 32-bit word of four
-// block scales per 64 columns, at the position the GEMM's scale-factor tile
-// layout gives it.
+// Work split: a lane owns whole 64-element groups (four 16-element blocks,
+// 128 bytes of BF16): it loads them with 16-byte loads, finds the block
+// maxima with NaN-propagating bf16x2 max, and writes 32 bytes of codes plus
+// one 32-bit word of four block scales per group, at the place the GEMM's
+// scale-factor tile layout gives it.  A row of G groups is spread over G
+// lanes (G <= 32: 32/G rows per warp) or over the whole warp (G > 32: G/32
+// groups per lane); the row maximum is one redux.sync over the row's lanes.
+//
+// Division: x / d for the 16 elements of a block that share d = g*s_b uses
+// Markstein's method (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 1990; also
+// Muller et al., Handbook of Floating-Point Arithmetic, ch. on FMA-based
+// division): with y = RN(1/d) from __frcp_rn, q0 = RN(x*y),
+// r = x - d*q0 (exact with an FMA) and q = RN(q0 + r*y) equals RN(x/d) when
+// no intermediate leaves the normal range.  Divisors below 2^-60 take IEEE
+// __fdiv_rn instead, which keeps every quotient that can reach a code
+// boundary (|x/d| >= 0.25) in the normal range.
 #include <cfloat>
 
 #include "common.cuh"
@@ -26,152 +37,178 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
-constexpr int kRouteChunk = 256;   // tokens per route-sort chunk (8 warps x 32 tokens)
+constexpr int kRouteChunk = 256;       // tokens per route-sort chunk (8 warps x 32 tokens)
+constexpr float kMarksteinMinDivisor = 8.6736174e-19f;   // 2^-60
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 
-template <int VPL>
-struct QuantRow {
-    uint32_t code[VPL];   // 8 nibbles per vector
-    uint32_t sfw[VPL];    // valid on lanes with (lane & 7) == 0: scales of 4 blocks
-    float g;
-    bool finite;
+// max|x| over 16 BF16 values (two 16-byte vectors), as FP32 bits; NaN propagates.
+__device__ __forceinline__ uint32_t block_absmax_bits(const uint4& a, const uint4& b) {
+    constexpr uint32_t kAbs = 0x7FFF7FFFu;
+    uint32_t m = bf16x2_max_nan(bf16x2_max_nan(a.x & kAbs, a.y & kAbs), bf16x2_max_nan(a.z & kAbs, a.w & kAbs));
+    m = bf16x2_max_nan(m, bf16x2_max_nan(bf16x2_max_nan(b.x & kAbs, b.y & kAbs),
+                                         bf16x2_max_nan(b.z & kAbs, b.w & kAbs)));
+    m = bf16x2_max_nan(m, m >> 16);      // low half = max of both halves
+    return m << 16;                      // BF16 bits -> FP32 bits
+}
+
+// Eight E2M1 codes of one 16-byte vector of BF16 values, quotient by d (rc = RN(1/d)).
+__device__ __forceinline__ uint32_t codes8(const uint4& v, float d, float rc, bool markstein) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t bytes[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+        float qlo, qhi;
+        if (markstein) {
+            const float q0l = __fmul_rn(lo, rc), q0h = __fmul_rn(hi, rc);
+            qlo = __fmaf_rn(__fmaf_rn(-q0l, d, lo), rc, q0l);
+            qhi = __fmaf_rn(__fmaf_rn(-q0h, d, hi), rc, q0h);
+        } else {
+            qlo = __fdiv_rn(lo, d);
+            qhi = __fdiv_rn(hi, d);
+        }
+        bytes[j] = cvt_e2m1x2(qlo, qhi);
+    }
+    const uint32_t mags = (bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24)) & 0x77777777u;
+    // sign bit of every code = sign of x (also when the magnitude rounds to 0)
+    uint32_t signs = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        signs |= ((w[j] >> 12) & 0x8u) << (8 * j);     // bit 15 -> bit 3 of byte j
+        signs |= ((w[j] >> 24) & 0x80u) << (8 * j);    // bit 31 -> bit 7 of byte j
+    }
+    return mags | signs;
+}
+
+// Quantised form of one 64-element group.
+struct GroupQ {
+    uint32_t code[8];   // 64 nibbles, element 2i in the low nibble of byte i
+    uint32_t sfw;       // four E4M3 block scales, block 0 in the low byte
 };
 
-// Quantise the row held as `xv` (lane's vectors; `nvec` vectors in the row).
-// If `amax_in` >= 0 it is used as max|row| (it must be that maximum).
-template <int VPL>
-__device__ __forceinline__ void quantize_warp_row(const uint4 (&xv)[VPL], int nvec, float amax_in,
-                                                  QuantRow<VPL>& q) {
-    const int lane = threadIdx.x & 31;
-    float vmax[VPL];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const uint32_t w[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            m = fmaxf(m, fabsf(bf16_lo(w[j])));
-            m = fmaxf(m, fabsf(bf16_hi(w[j])));
-        }
-        // fmaxf drops NaN: remember non-finite inputs separately
-        bool bad = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            bad |= ((w[j] & 0x7F80u) == 0x7F80u) || ((w[j] & 0x7F800000u) == 0x7F800000u);
-        }
-        if (bad) m = __int_as_float(0x7F800000);
-        vmax[i] = m;
-        amax = fmaxf(amax, m);
-    }
-    if (amax_in >= 0.0f) {
-        amax = amax_in;
-    } else {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    }
-    q.finite = amax <= FLT_MAX;
-    const float g = q.finite ? __fdiv_rn(amax, kOuterDivisor) : 0.0f;
-    q.g = g;
+// Quantise a group with outer scale g (finite); bm = its four block maxima (FP32 bits).
+__device__ __forceinline__ void quantize_group(const uint4 (&v)[8], const uint32_t (&bm)[4], float g, GroupQ& q) {
     const float d1 = __fmul_rn(g, 6.0f);
+    q.sfw = 0;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const float bmax = fmaxf(vmax[i], __shfl_xor_sync(0xFFFFFFFFu, vmax[i], 1));
-        const float r = d1 > 0.0f ? __fdiv_rn(bmax, d1) : 0.0f;
-        const uint32_t s_code = (d1 > 0.0f && q.finite) ? cvt_e4m3(r) : 0u;
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t s_code = d1 > 0.0f ? cvt_e4m3(__fdiv_rn(__uint_as_float(bm[b]), d1)) : 0u;
         const float d2 = __fmul_rn(g, e4m3_value(s_code));
-        uint32_t word = 0;
+        q.sfw |= s_code << (8 * b);
         if (d2 > 0.0f) {
-            const uint32_t w[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-            uint32_t signs = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-                word |= cvt_e2m1x2(__fdiv_rn(a, d2), __fdiv_rn(b, d2)) << (8 * j);
-                signs |= ((w[j] >> 15) & 1u) << (8 * j + 3);
-                signs |= ((w[j] >> 31) & 1u) << (8 * j + 7);
-            }
-            // the sign bit of every code is the sign of x (also when the magnitude rounds to 0)
-            word = (word & 0x77777777u) | signs;
+            const bool mk = d2 >= kMarksteinMinDivisor;
+            const float rc = mk ? __frcp_rn(d2) : 0.0f;
+            q.code[2 * b] = codes8(v[2 * b], d2, rc, mk);
+            q.code[2 * b + 1] = codes8(v[2 * b + 1], d2, rc, mk);
+        } else {
+            q.code[2 * b] = 0u;
+            q.code[2 * b + 1] = 0u;
         }
-        q.code[i] = word;
-        // gather the four block scales of this lane's 64-column group
-        const int base = lane & ~7;
-        const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, s_code, base + 0);
-        const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, s_code, base + 2);
-        const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, s_code, base + 4);
-        const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, s_code, base + 6);
-        q.sfw[i] = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
     }
-    (void)nvec;
 }
 
-template <int VPL>
-__device__ __forceinline__ void load_warp_row(const uint16_t* src, int nvec, uint4 (&xv)[VPL]) {
-    const int lane = threadIdx.x & 31;
+__device__ __forceinline__ void load_group(const uint16_t* src, uint4 (&v)[8]) {
     const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int v = lane + 32 * i;
-        xv[i] = v < nvec ? __ldg(s + v) : make_uint4(0, 0, 0, 0);
-    }
+    for (int i = 0; i < 8; ++i) v[i] = __ldg(s + i);
 }
 
-// Write a quantised row as row `r` of an NVFP4 matrix with `cols` columns.
-template <int VPL>
-__device__ __forceinline__ void store_warp_row(const QuantRow<VPL>& q, int nvec, int64_t r, int cols,
-                                               uint8_t* codes, uint8_t* sf) {
-    const int lane = threadIdx.x & 31;
-    uint32_t* crow = reinterpret_cast<uint32_t*>(codes + r * static_cast<int64_t>(cols / 2));
+__device__ __forceinline__ void store_group(const GroupQ& q, int64_t r, int grp, int cols, uint8_t* codes,
+                                            uint8_t* sf) {
+    uint4* c = reinterpret_cast<uint4*>(codes + r * static_cast<int64_t>(cols / 2) + grp * 32);
+    c[0] = make_uint4(q.code[0], q.code[1], q.code[2], q.code[3]);
+    c[1] = make_uint4(q.code[4], q.code[5], q.code[6], q.code[7]);
+    *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, cols)) = q.sfw;
+}
+
+// Lane layout of rows of G groups: LPR lanes per row, RPW rows per warp pass,
+// GPL groups per lane.
+struct RowLanes {
+    int LPR, RPW, slot, li;
+    unsigned mask;
+    bool active;
+    __device__ RowLanes(int G) {
+        const int lane = threadIdx.x & 31;
+        LPR = G <= 32 ? G : 32;
+        RPW = 32 / LPR;
+        slot = lane / LPR;
+        li = lane % LPR;
+        active = slot < RPW;
+        mask = LPR == 32 ? 0xFFFFFFFFu : (((1u << LPR) - 1u) << (slot * LPR));
+    }
+};
+
+// Quantise the GPL groups this lane owns of the row at `src`; amax_in >= 0 supplies
+// max|row| (it must be that maximum).  Returns g; finite = whether the row is finite.
+template <int GPL>
+__device__ __forceinline__ float quantize_row_lanes(const uint16_t* src, const RowLanes& rl, int G, float amax_in,
+                                                    GroupQ (&q)[GPL], bool& finite) {
+    uint4 v[GPL][8];
+    uint32_t bm[GPL][4];
+    uint32_t amax_bits = 0;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int v = lane + 32 * i;
-        if (v < nvec) {
-            crow[v] = q.code[i];
-            if ((lane & 7) == 0) {
-                *reinterpret_cast<uint32_t*>(sf + sf_offset(r, v / 2, cols)) = q.sfw[i];
+    for (int i = 0; i < GPL; ++i) {
+        const int grp = rl.li + rl.LPR * i;
+        if (grp < G) {
+            load_group(src + grp * 64, v[i]);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                bm[i][b] = block_absmax_bits(v[i][2 * b], v[i][2 * b + 1]);
+                amax_bits = max(amax_bits, bm[i][b]);
             }
         }
     }
-}
-
-// Zero the scales (and optionally the codes) of row r.
-__device__ __forceinline__ void zero_warp_row(int64_t r, int cols, uint8_t* codes, uint8_t* sf, bool zero_codes) {
-    const int lane = threadIdx.x & 31;
-    const int ngroups = cols / 64;
-    for (int q = lane; q < ngroups; q += 32) {
-        *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * q, cols)) = 0u;
+    amax_bits = __reduce_max_sync(rl.mask, amax_bits);
+    finite = amax_bits < 0x7F800000u;
+    float amax = __uint_as_float(amax_bits);
+    if (amax_in >= 0.0f) amax = amax_in;
+    const float g = finite ? __fdiv_rn(amax, kOuterDivisor) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < GPL; ++i) {
+        if (rl.li + rl.LPR * i < G) quantize_group(v[i], bm[i], g, q[i]);
     }
-    if (zero_codes) {
-        uint4* crow = reinterpret_cast<uint4*>(codes + r * static_cast<int64_t>(cols / 2));
-        for (int v = lane; v < cols / 32; v += 32) crow[v] = make_uint4(0, 0, 0, 0);
-    }
+    return g;
 }
 
 // ------------------------------------------------------------------ plain rows
-template <int VPL>
-__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
+template <int GPL>
+__global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int cols, int64_t ld, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf, float* __restrict__ g,
                                                             int* err) {
-    const int nvec = cols / 8;
+    const int G = cols / 64;
+    const RowLanes rl(G);
     const int64_t rows_pad = (rows + kTileM - 1) / kTileM * kTileM;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t r = warp; r < rows_pad; r += nwarps) {
-        if (r >= rows) {
-            zero_warp_row(r, cols, codes, sf, true);
+    for (int64_t base = warp * rl.RPW; base < rows_pad; base += nwarps * rl.RPW) {
+        const int64_t r = base + rl.slot;
+        if (!rl.active || r >= rows_pad) continue;
+        if (r >= rows) {   // padding rows of the last 128-row tile: zero codes and scales
+            for (int i = 0; i < GPL; ++i) {
+                const int grp = rl.li + rl.LPR * i;
+                if (grp < G) {
+                    GroupQ z = {};
+                    store_group(z, r, grp, cols, codes, sf);
+                }
+            }
             continue;
         }
-        uint4 xv[VPL];
-        load_warp_row<VPL>(x + r * ld, nvec, xv);
-        QuantRow<VPL> q;
-        quantize_warp_row<VPL>(xv, nvec, -1.0f, q);
-        if (!q.finite && (threadIdx.x & 31) == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
-        store_warp_row<VPL>(q, nvec, r, cols, codes, sf);
-        if ((threadIdx.x & 31) == 0) g[r] = q.g;
+        GroupQ q[GPL];
+        bool finite;
+        const float gr = quantize_row_lanes<GPL>(x + r * ld, rl, G, -1.0f, q, finite);
+        if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
+#pragma unroll
+        for (int i = 0; i < GPL; ++i) {
+            const int grp = rl.li + rl.LPR * i;
+            if (grp < G) store_group(q[i], r, grp, cols, codes, sf);
+        }
+        if (rl.li == 0) g[r] = gr;
     }
 }
 
@@ -186,31 +223,38 @@ __global__ void __launch_bounds__(256) route_hist_rank_kernel(const int32_t* __r
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t chunk = blockIdx.x;
     for (int i = threadIdx.x; i < kWarpsPerBlock * E; i += blockDim.x) wcount[i] = 0;
-    __syncthreads();
     const int64_t tok0 = chunk * kRouteChunk + w * 32;
     const int64_t npairs = T * k;
-    const unsigned lt_mask = (1u << lane) - 1u;
+    // all of this warp's ids first, so their loads overlap
     int my_e[32];
-    int my_rank[32];
 #pragma unroll
     for (int it = 0; it < 32; ++it) {
         if (it < k) {
             const int64_t p = tok0 * k + it * 32 + lane;
             int e = -1;
             if (p < npairs && tok0 < T) {
-                e = ids[p];
+                e = __ldg(ids + p);
                 if (e < 0 || e >= E) {
                     set_device_error(err, NVFP4_ERR_BAD_EXPERT_ID);
                     e = -1;
                 }
             }
+            my_e[it] = e;
+        }
+    }
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int my_rank[32];
+#pragma unroll
+    for (int it = 0; it < 32; ++it) {
+        if (it < k) {
+            const int e = my_e[it];
             const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
             const int before = __popc(m & lt_mask);
             const int base = e >= 0 ? wcount[w * E + e] : 0;
             __syncwarp();
             if (e >= 0 && before == 0) wcount[w * E + e] = base + __popc(m);
             __syncwarp();
-            my_e[it] = e;
             my_rank[it] = base + before;
         }
     }
@@ -234,14 +278,43 @@ __global__ void __launch_bounds__(256) route_hist_rank_kernel(const int32_t* __r
     }
 }
 
-// One block: per-expert totals, padded expert offsets, and each chunk's first row.
+// Block-wide exclusive prefix sum of one value per thread (blockDim.x = 1024).
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_tot, int32_t& total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int32_t t = warp_tot[lane];
+        int32_t ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t n = __shfl_up_sync(0xFFFFFFFFu, ti, o);
+            if (lane >= o) ti += n;
+        }
+        warp_tot[lane] = ti - t;
+        if (lane == 31) warp_tot[32] = ti;
+    }
+    __syncthreads();
+    total = warp_tot[32];
+    return warp_tot[w] + incl - v;
+}
+
+// One block of 1024 threads: per-expert totals, padded expert offsets, and each
+// chunk's first row.
 __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t n_chunks,
                                                           const int32_t* __restrict__ chunk_count,
                                                           int32_t* __restrict__ chunk_base,
                                                           int32_t* __restrict__ expert_count,
                                                           int32_t* __restrict__ offsets) {
     __shared__ int32_t seg_sum[1024];
-    __shared__ int32_t e_off[1025];
+    __shared__ int32_t e_off[1024];
+    __shared__ int32_t warp_tot[33];
     const int tid = threadIdx.x;
     const int S = blockDim.x / E;                  // threads per expert (>= 1)
     const int e = tid / S, seg = tid % S;
@@ -250,79 +323,80 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t n_chunk
     int32_t sum = 0;
     if (e < E) {
         const int32_t* cc = chunk_count + static_cast<int64_t>(e) * n_chunks;
-        for (int64_t c = c0; c < c1; ++c) sum += cc[c];
+        for (int64_t c = c0; c < c1; ++c) sum += __ldg(cc + c);
     }
     seg_sum[tid] = sum;
     __syncthreads();
-    if (e < E && seg == 0) {
+    int32_t padded = 0;
+    if (tid < E) {
         int32_t run = 0;
-        for (int s = 0; s < S; ++s) {
-            const int32_t v = seg_sum[tid + s];
-            seg_sum[tid + s] = run;
-            run += v;
-        }
-        expert_count[e] = run;
-        e_off[e] = (run + kTileM - 1) / kTileM * kTileM;   // padded size for now
+        for (int s = 0; s < S; ++s) run += seg_sum[tid * S + s];
+        expert_count[tid] = run;
+        padded = (run + kTileM - 1) / kTileM * kTileM;
     }
-    __syncthreads();
-    if (tid == 0) {
-        int32_t run = 0;
-        for (int i = 0; i < E; ++i) {
-            const int32_t v = e_off[i];
-            e_off[i] = run;
-            run += v;
-        }
-        e_off[E] = run;
+    int32_t total;
+    const int32_t start = block_exclusive_scan(padded, warp_tot, total);
+    if (tid < E) {
+        e_off[tid] = start;
+        offsets[tid] = start;
     }
+    if (tid == 0) offsets[E] = total;
     __syncthreads();
-    for (int i = tid; i <= E; i += blockDim.x) offsets[i] = e_off[i];
     if (e < E) {
-        int32_t run = e_off[e] + seg_sum[tid];
+        int32_t run = e_off[e];
+        for (int s = 0; s < seg; ++s) run += seg_sum[e * S + s];
         const int32_t* cc = chunk_count + static_cast<int64_t>(e) * n_chunks;
         int32_t* cb = chunk_base + static_cast<int64_t>(e) * n_chunks;
         for (int64_t c = c0; c < c1; ++c) {
             cb[c] = run;
-            run += cc[c];
+            run += __ldg(cc + c);
         }
     }
 }
 
-template <int VPL>
-__global__ void __launch_bounds__(256) route_quant_scatter_kernel(
+template <int GPL>
+__global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int E, int k, const int32_t* __restrict__ ids,
     const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int* err) {
-    const int lane = threadIdx.x & 31;
-    const int nvec = H / 8;
+    const int G = H / 64;
+    const RowLanes rl(G);
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t t = warp; t < T; t += nwarps) {
-        uint4 xv[VPL];
-        load_warp_row<VPL>(x + t * H, nvec, xv);
-        QuantRow<VPL> q;
-        quantize_warp_row<VPL>(xv, nvec, -1.0f, q);
-        if (!q.finite && lane == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
+    for (int64_t base = warp * rl.RPW; base < T; base += nwarps * rl.RPW) {
+        const int64_t t = base + rl.slot;
+        if (!rl.active || t >= T) continue;
+        GroupQ q[GPL];
+        bool finite;
+        const float gr = quantize_row_lanes<GPL>(x + t * H, rl, G, -1.0f, q, finite);
+        if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
         const int64_t chunk = t / kRouteChunk;
         for (int j = 0; j < k; ++j) {
             const int64_t p = t * k + j;
             const int e = __ldg(ids + p);
             if (e < 0 || e >= E) continue;   // reported by the histogram kernel
-            const int64_t r = b.chunk_base[static_cast<int64_t>(e) * b.n_chunks + chunk] + b.pair_rank[p];
-            store_warp_row<VPL>(q, nvec, r, H, b.a_codes, b.a_sf);
-            if (lane == 0) {
-                b.a_g[r] = q.g;
+            const int64_t r = __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) +
+                              __ldg(b.pair_rank + p);
+#pragma unroll
+            for (int i = 0; i < GPL; ++i) {
+                const int grp = rl.li + rl.LPR * i;
+                if (grp < G) store_group(q[i], r, grp, H, b.a_codes, b.a_sf);
+            }
+            if (rl.li == 0) {
+                b.a_g[r] = gr;
                 b.row_pair[r] = static_cast<int32_t>(p);
                 b.row_prob[r] = __ldg(probs + p);
                 b.amax2[r] = 0u;
             }
         }
     }
-    // pad rows: expert e's rows [offsets[e] + count_e, offsets[e+1])
+    // pad rows: expert e's rows [offsets[e] + count_e, offsets[e+1]); one warp zeroes one row's scales
+    const int lane = threadIdx.x & 31;
     const int64_t pad_slots = static_cast<int64_t>(E) * kTileM;
     for (int64_t s = warp; s < pad_slots; s += nwarps) {
         const int e = static_cast<int>(s / kTileM), j = static_cast<int>(s % kTileM);
         const int64_t r = static_cast<int64_t>(offsets[e]) + b.expert_count[e] + j;
         if (r >= offsets[e + 1]) continue;
-        zero_warp_row(r, H, b.a_codes, b.a_sf, false);
+        for (int grp = lane; grp < G; grp += 32) *reinterpret_cast<uint32_t*>(b.a_sf + sf_offset(r, 4 * grp, H)) = 0u;
         if (lane == 0) {
             b.a_g[r] = 0.0f;
             b.row_pair[r] = -1;
@@ -333,61 +407,72 @@ __global__ void __launch_bounds__(256) route_quant_scatter_kernel(
 }
 
 // ------------------------------------------------------------------ requant
-template <int VPL>
-__global__ void __launch_bounds__(256) requant_kernel(const uint16_t* __restrict__ h,
+template <int GPL>
+__global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) requant_kernel(const uint16_t* __restrict__ h,
                                                       const uint32_t* __restrict__ amax2,
                                                       const int32_t* __restrict__ row_pair,
                                                       const int32_t* __restrict__ offsets, int E, int I,
                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                       float* __restrict__ g, int* err) {
-    const int lane = threadIdx.x & 31;
-    const int nvec = I / 8;
+    const int G = I / 64;
+    const RowLanes rl(G);
     const int64_t rows = offsets[E];
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t r = warp; r < rows; r += nwarps) {
-        if (row_pair[r] < 0) {
-            zero_warp_row(r, I, codes, sf, false);
-            if (lane == 0) g[r] = 0.0f;
+    for (int64_t base = warp * rl.RPW; base < rows; base += nwarps * rl.RPW) {
+        const int64_t r = base + rl.slot;
+        if (!rl.active || r >= rows) continue;
+        if (__ldg(row_pair + r) < 0) {       // pad row: zero scales, g = 0 (codes are never read)
+            for (int i = 0; i < GPL; ++i) {
+                const int grp = rl.li + rl.LPR * i;
+                if (grp < G) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, I)) = 0u;
+            }
+            if (rl.li == 0) g[r] = 0.0f;
             continue;
         }
-        uint4 xv[VPL];
-        load_warp_row<VPL>(h + r * I, nvec, xv);
-        QuantRow<VPL> q;
-        quantize_warp_row<VPL>(xv, nvec, __uint_as_float(amax2[r]), q);
-        if (!q.finite && lane == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
-        store_warp_row<VPL>(q, nvec, r, I, codes, sf);
-        if (lane == 0) g[r] = q.g;
+        GroupQ q[GPL];
+        bool finite;
+        const float gr = quantize_row_lanes<GPL>(h + r * I, rl, G, __uint_as_float(__ldg(amax2 + r)), q, finite);
+        if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
+#pragma unroll
+        for (int i = 0; i < GPL; ++i) {
+            const int grp = rl.li + rl.LPR * i;
+            if (grp < G) store_group(q[i], r, grp, I, codes, sf);
+        }
+        if (rl.li == 0) g[r] = gr;
     }
 }
 
 int grid_for_warps(int64_t warps) {
     const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
     return static_cast<int>(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
+}
+
+// warps needed to cover `rows` rows of G groups in one pass
+int64_t warps_for_rows(int64_t rows, int G) {
+    const int rpw = G <= 32 ? 32 / G : 1;
+    return (rows + rpw - 1) / rpw;
 }
 
 }  // namespace
 
-// Dispatch on the number of 16-byte vectors each lane holds.
-#define NVFP4_VPL_DISPATCH(nvec, KERNEL, ...)                                       \
-    do {                                                                            \
-        const int vpl_ = ((nvec) + 31) / 32;                                        \
-        if (vpl_ <= 1) KERNEL<1> __VA_ARGS__;                                       \
-        else if (vpl_ <= 2) KERNEL<2> __VA_ARGS__;                                  \
-        else if (vpl_ <= 4) KERNEL<4> __VA_ARGS__;                                  \
-        else if (vpl_ <= 8) KERNEL<8> __VA_ARGS__;                                  \
-        else if (vpl_ <= 16) KERNEL<16> __VA_ARGS__;                                \
-        else KERNEL<32> __VA_ARGS__;                                                \
+// Dispatch on the number of 64-element groups each lane owns.
+#define NVFP4_GPL_DISPATCH(G, KERNEL, ...)                 \
+    do {                                                   \
+        const int gpl_ = ((G) + 31) / 32;                  \
+        if (gpl_ <= 1) KERNEL<1> __VA_ARGS__;              \
+        else if (gpl_ <= 2) KERNEL<2> __VA_ARGS__;         \
+        else KERNEL<4> __VA_ARGS__;                        \
     } while (0)
 
 cudaError_t launch_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
                                  uint8_t* sf, float* g, int* err, cudaStream_t st) {
     const int64_t rows_pad = (rows + kTileM - 1) / kTileM * kTileM;
     if (rows_pad == 0) return cudaSuccess;
-    const int grid = grid_for_warps(rows_pad);
     const int c = static_cast<int>(cols);
-    NVFP4_VPL_DISPATCH(c / 8, quantize_rows_kernel, <<<grid, 256, 0, st>>>(x, rows, c, ld, codes, sf, g, err));
+    const int grid = grid_for_warps(warps_for_rows(rows_pad, c / 64));
+    NVFP4_GPL_DISPATCH(c / 64, quantize_rows_kernel, <<<grid, 256, 0, st>>>(x, rows, c, ld, codes, sf, g, err));
     return cudaGetLastError();
 }
 
@@ -403,9 +488,9 @@ cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, 
     route_scan_kernel<<<1, 1024, 0, st>>>(E, b.n_chunks, b.chunk_count, b.chunk_base, b.expert_count, offsets);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t warps = T > static_cast<int64_t>(E) * kTileM ? T : static_cast<int64_t>(E) * kTileM;
-    const int grid = grid_for_warps(warps);
-    NVFP4_VPL_DISPATCH(H / 8, route_quant_scatter_kernel,
+    const int64_t tw = warps_for_rows(T, H / 64), pw = static_cast<int64_t>(E) * kTileM;
+    const int grid = grid_for_warps(tw > pw ? tw : pw);
+    NVFP4_GPL_DISPATCH(H / 64, route_quant_scatter_kernel,
                        <<<grid, 256, 0, st>>>(x, T, H, E, k, ids, probs, offsets, b, err));
     return cudaGetLastError();
 }
@@ -413,8 +498,8 @@ cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, 
 cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32_t* row_pair,
                            const int32_t* offsets, int E, int64_t rows_cap, int I, uint8_t* codes, uint8_t* sf,
                            float* g, int* err, cudaStream_t st) {
-    const int grid = grid_for_warps(rows_cap);
-    NVFP4_VPL_DISPATCH(I / 8, requant_kernel,
+    const int grid = grid_for_warps(warps_for_rows(rows_cap, I / 64));
+    NVFP4_GPL_DISPATCH(I / 64, requant_kernel,
                        <<<grid, 256, 0, st>>>(h, amax2, row_pair, offsets, E, I, codes, sf, g, err));
     return cudaGetLastError();
 }
