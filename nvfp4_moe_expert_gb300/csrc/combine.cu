@@ -10,8 +10,8 @@
 // applied before FC2, so the combine is a plain sum.
 //
 // HBM-bound: each thread owns 8 consecutive columns of one token (16-byte
-// loads of the k slot rows, one 16-byte store); a grid-stride loop over
-// T*H/8 such vectors keeps every load and store coalesced.
+// loads of the k slot rows, all issued before the adds, one 16-byte store);
+// a grid-stride loop over T*H/8 such vectors keeps every access coalesced.
 #include "common.cuh"
 
 namespace nvfp4 {
@@ -23,6 +23,8 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     return r;
 }
 
+// kMaxK > 0: k <= kMaxK slots, all loads issued before the adds (more bytes in flight).
+template <int kMaxK>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, int64_t T, int k, int H,
                                                       uint16_t* __restrict__ out) {
     const int vec_per_row = H / 8;
@@ -35,13 +37,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-        for (int s = 0; s < k; ++s) {
-            const uint4 w = __ldcs(src + static_cast<int64_t>(s) * vec_per_row);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        uint4 w[kMaxK];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(ws[j] << 16));
-                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __uint_as_float(ws[j] & 0xFFFF0000u));
+        for (int s = 0; s < kMaxK; ++s) {
+            if (s < k) w[s] = __ldcs(src + static_cast<int64_t>(s) * vec_per_row);
+        }
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s) {          // slots in top-k order
+            if (s < k) {
+                const uint32_t ws[4] = {w[s].x, w[s].y, w[s].z, w[s].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(ws[j] << 16));
+                    acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __uint_as_float(ws[j] & 0xFFFF0000u));
+                }
             }
         }
         uint4 o;
@@ -61,7 +70,12 @@ cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t*
     int64_t blocks = (nvec + 255) / 256;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
-    combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(y, T, k, H, out);
+    const unsigned g = static_cast<unsigned>(blocks);
+    if (k <= 2) combine_kernel<2><<<g, 256, 0, st>>>(y, T, k, H, out);
+    else if (k <= 4) combine_kernel<4><<<g, 256, 0, st>>>(y, T, k, H, out);
+    else if (k <= 8) combine_kernel<8><<<g, 256, 0, st>>>(y, T, k, H, out);
+    else if (k <= 16) combine_kernel<16><<<g, 256, 0, st>>>(y, T, k, H, out);
+    else combine_kernel<32><<<g, 256, 0, st>>>(y, T, k, H, out);
     return cudaGetLastError();
 }
 

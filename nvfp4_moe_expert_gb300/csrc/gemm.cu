@@ -67,7 +67,12 @@ constexpr int kStagePitch = 144;                      // 128 B of BF16 per row +
 constexpr int kStageWarpBytes = 32 * kStagePitch;     // one warp's 32 rows
 constexpr int kEpiStageOff = kStages * kStageBytes;
 constexpr int kScaleOff = kEpiStageOff + kEpiWarps * kStageWarpBytes;   // 128 floats per epilogue warp
-constexpr int kBarOff = kScaleOff + kEpiWarps * 128 * 4;
+constexpr int kOffsetsOff = kScaleOff + kEpiWarps * 128 * 4;             // expert offsets, up to 1025 ints
+constexpr int kSiluOff = kOffsetsOff + 4352;
+// SiLU of the BF16 values with 2^-8 <= |a| < 2^4 (bit patterns 0x3B80..0x417F and their
+// negatives): 3072 entries copied from the global table into shared memory per CTA
+constexpr uint32_t kSiluLo = 0x3B80u, kSiluSpan = 0x4180u - 0x3B80u;
+constexpr int kBarOff = kSiluOff + 2 * kSiluSpan * 4;
 constexpr int kBarrierBytes = 256;
 constexpr int kSmemBytes = kBarOff + kBarrierBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -84,11 +89,12 @@ __global__ void init_silu_table_kernel() {
     }
 }
 
-__device__ __forceinline__ int expert_of_row(const int32_t* __restrict__ off, int E, int row) {
+// Expert owning routed row `row`: largest e < E with off[e] <= row (off in shared memory).
+__device__ __forceinline__ int expert_of_row(const int32_t* off, int E, int row) {
     int lo = 0, hi = E;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (__ldg(off + mid) <= row) lo = mid;
+        if (off[mid] <= row) lo = mid;
         else hi = mid;
     }
     return lo;
@@ -137,6 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* scale_buf = reinterpret_cast<float*>(smem + kScaleOff);
+    int32_t* s_off = reinterpret_cast<int32_t*>(smem + kOffsetsOff);
+    float* s_silu = reinterpret_cast<float*>(smem + kSiluOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -159,13 +167,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
+    if (kFC1) {
+        for (int i = threadIdx.x; i < 2 * static_cast<int>(kSiluSpan); i += blockDim.x) {
+            const uint32_t bits = kSiluLo + (i % kSiluSpan) + (i >= static_cast<int>(kSiluSpan) ? 0x8000u : 0u);
+            s_silu[i] = __ldg(g_silu_table + bits);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     const int E = args.E;
-    const int num_m_tiles = __ldg(args.offsets + E) / kBM;
+    const int num_m_tiles = s_off[E] / kBM;
     const int n_tiles = kFC1 ? args.I / 128 : args.H / kBN;
     const int num_tiles = num_m_tiles * n_tiles;
     const int num_k64 = args.K / 64;
@@ -182,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, issued = 0, issued_parity = 0;
             for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
                 const int mt = t / n_tiles, nt = t % n_tiles;
-                const int e = expert_of_row(args.offsets, E, mt * kBM);
+                const int e = expert_of_row(s_off, E, mt * kBM);
                 int row0, row1;
                 if (kFC1) {
                     row0 = e * args.Nw + nt * 128;
@@ -295,26 +310,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* stage_buf = smem + kEpiStageOff + ew * kStageWarpBytes;
         float* sc = scale_buf + ew * 128;                    // this warp's 128 column scales
         uint32_t acc_phase = 0;
+        // this tile's row data and the weight scales of this warp's 128 columns
+        // (FC1: 64 gate then 64 up) are loaded one tile ahead, so their latency
+        // hides behind the previous tile's epilogue
+        int n_pair = -1;
+        float n_gr = 0.0f, n_p = 0.0f, n_sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        auto prefetch = [&](int tt) {
+            const int mt_ = tt / n_tiles, nt_ = tt % n_tiles;
+            const int e_ = expert_of_row(s_off, E, mt_ * kBM);
+            const int64_t row_ = static_cast<int64_t>(mt_) * kBM + q * 32 + lane;
+            n_pair = __ldg(args.row_pair + row_);
+            n_gr = __ldg(args.a_g + row_);
+            n_p = kFC1 ? __ldg(args.row_prob + row_) : 0.0f;
+            const float* gw = args.b_g + static_cast<int64_t>(e_) * args.Nw;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = lane + 32 * i;
+                n_sc[i] = kFC1 ? __ldg(gw + (c < 64 ? nt_ * 128 + 64 * half + c : args.I + nt_ * 128 + 64 * half + c - 64))
+                               : __ldg(gw + nt_ * kBN + 128 * half + c);
+            }
+        };
+        if (static_cast<int>(blockIdx.x) < num_tiles) prefetch(blockIdx.x);
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const int mt = t / n_tiles, nt = t % n_tiles;
-            const int e = expert_of_row(args.offsets, E, mt * kBM);
             const int64_t row = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
-            const int pair = __ldg(args.row_pair + row);
+            const int pair = n_pair;
             const bool live = pair >= 0;
-            const float gr = live ? __ldg(args.a_g + row) : 0.0f;
-            const float p = (kFC1 && live) ? __ldg(args.row_prob + row) : 0.0f;
-            // the weight scales of this warp's 128 columns (FC1: 64 gate then 64 up), staged per warp
-            {
-                const float* gw = args.b_g + static_cast<int64_t>(e) * args.Nw;
-                __syncwarp();
+            const float gr = live ? n_gr : 0.0f;
+            const float p = live ? n_p : 0.0f;
+            __syncwarp();
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = lane + 32 * i;
-                    sc[c] = kFC1 ? __ldg(gw + (c < 64 ? nt * 128 + 64 * half + c : args.I + nt * 128 + 64 * half + c - 64))
-                                 : __ldg(gw + nt * kBN + 128 * half + c);
-                }
-                __syncwarp();
-            }
+            for (int i = 0; i < 4; ++i) sc[lane + 32 * i] = n_sc[i];
+            __syncwarp();
+            if (t + static_cast<int>(gridDim.x) < num_tiles) prefetch(t + gridDim.x);
             if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
                 if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
@@ -358,7 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const __nv_bfloat16 gb = __float2bfloat16_rn(vg);
                         const __nv_bfloat16 ub = __float2bfloat16_rn(vu);
-                        const float s = __ldg(g_silu_table + __bfloat16_as_ushort(gb));
+                        const uint32_t gbits = __bfloat16_as_ushort(gb);
+                        const uint32_t gi = (gbits & 0x7FFFu) - kSiluLo;
+                        const float s = gi < kSiluSpan ? s_silu[gi + ((gbits >> 15) ? kSiluSpan : 0u)]
+                                                       : __ldg(g_silu_table + gbits);
                         const float t1 = __fmul_rn(s, __bfloat162float(ub));
                         hv[u] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(t1, p)));
                         hmax = fmaxf(hmax, fabsf(hv[u]));

@@ -56,33 +56,42 @@ __device__ __forceinline__ uint32_t block_absmax_bits(const uint4& a, const uint
     return m << 16;                      // BF16 bits -> FP32 bits
 }
 
+// RN(x / d) by Markstein's correction step, given rc = RN(1/d) (see the file header).
+__device__ __forceinline__ float div_markstein(float x, float d, float rc) {
+    const float q0 = __fmul_rn(x, rc);
+    return __fmaf_rn(__fmaf_rn(-q0, d, x), rc, q0);
+}
+
+// Eight E2M1 codes (RNE, saturating) of eight FP32 values; q[2j] goes to the low nibble of byte j.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+    return r;
+}
+
 // Eight E2M1 codes of one 16-byte vector of BF16 values, quotient by d (rc = RN(1/d)).
 __device__ __forceinline__ uint32_t codes8(const uint4& v, float d, float rc, bool markstein) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t bytes[4];
+    float q[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-        float qlo, qhi;
-        if (markstein) {
-            const float q0l = __fmul_rn(lo, rc), q0h = __fmul_rn(hi, rc);
-            qlo = __fmaf_rn(__fmaf_rn(-q0l, d, lo), rc, q0l);
-            qhi = __fmaf_rn(__fmaf_rn(-q0h, d, hi), rc, q0h);
-        } else {
-            qlo = __fdiv_rn(lo, d);
-            qhi = __fdiv_rn(hi, d);
-        }
-        bytes[j] = cvt_e2m1x2(qlo, qhi);
+        q[2 * j] = markstein ? div_markstein(lo, d, rc) : __fdiv_rn(lo, d);
+        q[2 * j + 1] = markstein ? div_markstein(hi, d, rc) : __fdiv_rn(hi, d);
     }
-    const uint32_t mags = (bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24)) & 0x77777777u;
-    // sign bit of every code = sign of x (also when the magnitude rounds to 0)
-    uint32_t signs = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        signs |= ((w[j] >> 12) & 0x8u) << (8 * j);     // bit 15 -> bit 3 of byte j
-        signs |= ((w[j] >> 24) & 0x80u) << (8 * j);    // bit 31 -> bit 7 of byte j
-    }
-    return mags | signs;
+    const uint32_t mags = e2m1x8(q) & 0x77777777u;
+    // sign bit of every code = sign of x (also when the magnitude rounds to 0):
+    // byte 1 of w[j] carries element 2j's sign in bit 7, byte 3 element 2j+1's
+    const uint32_t t01 = __byte_perm(w[0], w[1], 0x7531), t23 = __byte_perm(w[2], w[3], 0x7531);
+    const uint32_t even = __byte_perm(t01, t23, 0x6420), odd = __byte_perm(t01, t23, 0x7531);
+    return mags | ((even >> 4) & 0x08080808u) | (odd & 0x80808080u);
 }
 
 // Quantised form of one 64-element group.
@@ -91,13 +100,16 @@ struct GroupQ {
     uint32_t sfw;       // four E4M3 block scales, block 0 in the low byte
 };
 
-// Quantise a group with outer scale g (finite); bm = its four block maxima (FP32 bits).
-__device__ __forceinline__ void quantize_group(const uint4 (&v)[8], const uint32_t (&bm)[4], float g, GroupQ& q) {
-    const float d1 = __fmul_rn(g, 6.0f);
+// Quantise a group with outer scale g (finite); bm = its four block maxima (FP32 bits);
+// d1 = RN(6g) and rc1 = RN(1/d1) (or 0 when d1 is too small for the Markstein step).
+__device__ __forceinline__ void quantize_group(const uint4 (&v)[8], const uint32_t (&bm)[4], float g, float d1,
+                                               float rc1, GroupQ& q) {
     q.sfw = 0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-        const uint32_t s_code = d1 > 0.0f ? cvt_e4m3(__fdiv_rn(__uint_as_float(bm[b]), d1)) : 0u;
+        const float bmx = __uint_as_float(bm[b]);
+        const float r = rc1 != 0.0f ? div_markstein(bmx, d1, rc1) : __fdiv_rn(bmx, d1);
+        const uint32_t s_code = d1 > 0.0f ? cvt_e4m3(r) : 0u;
         const float d2 = __fmul_rn(g, e4m3_value(s_code));
         q.sfw |= s_code << (8 * b);
         if (d2 > 0.0f) {
@@ -168,9 +180,11 @@ __device__ __forceinline__ float quantize_row_lanes(const uint16_t* src, const R
     float amax = __uint_as_float(amax_bits);
     if (amax_in >= 0.0f) amax = amax_in;
     const float g = finite ? __fdiv_rn(amax, kOuterDivisor) : 0.0f;
+    const float d1 = __fmul_rn(g, 6.0f);
+    const float rc1 = d1 >= kMarksteinMinDivisor ? __frcp_rn(d1) : 0.0f;
 #pragma unroll
     for (int i = 0; i < GPL; ++i) {
-        if (rl.li + rl.LPR * i < G) quantize_group(v[i], bm[i], g, q[i]);
+        if (rl.li + rl.LPR * i < G) quantize_group(v[i], bm[i], g, d1, rc1, q[i]);
     }
     return g;
 }
@@ -365,17 +379,38 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_ker
     for (int64_t base = warp * rl.RPW; base < T; base += nwarps * rl.RPW) {
         const int64_t t = base + rl.slot;
         if (!rl.active || t >= T) continue;
+        const int64_t chunk = t / kRouteChunk;
+        // destination rows of the token's k slots: lane li < k of the row fetches slot li's,
+        // before the row itself is loaded, so the two dependent lookups overlap the row load
+        int my_dst = -1;
+        float my_prob = 0.0f;
+        if (rl.LPR >= k && rl.li < k) {
+            const int64_t p = t * k + rl.li;
+            const int e = __ldg(ids + p);
+            if (e >= 0 && e < E) {   // out-of-range ids are reported by the histogram kernel
+                my_dst = __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) + __ldg(b.pair_rank + p);
+                my_prob = __ldg(probs + p);
+            }
+        }
         GroupQ q[GPL];
         bool finite;
         const float gr = quantize_row_lanes<GPL>(x + t * H, rl, G, -1.0f, q, finite);
         if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
-        const int64_t chunk = t / kRouteChunk;
+        const int src0 = rl.slot * rl.LPR;
         for (int j = 0; j < k; ++j) {
             const int64_t p = t * k + j;
-            const int e = __ldg(ids + p);
-            if (e < 0 || e >= E) continue;   // reported by the histogram kernel
-            const int64_t r = __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) +
-                              __ldg(b.pair_rank + p);
+            int64_t r;
+            float pj;
+            if (rl.LPR >= k) {
+                r = __shfl_sync(rl.mask, my_dst, src0 + j);
+                pj = __shfl_sync(rl.mask, my_prob, src0 + j);
+                if (r < 0) continue;
+            } else {                 // rows narrower than k lanes: look the slot up directly
+                const int e = __ldg(ids + p);
+                if (e < 0 || e >= E) continue;
+                r = __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) + __ldg(b.pair_rank + p);
+                pj = __ldg(probs + p);
+            }
 #pragma unroll
             for (int i = 0; i < GPL; ++i) {
                 const int grp = rl.li + rl.LPR * i;
@@ -384,7 +419,7 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_ker
             if (rl.li == 0) {
                 b.a_g[r] = gr;
                 b.row_pair[r] = static_cast<int32_t>(p);
-                b.row_prob[r] = __ldg(probs + p);
+                b.row_prob[r] = pj;
                 b.amax2[r] = 0u;
             }
         }
