@@ -55,13 +55,16 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kBM = 128;
 constexpr int kBN = 256;
-constexpr int kBKBytes = 128;                         // 256 FP4 values of K
-constexpr int kABytes = kBM * kBKBytes;               // 16 KB
+constexpr int kBKBytes = 128;                         // bytes of K per row per stage (256 FP4 values)
+constexpr int kMmaPerStage = kBKBytes / 32;           // K=64 MMAs per stage
+// K-major operand tiles use the swizzle whose span equals the stage's row length
+constexpr int kSwizzleBytes = kBKBytes;               // 128 or 64
+constexpr int kABytes = kBM * kBKBytes;
 constexpr int kBBoxBytes = 128 * kBKBytes;            // one 128-row B box
-constexpr int kBBytes = kBN * kBKBytes;               // 32 KB
-constexpr int kSfaOff = kABytes + kBBytes;            // 4 scale tiles of A
-constexpr int kSfbOff = kSfaOff + 4 * kSfAtomBytes;   // 2 x 4 scale tiles of B
-constexpr int kStageBytes = kSfbOff + 8 * kSfAtomBytes;
+constexpr int kBBytes = kBN * kBKBytes;
+constexpr int kSfaOff = kABytes + kBBytes;            // kMmaPerStage scale tiles of A
+constexpr int kSfbOff = kSfaOff + kMmaPerStage * kSfAtomBytes;   // 2 x kMmaPerStage scale tiles of B
+constexpr int kStageBytes = kSfbOff + 2 * kMmaPerStage * kSfAtomBytes;
 static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 constexpr int kStagePitch = 144;                      // 128 B of BF16 per row + 16 B pad (no bank conflicts)
 constexpr int kStageWarpBytes = 32 * kStagePitch;     // one warp's 32 rows
@@ -77,8 +80,8 @@ constexpr int kBarrierBytes = 256;
 constexpr int kSmemBytes = kBarOff + kBarrierBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol0 = 256;                     // per stage: SFA 16 cols, SFB 32 cols
-constexpr uint32_t kSfColsPerStage = 48;
+constexpr uint32_t kSfCol0 = 256;                     // per stage: SFA 4, SFB 8 columns per MMA
+constexpr uint32_t kSfColsPerStage = 12 * kMmaPerStage;
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
 __global__ void init_silu_table_kernel() {
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_tiles = kFC1 ? args.I / 128 : args.H / kBN;
     const int num_tiles = num_m_tiles * n_tiles;
     const int num_k64 = args.K / 64;
-    const int num_ks = (num_k64 + 3) / 4;
+    const int num_ks = (num_k64 + kMmaPerStage - 1) / kMmaPerStage;
 
     bool failed = false;
 
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         failed = true;
                         break;
                     }
-                    const int nk = min(4, num_k64 - 4 * ks);
+                    const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
                     const uint32_t sf_bytes = static_cast<uint32_t>(nk) * kSfAtomBytes;
                     mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + 3 * sf_bytes);
                     uint8_t* st = smem + stage * kStageBytes;
@@ -219,13 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(st + kABytes, &tmB, &full[stage], ks * kBKBytes, row0, pol_b);
                     tma_load_2d(st + kABytes + kBBoxBytes, &tmB, &full[stage], ks * kBKBytes, row1, pol_b);
                     bulk_load(st + kSfaOff,
-                              args.a_sf + (static_cast<int64_t>(mt) * num_k64 + 4 * ks) * kSfAtomBytes, sf_bytes,
+                              args.a_sf + (static_cast<int64_t>(mt) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes, sf_bytes,
                               &full[stage], pol_a);
                     bulk_load(st + kSfbOff,
-                              args.b_sf + (static_cast<int64_t>(row0 / 128) * num_k64 + 4 * ks) * kSfAtomBytes,
+                              args.b_sf + (static_cast<int64_t>(row0 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
                               sf_bytes, &full[stage], pol_b);
-                    bulk_load(st + kSfbOff + 4 * kSfAtomBytes,
-                              args.b_sf + (static_cast<int64_t>(row1 / 128) * num_k64 + 4 * ks) * kSfAtomBytes,
+                    bulk_load(st + kSfbOff + kMmaPerStage * kSfAtomBytes,
+                              args.b_sf + (static_cast<int64_t>(row1 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
                               sf_bytes, &full[stage], pol_b);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -266,20 +269,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const int nk = min(4, num_k64 - 4 * ks);
+                    const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
                     const uint32_t st = smem_u32(smem + stage * kStageBytes);
                     const uint32_t sf_col = tmem + kSfCol0 + kSfColsPerStage * stage;
+                    const uint64_t adesc = sdesc_k_swizzled<kSwizzleBytes>(st);
+                    const uint64_t bdesc = sdesc_k_swizzled<kSwizzleBytes>(st + kABytes);
                     for (int j = 0; j < nk; ++j) {
                         tc_cp_32x128b_warpx4(sf_col + 4 * j, sdesc_sf(st + kSfaOff + kSfAtomBytes * j));
-                        tc_cp_32x128b_warpx4(sf_col + 16 + 8 * j, sdesc_sf(st + kSfbOff + kSfAtomBytes * j));
-                        tc_cp_32x128b_warpx4(sf_col + 16 + 8 * j + 4,
-                                             sdesc_sf(st + kSfbOff + 4 * kSfAtomBytes + kSfAtomBytes * j));
-                    }
-                    const uint64_t adesc = sdesc_k_sw128(st);
-                    const uint64_t bdesc = sdesc_k_sw128(st + kABytes);
-                    for (int j = 0; j < nk; ++j) {
-                        // +32 bytes of K per step = +2 in the descriptor's address field
-                        tc_mma_nvf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                        tc_cp_32x128b_warpx4(sf_col + 4 * kMmaPerStage + 8 * j,
+                                             sdesc_sf(st + kSfbOff + kSfAtomBytes * j));
+                        tc_cp_32x128b_warpx4(sf_col + 4 * kMmaPerStage + 8 * j + 4,
+                                             sdesc_sf(st + kSfbOff + kMmaPerStage * kSfAtomBytes + kSfAtomBytes * j));
+                        tc_mma_nvf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_col + 4 * j,
+                                    sf_col + 4 * kMmaPerStage + 8 * j,
                                     (ks | j) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
@@ -459,16 +461,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2D map over an NVFP4 code matrix [rows][row_bytes], 128 x 128-byte boxes, 128B swizzle.
+// 2D map over an NVFP4 code matrix [rows][row_bytes]: boxes of 128 rows x kBKBytes, swizzled
+// with the same span (the K-major canonical layout the MMA descriptors describe).
 bool make_code_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), 128};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzleBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -77,6 +77,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Bring a tensor-map box into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+// Bring `bytes` (multiple of 16) at a 16-byte aligned global address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -166,16 +178,19 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor (tcgen05 format): K-major, 128-byte swizzle,
-// 8-row groups 1024 bytes apart.  The tile base must be 1024-byte aligned;
-// advancing the start address by 32 bytes steps K by 64 FP4 elements.
-__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor (tcgen05 format) of a K-major tile whose rows are
+// kSpan bytes (128 or 64) long and swizzled with the same span, 8-row groups
+// 8*kSpan bytes apart.  The tile base must be aligned to 8*kSpan bytes (1024 is
+// used); advancing the start address by 32 bytes steps K by 64 FP4 elements.
+template <int kSpan>
+__device__ __forceinline__ uint64_t sdesc_k_swizzled(uint32_t saddr) {
+    static_assert(kSpan == 128 || kSpan == 64, "supported swizzle spans");
     uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address >> 4, bits 0-13
-    d |= static_cast<uint64_t>(1) << 16;                     // leading byte offset (unused here)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;             // stride byte offset, bits 32-45
-    d |= static_cast<uint64_t>(1) << 46;                     // descriptor version
-    d |= static_cast<uint64_t>(2) << 61;                     // swizzle: 128B
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);        // start address >> 4, bits 0-13
+    d |= static_cast<uint64_t>(1) << 16;                          // leading byte offset (unused here)
+    d |= static_cast<uint64_t>((8 * kSpan) >> 4) << 32;           // stride byte offset, bits 32-45
+    d |= static_cast<uint64_t>(1) << 46;                          // descriptor version
+    d |= static_cast<uint64_t>(kSpan == 128 ? 2 : 4) << 61;       // swizzle: 128B = 2, 64B = 4
     return d;
 }
 // Descriptor of a 32-row x 16-byte scale-factor block (no swizzle; 8-row groups 128 B apart).
