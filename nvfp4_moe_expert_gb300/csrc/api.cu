@@ -263,8 +263,8 @@ nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int
                                              expert_offsets_dev, b, err, static_cast<cudaStream_t>(stream)));
 }
 
-nvfp4_status moe_fc1_swiglu_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
-                                  void* ws_dev, size_t ws_bytes, float* fc1_debug_dev, void* stream) {
+static nvfp4_status moe_fc1_swiglu_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                                  void* ws_dev, size_t ws_bytes, float* fc1_debug_dev, void* stream, bool pdl) {
     moe_workspace_layout L;
     const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
     if (s != NVFP4_OK) return s;
@@ -273,11 +273,11 @@ nvfp4_status moe_fc1_swiglu_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, 
     int* err = device_error_ptr();
     if (!err) return NVFP4_ERR_CUDA;
     return from_cuda(launch_fc1(fc1_args(w, expert_offsets_dev, ws_dev, L, fc1_debug_dev, err),
-                                static_cast<cudaStream_t>(stream)));
+                                static_cast<cudaStream_t>(stream), pdl));
 }
 
-nvfp4_status moe_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
-                               void* ws_dev, size_t ws_bytes, void* stream) {
+static nvfp4_status moe_requant_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                               void* ws_dev, size_t ws_bytes, void* stream, bool pdl) {
     moe_workspace_layout L;
     const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
     if (s != NVFP4_OK) return s;
@@ -288,11 +288,11 @@ nvfp4_status moe_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, con
     return from_cuda(launch_requant(at<uint16_t>(ws_dev, L.h), at<uint32_t>(ws_dev, L.amax2),
                                     at<int32_t>(ws_dev, L.row_pair), expert_offsets_dev, w->E, L.rows_cap, w->I,
                                     at<uint8_t>(ws_dev, L.a2_codes), at<uint8_t>(ws_dev, L.a2_sf),
-                                    at<float>(ws_dev, L.a2_g), err, static_cast<cudaStream_t>(stream)));
+                                    at<float>(ws_dev, L.a2_g), err, static_cast<cudaStream_t>(stream), pdl));
 }
 
-nvfp4_status moe_fc2_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
-                           void* ws_dev, size_t ws_bytes, float* fc2_debug_dev, void* stream) {
+static nvfp4_status moe_fc2_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                           void* ws_dev, size_t ws_bytes, float* fc2_debug_dev, void* stream, bool pdl) {
     moe_workspace_layout L;
     const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
     if (s != NVFP4_OK) return s;
@@ -301,18 +301,39 @@ nvfp4_status moe_fc2_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const i
     int* err = device_error_ptr();
     if (!err) return NVFP4_ERR_CUDA;
     return from_cuda(launch_fc2(fc2_args(w, expert_offsets_dev, ws_dev, L, fc2_debug_dev, err),
-                                static_cast<cudaStream_t>(stream)));
+                                static_cast<cudaStream_t>(stream), pdl));
 }
 
-nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev, void* ws_dev,
-                              size_t ws_bytes, void* stream) {
+static nvfp4_status moe_combine_bf16_impl(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev, void* ws_dev,
+                              size_t ws_bytes, void* stream, bool pdl) {
     moe_workspace_layout L;
     const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
     if (s != NVFP4_OK) return s;
     if (T == 0) return NVFP4_OK;
     if (!out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
     return from_cuda(launch_combine(at<uint16_t>(ws_dev, L.y), T, k, w->H, static_cast<uint16_t*>(out_dev),
-                                    static_cast<cudaStream_t>(stream)));
+                                    static_cast<cudaStream_t>(stream), pdl));
+}
+
+// The stage entry points: each one's kernel is ordered after all earlier work on the stream.
+nvfp4_status moe_fc1_swiglu_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                                  void* ws_dev, size_t ws_bytes, float* fc1_debug_dev, void* stream) {
+    return moe_fc1_swiglu_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, fc1_debug_dev, stream, false);
+}
+
+nvfp4_status moe_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                               void* ws_dev, size_t ws_bytes, void* stream) {
+    return moe_requant_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, stream, false);
+}
+
+nvfp4_status moe_fc2_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                           void* ws_dev, size_t ws_bytes, float* fc2_debug_dev, void* stream) {
+    return moe_fc2_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, fc2_debug_dev, stream, false);
+}
+
+nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev, void* ws_dev,
+                              size_t ws_bytes, void* stream) {
+    return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, false);
 }
 
 nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
@@ -322,13 +343,15 @@ nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int
     if (s != NVFP4_OK) return s;
     if (T == 0) return NVFP4_OK;
     if (!expert_offsets_dev || !out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
-    s = moe_fc1_swiglu_nvfp4(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream);
+    // FC1 is ordered after everything queued before; the three kernels after it start
+    // early (programmatic dependent launch) and wait on their predecessor in the device
+    s = moe_fc1_swiglu_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, false);
     if (s != NVFP4_OK) return s;
-    s = moe_requant_nvfp4(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, stream);
+    s = moe_requant_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, stream, true);
     if (s != NVFP4_OK) return s;
-    s = moe_fc2_nvfp4(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream);
+    s = moe_fc2_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, true);
     if (s != NVFP4_OK) return s;
-    return moe_combine_bf16(w, T, k, out_dev, ws_dev, ws_bytes, stream);
+    return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, true);
 }
 
 nvfp4_status nvfp4_get_device_error(void* stream, int* device_status) {

@@ -27,6 +27,8 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 template <int kMaxK>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, int64_t T, int k, int H,
                                                       uint16_t* __restrict__ out) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int vec_per_row = H / 8;
     const int64_t nvec = T * vec_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -64,19 +66,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
 }  // namespace
 
-cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st) {
+cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st, bool pdl) {
     const int64_t nvec = T * (H / 8);
     if (nvec == 0) return cudaSuccess;
     int64_t blocks = (nvec + 255) / 256;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
-    const unsigned g = static_cast<unsigned>(blocks);
-    if (k <= 2) combine_kernel<2><<<g, 256, 0, st>>>(y, T, k, H, out);
-    else if (k <= 4) combine_kernel<4><<<g, 256, 0, st>>>(y, T, k, H, out);
-    else if (k <= 8) combine_kernel<8><<<g, 256, 0, st>>>(y, T, k, H, out);
-    else if (k <= 16) combine_kernel<16><<<g, 256, 0, st>>>(y, T, k, H, out);
-    else combine_kernel<32><<<g, 256, 0, st>>>(y, T, k, H, out);
-    return cudaGetLastError();
+    const dim3 g(static_cast<unsigned>(blocks));
+    if (k <= 2) return launch_pdl(pdl, combine_kernel<2>, g, 256, 0, st, y, T, k, H, out);
+    if (k <= 4) return launch_pdl(pdl, combine_kernel<4>, g, 256, 0, st, y, T, k, H, out);
+    if (k <= 8) return launch_pdl(pdl, combine_kernel<8>, g, 256, 0, st, y, T, k, H, out);
+    if (k <= 16) return launch_pdl(pdl, combine_kernel<16>, g, 256, 0, st, y, T, k, H, out);
+    return launch_pdl(pdl, combine_kernel<32>, g, 256, 0, st, y, T, k, H, out);
 }
 
 }  // namespace nvfp4

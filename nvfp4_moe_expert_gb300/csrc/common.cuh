@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -27,6 +28,35 @@ __device__ __forceinline__ void set_device_error(int* err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch.  Inside one library call, every kernel after
+// the first is launched with programmatic stream serialisation, so its CTAs may
+// be scheduled while the previous kernel (also this library's) is finishing.
+// Every kernel calls pdl_wait() before its first access to global memory (it
+// returns once the previous kernel has completed and its writes are visible;
+// at once for a normal launch) and then pdl_launch_dependents() so that the
+// next kernel can be scheduled early too.  The first kernel of a call is
+// launched normally, so it is ordered after whatever the caller queued before.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Cycles a pipeline wait may spin before it reports NVFP4_ERR_DEVICE_TIMEOUT (~2 s).
 constexpr long long kWaitBudgetCycles = 4000000000LL;
 
@@ -43,6 +73,7 @@ struct RouteBufs {
     int32_t* pair_rank;
     int32_t* expert_count;
     int64_t n_chunks;
+    int direct_rows;   // set by the route launcher: pair_rank holds destination rows
 };
 
 cudaError_t launch_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
@@ -54,7 +85,7 @@ cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, 
 
 cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32_t* row_pair,
                            const int32_t* offsets, int E, int64_t rows_cap, int I, uint8_t* codes, uint8_t* sf,
-                           float* g, int* err, cudaStream_t st);
+                           float* g, int* err, cudaStream_t st, bool pdl);
 
 struct GemmArgs {
     // operands
@@ -82,10 +113,10 @@ struct GemmArgs {
     int* err;
 };
 
-cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st);
-cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st, bool pdl);
+cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st, bool pdl);
 
-cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st);
+cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st, bool pdl);
 
 int device_sm_count();
 

@@ -170,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    // everything above touches only this CTA's shared memory and TMEM, so it overlaps the
+    // previous kernel's tail; global memory is read only after the wait
+    pdl_wait();
+    pdl_launch_dependents();
     for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
     if (kFC1) {
         for (int i = threadIdx.x; i < 2 * static_cast<int>(kSiluSpan); i += blockDim.x) {
@@ -515,21 +519,20 @@ cudaError_t prepare_device(bool fc1, cudaStream_t st) {
     return cudaSuccess;
 }
 
-cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st) {
+cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st, bool pdl) {
     cudaError_t e = prepare_device(fc1, st);
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb;
     if (!make_code_map(&ma, a.a_codes, a.rows_cap, a.K / 2)) return cudaErrorInvalidValue;
     if (!make_code_map(&mb, a.b_codes, static_cast<int64_t>(a.E) * a.Nw, a.K / 2)) return cudaErrorInvalidValue;
     const int grid = device_sm_count();
-    if (fc1) grouped_gemm_nvf4_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(ma, mb, a);
-    else grouped_gemm_nvf4_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(ma, mb, a);
-    return cudaGetLastError();
+    if (fc1) return launch_pdl(pdl, grouped_gemm_nvf4_kernel<true>, grid, kThreads, kSmemBytes, st, ma, mb, a);
+    return launch_pdl(pdl, grouped_gemm_nvf4_kernel<false>, grid, kThreads, kSmemBytes, st, ma, mb, a);
 }
 
 }  // namespace
 
-cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st) { return launch_gemm(true, a, st); }
-cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st) { return launch_gemm(false, a, st); }
+cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st, bool pdl) { return launch_gemm(true, a, st, pdl); }
+cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st, bool pdl) { return launch_gemm(false, a, st, pdl); }
 
 }  // namespace nvfp4

@@ -40,6 +40,26 @@ constexpr int kWarpsPerBlock = 8;
 constexpr int kRouteChunk = 256;       // tokens per route-sort chunk (8 warps x 32 tokens)
 constexpr float kMarksteinMinDivisor = 8.6736174e-19f;   // 2^-60
 
+// Lanes of the warp holding the same expert id as this lane (ids < 2^nbits, or -1 for
+// none): one ballot per bit of the id, so the cost does not grow with the number of
+// distinct ids in the warp.
+__device__ __forceinline__ unsigned match_expert(int e, int nbits) {
+    const unsigned valid = __ballot_sync(0xFFFFFFFFu, e >= 0);
+    unsigned m = e >= 0 ? valid : ~valid;
+    for (int b = 0; b < nbits; ++b) {
+        const bool bit = (e >> b) & 1;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+
+__host__ __device__ __forceinline__ int expert_id_bits(int E) {
+    int b = 0;
+    while ((1 << b) < E) ++b;
+    return b;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -76,22 +96,63 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8]) {
     return r;
 }
 
+// Both halves of a BF16 pair as an f32x2 operand (element 2j low, 2j+1 high).
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+    uint64_t x;
+    asm("{\n\t.reg .b32 lo, hi;\n\t"
+        "shl.b32 lo, %1, 16;\n\t"
+        "and.b32 hi, %1, 0xFFFF0000;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(x)
+        : "r"(w));
+    return x;
+}
+
+// div_markstein on both lanes of an f32x2 pair: rc2 = (rc, rc), nd2 = (-d, -d).
+__device__ __forceinline__ void div_markstein_x2(uint64_t x, uint64_t rc2, uint64_t nd2, float& lo, float& hi) {
+    uint64_t q0, r, q;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x), "l"(rc2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(nd2), "l"(x));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(rc2), "l"(q0));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(q));
+}
+
+__device__ __forceinline__ uint64_t f32x2_splat(float a) {
+    uint64_t x;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(x) : "f"(a));
+    return x;
+}
+
+// IEEE quotients for the divisors below the Markstein range; kept out of line so the
+// common path stays short (it is taken only for rows whose maximum is below ~2^-48).
+__device__ __noinline__ void quotients_fdiv(const uint32_t (&w)[4], float d, float (&q)[8]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        q[2 * j] = __fdiv_rn(__uint_as_float(w[j] << 16), d);
+        q[2 * j + 1] = __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), d);
+    }
+}
+
+__device__ __noinline__ float div_rn_slow(float a, float b) { return __fdiv_rn(a, b); }
+
 // Eight E2M1 codes of one 16-byte vector of BF16 values, quotient by d (rc = RN(1/d)).
 __device__ __forceinline__ uint32_t codes8(const uint4& v, float d, float rc, bool markstein) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float q[8];
+    if (markstein) {
+        const uint64_t rc2 = f32x2_splat(rc), nd2 = f32x2_splat(-d);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-        q[2 * j] = markstein ? div_markstein(lo, d, rc) : __fdiv_rn(lo, d);
-        q[2 * j + 1] = markstein ? div_markstein(hi, d, rc) : __fdiv_rn(hi, d);
+        for (int j = 0; j < 4; ++j) div_markstein_x2(bf16x2_to_f32x2(w[j]), rc2, nd2, q[2 * j], q[2 * j + 1]);
+    } else {
+        quotients_fdiv(w, d, q);
     }
-    const uint32_t mags = e2m1x8(q) & 0x77777777u;
-    // sign bit of every code = sign of x (also when the magnitude rounds to 0):
-    // byte 1 of w[j] carries element 2j's sign in bit 7, byte 3 element 2j+1's
+    // The sign bit of every code is the sign of x.  The conversion keeps the sign of
+    // the quotient (also of a zero), but for x = -0.0 the Markstein correction returns
+    // +0 (its residual (-0)(-d) + (-0) is +0), so x's sign bits are ORed in: byte 1 of
+    // w[j] carries element 2j's sign in bit 7, byte 3 element 2j+1's.
     const uint32_t t01 = __byte_perm(w[0], w[1], 0x7531), t23 = __byte_perm(w[2], w[3], 0x7531);
     const uint32_t even = __byte_perm(t01, t23, 0x6420), odd = __byte_perm(t01, t23, 0x7531);
-    return mags | ((even >> 4) & 0x08080808u) | (odd & 0x80808080u);
+    return e2m1x8(q) | ((even >> 4) & 0x08080808u) | (odd & 0x80808080u);
 }
 
 // Quantised form of one 64-element group.
@@ -108,7 +169,7 @@ __device__ __forceinline__ void quantize_group(const uint4 (&v)[8], const uint32
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         const float bmx = __uint_as_float(bm[b]);
-        const float r = rc1 != 0.0f ? div_markstein(bmx, d1, rc1) : __fdiv_rn(bmx, d1);
+        const float r = rc1 != 0.0f ? div_markstein(bmx, d1, rc1) : div_rn_slow(bmx, d1);
         const uint32_t s_code = d1 > 0.0f ? cvt_e4m3(r) : 0u;
         const float d2 = __fmul_rn(g, e4m3_value(s_code));
         q.sfw |= s_code << (8 * b);
@@ -158,16 +219,24 @@ struct RowLanes {
 // Quantise the GPL groups this lane owns of the row at `src`; amax_in >= 0 supplies
 // max|row| (it must be that maximum).  Returns g; finite = whether the row is finite.
 template <int GPL>
-__device__ __forceinline__ float quantize_row_lanes(const uint16_t* src, const RowLanes& rl, int G, float amax_in,
-                                                    GroupQ (&q)[GPL], bool& finite) {
-    uint4 v[GPL][8];
+__device__ __forceinline__ void load_row_lanes(const uint16_t* src, const RowLanes& rl, int G, uint4 (&v)[GPL][8]) {
+#pragma unroll
+    for (int i = 0; i < GPL; ++i) {
+        const int grp = rl.li + rl.LPR * i;
+        if (grp < G) load_group(src + grp * 64, v[i]);
+    }
+}
+
+// Quantise the row held in v (loaded by load_row_lanes).
+template <int GPL>
+__device__ __forceinline__ float quantize_loaded(const uint4 (&v)[GPL][8], const RowLanes& rl, int G, float amax_in,
+                                                 GroupQ (&q)[GPL], bool& finite) {
     uint32_t bm[GPL][4];
     uint32_t amax_bits = 0;
 #pragma unroll
     for (int i = 0; i < GPL; ++i) {
         const int grp = rl.li + rl.LPR * i;
         if (grp < G) {
-            load_group(src + grp * 64, v[i]);
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 bm[i][b] = block_absmax_bits(v[i][2 * b], v[i][2 * b + 1]);
@@ -189,12 +258,22 @@ __device__ __forceinline__ float quantize_row_lanes(const uint16_t* src, const R
     return g;
 }
 
+template <int GPL>
+__device__ __forceinline__ float quantize_row_lanes(const uint16_t* src, const RowLanes& rl, int G, float amax_in,
+                                                    GroupQ (&q)[GPL], bool& finite) {
+    uint4 v[GPL][8];
+    load_row_lanes<GPL>(src, rl, G, v);
+    return quantize_loaded<GPL>(v, rl, G, amax_in, q, finite);
+}
+
 // ------------------------------------------------------------------ plain rows
 template <int GPL>
 __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int cols, int64_t ld, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf, float* __restrict__ g,
                                                             int* err) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int G = cols / 64;
     const RowLanes rl(G);
     const int64_t rows_pad = (rows + kTileM - 1) / kTileM * kTileM;
@@ -234,36 +313,37 @@ __global__ void __launch_bounds__(256) route_hist_rank_kernel(const int32_t* __r
                                                                int32_t* __restrict__ chunk_count,
                                                                int32_t* __restrict__ pair_rank, int* err) {
     extern __shared__ int32_t wcount[];   // [8][E]
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t chunk = blockIdx.x;
     for (int i = threadIdx.x; i < kWarpsPerBlock * E; i += blockDim.x) wcount[i] = 0;
     const int64_t tok0 = chunk * kRouteChunk + w * 32;
     const int64_t npairs = T * k;
-    // all of this warp's ids first, so their loads overlap
+    // all of this warp's ids are loaded before any is used, so the loads overlap
     int my_e[32];
 #pragma unroll
     for (int it = 0; it < 32; ++it) {
-        if (it < k) {
-            const int64_t p = tok0 * k + it * 32 + lane;
-            int e = -1;
-            if (p < npairs && tok0 < T) {
-                e = __ldg(ids + p);
-                if (e < 0 || e >= E) {
-                    set_device_error(err, NVFP4_ERR_BAD_EXPERT_ID);
-                    e = -1;
-                }
-            }
-            my_e[it] = e;
+        const int64_t p = tok0 * k + it * 32 + lane;
+        my_e[it] = (it < k && p < npairs) ? __ldg(ids + p) : -1;
+    }
+#pragma unroll
+    for (int it = 0; it < 32; ++it) {
+        const bool real = it < k && tok0 * k + it * 32 + lane < npairs;
+        if (real && (my_e[it] < 0 || my_e[it] >= E)) {
+            set_device_error(err, NVFP4_ERR_BAD_EXPERT_ID);
+            my_e[it] = -1;
         }
     }
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
+    const int nbits = expert_id_bits(E);
     int my_rank[32];
 #pragma unroll
     for (int it = 0; it < 32; ++it) {
         if (it < k) {
             const int e = my_e[it];
-            const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+            const unsigned m = match_expert(e, nbits);
             const int before = __popc(m & lt_mask);
             const int base = e >= 0 ? wcount[w * E + e] : 0;
             __syncwarp();
@@ -329,6 +409,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t n_chunk
     __shared__ int32_t seg_sum[1024];
     __shared__ int32_t e_off[1024];
     __shared__ int32_t warp_tot[33];
+    pdl_wait();
+    pdl_launch_dependents();
     const int tid = threadIdx.x;
     const int S = blockDim.x / E;                  // threads per expert (>= 1)
     const int e = tid / S, seg = tid % S;
@@ -368,75 +450,188 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t n_chunk
     }
 }
 
+// One block of 1024 threads sorts all T*k pairs when they are few (one launch
+// instead of two; beyond a few thousand pairs one SM's issue rate makes the
+// chunked kernels faster): per-warp
+// expert counts over contiguous pair ranges, the padded expert offsets, then
+// every pair's destination row.  The result is the same stable counting sort
+// as the chunked kernels above (rows of an expert in (token, slot) order).
+constexpr int kBlockSortWarps = 32;
+constexpr int kBlockSortMaxE = 256;
+constexpr int64_t kBlockSortMaxPairs = 8192;
+
+__global__ void __launch_bounds__(1024) route_block_sort_kernel(const int32_t* __restrict__ ids, int64_t T, int E,
+                                                                int k, int32_t* __restrict__ pair_row,
+                                                                int32_t* __restrict__ expert_count,
+                                                                int32_t* __restrict__ offsets, int* err) {
+    extern __shared__ int32_t wc[];   // [32 warps][E]: counts, then running rows
+    __shared__ int32_t warp_tot[33];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    for (int i = tid; i < kBlockSortWarps * E; i += blockDim.x) wc[i] = 0;
+    __syncthreads();
+    const int64_t P = T * k;
+    const int64_t per = (P + kBlockSortWarps * 32 - 1) / (kBlockSortWarps * 32) * 32;
+    const int64_t p0 = w * per, p1 = min(P, p0 + per);
+    int32_t* mine = wc + w * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int nbits = expert_id_bits(E);
+    // counts of this warp's pairs; eight batches of ids are loaded before they are used
+    for (int64_t b0 = p0; b0 < p1; b0 += 8 * 32) {
+        int e8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t p = b0 + u * 32 + lane;
+            e8[u] = p < p1 ? __ldg(ids + p) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool real = b0 + u * 32 + lane < p1;
+            if (real && (e8[u] < 0 || e8[u] >= E)) {
+                set_device_error(err, NVFP4_ERR_BAD_EXPERT_ID);
+                e8[u] = -1;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const unsigned m = match_expert(e8[u], nbits);
+            if (e8[u] >= 0 && (m & lt_mask) == 0) mine[e8[u]] += __popc(m);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    int32_t cnt = 0;
+    if (tid < E) {
+        for (int ww = 0; ww < kBlockSortWarps; ++ww) cnt += wc[ww * E + tid];
+        expert_count[tid] = cnt;
+    }
+    int32_t total;
+    const int32_t start = block_exclusive_scan(tid < E ? (cnt + kTileM - 1) / kTileM * kTileM : 0, warp_tot, total);
+    if (tid < E) {
+        offsets[tid] = start;
+        int32_t run = start;   // first row of each warp's pairs of expert tid
+        for (int ww = 0; ww < kBlockSortWarps; ++ww) {
+            const int32_t c = wc[ww * E + tid];
+            wc[ww * E + tid] = run;
+            run += c;
+        }
+    }
+    if (tid == 0) offsets[E] = total;
+    __syncthreads();
+    for (int64_t b0 = p0; b0 < p1; b0 += 8 * 32) {
+        int e8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t p = b0 + u * 32 + lane;
+            e8[u] = p < p1 ? __ldg(ids + p) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (e8[u] < 0 || e8[u] >= E) e8[u] = -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e8[u];
+            const unsigned m = match_expert(e, nbits);
+            const int32_t base = e >= 0 ? mine[e] : 0;
+            __syncwarp();
+            if (e >= 0 && (m & lt_mask) == 0) mine[e] = base + __popc(m);
+            __syncwarp();
+            const int64_t p = b0 + u * 32 + lane;
+            if (p < p1) pair_row[p] = e >= 0 ? base + __popc(m & lt_mask) : -1;   // -1: bad id, skipped
+        }
+    }
+}
+
+// Destination rows of pair p (token t, chunk t / kRouteChunk): either stored directly
+// by route_block_sort_kernel, or chunk base + rank from the chunked kernels.
+__device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* ids, int E, int64_t p, int64_t chunk) {
+    if (b.direct_rows) return __ldg(b.pair_rank + p);
+    const int e = __ldg(ids + p);
+    const int32_t rank = __ldg(b.pair_rank + p);
+    if (e < 0 || e >= E) return -1;   // reported by the counting kernels
+    return __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) + rank;
+}
+
+// Blocks [0, pad_blocks) give one warp per expert for its pad rows
+// [offsets[e] + count_e, offsets[e+1]): zero scales, g = 0, row_pair = -1.
+// The remaining blocks quantise tokens (X read once) and write the k copies.
 template <int GPL>
 __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int E, int k, const int32_t* __restrict__ ids,
-    const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int* err) {
+    const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int pad_blocks, int* err) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int G = H / 64;
+    const int lane = threadIdx.x & 31;
+    if (static_cast<int>(blockIdx.x) < pad_blocks) {
+        const int e = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+        if (e >= E) return;
+        const int64_t r0 = static_cast<int64_t>(__ldg(offsets + e)) + __ldg(b.expert_count + e);
+        const int64_t r1 = __ldg(offsets + e + 1);
+        for (int64_t r = r0 + lane; r < r1; r += 32) {
+            b.a_g[r] = 0.0f;
+            b.row_pair[r] = -1;
+            b.row_prob[r] = 0.0f;
+            b.amax2[r] = 0u;
+        }
+        for (int64_t r = r0; r < r1; ++r) {
+            for (int grp = lane; grp < G; grp += 32)
+                *reinterpret_cast<uint32_t*>(b.a_sf + sf_offset(r, 4 * grp, H)) = 0u;
+        }
+        return;
+    }
     const RowLanes rl(G);
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x - pad_blocks) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x - pad_blocks) * blockDim.x) >> 5;
     for (int64_t base = warp * rl.RPW; base < T; base += nwarps * rl.RPW) {
         const int64_t t = base + rl.slot;
         if (!rl.active || t >= T) continue;
         const int64_t chunk = t / kRouteChunk;
-        // destination rows of the token's k slots: lane li < k of the row fetches slot li's,
-        // before the row itself is loaded, so the two dependent lookups overlap the row load
-        int my_dst = -1;
+        // lane li < k of the row looks up slot li's destination and probability; these
+        // loads and the row's are all in flight together
+        uint4 v[GPL][8];
+        load_row_lanes<GPL>(x + t * H, rl, G, v);
+        const bool slot_lane = rl.LPR >= k && rl.li < k;
+        int32_t my_dst = -1;
         float my_prob = 0.0f;
-        if (rl.LPR >= k && rl.li < k) {
+        if (slot_lane) {
             const int64_t p = t * k + rl.li;
-            const int e = __ldg(ids + p);
-            if (e >= 0 && e < E) {   // out-of-range ids are reported by the histogram kernel
-                my_dst = __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) + __ldg(b.pair_rank + p);
-                my_prob = __ldg(probs + p);
-            }
+            my_prob = __ldg(probs + p);
+            my_dst = pair_dest(b, ids, E, p, chunk);
         }
         GroupQ q[GPL];
         bool finite;
-        const float gr = quantize_row_lanes<GPL>(x + t * H, rl, G, -1.0f, q, finite);
+        const float gr = quantize_loaded<GPL>(v, rl, G, -1.0f, q, finite);
         if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
+        if (slot_lane && my_dst >= 0) {   // the routed row's per-row data, one slot per lane
+            b.a_g[my_dst] = gr;
+            b.row_pair[my_dst] = static_cast<int32_t>(t * k + rl.li);
+            b.row_prob[my_dst] = my_prob;
+            b.amax2[my_dst] = 0u;
+        }
         const int src0 = rl.slot * rl.LPR;
         for (int j = 0; j < k; ++j) {
             const int64_t p = t * k + j;
             int64_t r;
-            float pj;
             if (rl.LPR >= k) {
                 r = __shfl_sync(rl.mask, my_dst, src0 + j);
-                pj = __shfl_sync(rl.mask, my_prob, src0 + j);
-                if (r < 0) continue;
             } else {                 // rows narrower than k lanes: look the slot up directly
-                const int e = __ldg(ids + p);
-                if (e < 0 || e >= E) continue;
-                r = __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) + __ldg(b.pair_rank + p);
-                pj = __ldg(probs + p);
+                r = pair_dest(b, ids, E, p, chunk);
+                if (r >= 0 && rl.li == 0) {
+                    b.a_g[r] = gr;
+                    b.row_pair[r] = static_cast<int32_t>(p);
+                    b.row_prob[r] = __ldg(probs + p);
+                    b.amax2[r] = 0u;
+                }
             }
+            if (r < 0) continue;
 #pragma unroll
             for (int i = 0; i < GPL; ++i) {
                 const int grp = rl.li + rl.LPR * i;
                 if (grp < G) store_group(q[i], r, grp, H, b.a_codes, b.a_sf);
             }
-            if (rl.li == 0) {
-                b.a_g[r] = gr;
-                b.row_pair[r] = static_cast<int32_t>(p);
-                b.row_prob[r] = pj;
-                b.amax2[r] = 0u;
-            }
-        }
-    }
-    // pad rows: expert e's rows [offsets[e] + count_e, offsets[e+1]); one warp zeroes one row's scales
-    const int lane = threadIdx.x & 31;
-    const int64_t pad_slots = static_cast<int64_t>(E) * kTileM;
-    for (int64_t s = warp; s < pad_slots; s += nwarps) {
-        const int e = static_cast<int>(s / kTileM), j = static_cast<int>(s % kTileM);
-        const int64_t r = static_cast<int64_t>(offsets[e]) + b.expert_count[e] + j;
-        if (r >= offsets[e + 1]) continue;
-        for (int grp = lane; grp < G; grp += 32) *reinterpret_cast<uint32_t*>(b.a_sf + sf_offset(r, 4 * grp, H)) = 0u;
-        if (lane == 0) {
-            b.a_g[r] = 0.0f;
-            b.row_pair[r] = -1;
-            b.row_prob[r] = 0.0f;
-            b.amax2[r] = 0u;
         }
     }
 }
@@ -449,6 +644,8 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) requant_kernel(const ui
                                                       const int32_t* __restrict__ offsets, int E, int I,
                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                       float* __restrict__ g, int* err) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int G = I / 64;
     const RowLanes rl(G);
     const int64_t rows = offsets[E];
@@ -457,7 +654,12 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) requant_kernel(const ui
     for (int64_t base = warp * rl.RPW; base < rows; base += nwarps * rl.RPW) {
         const int64_t r = base + rl.slot;
         if (!rl.active || r >= rows) continue;
-        if (__ldg(row_pair + r) < 0) {       // pad row: zero scales, g = 0 (codes are never read)
+        // the row's flags and values are loaded together (a pad row's h is never used)
+        const int32_t pair = __ldg(row_pair + r);
+        const uint32_t amax_bits = __ldg(amax2 + r);
+        uint4 v[GPL][8];
+        load_row_lanes<GPL>(h + r * I, rl, G, v);
+        if (pair < 0) {       // pad row: zero scales, g = 0 (codes are never read)
             for (int i = 0; i < GPL; ++i) {
                 const int grp = rl.li + rl.LPR * i;
                 if (grp < G) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, I)) = 0u;
@@ -467,7 +669,7 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) requant_kernel(const ui
         }
         GroupQ q[GPL];
         bool finite;
-        const float gr = quantize_row_lanes<GPL>(h + r * I, rl, G, __uint_as_float(__ldg(amax2 + r)), q, finite);
+        const float gr = quantize_loaded<GPL>(v, rl, G, __uint_as_float(amax_bits), q, finite);
         if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
 #pragma unroll
         for (int i = 0; i < GPL; ++i) {
@@ -493,13 +695,10 @@ int64_t warps_for_rows(int64_t rows, int G) {
 }  // namespace
 
 // Dispatch on the number of 64-element groups each lane owns.
-#define NVFP4_GPL_DISPATCH(G, KERNEL, ...)                 \
-    do {                                                   \
-        const int gpl_ = ((G) + 31) / 32;                  \
-        if (gpl_ <= 1) KERNEL<1> __VA_ARGS__;              \
-        else if (gpl_ <= 2) KERNEL<2> __VA_ARGS__;         \
-        else KERNEL<4> __VA_ARGS__;                        \
-    } while (0)
+#define NVFP4_GPL_LAUNCH(PDL, G, KERNEL, GRID, ...)                                   \
+    (((G) + 31) / 32 <= 1   ? launch_pdl(PDL, KERNEL<1>, GRID, 256, 0, __VA_ARGS__)   \
+     : ((G) + 31) / 32 <= 2 ? launch_pdl(PDL, KERNEL<2>, GRID, 256, 0, __VA_ARGS__)   \
+                            : launch_pdl(PDL, KERNEL<4>, GRID, 256, 0, __VA_ARGS__))
 
 cudaError_t launch_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
                                  uint8_t* sf, float* g, int* err, cudaStream_t st) {
@@ -507,36 +706,42 @@ cudaError_t launch_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, 
     if (rows_pad == 0) return cudaSuccess;
     const int c = static_cast<int>(cols);
     const int grid = grid_for_warps(warps_for_rows(rows_pad, c / 64));
-    NVFP4_GPL_DISPATCH(c / 64, quantize_rows_kernel, <<<grid, 256, 0, st>>>(x, rows, c, ld, codes, sf, g, err));
-    return cudaGetLastError();
+    return NVFP4_GPL_LAUNCH(false, c / 64, quantize_rows_kernel, grid, st, x, rows, c, ld, codes, sf, g, err);
 }
 
 cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, int k, const int32_t* ids,
-                                    const float* probs, int32_t* offsets, const RouteBufs& b, int* err,
+                                    const float* probs, int32_t* offsets, const RouteBufs& b_in, int* err,
                                     cudaStream_t st) {
     if (T == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
-    const size_t smem = sizeof(int32_t) * kWarpsPerBlock * E;
-    route_hist_rank_kernel<<<static_cast<unsigned>(b.n_chunks), 256, smem, st>>>(ids, T, E, k, b.n_chunks,
-                                                                                 b.chunk_count, b.pair_rank, err);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    route_scan_kernel<<<1, 1024, 0, st>>>(E, b.n_chunks, b.chunk_count, b.chunk_base, b.expert_count, offsets);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int64_t tw = warps_for_rows(T, H / 64), pw = static_cast<int64_t>(E) * kTileM;
-    const int grid = grid_for_warps(tw > pw ? tw : pw);
-    NVFP4_GPL_DISPATCH(H / 64, route_quant_scatter_kernel,
-                       <<<grid, 256, 0, st>>>(x, T, H, E, k, ids, probs, offsets, b, err));
-    return cudaGetLastError();
+    RouteBufs b = b_in;
+    cudaError_t e;
+    if (E <= kBlockSortMaxE && T * k <= kBlockSortMaxPairs) {
+        b.direct_rows = 1;
+        const size_t smem = sizeof(int32_t) * kBlockSortWarps * E;
+        e = launch_pdl(false, route_block_sort_kernel, 1, kBlockSortWarps * 32, smem, st, ids, T, E, k, b.pair_rank,
+                       b.expert_count, offsets, err);
+        if (e != cudaSuccess) return e;
+    } else {
+        b.direct_rows = 0;
+        const size_t smem = sizeof(int32_t) * kWarpsPerBlock * E;
+        e = launch_pdl(false, route_hist_rank_kernel, static_cast<unsigned>(b.n_chunks), 256, smem, st, ids, T, E, k,
+                       b.n_chunks, b.chunk_count, b.pair_rank, err);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(true, route_scan_kernel, 1, 1024, 0, st, E, b.n_chunks, b.chunk_count, b.chunk_base,
+                       b.expert_count, offsets);
+        if (e != cudaSuccess) return e;
+    }
+    const int pad_blocks = (E + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int grid = pad_blocks + grid_for_warps(warps_for_rows(T, H / 64));
+    return NVFP4_GPL_LAUNCH(true, H / 64, route_quant_scatter_kernel, grid, st, x, T, H, E, k, ids, probs, offsets, b,
+                            pad_blocks, err);
 }
 
 cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32_t* row_pair,
                            const int32_t* offsets, int E, int64_t rows_cap, int I, uint8_t* codes, uint8_t* sf,
-                           float* g, int* err, cudaStream_t st) {
+                           float* g, int* err, cudaStream_t st, bool pdl) {
     const int grid = grid_for_warps(warps_for_rows(rows_cap, I / 64));
-    NVFP4_GPL_DISPATCH(I / 64, requant_kernel,
-                       <<<grid, 256, 0, st>>>(h, amax2, row_pair, offsets, E, I, codes, sf, g, err));
-    return cudaGetLastError();
+    return NVFP4_GPL_LAUNCH(pdl, I / 64, requant_kernel, grid, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
 }
 
 }  // namespace nvfp4
