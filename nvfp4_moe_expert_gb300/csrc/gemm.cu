@@ -16,13 +16,16 @@
 // fixed order, independent of its neighbours).
 //
 // Kernel design (sm_103a):
-//  * persistent: one 320-thread CTA per SM walks the (m-tile, n-tile) list;
+//  * persistent: one 352-thread CTA per SM walks the (m-tile, n-tile) list;
 //    the list length comes from the device-side expert offsets, so nothing
 //    is read back to the host;
-//  * warp 0 = TMA producer: A tile 128 rows x 256 K (16 KB, 128B swizzle),
-//    B tile 256 rows x 256 K as two 128-row boxes (FC1: the gate rows and
-//    the matching up rows, so one tile holds both halves of SwiGLU), and the
-//    scale-factor tiles by plain bulk copies; 3-stage mbarrier ring;
+//  * two TMA producers, because one issuing thread caps what an SM pulls from
+//    L2 well below what it can take in: warp 0 loads the A tile (128 rows x
+//    256 K, 16 KB, 128B swizzle) and its scale-factor tiles, warp 10 the B
+//    tile (256 rows x 256 K in one box: FC2 256 consecutive weight rows, FC1
+//    through a 4D map the 128 gate rows and the matching 128 up rows, so one
+//    tile holds both halves of SwiGLU) and its scale-factor tiles; 3-stage
+//    mbarrier ring, each stage's barrier counting both producers;
 //  * warp 1 = MMA issuer: tcgen05.cp moves the stage's scale factors into
 //    TMEM, then 4 x tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //    (M=128, N=256, K=64) accumulate in a 256-column FP32 TMEM tile;
@@ -52,7 +55,8 @@ namespace {
 constexpr int kStages = 3;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kThreads = 96 + kEpiThreads;            // + producer A, MMA, producer B warps
+constexpr int kProducerBWarp = 2 + kEpiWarps;
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBKBytes = 128;                         // bytes of K per row per stage (256 FP4 values)
@@ -60,7 +64,6 @@ constexpr int kMmaPerStage = kBKBytes / 32;           // K=64 MMAs per stage
 // K-major operand tiles use the swizzle whose span equals the stage's row length
 constexpr int kSwizzleBytes = kBKBytes;               // 128 or 64
 constexpr int kABytes = kBM * kBKBytes;
-constexpr int kBBoxBytes = 128 * kBKBytes;            // one 128-row B box
 constexpr int kBBytes = kBN * kBKBytes;
 constexpr int kSfaOff = kABytes + kBBytes;            // kMmaPerStage scale tiles of A
 constexpr int kSfbOff = kSfaOff + kMmaPerStage * kSfAtomBytes;   // 2 x kMmaPerStage scale tiles of B
@@ -109,8 +112,30 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     return r;
 }
 
+// Pairs of FP32 values in one 64-bit register (low = first) and their elementwise
+// round-to-nearest products: each lane is exactly __fmul_rn of its two inputs.
+__device__ __forceinline__ uint64_t f2(uint32_t lo_bits, uint32_t hi_bits) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// Elementwise maximum of two BF16 pairs (a NaN operand loses, as with fmaxf).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // The warp's 32 rows x 64 BF16 columns (packed[lane][0..31]) staged through shared
-// memory and written as 4 rows x 128 B per store instruction.  dst_row(r) gives
+// memory and written as 8 rows x 128 B per store instruction (32 bytes per lane).  dst_row(r) gives
 // the global address of row r's 64-column chunk, or nullptr to skip the row.
 template <typename RowPtr>
 __device__ __forceinline__ void store_rows_64(uint8_t* stage, const uint32_t (&packed)[32], RowPtr dst_row) {
@@ -121,13 +146,18 @@ __device__ __forceinline__ void store_rows_64(uint8_t* stage, const uint32_t (&p
         mine[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
     }
     __syncwarp();
-    const int sub = lane & 7;
+    const int sub = lane & 3;                 // 32-byte quarter of the 128-byte row
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int r = it * 4 + (lane >> 3);
-        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * kStagePitch + sub * 16);
+    for (int it = 0; it < 4; ++it) {
+        const int r = it * 8 + (lane >> 2);
+        const uint4 v0 = *reinterpret_cast<const uint4*>(stage + r * kStagePitch + sub * 32);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(stage + r * kStagePitch + sub * 32 + 16);
         uint16_t* dst = dst_row(r);
-        if (dst) reinterpret_cast<uint4*>(dst)[sub] = v;
+        if (dst) {
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + sub * 16),
+                         "r"(v0.x), "r"(v0.y), "r"(v0.z), "r"(v0.w), "r"(v1.x), "r"(v1.y), "r"(v1.z), "r"(v1.w)
+                         : "memory");
+        }
     }
     __syncwarp();
 }
@@ -153,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);           // producer A and producer B
             mbar_init(&empty[s], 1);
         }
         mbar_init(tmem_full, 1);
@@ -195,24 +225,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool failed = false;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == kProducerBWarp) {
+        // ------------------------------------------------------------ producers
         if (lane == 0) {
-            const uint64_t pol_a = policy_evict_last();
-            const uint64_t pol_b = policy_evict_normal();
+            const bool is_a = warp == 0;
+            const uint64_t pol = is_a ? policy_evict_last() : policy_evict_normal();
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;
             for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
                 const int mt = t / n_tiles, nt = t % n_tiles;
                 const int e = expert_of_row(s_off, E, mt * kBM);
-                int row0, row1;
-                if (kFC1) {
-                    row0 = e * args.Nw + nt * 128;
-                    row1 = row0 + args.I;
-                } else {
-                    row0 = e * args.Nw + nt * kBN;
-                    row1 = row0 + 128;
-                }
+                // first weight rows of the tile's two 128-row halves (their scale tiles)
+                const int row0 = kFC1 ? e * args.Nw + nt * 128 : e * args.Nw + nt * kBN;
+                const int row1 = kFC1 ? row0 + args.I : row0 + 128;
                 for (int ks = 0; ks < num_ks; ++ks) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetCycles)) {
                         failed = true;
@@ -220,20 +245,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
                     const uint32_t sf_bytes = static_cast<uint32_t>(nk) * kSfAtomBytes;
-                    mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + 3 * sf_bytes);
                     uint8_t* st = smem + stage * kStageBytes;
-                    tma_load_2d(st, &tmA, &full[stage], ks * kBKBytes, mt * kBM, pol_a);
-                    tma_load_2d(st + kABytes, &tmB, &full[stage], ks * kBKBytes, row0, pol_b);
-                    tma_load_2d(st + kABytes + kBBoxBytes, &tmB, &full[stage], ks * kBKBytes, row1, pol_b);
-                    bulk_load(st + kSfaOff,
-                              args.a_sf + (static_cast<int64_t>(mt) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes, sf_bytes,
-                              &full[stage], pol_a);
-                    bulk_load(st + kSfbOff,
-                              args.b_sf + (static_cast<int64_t>(row0 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
-                              sf_bytes, &full[stage], pol_b);
-                    bulk_load(st + kSfbOff + kMmaPerStage * kSfAtomBytes,
-                              args.b_sf + (static_cast<int64_t>(row1 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
-                              sf_bytes, &full[stage], pol_b);
+                    if (is_a) {
+                        mbar_arrive_expect_tx(&full[stage], kABytes + sf_bytes);
+                        tma_load_2d(st, &tmA, &full[stage], ks * kBKBytes, mt * kBM, pol);
+                        bulk_load(st + kSfaOff,
+                                  args.a_sf + (static_cast<int64_t>(mt) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
+                                  sf_bytes, &full[stage], pol);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], kBBytes + 2 * sf_bytes);
+                        if (kFC1) tma_load_4d(st + kABytes, &tmB, &full[stage], ks * kBKBytes, nt * 128, 0, e, pol);
+                        else tma_load_2d(st + kABytes, &tmB, &full[stage], ks * kBKBytes, row0, pol);
+                        bulk_load(st + kSfbOff,
+                                  args.b_sf + (static_cast<int64_t>(row0 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
+                                  sf_bytes, &full[stage], pol);
+                        bulk_load(st + kSfbOff + kMmaPerStage * kSfAtomBytes,
+                                  args.b_sf + (static_cast<int64_t>(row1 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
+                                  sf_bytes, &full[stage], pol);
+                    }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -246,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
                 // let every copy still in flight land before the CTA's shared memory goes away
+                // (a stage the other producer never filled runs out its bounded wait)
                 for (int s = 0; s < kStages; ++s) {
                     if (issued & (1u << s)) {
                         mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, kWaitBudgetCycles);
@@ -377,31 +407,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float* su = sc + 64;                   // up scales
                 float* dbg = args.debug ? args.debug + row * (2 * I) + nt * 128 + 64 * half : nullptr;
                 uint32_t packed[32];
-                float hmax = 0.0f;
+                uint32_t hmax2 = 0u;                         // running max of |h| as a BF16 pair
+                const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
+                const uint64_t p2 = f2(__float_as_uint(p), __float_as_uint(p));
 #pragma unroll
-                for (int j = 0; j < 64; j += 2) {
-                    float hv[2];
+                for (int j = 0; j < 64; j += 2) {       // columns j, j+1: ((acc*g^x)*g^w), both halves
+                    const uint64_t vg2 = f2_mul(f2_mul(f2(acc[j >> 5][j & 31], acc[j >> 5][(j & 31) + 1]), gr2),
+                                                *reinterpret_cast<const uint64_t*>(sg + j));
+                    const uint64_t vu2 = f2_mul(f2_mul(f2(acc[2 + (j >> 5)][j & 31], acc[2 + (j >> 5)][(j & 31) + 1]), gr2),
+                                                *reinterpret_cast<const uint64_t*>(su + j));
+                    float vg[2], vu[2];
+                    f2_unpack(vg2, vg[0], vg[1]);
+                    f2_unpack(vu2, vu[0], vu[1]);
+                    if (dbg && live) {
+                        dbg[j] = vg[0];
+                        dbg[j + 1] = vg[1];
+                        dbg[I + j] = vu[0];
+                        dbg[I + j + 1] = vu[1];
+                    }
+                    const uint32_t gb = bf16x2_rn(vg[0], vg[1]), ub = bf16x2_rn(vu[0], vu[1]);
+                    float sl[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int c = j + u;
-                        const float vg = __fmul_rn(__fmul_rn(__uint_as_float(acc[c >> 5][c & 31]), gr), sg[c]);
-                        const float vu = __fmul_rn(__fmul_rn(__uint_as_float(acc[2 + (c >> 5)][c & 31]), gr), su[c]);
-                        if (dbg && live) {
-                            dbg[c] = vg;
-                            dbg[I + c] = vu;
-                        }
-                        const __nv_bfloat16 gb = __float2bfloat16_rn(vg);
-                        const __nv_bfloat16 ub = __float2bfloat16_rn(vu);
-                        const uint32_t gbits = __bfloat16_as_ushort(gb);
+                        const uint32_t gbits = u ? gb >> 16 : gb & 0xFFFFu;
                         const uint32_t gi = (gbits & 0x7FFFu) - kSiluLo;
-                        const float s = gi < kSiluSpan ? s_silu[gi + ((gbits >> 15) ? kSiluSpan : 0u)]
-                                                       : __ldg(g_silu_table + gbits);
-                        const float t1 = __fmul_rn(s, __bfloat162float(ub));
-                        hv[u] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(t1, p)));
-                        hmax = fmaxf(hmax, fabsf(hv[u]));
+                        sl[u] = gi < kSiluSpan ? s_silu[gi + ((gbits >> 15) ? kSiluSpan : 0u)]
+                                               : __ldg(g_silu_table + gbits);
                     }
-                    packed[j >> 1] = bf16x2_rn(hv[0], hv[1]);
+                    // silu(gate) * up in FP32, then * p, one BF16 rounding
+                    const uint64_t h2 = f2_mul(f2_mul(f2(__float_as_uint(sl[0]), __float_as_uint(sl[1])),
+                                                      f2(ub << 16, ub & 0xFFFF0000u)),
+                                               p2);
+                    float h[2];
+                    f2_unpack(h2, h[0], h[1]);
+                    packed[j >> 1] = bf16x2_rn(h[0], h[1]);
+                    hmax2 = bf16x2_max(hmax2, packed[j >> 1] & 0x7FFF7FFFu);
                 }
+                const float hmax = __uint_as_float((bf16x2_max(hmax2, hmax2 >> 16) & 0xFFFFu) << 16);
                 if (live) atomicMax(args.amax2 + row, __float_as_uint(hmax));
                 const int64_t row0 = static_cast<int64_t>(mt) * kBM + q * 32;
                 uint16_t* hbase = args.h + nt * 128 + 64 * half;
@@ -412,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const int H = args.H;
                 const float* sw = sc;
+                const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
                 float* dbg = args.debug ? args.debug + row * H + nt * kBN + 128 * half : nullptr;
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {            // two 64-column chunks
@@ -419,9 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 64; j += 2) {
                         const int c = 64 * c2 + j;
-                        const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(acc[c >> 5][c & 31]), gr), sw[c]);
-                        const float v1 =
-                            __fmul_rn(__fmul_rn(__uint_as_float(acc[(c + 1) >> 5][(c + 1) & 31]), gr), sw[c + 1]);
+                        const uint64_t v2 = f2_mul(f2_mul(f2(acc[c >> 5][c & 31], acc[c >> 5][(c & 31) + 1]), gr2),
+                                                   *reinterpret_cast<const uint64_t*>(sw + c));
+                        float v0, v1;
+                        f2_unpack(v2, v0, v1);
                         if (dbg && live) {
                             dbg[c] = v0;
                             dbg[c + 1] = v1;
@@ -465,18 +509,37 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2D map over an NVFP4 code matrix [rows][row_bytes]: boxes of 128 rows x kBKBytes, swizzled
-// with the same span (the K-major canonical layout the MMA descriptors describe).
-bool make_code_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
+constexpr CUtensorMapSwizzle kSwizzleMode =
+    kSwizzleBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+
+// 2D map over an NVFP4 code matrix [rows][row_bytes]: boxes of box_rows rows x kBKBytes,
+// swizzled with the same span (the K-major canonical layout the MMA descriptors describe).
+bool make_code_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), 128};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzleBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzleMode, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4D map over the FC1 weight codes [E][2][I][row_bytes] (gate rows, then up rows, per
+// expert): a box is 128 gate rows and the 128 up rows of the same columns, so one copy
+// lands them as 256 consecutive 128-byte rows (gate first), as two 2D boxes would.
+bool make_gateup_map(CUtensorMap* m, const void* base, int E, int I, int64_t row_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(I), 2,
+                                static_cast<cuuint64_t>(E)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(I * row_bytes),
+                                   static_cast<cuuint64_t>(2 * I * row_bytes)};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(kBKBytes), 128, 2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzleMode, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -523,8 +586,10 @@ cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st, bool pdl) 
     cudaError_t e = prepare_device(fc1, st);
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb;
-    if (!make_code_map(&ma, a.a_codes, a.rows_cap, a.K / 2)) return cudaErrorInvalidValue;
-    if (!make_code_map(&mb, a.b_codes, static_cast<int64_t>(a.E) * a.Nw, a.K / 2)) return cudaErrorInvalidValue;
+    if (!make_code_map(&ma, a.a_codes, a.rows_cap, a.K / 2, kBM)) return cudaErrorInvalidValue;
+    if (fc1 ? !make_gateup_map(&mb, a.b_codes, a.E, a.I, a.K / 2)
+            : !make_code_map(&mb, a.b_codes, static_cast<int64_t>(a.E) * a.Nw, a.K / 2, kBN))
+        return cudaErrorInvalidValue;
     const int grid = device_sm_count();
     if (fc1) return launch_pdl(pdl, grouped_gemm_nvf4_kernel<true>, grid, kThreads, kSmemBytes, st, ma, mb, a);
     return launch_pdl(pdl, grouped_gemm_nvf4_kernel<false>, grid, kThreads, kSmemBytes, st, ma, mb, a);
