@@ -26,6 +26,9 @@
 //    through a 4D map the 128 gate rows and the matching 128 up rows, so one
 //    tile holds both halves of SwiGLU) and its scale-factor tiles; 3-stage
 //    mbarrier ring, each stage's barrier counting both producers;
+//  * producers and MMA issuer run warp-uniform loops and issue through an
+//    elect.sync-chosen lane (a single diverged lane issues tcgen05 work at
+//    well under half the rate);
 //  * warp 1 = MMA issuer: tcgen05.cp moves the stage's scale factors into
 //    TMEM, then 4 x tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //    (M=128, N=256, K=64) accumulate in a 256-column FP32 TMEM tile;
@@ -225,116 +228,121 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool failed = false;
 
+    // The producer and MMA warps run their loops with all 32 lanes in step (every value
+    // warp-uniform, waits taken by all lanes and agreed with a vote); the TMA and tcgen05
+    // instructions are issued by the lane elect.sync picks.
     if (warp == 0 || warp == kProducerBWarp) {
         // ------------------------------------------------------------ producers
-        if (lane == 0) {
-            const bool is_a = warp == 0;
-            const uint64_t pol = is_a ? policy_evict_last() : policy_evict_normal();
-            int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_parity = 0;
-            for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
-                const int mt = t / n_tiles, nt = t % n_tiles;
-                const int e = expert_of_row(s_off, E, mt * kBM);
-                // first weight rows of the tile's two 128-row halves (their scale tiles)
-                const int row0 = kFC1 ? e * args.Nw + nt * 128 : e * args.Nw + nt * kBN;
-                const int row1 = kFC1 ? row0 + args.I : row0 + 128;
-                for (int ks = 0; ks < num_ks; ++ks) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetCycles)) {
-                        failed = true;
-                        break;
-                    }
-                    const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
-                    const uint32_t sf_bytes = static_cast<uint32_t>(nk) * kSfAtomBytes;
-                    uint8_t* st = smem + stage * kStageBytes;
-                    if (is_a) {
-                        mbar_arrive_expect_tx(&full[stage], kABytes + sf_bytes);
-                        tma_load_2d(st, &tmA, &full[stage], ks * kBKBytes, mt * kBM, pol);
-                        bulk_load(st + kSfaOff,
-                                  args.a_sf + (static_cast<int64_t>(mt) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
-                                  sf_bytes, &full[stage], pol);
-                    } else {
-                        mbar_arrive_expect_tx(&full[stage], kBBytes + 2 * sf_bytes);
-                        if (kFC1) tma_load_4d(st + kABytes, &tmB, &full[stage], ks * kBKBytes, nt * 128, 0, e, pol);
-                        else tma_load_2d(st + kABytes, &tmB, &full[stage], ks * kBKBytes, row0, pol);
-                        bulk_load(st + kSfbOff,
-                                  args.b_sf + (static_cast<int64_t>(row0 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
-                                  sf_bytes, &full[stage], pol);
-                        bulk_load(st + kSfbOff + kMmaPerStage * kSfAtomBytes,
-                                  args.b_sf + (static_cast<int64_t>(row1 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
-                                  sf_bytes, &full[stage], pol);
-                    }
-                    issued |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+        const bool is_a = warp == 0;
+        const uint64_t pol = is_a ? policy_evict_last() : policy_evict_normal();
+        int stage = 0;
+        uint32_t phase = 0, issued = 0, issued_parity = 0;
+        for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
+            const int mt = t / n_tiles, nt = t % n_tiles;
+            const int e = expert_of_row(s_off, E, mt * kBM);
+            // first weight rows of the tile's two 128-row halves (their scale tiles)
+            const int row0 = kFC1 ? e * args.Nw + nt * 128 : e * args.Nw + nt * kBN;
+            const int row1 = kFC1 ? row0 + args.I : row0 + 128;
+            for (int ks = 0; ks < num_ks; ++ks) {
+                const bool ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetCycles);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    failed = true;
+                    break;
+                }
+                const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
+                const uint32_t sf_bytes = static_cast<uint32_t>(nk) * kSfAtomBytes;
+                uint8_t* st = smem + stage * kStageBytes;
+                if (is_a) {
+                    mbar_arrive_expect_tx_elect(&full[stage], kABytes + sf_bytes);
+                    tma_load_2d_elect(st, &tmA, &full[stage], ks * kBKBytes, mt * kBM, pol);
+                    bulk_load_elect(st + kSfaOff,
+                                    args.a_sf + (static_cast<int64_t>(mt) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
+                                    sf_bytes, &full[stage], pol);
+                } else {
+                    mbar_arrive_expect_tx_elect(&full[stage], kBBytes + 2 * sf_bytes);
+                    if (kFC1) tma_load_4d_elect(st + kABytes, &tmB, &full[stage], ks * kBKBytes, nt * 128, 0, e, pol);
+                    else tma_load_2d_elect(st + kABytes, &tmB, &full[stage], ks * kBKBytes, row0, pol);
+                    bulk_load_elect(st + kSfbOff,
+                                    args.b_sf + (static_cast<int64_t>(row0 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
+                                    sf_bytes, &full[stage], pol);
+                    bulk_load_elect(st + kSfbOff + kMmaPerStage * kSfAtomBytes,
+                                    args.b_sf + (static_cast<int64_t>(row1 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
+                                    sf_bytes, &full[stage], pol);
+                }
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            if (failed) {
-                set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
-                *abort_flag = 1;
-                // let every copy still in flight land before the CTA's shared memory goes away
-                // (a stage the other producer never filled runs out its bounded wait)
-                for (int s = 0; s < kStages; ++s) {
-                    if (issued & (1u << s)) {
-                        mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, kWaitBudgetCycles);
-                    }
+        }
+        if (failed) {
+            if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            // let every copy still in flight land before the CTA's shared memory goes away
+            // (a stage the other producer never filled runs out its bounded wait)
+            for (int s = 0; s < kStages; ++s) {
+                if (issued & (1u << s)) {
+                    mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, kWaitBudgetCycles);
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_nvf4(kBM, kBN);
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
-            bool issued_any = false;
-            for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
-                if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, kWaitBudgetCycles)) {
+        const uint32_t idesc = idesc_nvf4(kBM, kBN);
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool issued_any = false;
+        for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
+            const bool ok = mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, kWaitBudgetCycles);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {
+                failed = true;
+                break;
+            }
+            acc_phase ^= 1u;
+            tc_fence_after();
+            for (int ks = 0; ks < num_ks; ++ks) {
+                const bool okf = mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetCycles);
+                if (!__all_sync(0xFFFFFFFFu, okf)) {
                     failed = true;
                     break;
                 }
-                acc_phase ^= 1u;
                 tc_fence_after();
-                for (int ks = 0; ks < num_ks; ++ks) {
-                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetCycles)) {
-                        failed = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
-                    const uint32_t st = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sf_col = tmem + kSfCol0 + kSfColsPerStage * stage;
-                    const uint64_t adesc = sdesc_k_swizzled<kSwizzleBytes>(st);
-                    const uint64_t bdesc = sdesc_k_swizzled<kSwizzleBytes>(st + kABytes);
-                    for (int j = 0; j < nk; ++j) {
-                        tc_cp_32x128b_warpx4(sf_col + 4 * j, sdesc_sf(st + kSfaOff + kSfAtomBytes * j));
-                        tc_cp_32x128b_warpx4(sf_col + 4 * kMmaPerStage + 8 * j,
-                                             sdesc_sf(st + kSfbOff + kSfAtomBytes * j));
-                        tc_cp_32x128b_warpx4(sf_col + 4 * kMmaPerStage + 8 * j + 4,
-                                             sdesc_sf(st + kSfbOff + kMmaPerStage * kSfAtomBytes + kSfAtomBytes * j));
-                        tc_mma_nvf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_col + 4 * j,
-                                    sf_col + 4 * kMmaPerStage + 8 * j,
-                                    (ks | j) != 0 ? 1u : 0u);
-                    }
-                    issued_any = true;
-                    tc_commit(&empty[stage]);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
+                const uint32_t st = smem_u32(smem + stage * kStageBytes);
+                const uint32_t sf_col = tmem + kSfCol0 + kSfColsPerStage * stage;
+                const uint64_t adesc = sdesc_k_swizzled<kSwizzleBytes>(st);
+                const uint64_t bdesc = sdesc_k_swizzled<kSwizzleBytes>(st + kABytes);
+#pragma unroll
+                for (int j = 0; j < kMmaPerStage; ++j) {
+                    if (j < nk) {
+                        tc_cp_32x128b_warpx4_elect(sf_col + 4 * j, sdesc_sf(st + kSfaOff + kSfAtomBytes * j));
+                        tc_cp_32x128b_warpx4_elect(sf_col + 4 * kMmaPerStage + 8 * j,
+                                                   sdesc_sf(st + kSfbOff + kSfAtomBytes * j));
+                        tc_cp_32x128b_warpx4_elect(
+                            sf_col + 4 * kMmaPerStage + 8 * j + 4,
+                            sdesc_sf(st + kSfbOff + kMmaPerStage * kSfAtomBytes + kSfAtomBytes * j));
+                        tc_mma_nvf4_elect(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_col + 4 * j,
+                                          sf_col + 4 * kMmaPerStage + 8 * j, (ks | j) != 0 ? 1u : 0u);
                     }
                 }
-                if (failed) break;
-                tc_commit(tmem_full);
+                issued_any = true;
+                tc_commit_elect(&empty[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            if (failed) {
-                set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
-                *abort_flag = 1;
-                if (issued_any) {   // wait for the MMAs already issued before TMEM is released
-                    tc_commit(drain);
-                    mbar_wait_bounded(drain, 0, nullptr, kWaitBudgetCycles);
-                }
+            if (failed) break;
+            tc_commit_elect(tmem_full);
+        }
+        if (failed) {
+            if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            if (issued_any) {   // wait for the MMAs already issued before TMEM is released
+                tc_commit_elect(drain);
+                mbar_wait_bounded(drain, 0, nullptr, kWaitBudgetCycles);
             }
         }
     } else {

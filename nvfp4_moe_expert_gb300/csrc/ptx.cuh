@@ -219,6 +219,66 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// ------------------------------------------------------------------ elected-lane issue
+// Variants for code that the whole warp executes in step: every lane runs the asm and
+// elect.sync picks one lane to issue the instruction.  Keeping the issuing loop
+// warp-uniform lets its operands live in uniform registers; issuing the same stream
+// of tcgen05 operations from one lane of a diverged warp is much slower.
+#define NVFP4_ELECT "{\n\t.reg .pred ep;\n\t.reg .b32 er;\n\telect.sync er|ep, 0xffffffff;\n\t@ep "
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, uint32_t bytes) {
+    asm volatile(NVFP4_ELECT "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_elect(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                  uint64_t policy) {
+    asm volatile(NVFP4_ELECT
+                 "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_elect(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                  int z, int w, uint64_t policy) {
+    asm volatile(NVFP4_ELECT
+                 "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;\n\t}" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w),
+                 "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_load_elect(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                uint64_t policy) {
+    asm volatile(NVFP4_ELECT
+                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;\n\t}" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_elect(uint32_t taddr, uint64_t sdesc) {
+    asm volatile(NVFP4_ELECT "tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_mma_nvf4_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred ep, acc;\n\t.reg .b32 er;\n\telect.sync er|ep, 0xffffffff;\n\t"
+        "setp.ne.b32 acc, %4, 0;\n\t"
+        "@ep tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], acc;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+// tcgen05.commit from the elected lane: it tracks the operations that lane issued, so the
+// same (deterministic) lane must have issued them through the _elect variants above.
+__device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
+    asm volatile(NVFP4_ELECT "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+#undef NVFP4_ELECT
+
 // ------------------------------------------------------------------ converts
 // Two FP32 -> packed E2M1 pair, round-to-nearest-even, saturating; `lo` goes to bits 0-3.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
