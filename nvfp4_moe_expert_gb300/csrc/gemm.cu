@@ -36,8 +36,9 @@
 //    half of the tile's columns.  They copy their accumulator columns to
 //    registers and release TMEM at once, so the next tile's MMAs run while
 //    they apply the FP32 scales (staged in shared memory per tile), BF16
-//    casts and the fused SwiGLU x prob, then write rows through a per-warp
-//    shared-memory transpose as whole 128-byte lines.
+//    casts and the fused SwiGLU x prob; FC1 lanes write their own h rows
+//    with 32-byte stores, FC2 rows (scattered to (token, slot) places) go
+//    through a per-warp shared-memory transpose as whole 128-byte lines.
 //  Every row's arithmetic is the same whatever tile, expert or batch it is
 //  in: one tile shape, no split-K, K always walked 0..K-1 in 64-wide steps.
 //  All waits are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
@@ -73,7 +74,7 @@ constexpr int kSfbOff = kSfaOff + kMmaPerStage * kSfAtomBytes;   // 2 x kMmaPerS
 constexpr int kStageBytes = kSfbOff + 2 * kMmaPerStage * kSfAtomBytes;
 static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 constexpr int kStagePitch = 144;                      // 128 B of BF16 per row + 16 B pad (no bank conflicts)
-constexpr int kStageWarpBytes = 32 * kStagePitch;     // one warp's 32 rows
+constexpr int kStageWarpBytes = 32 * kStagePitch;     // one warp's 32 rows (FC2 output transpose)
 constexpr int kEpiStageOff = kStages * kStageBytes;
 constexpr int kScaleOff = kEpiStageOff + kEpiWarps * kStageWarpBytes;   // 128 floats per epilogue warp
 constexpr int kOffsetsOff = kScaleOff + kEpiWarps * 128 * 4;             // expert offsets, up to 1025 ints
@@ -137,7 +138,22 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
     return r;
 }
 
-// The warp's 32 rows x 64 BF16 columns (packed[lane][0..31]) staged through shared
+// FC1 output: 64 BF16 values (packed[0..31], column pairs) of this lane's row at dst
+// (32-byte aligned) as four 32-byte stores: each lane owns one row, so every store is
+// a whole 32-byte sector and needs no exchange between lanes.  (FC2's rows go to
+// scattered (token, slot) places, where whole 128-byte lines through
+// store_rows_64 write faster.)
+__device__ __forceinline__ void store_row_64(uint16_t* dst, const uint32_t (&packed)[32]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * k),
+                     "r"(packed[8 * k]), "r"(packed[8 * k + 1]), "r"(packed[8 * k + 2]), "r"(packed[8 * k + 3]),
+                     "r"(packed[8 * k + 4]), "r"(packed[8 * k + 5]), "r"(packed[8 * k + 6]), "r"(packed[8 * k + 7])
+                     : "memory");
+    }
+}
+
+// FC2 output: the warp's 32 rows x 64 BF16 columns (packed[lane][0..31]) staged through shared
 // memory and written as 8 rows x 128 B per store instruction (32 bytes per lane).  dst_row(r) gives
 // the global address of row r's 64-column chunk, or nullptr to skip the row.
 template <typename RowPtr>
@@ -351,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                              // TMEM lane quarter of this warp
         const int half = ew >> 2;                            // which half of the tile's columns
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        uint8_t* stage_buf = smem + kEpiStageOff + ew * kStageWarpBytes;
         float* sc = scale_buf + ew * 128;                    // this warp's 128 column scales
+        uint8_t* stage_buf = smem + kEpiStageOff + ew * kStageWarpBytes;
         uint32_t acc_phase = 0;
         // this tile's row data and the weight scales of this warp's 128 columns
         // (FC1: 64 gate then 64 up) are loaded one tile ahead, so their latency
@@ -453,12 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float hmax = __uint_as_float((bf16x2_max(hmax2, hmax2 >> 16) & 0xFFFFu) << 16);
                 if (live) atomicMax(args.amax2 + row, __float_as_uint(hmax));
-                const int64_t row0 = static_cast<int64_t>(mt) * kBM + q * 32;
-                uint16_t* hbase = args.h + nt * 128 + 64 * half;
-                store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
-                    const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
-                    return pr >= 0 ? hbase + (row0 + r) * I : nullptr;
-                });
+                if (live) store_row_64(args.h + row * I + nt * 128 + 64 * half, packed);
             } else {
                 const int H = args.H;
                 const float* sw = sc;
