@@ -330,6 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sf_col = tmem + kSfCol0 + kSfColsPerStage * stage;
                 const uint64_t adesc = sdesc_k_swizzled<kSwizzleBytes>(st);
                 const uint64_t bdesc = sdesc_k_swizzled<kSwizzleBytes>(st + kABytes);
+                if (kMmaPerStage == 4 && nk == 4) {   // a full stage: one issue block
+                    tc_stage4_nvf4_elect(tmem, adesc, bdesc, idesc, sdesc_sf(st + kSfaOff), sdesc_sf(st + kSfbOff),
+                                         sdesc_sf(st + kSfbOff + kMmaPerStage * kSfAtomBytes), sf_col, ks != 0 ? 1u : 0u);
+                } else {
 #pragma unroll
                 for (int j = 0; j < kMmaPerStage; ++j) {
                     if (j < nk) {
@@ -342,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_nvf4_elect(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_col + 4 * j,
                                           sf_col + 4 * kMmaPerStage + 8 * j, (ks | j) != 0 ? 1u : 0u);
                     }
+                }
                 }
                 issued_any = true;
                 tc_commit_elect(&empty[stage]);

@@ -277,6 +277,55 @@ __device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
                      smem_u32(bar))
                  : "memory");
 }
+// One full stage of the block-scaled main loop from the elected lane: for j = 0..3,
+// copy the A scales (512-byte tile at sfa + 512 j) to TMEM column sf_col + 4 j, the two
+// B scale tiles (sfb0/sfb1 + 512 j) to sf_col + 16 + 8 j and + 4, then
+// D += A[k 64j..] x B[k 64j..] with those scales; `acc0` = accumulate for j = 0 (the
+// later MMAs of the stage always accumulate).  Descriptor start fields advance by
+// 512 B (32 units of 16 B) per scale tile and 32 B (2 units) per K=64 step.
+__device__ __forceinline__ void tc_stage4_nvf4_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                     uint64_t sfa, uint64_t sfb0, uint64_t sfb1, uint32_t sf_col,
+                                                     uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred ep, p0, p1;\n\t.reg .b32 er, ca, cb0, cb1;\n\t.reg .b64 a, b, s0, s1, s2;\n\t"
+        "elect.sync er|ep, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %8, 0;\n\t"
+        "setp.eq.b32 p1, %8, %8;\n\t"
+        // j = 0
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [%7], %4;\n\t"
+        "add.u32 cb0, %7, 16;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [cb0], %5;\n\t"
+        "add.u32 cb1, %7, 20;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [cb1], %6;\n\t"
+        "@ep tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%7], [cb0], p0;\n\t"
+        // j = 1
+        "add.u32 ca, %7, 4;\n\t add.u32 cb0, %7, 24;\n\t add.u32 cb1, %7, 28;\n\t"
+        "add.s64 s0, %4, 32;\n\t add.s64 s1, %5, 32;\n\t add.s64 s2, %6, 32;\n\t"
+        "add.s64 a, %1, 2;\n\t add.s64 b, %2, 2;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [ca], s0;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [cb0], s1;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [cb1], s2;\n\t"
+        "@ep tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a, b, %3, [ca], [cb0], p1;\n\t"
+        // j = 2
+        "add.u32 ca, %7, 8;\n\t add.u32 cb0, %7, 32;\n\t add.u32 cb1, %7, 36;\n\t"
+        "add.s64 s0, %4, 64;\n\t add.s64 s1, %5, 64;\n\t add.s64 s2, %6, 64;\n\t"
+        "add.s64 a, %1, 4;\n\t add.s64 b, %2, 4;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [ca], s0;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [cb0], s1;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [cb1], s2;\n\t"
+        "@ep tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a, b, %3, [ca], [cb0], p1;\n\t"
+        // j = 3
+        "add.u32 ca, %7, 12;\n\t add.u32 cb0, %7, 40;\n\t add.u32 cb1, %7, 44;\n\t"
+        "add.s64 s0, %4, 96;\n\t add.s64 s1, %5, 96;\n\t add.s64 s2, %6, 96;\n\t"
+        "add.s64 a, %1, 6;\n\t add.s64 b, %2, 6;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [ca], s0;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [cb0], s1;\n\t"
+        "@ep tcgen05.cp.cta_group::1.32x128b.warpx4 [cb1], s2;\n\t"
+        "@ep tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a, b, %3, [ca], [cb0], p1;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "l"(sfa), "l"(sfb0), "l"(sfb1), "r"(sf_col), "r"(acc0)
+        : "memory");
+}
 #undef NVFP4_ELECT
 
 // ------------------------------------------------------------------ converts

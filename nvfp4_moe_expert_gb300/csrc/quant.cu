@@ -108,12 +108,17 @@ __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
     return x;
 }
 
-// div_markstein on both lanes of an f32x2 pair: rc2 = (rc, rc), nd2 = (-d, -d).
-__device__ __forceinline__ void div_markstein_x2(uint64_t x, uint64_t rc2, uint64_t nd2, float& lo, float& hi) {
+// RN(x / d) on both lanes of an f32x2 pair by Markstein's step, written in terms of
+// nx = -x and nrc = (-rc, -rc), d2 = (d, d):
+//   q0 = RN(nx * nrc) = RN(x * rc),  r' = q0*d + nx = -(x - q0*d) exactly,
+//   q = RN(r' * nrc + q0) = RN(q0 + (x - q0*d) * rc),
+// the same values as the usual form.  For x = +-0 this form also returns the zero with
+// x's sign (the usual form turns x = -0 into +0), so the code's sign bit needs no fix-up.
+__device__ __forceinline__ void div_markstein_neg_x2(uint64_t nx, uint64_t nrc2, uint64_t d2, float& lo, float& hi) {
     uint64_t q0, r, q;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x), "l"(rc2));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(nd2), "l"(x));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(rc2), "l"(q0));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(nx), "l"(nrc2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(d2), "l"(nx));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(nrc2), "l"(q0));
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(q));
 }
 
@@ -140,19 +145,16 @@ __device__ __forceinline__ uint32_t codes8(const uint4& v, float d, float rc, bo
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float q[8];
     if (markstein) {
-        const uint64_t rc2 = f32x2_splat(rc), nd2 = f32x2_splat(-d);
+        const uint64_t nrc2 = f32x2_splat(-rc), d2 = f32x2_splat(d);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) div_markstein_x2(bf16x2_to_f32x2(w[j]), rc2, nd2, q[2 * j], q[2 * j + 1]);
+        for (int j = 0; j < 4; ++j)
+            div_markstein_neg_x2(bf16x2_to_f32x2(w[j] ^ 0x80008000u), nrc2, d2, q[2 * j], q[2 * j + 1]);
     } else {
-        quotients_fdiv(w, d, q);
+        quotients_fdiv(w, d, q);   // IEEE division keeps the sign of a zero quotient
     }
-    // The sign bit of every code is the sign of x.  The conversion keeps the sign of
-    // the quotient (also of a zero), but for x = -0.0 the Markstein correction returns
-    // +0 (its residual (-0)(-d) + (-0) is +0), so x's sign bits are ORed in: byte 1 of
-    // w[j] carries element 2j's sign in bit 7, byte 3 element 2j+1's.
-    const uint32_t t01 = __byte_perm(w[0], w[1], 0x7531), t23 = __byte_perm(w[2], w[3], 0x7531);
-    const uint32_t even = __byte_perm(t01, t23, 0x6420), odd = __byte_perm(t01, t23, 0x7531);
-    return e2m1x8(q) | ((even >> 4) & 0x08080808u) | (odd & 0x80808080u);
+    // The conversion keeps the quotient's sign, also of a zero (-0.0 and tiny negatives
+    // give code 8), and every quotient above carries x's sign: the code's sign is x's.
+    return e2m1x8(q);
 }
 
 // Quantised form of one 64-element group.
