@@ -90,7 +90,7 @@ size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
  *
  *  x_dev      BF16 [rows][ld], 16-byte aligned, ld % 8 == 0, ld >= cols
  *  rows       >= 0;  cols % 64 == 0, 64 <= cols <= 8192
- *  codes_dev  uint8 [nvfp4_rows_padded(rows)][cols/2], 16-byte aligned
+ *  codes_dev  uint8 [nvfp4_rows_padded(rows)][cols/2], 32-byte aligned
  *  sf_dev     nvfp4_sf_bytes(rows, cols) bytes, 16-byte aligned
  *  g_dev      float [rows]
  * The rows between rows and rows_pad get zero codes and zero scales.

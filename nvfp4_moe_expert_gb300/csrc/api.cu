@@ -210,7 +210,7 @@ nvfp4_status nvfp4_quantize_rows(const void* x_dev, int64_t rows, int64_t cols, 
     if (rows < 0 || cols < 64 || cols > 8192 || cols % 64 || ld < cols || ld % 8) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0) return NVFP4_OK;
     if (!x_dev || !codes_dev || !sf_dev || !g_dev) return NVFP4_ERR_INVALID_ARG;
-    if (!aligned(x_dev, 16) || !aligned(codes_dev, 16) || !aligned(sf_dev, 16) || !aligned(g_dev, 4))
+    if (!aligned(x_dev, 16) || !aligned(codes_dev, 32) || !aligned(sf_dev, 16) || !aligned(g_dev, 4))
         return NVFP4_ERR_INVALID_ARG;
     int* err = device_error_ptr();
     if (!err) return NVFP4_ERR_CUDA;

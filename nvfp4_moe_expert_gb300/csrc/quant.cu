@@ -193,11 +193,14 @@ __device__ __forceinline__ void load_group(const uint16_t* src, uint4 (&v)[8]) {
     for (int i = 0; i < 8; ++i) v[i] = __ldg(s + i);
 }
 
+// The group's 32 bytes of codes go out in one 32-byte store (a whole sector: fewer,
+// fuller L2 write transactions than two 16-byte halves), its scale word in one 4-byte store.
 __device__ __forceinline__ void store_group(const GroupQ& q, int64_t r, int grp, int cols, uint8_t* codes,
                                             uint8_t* sf) {
-    uint4* c = reinterpret_cast<uint4*>(codes + r * static_cast<int64_t>(cols / 2) + grp * 32);
-    c[0] = make_uint4(q.code[0], q.code[1], q.code[2], q.code[3]);
-    c[1] = make_uint4(q.code[4], q.code[5], q.code[6], q.code[7]);
+    uint8_t* c = codes + r * static_cast<int64_t>(cols / 2) + grp * 32;
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(c), "r"(q.code[0]), "r"(q.code[1]),
+                 "r"(q.code[2]), "r"(q.code[3]), "r"(q.code[4]), "r"(q.code[5]), "r"(q.code[6]), "r"(q.code[7])
+                 : "memory");
     *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, cols)) = q.sfw;
 }
 

@@ -98,6 +98,8 @@ def test_quantize_rows_validation(lib):
     # null / misaligned pointers
     assert lib.nvfp4_quantize_rows(None, 4, 128, 128, p, p, p, None) == 1
     assert lib.nvfp4_quantize_rows(ctypes.c_void_p(258), 4, 128, 128, p, p, p, None) == 1
+    # codes are written with 32-byte stores: a 16- but not 32-byte aligned buffer is refused
+    assert lib.nvfp4_quantize_rows(p, 4, 128, 128, ctypes.c_void_p(272), p, p, None) == 1
     # zero rows is a no-op
     assert lib.nvfp4_quantize_rows(None, 0, 128, 128, None, None, None, None) == 0
 
