@@ -17,7 +17,9 @@ of the same shapes stand in for them):
   tokens, Zipf routing, 1% outlier channels, weights N(0, 0.015)
 
 Recipe: numpy PCG64; sub-streams seed+0 (X), +1 (W1), +2 (W2), +3 (router
-logits), +4 (outlier channels), +5 (sequence lengths).  Values are drawn in
+logits), +4 (outlier channels), +5 (sequence lengths), +6 (router weights for
+the router step, W_r ~ N(0, 1/H) so that logits of N(0,1) inputs are about
+N(0,1)).  Values are drawn in
 float32 and rounded to BF16 (round-to-nearest-even on the bit pattern).
 Routing: softmax over experts in FP64, top-k by (probability descending,
 expert id ascending), probabilities renormalised over the k chosen experts in
@@ -121,6 +123,13 @@ def make_routing(cfg, T=None, stream=0):
     top = np.take_along_axis(probs, order, axis=1)
     top = top / top.sum(axis=1, keepdims=True)
     return order.astype(np.int32), top.astype(np.float32)
+
+
+def make_router_weights(cfg):
+    """BF16 router weights W_r [E, H] as uint16 bits, N(0, 1/H) (rows = experts)."""
+    rng = _rng(cfg.seed, 6)
+    w = rng.standard_normal((cfg.E, cfg.H), dtype=np.float32) * np.float32(1.0 / np.sqrt(cfg.H))
+    return f32_to_bf16_bits(w)
 
 
 def make_layer(cfg, T=None, experts=None):

@@ -21,7 +21,9 @@ The oracle is a slow, literal restatement of what the source pages define:
   agent-driven" (spke.com/ko/ai/article/3192), section 4.4 "Expert GEMM: two
   layouts, same row result": SiLU(gate)*up in FP32 with one rounding of the
   product; section 4.5 "Cross-GPU reduction": the expert outputs are summed in
-  FP32 in top-k slot order.
+  FP32 in top-k slot order; sections 2 and 4.1 (router step, ``router.py``):
+  one FP32-output router GEMM for every batch size and a top-k whose ties and
+  order are fixed.
 
 Floating point: FP64 where the contract does not fix the precision (GEMM
 accumulation, SiLU), IEEE FP32 (numpy float32, correctly rounded, no FMA
@@ -43,6 +45,7 @@ from .formats import (  # noqa: F401
 from .quant import (  # noqa: F401
     quantize_rows, dequantize_rows, pack_nibbles, unpack_nibbles, OUTER_DIVISOR,
 )
+from .router import router_logits_f64, topk_order, topk_probs, router_topk  # noqa: F401
 from .moe import (  # noqa: F401
     route_sort,
     qgemm_f64,
