@@ -262,6 +262,27 @@ nvfp4_status moe_fc2_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
 nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev,
                               void* ws_dev, size_t ws_bytes, void* stream);
 
+/* moe_router_topk -- the router step that produces the inputs of
+ * moe_route_sort_amax: logits[t, e] = sum_h x[t, h] * W_r[e, h] (BF16 inputs, FP32
+ * tensor-core accumulation, K walked in one fixed order, so a token's logits, ids and
+ * probabilities do not depend on T or on the other tokens), then the k largest logits
+ * (larger first, lower expert id first on equal logits) and their probabilities, the
+ * softmax over all experts renormalised over the k chosen (computed as the softmax of the
+ * chosen, p_j = exp(l_j - l_1) / sum_i exp(l_i - l_1), FP32, sum in slot order).
+ * ("Finishing RL training faster: bitwise consistency, high performance, agent-driven",
+ * section 4.1 "Dense GEMM": one FP32-output router GEMM for every batch size; section 2:
+ * top-k ties and order fixed.)
+ *  x_dev           BF16 [T][H], 16-byte aligned; H % 64 == 0
+ *  w_router_dev    BF16 [E][H] (row e = expert e), 16-byte aligned; E % 16 == 0, 16 <= E <= 256
+ *  k               1 <= k <= min(E, 32)
+ *  topk_ids_dev    int32 [T][k] out, slot order; 4-byte aligned
+ *  topk_w_dev      float [T][k] out, 4-byte aligned
+ *  logits_dev      float [T][E] out, 32-byte aligned, or NULL
+ * The caller owns every buffer; nothing is allocated.  Non-finite logits are recorded as
+ * NVFP4_ERR_NONFINITE (nvfp4_get_device_error). */
+nvfp4_status moe_router_topk(const void* x_dev, int64_t T, int H, const void* w_router_dev, int E, int k,
+                             int32_t* topk_ids_dev, float* topk_w_dev, float* logits_dev, void* stream);
+
 /* Synchronise `stream`, then report and clear this device's error word:
  * *device_status receives NVFP4_OK or the first device error recorded since
  * the last call.  Returns NVFP4_ERR_CUDA if the synchronisation failed. */

@@ -69,6 +69,7 @@ _SIGNATURES = {
     "moe_combine_bf16": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
     "nvfp4_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_int)]),
     "moe_route_sort_amax_noalloc": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_router_topk": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -213,6 +214,23 @@ def moe_route_sort_amax_noalloc(x, topk_ids, topk_w, E, expert_offsets, out, str
     _check("moe_route_sort_amax_noalloc", lib().moe_route_sort_amax_noalloc(
         _ptr(x), T, H, E, k, _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets), _ptr(out),
         out.numel(), _stream(stream)))
+
+
+def moe_router_topk(x, w_router, k, with_logits=False, stream=None):
+    """Router step: (topk_ids int32 [T, k], topk_w float32 [T, k], logits float32 [T, E] or None)
+    of BF16 activations x [T, H] and BF16 router weights w_router [E, H]."""
+    _need_cuda(x, w_router)
+    if x.dtype != torch.bfloat16 or w_router.dtype != torch.bfloat16:
+        raise ValueError("x and w_router must be bf16")
+    T, H = x.shape
+    E = w_router.shape[0]
+    ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    logits = torch.empty((T, E), dtype=torch.float32, device=x.device) if with_logits else None
+    _check("moe_router_topk", lib().moe_router_topk(
+        _ptr(x), T, H, _ptr(w_router), E, k, _ptr(ids), _ptr(w),
+        _ptr(logits) if logits is not None else None, _stream(stream)))
+    return ids, w, logits
 
 
 def moe_expert_forward_nvfp4(weights, T, k, expert_offsets, out, ws, stream=None):

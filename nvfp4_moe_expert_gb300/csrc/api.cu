@@ -354,6 +354,23 @@ nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int
     return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, true);
 }
 
+nvfp4_status moe_router_topk(const void* x_dev, int64_t T, int H, const void* w_router_dev, int E, int k,
+                             int32_t* topk_ids_dev, float* topk_w_dev, float* logits_dev, void* stream) {
+    if (T < 0 || H <= 0 || H % 64 != 0 || H > (1 << 20) || E < 16 || E > 256 || E % 16 != 0 || k < 1 || k > E ||
+        k > 32)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return NVFP4_OK;
+    if (!x_dev || !w_router_dev || !topk_ids_dev || !topk_w_dev) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x_dev, 16) || !aligned(w_router_dev, 16) || !aligned(topk_ids_dev, 4) || !aligned(topk_w_dev, 4) ||
+        (logits_dev && !aligned(logits_dev, 32)))
+        return NVFP4_ERR_INVALID_ARG;
+    int* err = device_error_ptr();
+    if (!err) return NVFP4_ERR_CUDA;
+    return from_cuda(launch_router_topk(static_cast<const uint16_t*>(x_dev), T, H,
+                                        static_cast<const uint16_t*>(w_router_dev), E, k, topk_ids_dev, topk_w_dev,
+                                        logits_dev, err, static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_get_device_error(void* stream, int* device_status) {
     if (!device_status) return NVFP4_ERR_INVALID_ARG;
     *device_status = NVFP4_OK;

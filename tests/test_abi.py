@@ -104,6 +104,18 @@ def test_quantize_rows_validation(lib):
     assert lib.nvfp4_quantize_rows(None, 0, 128, 128, None, None, None, None) == 0
 
 
+def test_router_validation(lib):
+    p = ctypes.c_void_p(4096)
+    ok = lambda T, H, E, k, x=p, w=p, ids=p, pw=p, lg=None: lib.moe_router_topk(x, T, H, w, E, k, ids, pw, lg, None)
+    assert ok(0, 256, 16, 4) == 0                         # nothing to do, nothing launched
+    assert ok(8, 250, 16, 4) == 2                         # H % 64
+    assert ok(8, 256, 8, 4) == 2 and ok(8, 256, 24, 4) == 2 and ok(8, 256, 272, 4) == 2   # E
+    assert ok(8, 256, 16, 0) == 2 and ok(8, 256, 16, 17) == 2 and ok(8, 256, 64, 33) == 2  # k
+    assert ok(8, 256, 16, 4, x=None) == 1
+    assert ok(8, 256, 16, 4, x=ctypes.c_void_p(4104)) == 1              # 8-byte aligned x
+    assert ok(8, 256, 16, 4, lg=ctypes.c_void_p(4112)) == 1             # logits need 32 bytes
+
+
 def test_route_validation(lib):
     p = ctypes.c_void_p(4096)
     ok_ws = M.moe_workspace_layout_query(16, 256, 128, 8, 2).route_end
