@@ -391,6 +391,38 @@ def run_ours(args, cfg, rank, world, local_rank):
     roof = dict(kernels[dominant])
     roof["peak_note"] = "of " + peak_kind
 
+    # ---- router step (produces the step's routing; timed on its own, not part of the step)
+    router = None
+    if cfg.E % 16 == 0 and 16 <= cfg.E <= 256 and cfg.H % 64 == 0:
+        wr = to_dev(S.make_router_weights(cfg))
+        M.moe_router_topk(x, wr, k)
+        rev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_attr)]
+        for i in range(n_attr):
+            rev[i][0].record(stream)
+            M.moe_router_topk(x, wr, k)
+            rev[i][1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        r_ms = statistics.mean(a.elapsed_time(b) for a, b in rev)
+        r_bytes = T * H * 2 + E * H * 2 + T * k * 8
+        r_flops = 2 * T * H * E
+        bf16 = float(peaks["bf16_tflops"])
+        hbm = float(peaks["hbm_gbs"])
+        if r_flops / (bf16 * 1e12) > r_bytes / (hbm * 1e9):
+            ach = r_flops / (r_ms * 1e-3) / 1e12
+            router = {"bound": "tensor", "achieved": round(ach, 2), "peak": bf16, "unit": "TFLOP/s",
+                      "frac": round(ach / bf16, 4)}
+        else:
+            ach = r_bytes / (r_ms * 1e-3) / 1e9
+            router = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                      "frac": round(ach / hbm, 4)}
+        router |= {"ms": round(r_ms, 4), "algorithmic": f"{r_bytes:.4g} bytes, {r_flops:.4g} FLOP per launch",
+                   "peak_note": "of " + peak_kind,
+                   "note": "moe_router_topk: BF16 router GEMM + top-k + softmax over the chosen, "
+                           "T x E logits; timed on its own (the step takes routing as an input)"}
+        if M.nvfp4_get_device_error() != 0:
+            raise RuntimeError("device error in the router step")
+
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region.
     # A serving loop: every step copies its own inputs in and its output back, on two copy
     # streams, with device buffers double-buffered so that step i's copies overlap the compute of
@@ -462,6 +494,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "roofline": roof,
         "kernels": kernels,
         "weight_quant_ms": round(wq_ms, 3),
+        "router_step": router,
         "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "every step copies its pinned host X/ids/probs in and its output out; two copy "
