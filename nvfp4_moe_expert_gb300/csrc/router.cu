@@ -16,8 +16,8 @@
 // through TMA (128 bytes of K per row per stage, 128B swizzle, 4-stage ring); warp 1 issues
 // tcgen05.mma.kind::f16 (M=128, N=E, K=16) into an FP32 TMEM accumulator, walking K from 0 to
 // H-1 in one fixed order whatever T is; warps 2-5, one token per thread, copy the token's E
-// logits from TMEM into the (then idle) stage buffers, select the top k in k passes and write
-// ids and probabilities.  All waits are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
+// logits from TMEM into registers (E <= 128) or into the (then idle) stage buffers, select the
+// top k in k passes and write ids and probabilities.  All waits are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
 #include <cmath>
 #include <mutex>
 
@@ -41,7 +41,9 @@ constexpr uint32_t kRTmemCols = 256;
 // epilogue staging in the stage buffers: 128 rows of E logits (stride E+1 floats: no bank
 // conflicts when the threads read one column), then 128 rows of 32 selected ids
 constexpr int kRIdsOff = kRBM * (kRMaxE + 1) * 4;
-static_assert(kRIdsOff + kRBM * 32 * 4 <= kRBarOff, "epilogue staging fits in the stage buffers");
+constexpr int kRSelVOff = kRIdsOff + kRBM * 32 * 4;      // then 128 rows of 32 selected logits
+static_assert(kRSelVOff + kRBM * 32 * 4 <= kRBarOff, "epilogue staging fits in the stage buffers");
+constexpr int kRRegE = 128;                               // up to this many experts: logits in registers
 
 // (va, ia) comes before (vb, ib) in the selection order
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
@@ -167,19 +169,17 @@ __global__ void __launch_bounds__(kRThreads, 1)
         } else {
             tc_fence_after();
             // every MMA has completed, so no copy or MMA touches the stage buffers any more
-            float* row = reinterpret_cast<float*>(smem) + r * (kRMaxE + 1);
             int32_t* sel = reinterpret_cast<int32_t*>(smem + kRIdsOff) + r * 32;
+            float* selv = reinterpret_cast<float*>(smem + kRSelVOff) + r * 32;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
             bool finite = true;
-            for (int c = 0; c < E; c += 16) {           // E % 16 == 0: every column read is a logit
-                uint32_t v[16];
+            // one 16-column chunk of the token's logits from TMEM (E % 16 == 0: every column
+            // read is a logit), optionally stored to the logits output
+            auto load16 = [&](int c, uint32_t (&v)[16]) {
                 tmem_ld_32x32b_x16(taddr + c, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    row[c + i] = __uint_as_float(v[i]);
-                    finite = finite && (v[i] & 0x7F800000u) != 0x7F800000u;
-                }
+                for (int i = 0; i < 16; ++i) finite = finite && (v[i] & 0x7F800000u) != 0x7F800000u;
                 if (logits != nullptr && t < T) {
                     float* dst = logits + t * E + c;    // 64-byte aligned (E % 16 == 0, base 32-aligned)
 #pragma unroll
@@ -190,54 +190,108 @@ __global__ void __launch_bounds__(kRThreads, 1)
                                      : "memory");
                     }
                 }
+            };
+            // k passes; each takes the first entry (in selection order) after the previous
+            // pick, scanning in eight independent chains (columns e = 8m + u) merged at the
+            // end: the same pick as one chain over all columns, with 8x shorter dependencies
+            auto merge = [&](const float (&bv)[8], const int (&bid)[8], float& best_v, int& best_id) {
+                best_v = bv[0];
+                best_id = bid[0];
+#pragma unroll
+                for (int u = 1; u < 8; ++u) {
+                    if (bid[u] >= 0 && (best_id < 0 || before(bv[u], bid[u], best_v, best_id))) {
+                        best_v = bv[u];
+                        best_id = bid[u];
+                    }
+                }
+            };
+            if (E <= kRRegE) {
+                // logits in registers (E <= 128)
+                float lv[kRRegE];
+#pragma unroll
+                for (int c = 0; c < kRRegE / 16; ++c) {
+                    if (16 * c < E) {
+                        uint32_t v[16];
+                        load16(16 * c, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) lv[16 * c + i] = __uint_as_float(v[i]);
+                    }
+                }
+                if (t < T) {
+                    float pv = INFINITY;
+                    int pid = -1;
+                    for (int j = 0; j < k; ++j) {
+                        float bv[8];
+                        int bid[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            bv[u] = -INFINITY;
+                            bid[u] = -1;
+                        }
+#pragma unroll
+                        for (int e = 0; e < kRRegE; ++e) {
+                            if (e < E) {
+                                const int u = e & 7;
+                                const float v = lv[e];
+                                const bool after = v < pv || (v == pv && e > pid);
+                                if (after && (bid[u] < 0 || before(v, e, bv[u], bid[u]))) {
+                                    bv[u] = v;
+                                    bid[u] = e;
+                                }
+                            }
+                        }
+                        merge(bv, bid, pv, pid);
+                        sel[j] = pid;
+                        selv[j] = pv;
+                    }
+                }
+            } else {
+                // logits staged in shared memory (rows of stride E+1 floats: no bank conflicts)
+                float* row = reinterpret_cast<float*>(smem) + r * (kRMaxE + 1);
+                for (int c = 0; c < E; c += 16) {
+                    uint32_t v[16];
+                    load16(c, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) row[c + i] = __uint_as_float(v[i]);
+                }
+                if (t < T) {
+                    float pv = INFINITY;
+                    int pid = -1;
+                    for (int j = 0; j < k; ++j) {
+                        float bv[8];
+                        int bid[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            bv[u] = -INFINITY;
+                            bid[u] = -1;
+                        }
+                        for (int e0 = 0; e0 < E; e0 += 8) {   // E % 16 == 0
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const int e = e0 + u;
+                                const float v = row[e];
+                                const bool after = v < pv || (v == pv && e > pid);
+                                if (after && (bid[u] < 0 || before(v, e, bv[u], bid[u]))) {
+                                    bv[u] = v;
+                                    bid[u] = e;
+                                }
+                            }
+                        }
+                        merge(bv, bid, pv, pid);
+                        sel[j] = pid;
+                        selv[j] = pv;
+                    }
+                }
             }
             if (t < T) {
                 if (!finite) set_device_error(err, NVFP4_ERR_NONFINITE);
-                // k passes: each takes the first entry (in selection order) after the previous pick
-                float pv = INFINITY;
-                int pid = -1;
-                for (int j = 0; j < k; ++j) {
-                    // eight independent chains (columns e = 8m + u), merged at the end: the
-                    // same pick as one chain over all columns, with 8x shorter dependencies
-                    float bv[8];
-                    int bid[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        bv[u] = -INFINITY;
-                        bid[u] = -1;
-                    }
-                    for (int e0 = 0; e0 < E; e0 += 8) {   // E % 16 == 0
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int e = e0 + u;
-                            const float v = row[e];
-                            const bool after = v < pv || (v == pv && e > pid);
-                            if (after && (bid[u] < 0 || before(v, e, bv[u], bid[u]))) {
-                                bv[u] = v;
-                                bid[u] = e;
-                            }
-                        }
-                    }
-                    float best_v = bv[0];
-                    int best_id = bid[0];
-#pragma unroll
-                    for (int u = 1; u < 8; ++u) {
-                        if (bid[u] >= 0 && (best_id < 0 || before(bv[u], bid[u], best_v, best_id))) {
-                            best_v = bv[u];
-                            best_id = bid[u];
-                        }
-                    }
-                    sel[j] = best_id;
-                    pv = best_v;
-                    pid = best_id;
-                }
-                const float l1 = row[sel[0] < 0 ? 0 : sel[0]];
+                const float l1 = sel[0] < 0 ? 0.0f : selv[0];
                 float sum = 0.0f;
-                for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, expf(__fsub_rn(row[sel[j] < 0 ? 0 : sel[j]], l1)));
+                for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, sel[j] < 0 ? 0.0f : expf(__fsub_rn(selv[j], l1)));
                 for (int j = 0; j < k; ++j) {
                     const int id = sel[j];
                     ids[t * k + j] = id < 0 ? 0 : id;
-                    probs[t * k + j] = id < 0 ? 0.0f : __fdiv_rn(expf(__fsub_rn(row[id], l1)), sum);
+                    probs[t * k + j] = id < 0 ? 0.0f : __fdiv_rn(expf(__fsub_rn(selv[j], l1)), sum);
                 }
             }
         }
