@@ -179,6 +179,12 @@ int device_sm_count() {
 
 using namespace nvfp4;
 
+namespace nvfp4 {
+// defined in router.cu
+cudaError_t launch_router_topk(const uint16_t* x, int64_t T, int H, const uint16_t* w, int E, int k, int32_t* ids,
+                               float* probs, float* logits, int* err, cudaStream_t st);
+}  // namespace nvfp4
+
 extern "C" {
 
 const char* nvfp4_status_string(int status) {

@@ -118,9 +118,6 @@ cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st, bool pdl);
 
 cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st, bool pdl);
 
-cudaError_t launch_router_topk(const uint16_t* x, int64_t T, int H, const uint16_t* w, int E, int k, int32_t* ids,
-                               float* probs, float* logits, int* err, cudaStream_t st);
-
 int device_sm_count();
 
 // Device address of this device's error word (nullptr if it cannot be looked up).

@@ -210,14 +210,6 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
     d |= static_cast<uint64_t>(1) << 46;
     return d;
 }
-// Instruction descriptor of kind::f16 with BF16 A and B (both K-major) and an FP32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4)                                  // D format: F32
-           | (1u << 7)                                // A format: BF16
-           | (1u << 10)                               // B format: BF16
-           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
-           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
-}
 // Instruction descriptor of kind::mxf4nvf4: A and B E2M1, K-major, UE4M3 scales.
 __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
     return (1u << 7)                                  // A format: E2M1
@@ -285,18 +277,6 @@ __device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
                      smem_u32(bar))
                  : "memory");
 }
-// D(tmem, FP32) (+)= A(smem, BF16) x B(smem, BF16)^T, M=128, N from idesc, K=16, from the
-// elected lane.  A and B are both BF16 (kind::f16 takes one type for both operands).
-__device__ __forceinline__ void tc_mma_bf16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                                  uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred ep, acc;\n\t.reg .b32 er;\n\telect.sync er|ep, 0xffffffff;\n\t"
-        "setp.ne.b32 acc, %4, 0;\n\t"
-        "@ep tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, acc;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // One full stage of the block-scaled main loop from the elected lane: for j = 0..3,
 // copy the A scales (512-byte tile at sfa + 512 j) to TMEM column sf_col + 4 j, the two
 // B scale tiles (sfb0/sfb1 + 512 j) to sf_col + 16 + 8 j and + 4, then

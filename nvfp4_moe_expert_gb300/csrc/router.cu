@@ -45,6 +45,29 @@ constexpr int kRSelVOff = kRIdsOff + kRBM * 32 * 4;      // then 128 rows of 32 
 static_assert(kRSelVOff + kRBM * 32 * 4 <= kRBarOff, "epilogue staging fits in the stage buffers");
 constexpr int kRRegE = 128;                               // up to this many experts: logits in registers
 
+// Instruction descriptor of tcgen05.mma kind::f16 with BF16 A and B (both K-major) and an FP32
+// accumulator.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4)                                  // D format: F32
+           | (1u << 7)                                // A format: BF16
+           | (1u << 10)                               // B format: BF16
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// D(tmem, FP32) (+)= A(smem, BF16) x B(smem, BF16)^T, M=128, N from idesc, K=16, issued by the
+// lane elect.sync picks (the whole warp executes this in step).  A and B are both BF16:
+// kind::f16 takes one type for both operands.
+__device__ __forceinline__ void tc_mma_bf16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred ep, acc;\n\t.reg .b32 er;\n\telect.sync er|ep, 0xffffffff;\n\t"
+        "setp.ne.b32 acc, %4, 0;\n\t"
+        "@ep tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, acc;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // (va, ia) comes before (vb, ib) in the selection order
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
