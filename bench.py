@@ -227,6 +227,32 @@ def oracle_sample_rate(cfg, seconds=12.0, n_experts=8):
     return tokens_per_s, desc, os.cpu_count()
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest of every rank's value of x (a job's time is its slowest rank's).  NCCL
+    reduces device tensors, gloo host tensors."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, steps, total_ms):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (total_ms * 1e-3)
+
+
+def rank_inputs(cfg, rank):
+    """This rank's token shard (weak scaling: each rank draws its own seeded tokens and routing;
+    the experts' weights are the same on every rank)."""
+    x = S.make_x(cfg, stream=rank)
+    ids, w = S.make_routing(cfg, stream=rank)
+    return x, ids, w
+
+
 def run_reference(args, cfg, rank, world):
     if rank != 0:
         return None
@@ -295,8 +321,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     def to_dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
-    x_np = S.make_x(cfg, stream=rank)
-    ids_np, w_np = S.make_routing(cfg, stream=rank)
+    x_np, ids_np, w_np = rank_inputs(cfg, rank)
     w1_np, w2_np = S.make_weights(cfg)
     w1, w2 = to_dev(w1_np), to_dev(w2_np)
     del w1_np, w2_np
@@ -349,14 +374,10 @@ def run_ours(args, cfg, rank, world, local_rank):
         dist.barrier()
     clocks = sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     if M.nvfp4_get_device_error() != 0:
         raise RuntimeError("device error during the timed steps")
-    value = T * world * K / (total_ms * 1e-3)
+    value = job_tokens_per_s(T, world, K, total_ms)
 
     # ---- per-stage attribution (separate pass, same launches, events between stages)
     names = ["route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"]
@@ -474,11 +495,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     stream.wait_event(d2h_done[K2 & 1])
     e_e.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_s.elapsed_time(e_e) / K2
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / K2, world, dev)
     if not torch.equal(out_h[(K2 - 1) & 1].view(torch.int16), out.cpu().view(torch.int16)):
         raise SystemExit("bench: end-to-end output differs from the device-resident run")
     h2d = x.numel() * 2 + ids.numel() * 4 + pw.numel() * 4
