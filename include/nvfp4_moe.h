@@ -67,7 +67,9 @@ typedef enum {
     NVFP4_ERR_CUDA = 4,                 /* a CUDA runtime/driver call or launch failed */
     NVFP4_ERR_BAD_EXPERT_ID = 5,        /* device: a top-k id outside [0, E) */
     NVFP4_ERR_NONFINITE = 6,            /* device: a row maximum was Inf or NaN */
-    NVFP4_ERR_DEVICE_TIMEOUT = 7        /* device: a bounded pipeline wait ran out */
+    NVFP4_ERR_DEVICE_TIMEOUT = 7,       /* device: a bounded pipeline wait ran out */
+    NVFP4_ERR_CAPACITY = 8              /* device: an expert got more (token, slot) pairs than the
+                                           fixed capacity; the excess pairs were dropped */
 } nvfp4_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -261,6 +263,28 @@ nvfp4_status moe_fc2_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
                            size_t ws_bytes, float* fc2_debug_dev, void* stream);
 nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev,
                               void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Fixed-capacity ("masked") layout -- a second way to lay the routed rows out: expert e owns
+ * rows [e*capacity, (e+1)*capacity) whatever the batch, its pairs first (token, slot order),
+ * then pad rows; expert_offsets[e] = e*capacity.  ("Finishing RL training faster: bitwise
+ * consistency, high performance, agent-driven", section 4.4 "Expert GEMM: two layouts, same row
+ * result": the rollout's masked per-expert layout and the trainer's contiguous one must give
+ * bitwise-identical rows.)  Every routed row is computed exactly as in the contiguous layout, so
+ * moe_expert_forward_nvfp4_masked returns the same output bits as moe_expert_forward_nvfp4 as
+ * long as no expert gets more than `capacity` pairs; pairs past it are dropped, the device error
+ * word records NVFP4_ERR_CAPACITY and the output is then unspecified.
+ *  capacity   rows per expert, a multiple of 128, >= 128, E*capacity < 2^30
+ * The workspace has E*capacity routed rows: size it with the _masked queries.  T == 0 writes
+ * nothing. */
+nvfp4_status moe_workspace_layout_query_masked(int64_t T, int H, int I, int E, int k, int capacity,
+                                               moe_workspace_layout* layout);
+size_t moe_workspace_bytes_masked(int64_t T, int H, int I, int E, int k, int capacity);
+nvfp4_status moe_route_sort_amax_masked(const void* x_dev, int64_t T, int H, int E, int k,
+                                        const int32_t* topk_ids_dev, const float* topk_w_dev, int capacity,
+                                        int32_t* expert_offsets_dev, void* ws_dev, size_t ws_bytes, void* stream);
+nvfp4_status moe_expert_forward_nvfp4_masked(const moe_nvfp4_weights* w, int64_t T, int k, int capacity,
+                                             const int32_t* expert_offsets_dev, void* out_dev, void* ws_dev,
+                                             size_t ws_bytes, void* stream);
 
 /* moe_router_topk -- the router step that produces the inputs of
  * moe_route_sort_amax: logits[t, e] = sum_h x[t, h] * W_r[e, h] (BF16 inputs, FP32

@@ -25,7 +25,7 @@ NVFP4_OK = 0
 STATUS_NAMES = {
     0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED_SHAPE",
     3: "NVFP4_ERR_WORKSPACE_TOO_SMALL", 4: "NVFP4_ERR_CUDA", 5: "NVFP4_ERR_BAD_EXPERT_ID",
-    6: "NVFP4_ERR_NONFINITE", 7: "NVFP4_ERR_DEVICE_TIMEOUT",
+    6: "NVFP4_ERR_NONFINITE", 7: "NVFP4_ERR_DEVICE_TIMEOUT", 8: "NVFP4_ERR_CAPACITY",
 }
 
 
@@ -70,6 +70,12 @@ _SIGNATURES = {
     "nvfp4_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_int)]),
     "moe_route_sort_amax_noalloc": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_router_topk": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
+    "moe_workspace_layout_query_masked": (_I32, [_I64, _I32, _I32, _I32, _I32, _I32,
+                                                 ctypes.POINTER(moe_workspace_layout)]),
+    "moe_workspace_bytes_masked": (_SZ, [_I64, _I32, _I32, _I32, _I32, _I32]),
+    "moe_route_sort_amax_masked": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "moe_expert_forward_nvfp4_masked": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _I32, _P, _P, _P,
+                                               _SZ, _P]),
 }
 
 _lib = None
@@ -231,6 +237,36 @@ def moe_router_topk(x, w_router, k, with_logits=False, stream=None):
         _ptr(x), T, H, _ptr(w_router), E, k, _ptr(ids), _ptr(w),
         _ptr(logits) if logits is not None else None, _stream(stream)))
     return ids, w, logits
+
+
+def moe_workspace_layout_query_masked(T, H, I, E, k, capacity):
+    L = moe_workspace_layout()
+    _check("moe_workspace_layout_query_masked",
+           lib().moe_workspace_layout_query_masked(T, H, I, E, k, capacity, ctypes.byref(L)))
+    return L
+
+
+def alloc_workspace_masked(T, H, I, E, k, capacity, device="cuda"):
+    n = lib().moe_workspace_bytes_masked(T, H, I, E, k, capacity)
+    if n == 0:
+        raise NVFP4Error("moe_workspace_bytes_masked", 2)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_route_sort_amax_masked(x, topk_ids, topk_w, E, capacity, expert_offsets, ws, stream=None):
+    """Route sort into the fixed-capacity layout (expert e at rows [e*capacity, ...))."""
+    _need_cuda(x, topk_ids, topk_w, expert_offsets, ws)
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    _check("moe_route_sort_amax_masked", lib().moe_route_sort_amax_masked(
+        _ptr(x), T, H, E, k, _ptr(topk_ids), _ptr(topk_w), capacity, _ptr(expert_offsets), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_expert_forward_nvfp4_masked(weights, T, k, capacity, expert_offsets, out, ws, stream=None):
+    _need_cuda(expert_offsets, out, ws)
+    _check("moe_expert_forward_nvfp4_masked", lib().moe_expert_forward_nvfp4_masked(
+        weights.ref(), T, k, capacity, _ptr(expert_offsets), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_expert_forward_nvfp4(weights, T, k, expert_offsets, out, ws, stream=None):

@@ -49,7 +49,8 @@ bool moe_shape_ok(int64_t T, int H, int I, int E, int k) {
     return true;
 }
 
-void compute_layout(int64_t T, int H, int I, int E, int k, moe_workspace_layout* L) {
+// capacity > 0: the fixed-capacity layout, E*capacity routed rows (expert e at e*capacity).
+void compute_layout(int64_t T, int H, int I, int E, int k, moe_workspace_layout* L, int capacity = 0) {
     std::memset(L, 0, sizeof(*L));
     L->T = T;
     L->H = H;
@@ -58,7 +59,8 @@ void compute_layout(int64_t T, int H, int I, int E, int k, moe_workspace_layout*
     L->k = k;
     const int64_t R = T * k;
     const int64_t live_experts = R < E ? R : E;
-    L->rows_cap = (R + live_experts * (kTileM - 1) + kTileM - 1) / kTileM * kTileM;
+    L->rows_cap = capacity > 0 ? static_cast<int64_t>(E) * capacity
+                               : (R + live_experts * (kTileM - 1) + kTileM - 1) / kTileM * kTileM;
     L->n_chunks = (T + 255) / 256;
     const int64_t rc = L->rows_cap;
     size_t o = 0;
@@ -94,15 +96,20 @@ T* at(void* ws, size_t off) {
 }
 
 // Shared validation of the calls that run on a filled workspace.
+bool capacity_ok(int E, int capacity) {
+    return capacity >= kTileM && capacity % kTileM == 0 && static_cast<int64_t>(E) * capacity < (int64_t(1) << 30);
+}
+
 nvfp4_status check_forward_args(const moe_nvfp4_weights* w, int64_t T, int k, const void* ws, size_t ws_bytes,
-                                moe_workspace_layout* L) {
+                                moe_workspace_layout* L, int capacity = 0) {
     if (!w || !ws) return NVFP4_ERR_INVALID_ARG;
     if (!w->w1_codes || !w->w1_sf || !w->w1_g || !w->w2_codes || !w->w2_sf || !w->w2_g) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(w->w1_codes, 16) || !aligned(w->w1_sf, 16) || !aligned(w->w2_codes, 16) || !aligned(w->w2_sf, 16) ||
         !aligned(ws, 256))
         return NVFP4_ERR_INVALID_ARG;
     if (!moe_shape_ok(T, w->H, w->I, w->E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    compute_layout(T, w->H, w->I, w->E, k, L);
+    if (capacity != 0 && !capacity_ok(w->E, capacity)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    compute_layout(T, w->H, w->I, w->E, k, L, capacity);
     if (ws_bytes < L->total) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
     return NVFP4_OK;
 }
@@ -180,6 +187,10 @@ int device_sm_count() {
 using namespace nvfp4;
 
 namespace nvfp4 {
+// defined in quant.cu: the route sort with an optional fixed capacity per expert
+cudaError_t launch_route_sort_quant_cap(const uint16_t* x, int64_t T, int H, int E, int k, const int32_t* ids,
+                                        const float* probs, int32_t* offsets, const RouteBufs& b, int capacity,
+                                        int* err, cudaStream_t st);
 // defined in router.cu
 cudaError_t launch_router_topk(const uint16_t* x, int64_t T, int H, const uint16_t* w, int E, int k, int32_t* ids,
                                float* probs, float* logits, int* err, cudaStream_t st);
@@ -197,6 +208,7 @@ const char* nvfp4_status_string(int status) {
         case NVFP4_ERR_BAD_EXPERT_ID: return "NVFP4_ERR_BAD_EXPERT_ID";
         case NVFP4_ERR_NONFINITE: return "NVFP4_ERR_NONFINITE";
         case NVFP4_ERR_DEVICE_TIMEOUT: return "NVFP4_ERR_DEVICE_TIMEOUT";
+        case NVFP4_ERR_CAPACITY: return "NVFP4_ERR_CAPACITY";
         default: return "NVFP4_UNKNOWN_STATUS";
     }
 }
@@ -239,17 +251,18 @@ size_t moe_workspace_bytes(int64_t T, int H, int I, int E, int k) {
     return L.total;
 }
 
-nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int k, const int32_t* topk_ids_dev,
-                                 const float* topk_w_dev, int32_t* expert_offsets_dev, void* ws_dev, size_t ws_bytes,
-                                 void* stream) {
+static nvfp4_status route_impl(const void* x_dev, int64_t T, int H, int E, int k, const int32_t* topk_ids_dev,
+                               const float* topk_w_dev, int32_t* expert_offsets_dev, void* ws_dev, size_t ws_bytes,
+                               int capacity, void* stream) {
     if (!moe_shape_ok(T, H, 128, E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (capacity != 0 && !capacity_ok(E, capacity)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!expert_offsets_dev || !ws_dev) return NVFP4_ERR_INVALID_ARG;
     if (T > 0 && (!x_dev || !topk_ids_dev || !topk_w_dev)) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(x_dev, 16) || !aligned(ws_dev, 256) || !aligned(topk_ids_dev, 4) || !aligned(topk_w_dev, 4) ||
         !aligned(expert_offsets_dev, 4))
         return NVFP4_ERR_INVALID_ARG;
     moe_workspace_layout L;
-    compute_layout(T, H, 128, E, k, &L);
+    compute_layout(T, H, 128, E, k, &L, capacity);
     if (ws_bytes < L.route_end) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
     int* err = device_error_ptr();
     if (!err) return NVFP4_ERR_CUDA;
@@ -265,14 +278,44 @@ nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int
     b.pair_rank = at<int32_t>(ws_dev, L.pair_rank);
     b.expert_count = at<int32_t>(ws_dev, L.expert_count);
     b.n_chunks = L.n_chunks;
-    return from_cuda(launch_route_sort_quant(static_cast<const uint16_t*>(x_dev), T, H, E, k, topk_ids_dev, topk_w_dev,
-                                             expert_offsets_dev, b, err, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_route_sort_quant_cap(static_cast<const uint16_t*>(x_dev), T, H, E, k, topk_ids_dev,
+                                                 topk_w_dev, expert_offsets_dev, b, capacity, err,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int k, const int32_t* topk_ids_dev,
+                                 const float* topk_w_dev, int32_t* expert_offsets_dev, void* ws_dev, size_t ws_bytes,
+                                 void* stream) {
+    return route_impl(x_dev, T, H, E, k, topk_ids_dev, topk_w_dev, expert_offsets_dev, ws_dev, ws_bytes, 0, stream);
+}
+
+nvfp4_status moe_route_sort_amax_masked(const void* x_dev, int64_t T, int H, int E, int k,
+                                        const int32_t* topk_ids_dev, const float* topk_w_dev, int capacity,
+                                        int32_t* expert_offsets_dev, void* ws_dev, size_t ws_bytes, void* stream) {
+    if (capacity == 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    return route_impl(x_dev, T, H, E, k, topk_ids_dev, topk_w_dev, expert_offsets_dev, ws_dev, ws_bytes, capacity,
+                      stream);
+}
+
+nvfp4_status moe_workspace_layout_query_masked(int64_t T, int H, int I, int E, int k, int capacity,
+                                               moe_workspace_layout* out) {
+    if (!out) return NVFP4_ERR_INVALID_ARG;
+    if (!moe_shape_ok(T, H, I, E, k) || !capacity_ok(E, capacity)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    compute_layout(T, H, I, E, k, out, capacity);
+    return NVFP4_OK;
+}
+
+size_t moe_workspace_bytes_masked(int64_t T, int H, int I, int E, int k, int capacity) {
+    if (!moe_shape_ok(T, H, I, E, k) || !capacity_ok(E, capacity)) return 0;
+    moe_workspace_layout L;
+    compute_layout(T, H, I, E, k, &L, capacity);
+    return L.total;
 }
 
 static nvfp4_status moe_fc1_swiglu_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
-                                  void* ws_dev, size_t ws_bytes, float* fc1_debug_dev, void* stream, bool pdl) {
+                                  void* ws_dev, size_t ws_bytes, float* fc1_debug_dev, void* stream, bool pdl, int capacity = 0) {
     moe_workspace_layout L;
-    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
     if (s != NVFP4_OK) return s;
     if (!expert_offsets_dev) return NVFP4_ERR_INVALID_ARG;
     if (T == 0) return NVFP4_OK;
@@ -283,9 +326,9 @@ static nvfp4_status moe_fc1_swiglu_nvfp4_impl(const moe_nvfp4_weights* w, int64_
 }
 
 static nvfp4_status moe_requant_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
-                               void* ws_dev, size_t ws_bytes, void* stream, bool pdl) {
+                               void* ws_dev, size_t ws_bytes, void* stream, bool pdl, int capacity = 0) {
     moe_workspace_layout L;
-    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
     if (s != NVFP4_OK) return s;
     if (!expert_offsets_dev) return NVFP4_ERR_INVALID_ARG;
     if (T == 0) return NVFP4_OK;
@@ -298,9 +341,9 @@ static nvfp4_status moe_requant_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T
 }
 
 static nvfp4_status moe_fc2_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
-                           void* ws_dev, size_t ws_bytes, float* fc2_debug_dev, void* stream, bool pdl) {
+                           void* ws_dev, size_t ws_bytes, float* fc2_debug_dev, void* stream, bool pdl, int capacity = 0) {
     moe_workspace_layout L;
-    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
     if (s != NVFP4_OK) return s;
     if (!expert_offsets_dev) return NVFP4_ERR_INVALID_ARG;
     if (T == 0) return NVFP4_OK;
@@ -311,9 +354,9 @@ static nvfp4_status moe_fc2_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, in
 }
 
 static nvfp4_status moe_combine_bf16_impl(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev, void* ws_dev,
-                              size_t ws_bytes, void* stream, bool pdl) {
+                              size_t ws_bytes, void* stream, bool pdl, int capacity = 0) {
     moe_workspace_layout L;
-    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
     if (s != NVFP4_OK) return s;
     if (T == 0) return NVFP4_OK;
     if (!out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
@@ -375,6 +418,24 @@ nvfp4_status moe_router_topk(const void* x_dev, int64_t T, int H, const void* w_
     return from_cuda(launch_router_topk(static_cast<const uint16_t*>(x_dev), T, H,
                                         static_cast<const uint16_t*>(w_router_dev), E, k, topk_ids_dev, topk_w_dev,
                                         logits_dev, err, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_expert_forward_nvfp4_masked(const moe_nvfp4_weights* w, int64_t T, int k, int capacity,
+                                             const int32_t* expert_offsets_dev, void* out_dev, void* ws_dev,
+                                             size_t ws_bytes, void* stream) {
+    if (capacity == 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    moe_workspace_layout L;
+    nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
+    if (s != NVFP4_OK) return s;
+    if (T == 0) return NVFP4_OK;
+    if (!expert_offsets_dev || !out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
+    s = moe_fc1_swiglu_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, false, capacity);
+    if (s != NVFP4_OK) return s;
+    s = moe_requant_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, stream, true, capacity);
+    if (s != NVFP4_OK) return s;
+    s = moe_fc2_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, true, capacity);
+    if (s != NVFP4_OK) return s;
+    return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, true, capacity);
 }
 
 nvfp4_status nvfp4_get_device_error(void* stream, int* device_status) {

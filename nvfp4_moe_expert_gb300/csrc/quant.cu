@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t n_chunk
                                                           const int32_t* __restrict__ chunk_count,
                                                           int32_t* __restrict__ chunk_base,
                                                           int32_t* __restrict__ expert_count,
-                                                          int32_t* __restrict__ offsets) {
+                                                          int32_t* __restrict__ offsets, int capacity, int* err) {
     __shared__ int32_t seg_sum[1024];
     __shared__ int32_t e_off[1024];
     __shared__ int32_t warp_tot[33];
@@ -428,15 +428,19 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t n_chunk
     }
     seg_sum[tid] = sum;
     __syncthreads();
-    int32_t padded = 0;
+    int32_t padded = 0, count = 0;
     if (tid < E) {
-        int32_t run = 0;
-        for (int s = 0; s < S; ++s) run += seg_sum[tid * S + s];
-        expert_count[tid] = run;
-        padded = (run + kTileM - 1) / kTileM * kTileM;
+        for (int s = 0; s < S; ++s) count += seg_sum[tid * S + s];
+        expert_count[tid] = count;
+        padded = (count + kTileM - 1) / kTileM * kTileM;
     }
     int32_t total;
-    const int32_t start = block_exclusive_scan(padded, warp_tot, total);
+    int32_t start = block_exclusive_scan(padded, warp_tot, total);
+    if (capacity > 0) {                       // fixed-capacity layout: expert e owns rows [e*C, (e+1)*C)
+        start = tid * capacity;
+        total = E * capacity;
+        if (tid < E && count > capacity) set_device_error(err, NVFP4_ERR_CAPACITY);
+    }
     if (tid < E) {
         e_off[tid] = start;
         offsets[tid] = start;
@@ -468,9 +472,10 @@ constexpr int64_t kBlockSortMaxPairs = 8192;
 __global__ void __launch_bounds__(1024) route_block_sort_kernel(const int32_t* __restrict__ ids, int64_t T, int E,
                                                                 int k, int32_t* __restrict__ pair_row,
                                                                 int32_t* __restrict__ expert_count,
-                                                                int32_t* __restrict__ offsets, int* err) {
+                                                                int32_t* __restrict__ offsets, int capacity, int* err) {
     extern __shared__ int32_t wc[];   // [32 warps][E]: counts, then running rows
     __shared__ int32_t warp_tot[33];
+    __shared__ int32_t s_start[kBlockSortMaxE];
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -512,8 +517,14 @@ __global__ void __launch_bounds__(1024) route_block_sort_kernel(const int32_t* _
         expert_count[tid] = cnt;
     }
     int32_t total;
-    const int32_t start = block_exclusive_scan(tid < E ? (cnt + kTileM - 1) / kTileM * kTileM : 0, warp_tot, total);
+    int32_t start = block_exclusive_scan(tid < E ? (cnt + kTileM - 1) / kTileM * kTileM : 0, warp_tot, total);
+    if (capacity > 0) {                       // fixed-capacity layout: expert e owns rows [e*C, (e+1)*C)
+        start = tid * capacity;
+        total = E * capacity;
+        if (tid < E && cnt > capacity) set_device_error(err, NVFP4_ERR_CAPACITY);
+    }
     if (tid < E) {
+        s_start[tid] = start;
         offsets[tid] = start;
         int32_t run = start;   // first row of each warp's pairs of expert tid
         for (int ww = 0; ww < kBlockSortWarps; ++ww) {
@@ -544,19 +555,25 @@ __global__ void __launch_bounds__(1024) route_block_sort_kernel(const int32_t* _
             if (e >= 0 && (m & lt_mask) == 0) mine[e] = base + __popc(m);
             __syncwarp();
             const int64_t p = b0 + u * 32 + lane;
-            if (p < p1) pair_row[p] = e >= 0 ? base + __popc(m & lt_mask) : -1;   // -1: bad id, skipped
+            int32_t row = e >= 0 ? base + __popc(m & lt_mask) : -1;              // -1: bad id, skipped
+            if (capacity > 0 && row >= 0 && row - s_start[e] >= capacity) row = -1;   // over capacity: dropped
+            if (p < p1) pair_row[p] = row;
         }
     }
 }
 
 // Destination rows of pair p (token t, chunk t / kRouteChunk): either stored directly
 // by route_block_sort_kernel, or chunk base + rank from the chunked kernels.
-__device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* ids, int E, int64_t p, int64_t chunk) {
+// With a fixed capacity C (> 0), a pair whose row falls past its expert's C rows is dropped
+// (-1; reported by the counting kernels).
+__device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* ids, int E, int64_t p, int64_t chunk,
+                                             int capacity) {
     if (b.direct_rows) return __ldg(b.pair_rank + p);
     const int e = __ldg(ids + p);
     const int32_t rank = __ldg(b.pair_rank + p);
     if (e < 0 || e >= E) return -1;   // reported by the counting kernels
-    return __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) + rank;
+    const int32_t row = __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) + rank;
+    return (capacity > 0 && row - e * capacity >= capacity) ? -1 : row;
 }
 
 // Blocks [0, pad_blocks) give one warp per expert for its pad rows
@@ -565,7 +582,8 @@ __device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* 
 template <int GPL>
 __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int E, int k, const int32_t* __restrict__ ids,
-    const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int pad_blocks, int* err) {
+    const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int pad_blocks, int capacity,
+    int* err) {
     pdl_wait();
     pdl_launch_dependents();
     const int G = H / 64;
@@ -604,7 +622,7 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_ker
         if (slot_lane) {
             const int64_t p = t * k + rl.li;
             my_prob = __ldg(probs + p);
-            my_dst = pair_dest(b, ids, E, p, chunk);
+            my_dst = pair_dest(b, ids, E, p, chunk, capacity);
         }
         GroupQ q[GPL];
         bool finite;
@@ -623,7 +641,7 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_ker
             if (rl.LPR >= k) {
                 r = __shfl_sync(rl.mask, my_dst, src0 + j);
             } else {                 // rows narrower than k lanes: look the slot up directly
-                r = pair_dest(b, ids, E, p, chunk);
+                r = pair_dest(b, ids, E, p, chunk, capacity);
                 if (r >= 0 && rl.li == 0) {
                     b.a_g[r] = gr;
                     b.row_pair[r] = static_cast<int32_t>(p);
@@ -714,17 +732,19 @@ cudaError_t launch_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, 
     return NVFP4_GPL_LAUNCH(false, c / 64, quantize_rows_kernel, grid, st, x, rows, c, ld, codes, sf, g, err);
 }
 
-cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, int k, const int32_t* ids,
-                                    const float* probs, int32_t* offsets, const RouteBufs& b_in, int* err,
-                                    cudaStream_t st) {
-    if (T == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
+// capacity > 0: the fixed-capacity layout (expert e's rows at [e*C, e*C + count_e), pad rows to
+// (e+1)*C; pairs past the capacity are dropped and NVFP4_ERR_CAPACITY is recorded).
+cudaError_t launch_route_sort_quant_cap(const uint16_t* x, int64_t T, int H, int E, int k, const int32_t* ids,
+                                        const float* probs, int32_t* offsets, const RouteBufs& b_in, int capacity,
+                                        int* err, cudaStream_t st) {
+    if (T == 0) return capacity > 0 ? cudaSuccess : cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
     RouteBufs b = b_in;
     cudaError_t e;
     if (E <= kBlockSortMaxE && T * k <= kBlockSortMaxPairs) {
         b.direct_rows = 1;
         const size_t smem = sizeof(int32_t) * kBlockSortWarps * E;
         e = launch_pdl(false, route_block_sort_kernel, 1, kBlockSortWarps * 32, smem, st, ids, T, E, k, b.pair_rank,
-                       b.expert_count, offsets, err);
+                       b.expert_count, offsets, capacity, err);
         if (e != cudaSuccess) return e;
     } else {
         b.direct_rows = 0;
@@ -733,13 +753,19 @@ cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, 
                        b.n_chunks, b.chunk_count, b.pair_rank, err);
         if (e != cudaSuccess) return e;
         e = launch_pdl(true, route_scan_kernel, 1, 1024, 0, st, E, b.n_chunks, b.chunk_count, b.chunk_base,
-                       b.expert_count, offsets);
+                       b.expert_count, offsets, capacity, err);
         if (e != cudaSuccess) return e;
     }
     const int pad_blocks = (E + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int grid = pad_blocks + grid_for_warps(warps_for_rows(T, H / 64));
     return NVFP4_GPL_LAUNCH(true, H / 64, route_quant_scatter_kernel, grid, st, x, T, H, E, k, ids, probs, offsets, b,
-                            pad_blocks, err);
+                            pad_blocks, capacity, err);
+}
+
+cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, int k, const int32_t* ids,
+                                    const float* probs, int32_t* offsets, const RouteBufs& b, int* err,
+                                    cudaStream_t st) {
+    return launch_route_sort_quant_cap(x, T, H, E, k, ids, probs, offsets, b, 0, err, st);
 }
 
 cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32_t* row_pair,

@@ -116,6 +116,23 @@ def test_router_validation(lib):
     assert ok(8, 256, 16, 4, lg=ctypes.c_void_p(4112)) == 1             # logits need 32 bytes
 
 
+def test_masked_layout_validation(lib):
+    p = ctypes.c_void_p(4096)
+    L = M.moe_workspace_layout()
+    assert lib.moe_workspace_layout_query_masked(100, 256, 128, 8, 2, 256, ctypes.byref(L)) == 0
+    assert L.rows_cap == 8 * 256                          # E * capacity rows, expert e at e * capacity
+    assert lib.moe_workspace_bytes_masked(100, 256, 128, 8, 2, 256) == L.total
+    assert lib.moe_workspace_bytes_masked(100, 256, 128, 8, 2, 200) == 0       # not a multiple of 128
+    assert lib.moe_workspace_layout_query_masked(100, 256, 128, 8, 2, 0, ctypes.byref(L)) == 2
+    assert lib.moe_route_sort_amax_masked(p, 16, 256, 8, 2, p, p, 64, p, p, 1 << 30, None) == 2
+    assert lib.moe_route_sort_amax_masked(p, 16, 256, 8, 2, p, p, 128, p, None, 1 << 30, None) == 1
+    small = lib.moe_workspace_bytes_masked(16, 256, 128, 8, 2, 128)
+    route_end = M.moe_workspace_layout_query_masked(16, 256, 128, 8, 2, 128).route_end
+    assert small > route_end
+    assert lib.moe_route_sort_amax_masked(p, 16, 256, 8, 2, p, p, 128, p, p, route_end - 1, None) == 3
+    assert M.nvfp4_status_string(8) == "NVFP4_ERR_CAPACITY"
+
+
 def test_route_validation(lib):
     p = ctypes.c_void_p(4096)
     ok_ws = M.moe_workspace_layout_query(16, 256, 128, 8, 2).route_end

@@ -30,8 +30,10 @@ def torchrun(args, timeout=240):
     return [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
 
 
-def test_max_over_ranks_and_shards_gloo():
-    lines = sorted(torchrun([os.path.join("tests", "_ranks_worker.py")]), key=lambda d: d["rank"])
+def test_max_over_ranks_and_shards_gloo(tmp_path):
+    out = str(tmp_path / "rank")
+    torchrun([os.path.join("tests", "_ranks_worker.py"), out])
+    lines = [json.load(open(f"{out}.{r}.json")) for r in range(2)]
     assert [d["rank"] for d in lines] == [0, 1] and all(d["world"] == 2 for d in lines)
     assert all(d["max_ms"] == 15.0 for d in lines)                     # the slowest rank's time
     assert all(d["tokens_per_s"] == pytest.approx(64 * 2 * 3 / 15e-3) for d in lines)
