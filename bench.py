@@ -444,6 +444,33 @@ def run_ours(args, cfg, rank, world, local_rank):
         if M.nvfp4_get_device_error() != 0:
             raise RuntimeError("device error in the router step")
 
+    # ---- the same step in the fixed-capacity layout (expert e at rows [e*C, (e+1)*C)), C the
+    # smallest multiple of 128 that holds the fullest expert; timed on its own
+    counts = np.bincount(ids_np.ravel(), minlength=E)
+    C = 128 * ((int(counts.max()) + 127) // 128)
+    ws_m = M.alloc_workspace_masked(T, H, cfg.I, E, k, C)
+    out_m = torch.empty_like(out)
+    M.moe_route_sort_amax_masked(x, ids, pw, E, C, offs, ws_m)
+    M.moe_expert_forward_nvfp4_masked(weights, T, k, C, offs, out_m, ws_m)
+    mev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_attr)]
+    for i in range(n_attr):
+        mev[i][0].record(stream)
+        M.moe_route_sort_amax_masked(x, ids, pw, E, C, offs, ws_m)
+        M.moe_expert_forward_nvfp4_masked(weights, T, k, C, offs, out_m, ws_m)
+        mev[i][1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if M.nvfp4_get_device_error() != 0:
+        raise RuntimeError("device error in the masked-layout step")
+    m_ms = statistics.mean(a.elapsed_time(b) for a, b in mev)
+    masked = {"ms_per_step": round(m_ms, 4), "tokens_per_s": round(T / (m_ms * 1e-3), 1), "capacity": C,
+              "rows": E * C, "contiguous_rows": int(sum((c + 127) // 128 * 128 for c in counts)),
+              "bitwise_equal_to_contiguous": bool(torch.equal(out_m.view(torch.int16), out.view(torch.int16))),
+              "note": "route sort + expert forward in the fixed-capacity layout; timed on its own"}
+    # the contiguous step's output is recomputed so `out` holds it again for the checks below
+    M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+    M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region.
     # A serving loop: every step copies its own inputs in and its output back, on two copy
     # streams, with device buffers double-buffered so that step i's copies overlap the compute of
@@ -512,6 +539,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "kernels": kernels,
         "weight_quant_ms": round(wq_ms, 3),
         "router_step": router,
+        "masked_step": masked,
         "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "every step copies its pinned host X/ids/probs in and its output out; two copy "
