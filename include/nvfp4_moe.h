@@ -251,7 +251,9 @@ nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int
  * "unfused API").  fc1_debug_dev / fc2_debug_dev may be NULL; if given they
  * receive the FP32 pre-cast epilogue values v of every real routed row:
  * float [rows_cap][2I] (gate columns then up columns) and float
- * [rows_cap][H]; pad rows are not written. */
+ * [rows_cap][H]; pad rows are not written.  They take the contiguous layout
+ * that moe_route_sort_amax writes; a workspace filled by
+ * moe_route_sort_amax_masked runs through moe_expert_forward_nvfp4_masked. */
 nvfp4_status moe_fc1_swiglu_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
                                   const int32_t* expert_offsets_dev, void* ws_dev,
                                   size_t ws_bytes, float* fc1_debug_dev, void* stream);
