@@ -19,7 +19,8 @@ of the same shapes stand in for them):
 Recipe: numpy PCG64; sub-streams seed+0 (X), +1 (W1), +2 (W2), +3 (router
 logits), +4 (outlier channels), +5 (sequence lengths), +6 (router weights for
 the router step, W_r ~ N(0, 1/H) so that logits of N(0,1) inputs are about
-N(0,1)).  Values are drawn in
+N(0,1)), +7 (the output gradient of the backward, dOut ~ N(0, 1)).  Values are
+drawn in
 float32 and rounded to BF16 (round-to-nearest-even on the bit pattern).
 Routing: softmax over experts in FP64, top-k by (probability descending,
 expert id ascending), probabilities renormalised over the k chosen experts in
@@ -130,6 +131,13 @@ def make_router_weights(cfg):
     rng = _rng(cfg.seed, 6)
     w = rng.standard_normal((cfg.E, cfg.H), dtype=np.float32) * np.float32(1.0 / np.sqrt(cfg.H))
     return f32_to_bf16_bits(w)
+
+
+def make_grad_out(cfg, T=None, stream=0):
+    """BF16 output gradient dOut [T, H] as uint16 bits, N(0, 1)."""
+    T = cfg.T if T is None else T
+    rng = _rng(cfg.seed + 1000 * stream, 7)
+    return f32_to_bf16_bits(rng.standard_normal((T, cfg.H), dtype=np.float32))
 
 
 def make_layer(cfg, T=None, experts=None):

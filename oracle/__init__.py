@@ -23,7 +23,10 @@ The oracle is a slow, literal restatement of what the source pages define:
   product; section 4.5 "Cross-GPU reduction": the expert outputs are summed in
   FP32 in top-k slot order; sections 2 and 4.1 (router step, ``router.py``):
   one FP32-output router GEMM for every batch size and a top-k whose ties and
-  order are fixed.
+  order are fixed;
+* the miniTE page again, sections "How it differs" and its results paragraph
+  (``backward.py``): the straight-through backward, BF16 GEMMs on the saved
+  BF16 originals, measured by gradient relative L2 against an FP32 reference.
 
 Floating point: FP64 where the contract does not fix the precision (GEMM
 accumulation, SiLU), IEEE FP32 (numpy float32, correctly rounded, no FMA
@@ -46,6 +49,7 @@ from .quant import (  # noqa: F401
     quantize_rows, dequantize_rows, pack_nibbles, unpack_nibbles, OUTER_DIVISOR,
 )
 from .router import router_logits_f64, topk_order, topk_probs, router_topk  # noqa: F401
+from .backward import moe_backward_ste, forward_saved_activations, silu_and_derivative  # noqa: F401
 from .moe import (  # noqa: F401
     route_sort,
     qgemm_f64,
