@@ -333,7 +333,6 @@ def run_ours(args, cfg, rank, world, local_rank):
     ev1.record(stream)
     torch.cuda.synchronize()
     wq_ms = ev0.elapsed_time(ev1)
-    del w1, w2
 
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
     x = to_dev(x_np)
@@ -528,6 +527,12 @@ def run_ours(args, cfg, rank, world, local_rank):
     h2d = x.numel() * 2 + ids.numel() * 4 + pw.numel() * 4
     d2h = out.numel() * 2
 
+    # ---- straight-through backward of the same layer (timed on its own, not part of the step):
+    # a forward that saves FC1's FP32 values, then moe_expert_backward_ste on a seeded dOut
+    backward = backward_step(M, torch, cfg, weights, w1, w2, x, ids, pw, ws, offs, flush, stream, dev, to_dev,
+                             min(K, 20), peaks, peak_kind)
+    del w1, w2
+
     line = {
         "metric": "nvfp4_moe_expert_forward_tokens_per_s", "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
@@ -540,6 +545,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "weight_quant_ms": round(wq_ms, 3),
         "router_step": router,
         "masked_step": masked,
+        "backward_step": backward,
         "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "every step copies its pinned host X/ids/probs in and its output out; two copy "
@@ -549,6 +555,54 @@ def run_ours(args, cfg, rank, world, local_rank):
         "clocks": clocks,
     }
     return line
+
+
+def backward_step(M, torch, cfg, weights, w1, w2, x, ids, pw, ws, offs, flush, stream, dev, to_dev, n, peaks,
+                  peak_kind):
+    """CUDA-event time of moe_expert_backward_ste (four BF16 grouped GEMMs, the SwiGLU x prob
+    derivative, transposes and the slot-order sum) on this workload, L2 flushed between calls."""
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    wt = M.MoEWeightsBF16T(w1, w2)
+    lay = M.moe_workspace_layout_query(T, H, I, E, k)
+    fc1_pre = torch.empty((lay.rows_cap, 2 * I), dtype=torch.float32, device=dev)
+    dout = to_dev(S.make_grad_out(cfg))
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    dw1 = torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev)
+    dw2 = torch.empty((E, H, I), dtype=torch.float32, device=dev)
+    dprob = torch.empty((T, k), dtype=torch.float32, device=dev)
+    bws = M.alloc_backward_workspace(T, H, I, E, k, dev)
+    M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+    M.moe_fc1_swiglu_nvfp4(weights, T, k, offs, ws, debug=fc1_pre)
+    M.moe_requant_nvfp4(weights, T, k, offs, ws)
+    M.moe_fc2_nvfp4(weights, T, k, offs, ws)
+    M.moe_combine_bf16(weights, T, k, out, ws)
+
+    def bwd():
+        M.moe_expert_backward_ste(wt, T, k, x, dout, offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws)
+
+    for _ in range(3):
+        bwd()
+        flush.zero_()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        bwd()
+        ev[i][1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if M.nvfp4_get_device_error() != 0:
+        raise RuntimeError("device error in the backward step")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    flops = 12 * T * k * H * I           # four GEMMs of 2*R*H*I, two of them over 2I
+    bf16 = float(peaks["bf16_tflops"])
+    ach = flops / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1), "bound": "tensor",
+            "achieved": round(ach, 2), "peak": bf16, "unit": "TFLOP/s", "frac": round(ach / bf16, 4),
+            "peak_note": "of " + peak_kind, "algorithmic": f"{flops:.4g} FLOP per call (12 T k H I)",
+            "finite": bool(torch.isfinite(dw1).all() and torch.isfinite(dw2).all()),
+            "note": "moe_expert_backward_ste: STE gradients dX, dW1, dW2, dprob from the saved BF16 "
+                    "originals; timed on its own after a forward that saves FC1's values"}
 
 
 def main():

@@ -309,6 +309,81 @@ nvfp4_status moe_expert_forward_nvfp4_masked(const moe_nvfp4_weights* w, int64_t
 nvfp4_status moe_router_topk(const void* x_dev, int64_t T, int H, const void* w_router_dev, int E, int k,
                              int32_t* topk_ids_dev, float* topk_w_dev, float* logits_dev, void* stream);
 
+/* ---- Straight-through (STE) backward ----------------------------------------------------
+ * ("miniTE diagnoses and narrows the cross-engine execution gap of NVFP4 RL", section "How it
+ * differs": the backward is a straight-through approximation, BF16 GEMMs on the saved original
+ * BF16 activations and weights; no quantisation runs backward.)  Each quantiser is taken as the
+ * identity and every other op is differentiated where it ran, with the rows of the forward's
+ * contiguous layout (moe_route_sort_amax); pair(r) = token*k + slot, t(r), p(r) as there:
+ *   dh[r]        = bf16( dOut[t(r)] W2[e] )                            BF16 GEMM, FP32 accumulate
+ *   a, u         = bf16 of the forward's FC1 values of r (the gate/up the SwiGLU ran on)
+ *   dgate, dup   = bf16( dh p u silu'(a) ), bf16( dh p silu(a) ),     silu(a) = a / (1 + e^-a),
+ *                  silu'(a) = s (1 + a (1 - s)), s = 1 / (1 + e^-a)   (FP32)
+ *   dprob[pair]  = sum_i dh_i silu(a_i) u_i                             (FP32)
+ *   dxs[pair]    = bf16( [dgate, dup] W1[e] )                          BF16 GEMM
+ *   dX[t]        = bf16( sum over slots 0..k-1 in order of dxs[t*k+j], FP32 )
+ *   dW2[e]       = sum over e's rows of dOut[t(r)]^T h[r]               FP32
+ *   dW1[e]       = sum over e's rows of [dgate, dup][r]^T x[t(r)]        FP32
+ * A token's dX and dprob do not depend on the other tokens of the batch. */
+
+/* The BF16 original weights, transposed per expert (nvfp4_transpose_bf16), so that the
+ * backward GEMMs read them K-major:
+ *   w1t  BF16 [E][H][2I], w1t[e][h][j] = W1[e][j][h]  (16-byte aligned)
+ *   w2t  BF16 [E][I][H],  w2t[e][i][h] = W2[e][h][i]  (16-byte aligned) */
+typedef struct {
+    const void* w1t;
+    const void* w2t;
+    int32_t E, H, I;
+} moe_bf16_weights_t;
+
+/* out[b][c][r] = in[b][r][c] for BF16 matrices; rows % 64 == 0, cols % 64 == 0,
+ * batch <= 65535, rows and cols <= 2^26; in and out 16-byte aligned and not overlapping. */
+nvfp4_status nvfp4_transpose_bf16(const void* in_dev, int64_t batch, int64_t rows, int64_t cols, void* out_dev,
+                                  void* stream);
+
+/* Byte offsets of the backward workspace's scratch buffers (256-byte aligned); rows_cap is
+ * the forward layout's. */
+typedef struct {
+    int64_t T; int32_t H, I, E, k;
+    int64_t rows_cap;
+    size_t dy_rows;   /* bf16 [rows_cap][H]  dOut gathered per routed row */
+    size_t dh;        /* bf16 [rows_cap][I] */
+    size_t dgu;       /* bf16 [rows_cap][2I] dgate then dup */
+    size_t dx_pairs;  /* bf16 [T*k][H]       dX per (token, slot) */
+    size_t dy_t;      /* bf16 [H][rows_cap] */
+    size_t h_t;       /* bf16 [I][rows_cap] */
+    size_t dgu_t;     /* bf16 [2I][rows_cap] */
+    size_t x_t;       /* bf16 [H][rows_cap] */
+    size_t total;
+} moe_backward_layout;
+
+nvfp4_status moe_backward_layout_query(int64_t T, int H, int I, int E, int k, moe_backward_layout* layout);
+size_t moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k);
+
+/* moe_expert_backward_ste -- the gradients of one forward, from what it saved.
+ *  w                    transposed BF16 originals (host struct, device pointers)
+ *  T, k                 as given to the forward
+ *  x_dev                BF16 [T][H], the forward's input; 16-byte aligned
+ *  dout_dev             BF16 [T][H], the gradient of the forward's output; 16-byte aligned
+ *  expert_offsets_dev   as moe_route_sort_amax wrote it for this forward (contiguous layout)
+ *  fwd_ws_dev, fwd_ws_bytes  the forward's workspace after the forward (its row map, router
+ *                       probabilities and h are read)
+ *  fc1_pre_dev          FP32 [rows_cap][2I], what moe_fc1_swiglu_nvfp4 wrote to its
+ *                       fc1_debug_dev in this forward; 16-byte aligned
+ *  dx_dev               BF16 [T][H] out; 16-byte aligned
+ *  dw1_dev, dw2_dev     FP32 [E][2I][H] and [E][H][I] out (overwritten); 32-byte aligned
+ *  dprob_dev            FP32 [T][k] out, the gradient of topk_w; 4-byte aligned
+ *  bwd_ws_dev, bwd_ws_bytes  scratch, moe_backward_workspace_bytes(T, H, I, E, k) bytes,
+ *                       256-byte aligned
+ * Nothing is allocated and nothing synchronises; every output is written in stream order.
+ * T == 0 zeroes dW1 and dW2.  Argument errors as for moe_expert_forward_nvfp4; device error
+ * NVFP4_ERR_DEVICE_TIMEOUT (a pipeline wait ran out). */
+nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int k, const void* x_dev,
+                                     const void* dout_dev, const int32_t* expert_offsets_dev, const void* fwd_ws_dev,
+                                     size_t fwd_ws_bytes, const float* fc1_pre_dev, void* dx_dev, float* dw1_dev,
+                                     float* dw2_dev, float* dprob_dev, void* bwd_ws_dev, size_t bwd_ws_bytes,
+                                     void* stream);
+
 /* Synchronise `stream`, then report and clear this device's error word:
  * *device_status receives NVFP4_OK or the first device error recorded since
  * the last call.  Returns NVFP4_ERR_CUDA if the synchronisation failed. */

@@ -7,7 +7,10 @@ entry points have the names of the C ABI in ``include/nvfp4_moe.h``:
     nvfp4_quantize_rows, moe_route_sort_amax, moe_expert_forward_nvfp4,
     moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16,
     moe_workspace_bytes, moe_workspace_layout_query, nvfp4_sf_bytes,
-    nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string
+    nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string,
+    moe_router_topk, the fixed-capacity moe_*_masked calls, and the
+    straight-through backward: nvfp4_transpose_bf16, moe_backward_layout_query,
+    moe_backward_workspace_bytes, moe_expert_backward_ste
 
 There is no CPU fallback: if the library is missing or a call fails, an
 exception is raised.
@@ -53,6 +56,19 @@ class moe_workspace_layout(ctypes.Structure):
         "pair_rank", "expert_count", "route_end", "h", "a2_codes", "a2_sf", "a2_g", "y", "total")]
 
 
+class moe_bf16_weights_t(ctypes.Structure):
+    _fields_ = [("w1t", ctypes.c_void_p), ("w2t", ctypes.c_void_p),
+                ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32)]
+
+
+class moe_backward_layout(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+        ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("rows_cap", ctypes.c_int64),
+    ] + [(n, ctypes.c_size_t) for n in (
+        "dy_rows", "dh", "dgu", "dx_pairs", "dy_t", "h_t", "dgu_t", "x_t", "total")]
+
+
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 _SIGNATURES = {
     "nvfp4_status_string": (ctypes.c_char_p, [_I32]),
@@ -76,6 +92,11 @@ _SIGNATURES = {
     "moe_route_sort_amax_masked": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _SZ, _P]),
     "moe_expert_forward_nvfp4_masked": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _I32, _P, _P, _P,
                                                _SZ, _P]),
+    "nvfp4_transpose_bf16": (_I32, [_P, _I64, _I64, _I64, _P, _P]),
+    "moe_backward_layout_query": (_I32, [_I64, _I32, _I32, _I32, _I32, ctypes.POINTER(moe_backward_layout)]),
+    "moe_backward_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
+    "moe_expert_backward_ste": (_I32, [ctypes.POINTER(moe_bf16_weights_t), _I64, _I32, _P, _P, _P, _P, _SZ, _P,
+                                       _P, _P, _P, _P, _P, _SZ, _P]),
 }
 
 _lib = None
@@ -299,12 +320,70 @@ def moe_combine_bf16(weights, T, k, out, ws, stream=None):
         weights.ref(), T, k, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
 
 
+# ---------------------------------------------------------------- straight-through backward
+def nvfp4_transpose_bf16(x, out=None, stream=None):
+    """BF16 [B, R, C] (or [R, C]) -> its per-matrix transpose [B, C, R] ([C, R])."""
+    _need_cuda(x, out)
+    if x.dtype != torch.bfloat16 or x.dim() not in (2, 3):
+        raise ValueError("x must be a 2-D or 3-D bfloat16 tensor")
+    b, r, c = (1,) + tuple(x.shape) if x.dim() == 2 else tuple(x.shape)
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-2]) + (c, r), dtype=torch.bfloat16, device=x.device)
+    _check("nvfp4_transpose_bf16", lib().nvfp4_transpose_bf16(_ptr(x), b, r, c, _ptr(out), _stream(stream)))
+    return out
+
+
+class MoEWeightsBF16T:
+    """The BF16 original expert weights transposed per expert for the backward
+    (w1t [E, H, 2I], w2t [E, I, H]) and the C struct pointing at them."""
+
+    def __init__(self, w1, w2, stream=None):
+        self.E, two_i, self.H = w1.shape
+        self.I = two_i // 2
+        self.w1t = nvfp4_transpose_bf16(w1.contiguous(), stream=stream)
+        self.w2t = nvfp4_transpose_bf16(w2.contiguous(), stream=stream)
+        self.struct = moe_bf16_weights_t(self.w1t.data_ptr(), self.w2t.data_ptr(), self.E, self.H, self.I)
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+def moe_backward_layout_query(T, H, I, E, k):
+    L = moe_backward_layout()
+    _check("moe_backward_layout_query", lib().moe_backward_layout_query(T, H, I, E, k, ctypes.byref(L)))
+    return L
+
+
+def alloc_backward_workspace(T, H, I, E, k, device="cuda"):
+    n = lib().moe_backward_workspace_bytes(T, H, I, E, k)
+    if n == 0:
+        raise NVFP4Error("moe_backward_workspace_bytes", 2)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_expert_backward_ste(wt, T, k, x, dout, expert_offsets, ws, fc1_pre, dx, dw1, dw2, dprob, bws,
+                            stream=None):
+    """STE gradients (dx, dw1, dw2, dprob written in place) of the forward whose route
+    sort filled `ws` / `expert_offsets` and whose FC1 stage wrote `fc1_pre`."""
+    _need_cuda(x, dout, expert_offsets, ws, fc1_pre, dx, dw1, dw2, dprob, bws)
+    _check("moe_expert_backward_ste", lib().moe_expert_backward_ste(
+        wt.ref(), T, k, _ptr(x), _ptr(dout), _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(fc1_pre),
+        _ptr(dx), _ptr(dw1), _ptr(dw2), _ptr(dprob), _ptr(bws), bws.numel(), _stream(stream)))
+
+
 class MoELayer:
-    """Convenience wrapper: owns quantised weights and a workspace sized per call."""
+    """Convenience wrapper: owns quantised weights and a workspace sized per call.
+
+    ``forward(..., save_for_backward=True)`` runs the forward stage by stage and keeps
+    what the straight-through backward reads (the route, h, FC1's FP32 values);
+    ``backward(dout)`` then returns (dx, dw1, dw2, dprob)."""
 
     def __init__(self, w1, w2, stream=None):
         self.weights = quantize_moe_weights(w1, w2, stream=stream)
         self.E, self.H, self.I = self.weights.E, self.weights.H, self.weights.I
+        self._w_bf16 = (w1, w2)
+        self._wt = None
+        self._saved = None
         self._ws = {}
 
     def workspace(self, T, k, device):
@@ -314,7 +393,7 @@ class MoELayer:
             self._ws[key] = alloc_workspace(T, self.H, self.I, self.E, k, device)
         return self._ws[key]
 
-    def forward(self, x, topk_ids, topk_w, out=None, stream=None):
+    def forward(self, x, topk_ids, topk_w, out=None, stream=None, save_for_backward=False):
         T, H = x.shape
         k = topk_ids.shape[1]
         ws = self.workspace(T, k, x.device)
@@ -322,8 +401,36 @@ class MoELayer:
         if out is None:
             out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
         moe_route_sort_amax(x, topk_ids, topk_w, self.E, offs, ws, stream=stream)
-        moe_expert_forward_nvfp4(self.weights, T, k, offs, out, ws, stream=stream)
+        if not save_for_backward:
+            self._saved = None
+            moe_expert_forward_nvfp4(self.weights, T, k, offs, out, ws, stream=stream)
+            return out
+        L = moe_workspace_layout_query(T, self.H, self.I, self.E, k)
+        fc1_pre = torch.empty((L.rows_cap, 2 * self.I), dtype=torch.float32, device=x.device)
+        moe_fc1_swiglu_nvfp4(self.weights, T, k, offs, ws, debug=fc1_pre, stream=stream)
+        moe_requant_nvfp4(self.weights, T, k, offs, ws, stream=stream)
+        moe_fc2_nvfp4(self.weights, T, k, offs, ws, stream=stream)
+        moe_combine_bf16(self.weights, T, k, out, ws, stream=stream)
+        self._saved = (x, offs, ws, fc1_pre, T, k)
         return out
+
+    def backward(self, dout, stream=None):
+        """(dx bf16 [T, H], dw1 f32 [E, 2I, H], dw2 f32 [E, H, I], dprob f32 [T, k]) of the
+        last forward run with save_for_backward=True."""
+        if self._saved is None:
+            raise RuntimeError("backward needs a forward with save_for_backward=True")
+        x, offs, ws, fc1_pre, T, k = self._saved
+        if self._wt is None:
+            self._wt = MoEWeightsBF16T(*self._w_bf16, stream=stream)
+        dev = x.device
+        dx = torch.empty((T, self.H), dtype=torch.bfloat16, device=dev)
+        dw1 = torch.empty((self.E, 2 * self.I, self.H), dtype=torch.float32, device=dev)
+        dw2 = torch.empty((self.E, self.H, self.I), dtype=torch.float32, device=dev)
+        dprob = torch.empty((T, k), dtype=torch.float32, device=dev)
+        bws = alloc_backward_workspace(T, self.H, self.I, self.E, k, dev)
+        moe_expert_backward_ste(self._wt, T, k, x, dout, offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws,
+                                stream=stream)
+        return dx, dw1, dw2, dprob
 
 
 # ---------------------------------------------------------------- layout helpers

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libnvfp4moe.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["quant.cu", "gemm.cu", "combine.cu", "router.cu", "api.cu", "route_noalloc.cu"]
+SOURCES = ["quant.cu", "gemm.cu", "combine.cu", "router.cu", "api.cu", "route_noalloc.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

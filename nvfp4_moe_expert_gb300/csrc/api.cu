@@ -4,6 +4,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "backward.cuh"
 #include "common.cuh"
 
 namespace nvfp4 {
@@ -86,6 +87,35 @@ void compute_layout(int64_t T, int H, int I, int E, int k, moe_workspace_layout*
     L->a2_g = take(rc * 4);
     L->y = take(R * H * 2);
     L->total = o;
+}
+
+// Scratch of the straight-through backward (sizes from the forward's contiguous layout).
+void compute_backward_layout(int64_t T, int H, int I, int E, int k, moe_backward_layout* B) {
+    moe_workspace_layout L;
+    compute_layout(T, H, I, E, k, &L);
+    std::memset(B, 0, sizeof(*B));
+    B->T = T;
+    B->H = H;
+    B->I = I;
+    B->E = E;
+    B->k = k;
+    const int64_t rc = L.rows_cap;
+    B->rows_cap = rc;
+    size_t o = 0;
+    auto take = [&o](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    B->dy_rows = take(rc * H * 2);
+    B->dh = take(rc * I * 2);
+    B->dgu = take(rc * 2 * I * 2);
+    B->dx_pairs = take(T * k * H * 2);
+    B->dy_t = take(rc * H * 2);
+    B->h_t = take(rc * I * 2);
+    B->dgu_t = take(rc * 2 * I * 2);
+    B->x_t = take(rc * H * 2);
+    B->total = o;
 }
 
 nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
@@ -436,6 +466,95 @@ nvfp4_status moe_expert_forward_nvfp4_masked(const moe_nvfp4_weights* w, int64_t
     s = moe_fc2_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, true, capacity);
     if (s != NVFP4_OK) return s;
     return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, true, capacity);
+}
+
+nvfp4_status nvfp4_transpose_bf16(const void* in_dev, int64_t batch, int64_t rows, int64_t cols, void* out_dev,
+                                  void* stream) {
+    if (batch < 0 || batch > 65535 || rows < 0 || cols < 0 || rows % 64 || cols % 64 || rows > (int64_t(1) << 26) ||
+        cols > (int64_t(1) << 26))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (batch == 0 || rows == 0 || cols == 0) return NVFP4_OK;
+    if (!in_dev || !out_dev) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(in_dev, 16) || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(launch_transpose_bf16(static_cast<const uint16_t*>(in_dev), batch, rows, cols,
+                                           static_cast<uint16_t*>(out_dev), static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status moe_backward_layout_query(int64_t T, int H, int I, int E, int k, moe_backward_layout* out) {
+    if (!out) return NVFP4_ERR_INVALID_ARG;
+    if (!moe_shape_ok(T, H, I, E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    compute_backward_layout(T, H, I, E, k, out);
+    return NVFP4_OK;
+}
+
+size_t moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k) {
+    if (!moe_shape_ok(T, H, I, E, k)) return 0;
+    moe_backward_layout B;
+    compute_backward_layout(T, H, I, E, k, &B);
+    return B.total;
+}
+
+nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int k, const void* x_dev,
+                                     const void* dout_dev, const int32_t* expert_offsets_dev, const void* fwd_ws_dev,
+                                     size_t fwd_ws_bytes, const float* fc1_pre_dev, void* dx_dev, float* dw1_dev,
+                                     float* dw2_dev, float* dprob_dev, void* bwd_ws_dev, size_t bwd_ws_bytes,
+                                     void* stream) {
+    if (!w) return NVFP4_ERR_INVALID_ARG;
+    if (!moe_shape_ok(T, w->H, w->I, w->E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!w->w1t || !w->w2t || !dw1_dev || !dw2_dev) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(w->w1t, 16) || !aligned(w->w2t, 16) || !aligned(dw1_dev, 32) || !aligned(dw2_dev, 32))
+        return NVFP4_ERR_INVALID_ARG;
+    const int H = w->H, I = w->I, E = w->E;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(dw1_dev, 0, static_cast<size_t>(E) * 2 * I * H * 4, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dw2_dev, 0, static_cast<size_t>(E) * H * I * 4, st);
+        return from_cuda(e);
+    }
+    if (!x_dev || !dout_dev || !expert_offsets_dev || !fwd_ws_dev || !fc1_pre_dev || !dx_dev || !dprob_dev ||
+        !bwd_ws_dev)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x_dev, 16) || !aligned(dout_dev, 16) || !aligned(expert_offsets_dev, 4) || !aligned(fwd_ws_dev, 256) ||
+        !aligned(fc1_pre_dev, 16) || !aligned(dx_dev, 16) || !aligned(dprob_dev, 4) || !aligned(bwd_ws_dev, 256))
+        return NVFP4_ERR_INVALID_ARG;
+    moe_workspace_layout L;
+    compute_layout(T, H, I, E, k, &L);
+    moe_backward_layout B;
+    compute_backward_layout(T, H, I, E, k, &B);
+    if (fwd_ws_bytes < L.total || bwd_ws_bytes < B.total) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+    int* err = device_error_ptr();
+    if (!err) return NVFP4_ERR_CUDA;
+    void* fws = const_cast<void*>(fwd_ws_dev);
+    BackwardArgs a{};
+    a.T = T;
+    a.H = H;
+    a.I = I;
+    a.E = E;
+    a.k = k;
+    a.rows_cap = L.rows_cap;
+    a.w1t = static_cast<const uint16_t*>(w->w1t);
+    a.w2t = static_cast<const uint16_t*>(w->w2t);
+    a.x = static_cast<const uint16_t*>(x_dev);
+    a.dout = static_cast<const uint16_t*>(dout_dev);
+    a.offsets = expert_offsets_dev;
+    a.row_pair = at<int32_t>(fws, L.row_pair);
+    a.row_prob = at<float>(fws, L.row_prob);
+    a.h = at<uint16_t>(fws, L.h);
+    a.fc1_pre = fc1_pre_dev;
+    a.dx = static_cast<uint16_t*>(dx_dev);
+    a.dw1 = dw1_dev;
+    a.dw2 = dw2_dev;
+    a.dprob = dprob_dev;
+    a.dy_rows = at<uint16_t>(bwd_ws_dev, B.dy_rows);
+    a.dh = at<uint16_t>(bwd_ws_dev, B.dh);
+    a.dgu = at<uint16_t>(bwd_ws_dev, B.dgu);
+    a.dx_pairs = at<uint16_t>(bwd_ws_dev, B.dx_pairs);
+    a.dy_t = at<uint16_t>(bwd_ws_dev, B.dy_t);
+    a.h_t = at<uint16_t>(bwd_ws_dev, B.h_t);
+    a.dgu_t = at<uint16_t>(bwd_ws_dev, B.dgu_t);
+    a.x_t = at<uint16_t>(bwd_ws_dev, B.x_t);
+    a.err = err;
+    return from_cuda(launch_moe_backward_ste(a, st));
 }
 
 nvfp4_status nvfp4_get_device_error(void* stream, int* device_status) {

@@ -164,6 +164,42 @@ def test_forward_validation(lib):
     assert lib.moe_combine_bf16(ctypes.byref(w), 16, 2, ws, ws, need - 1, None) == 3
 
 
+def test_backward_layout(lib):
+    T, H, I, E, k = 4096, 2048, 768, 128, 8
+    B_ = M.moe_backward_layout_query(T, H, I, E, k)
+    L = M.moe_workspace_layout_query(T, H, I, E, k)
+    assert B_.rows_cap == L.rows_cap
+    offs = [B_.dy_rows, B_.dh, B_.dgu, B_.dx_pairs, B_.dy_t, B_.h_t, B_.dgu_t, B_.x_t, B_.total]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    rc = L.rows_cap
+    sizes = [rc * H * 2, rc * I * 2, rc * 2 * I * 2, T * k * H * 2, rc * H * 2, rc * I * 2, rc * 2 * I * 2, rc * H * 2]
+    assert all(b - a >= n for a, b, n in zip(offs[:-1], offs[1:], sizes))
+    assert B_.total == lib.moe_backward_workspace_bytes(T, H, I, E, k)
+    assert lib.moe_backward_workspace_bytes(T, 2000, I, E, k) == 0
+
+
+def test_backward_validation(lib):
+    p = 4096
+    w = M.moe_bf16_weights_t(p, p, 8, 256, 128)
+    fwd = M.moe_workspace_bytes(16, 256, 128, 8, 2)
+    bwd = lib.moe_backward_workspace_bytes(16, 256, 128, 8, 2)
+    q = ctypes.c_void_p(p)
+    f = lambda w_=ctypes.byref(w), T=16, k=2, dw=q, fws=fwd, bws=bwd, x=q: lib.moe_expert_backward_ste(  # noqa: E731
+        w_, T, k, x, q, q, q, fws, q, q, dw, dw, q, q, bws, None)
+    assert f(w_=None) == 1
+    assert f(k=9) == 2
+    assert f(fws=fwd - 1) == 3 and f(bws=bwd - 1) == 3
+    assert f(dw=ctypes.c_void_p(p + 16)) == 1               # weight gradients are stored 32 bytes at a time
+    assert f(x=None) == 1
+    assert f(x=ctypes.c_void_p(p + 8)) == 1
+    assert lib.moe_expert_backward_ste(ctypes.byref(M.moe_bf16_weights_t(0, p, 8, 256, 128)), 16, 2, q, q, q, q,
+                                       fwd, q, q, q, q, q, q, bwd, None) == 1
+    t = lib.nvfp4_transpose_bf16
+    assert t(q, 2, 100, 64, q, None) == 2 and t(q, 2, 64, 96, q, None) == 2 and t(q, 70000, 64, 64, q, None) == 2
+    assert t(None, 2, 64, 64, q, None) == 1 and t(q, 2, 64, 64, ctypes.c_void_p(p + 2), None) == 1
+    assert t(None, 0, 64, 64, None, None) == 0              # empty: nothing launched
+
+
 def test_device_error_requires_pointer(lib):
     assert lib.nvfp4_get_device_error(None, None) == 1
 
