@@ -365,6 +365,16 @@ def moe_expert_backward_ste(wt, T, k, x, dout, expert_offsets, ws, fc1_pre, dx, 
                             stream=None):
     """STE gradients (dx, dw1, dw2, dprob written in place) of the forward whose route
     sort filled `ws` / `expert_offsets` and whose FC1 stage wrote `fc1_pre`."""
+    E, H, I = wt.E, wt.H, wt.I
+    want = ((x, torch.bfloat16, (T, H)), (dout, torch.bfloat16, (T, H)), (dx, torch.bfloat16, (T, H)),
+            (dw1, torch.float32, (E, 2 * I, H)), (dw2, torch.float32, (E, H, I)), (dprob, torch.float32, (T, k)),
+            (expert_offsets, torch.int32, (E + 1,)))
+    for t, dt, shape in want:
+        if T > 0 or t is dw1 or t is dw2:
+            if t.dtype != dt or tuple(t.shape) != shape:
+                raise ValueError(f"expected {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
+    if T > 0 and (fc1_pre.dtype != torch.float32 or fc1_pre.numel() < 2 * I * nvfp4_rows_padded(1)):
+        raise ValueError("fc1_pre must be the float32 [rows_cap, 2I] buffer FC1 wrote")
     _need_cuda(x, dout, expert_offsets, ws, fc1_pre, dx, dw1, dw2, dprob, bws)
     _check("moe_expert_backward_ste", lib().moe_expert_backward_ste(
         wt.ref(), T, k, _ptr(x), _ptr(dout), _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(fc1_pre),

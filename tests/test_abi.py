@@ -210,3 +210,27 @@ def test_product_path_has_no_oracle_import():
         if path.endswith((".py", ".cu", ".cuh", ".h")):
             src = open(path).read()
             assert "oracle" not in src.replace("the oracle", ""), path
+
+
+def test_backward_binding_checks_tensors(lib):
+    import torch
+    E, H, I, T, k = 4, 256, 128, 8, 2
+    wt = type("W", (), {"E": E, "H": H, "I": I})()
+    bf, f32 = torch.bfloat16, torch.float32
+    ok = dict(x=torch.zeros(T, H, dtype=bf), dout=torch.zeros(T, H, dtype=bf),
+              offs=torch.zeros(E + 1, dtype=torch.int32), ws=torch.zeros(16, dtype=torch.uint8),
+              pre=torch.zeros(256, 2 * I, dtype=f32), dx=torch.zeros(T, H, dtype=bf),
+              dw1=torch.zeros(E, 2 * I, H), dw2=torch.zeros(E, H, I), dprob=torch.zeros(T, k))
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        M.moe_expert_backward_ste(wt, T, k, a["x"], a["dout"], a["offs"], a["ws"], a["pre"], a["dx"], a["dw1"],
+                                  a["dw2"], a["dprob"], a["ws"])
+    with pytest.raises(ValueError, match="float32"):
+        call(dw1=torch.zeros(E, 2 * I, H, dtype=bf))
+    with pytest.raises(ValueError, match=r"\(8, 2\)"):
+        call(dprob=torch.zeros(T, k + 1))
+    with pytest.raises(ValueError, match="fc1_pre"):
+        call(pre=torch.zeros(4, dtype=f32))
+    with pytest.raises(ValueError, match="CUDA"):      # right shapes, but host tensors: refused before any call
+        call()
