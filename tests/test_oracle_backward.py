@@ -153,3 +153,18 @@ def test_bf16_stages_bound():
         rel = np.linalg.norm(st[name] - ex[name]) / np.linalg.norm(ex[name])
         assert 0 < rel <= 2 * np.sqrt(stages) * u, (name, rel)
     assert np.array_equal(st["dw2"], ex["dw2"])               # dW2 needs no rounded tensor
+
+
+def test_silu_derivative_closed_forms():
+    # sigma(0) = 1/2; sigma(ln 3) = 3/4; sigma(-ln 3) = 1/4; the limits 0 and 1
+    a = np.array([0.0, np.log(3.0), -np.log(3.0), 40.0, -40.0])
+    silu, d = B.silu_and_derivative(a)
+    want_silu = np.array([0.0, 0.75 * np.log(3.0), -0.25 * np.log(3.0), 40.0, 0.0])
+    want_d = np.array([0.5, 0.75 * (1 + 0.25 * np.log(3.0)), 0.25 * (1 - 0.75 * np.log(3.0)), 1.0, 0.0])
+    assert np.allclose(silu, want_silu, rtol=1e-15, atol=1e-15)
+    assert np.allclose(d, want_d, rtol=1e-15, atol=1e-15)
+    # and the derivative is the slope of silu
+    x = np.linspace(-8, 8, 161)
+    eps = 1e-6
+    fd = (B.silu_and_derivative(x + eps)[0] - B.silu_and_derivative(x - eps)[0]) / (2 * eps)
+    assert np.abs(B.silu_and_derivative(x)[1] - fd).max() < 1e-8
