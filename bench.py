@@ -149,6 +149,37 @@ def roofline_of(name, work, ms, peaks, peak_kind):
             "algorithmic": f"{b:.4g} bytes per launch"}
 
 
+def backward_work(cfg):
+    """Algorithmic FLOPs and bytes of one moe_expert_backward_ste call: four BF16 GEMMs
+    (2RHI, 2R(2I)H, 2RHI, 2R(2I)H FLOPs); the transposed BF16 weights read once, the FP32
+    weight gradients written once, x, dOut, the saved h (BF16) and FC1 values (FP32) read,
+    dX and dprob written."""
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    R = T * k
+    flops = 12 * R * H * I
+    nbytes = (E * 3 * I * H * 2 + E * 3 * I * H * 4 + 2 * T * H * 2 + R * I * 2 + R * 2 * I * 4
+              + T * H * 2 + R * 4)
+    return {"flops": flops, "bytes": nbytes}
+
+
+def backward_roofline(work, ms, peaks, peak_kind):
+    """The binding bound of the backward (BF16 tensor peak or HBM copy bandwidth) and the
+    fraction of it that `ms` per call reaches."""
+    hbm = float(peaks["hbm_gbs"])
+    bf16 = float(peaks["bf16_tflops"])
+    t_mem = work["bytes"] / (hbm * 1e9)
+    t_cmp = work["flops"] / (bf16 * 1e12)
+    out = {"algorithmic": f"{work['flops']:.4g} FLOP (12 T k H I) and {work['bytes']:.4g} bytes per call",
+           "bound_ms": round(1e3 * max(t_mem, t_cmp), 4), "peak_note": "of " + peak_kind}
+    if t_cmp > t_mem:
+        ach = work["flops"] / (ms * 1e-3) / 1e12
+        return out | {"bound": "tensor", "achieved": round(ach, 2), "peak": bf16, "unit": "TFLOP/s",
+                      "frac": round(ach / bf16, 4)}
+    ach = work["bytes"] / (ms * 1e-3) / 1e9
+    return out | {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                  "frac": round(ach / hbm, 4)}
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -594,12 +625,11 @@ def backward_step(M, torch, cfg, weights, w1, w2, x, ids, pw, ws, offs, flush, s
     if M.nvfp4_get_device_error() != 0:
         raise RuntimeError("device error in the backward step")
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    flops = 12 * T * k * H * I           # four GEMMs of 2*R*H*I, two of them over 2I
-    bf16 = float(peaks["bf16_tflops"])
-    ach = flops / (ms * 1e-3) / 1e12
-    return {"ms": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1), "bound": "tensor",
-            "achieved": round(ach, 2), "peak": bf16, "unit": "TFLOP/s", "frac": round(ach / bf16, 4),
-            "peak_note": "of " + peak_kind, "algorithmic": f"{flops:.4g} FLOP per call (12 T k H I)",
+    work = backward_work(cfg)
+    tflops = work["flops"] / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
+            **backward_roofline(work, ms, peaks, peak_kind),
+            "gemm_tflops": round(tflops, 2),
             "finite": bool(torch.isfinite(dw1).all() and torch.isfinite(dw2).all()),
             "note": "moe_expert_backward_ste: STE gradients dX, dW1, dW2, dprob from the saved BF16 "
                     "originals; timed on its own after a forward that saves FC1's values"}

@@ -51,3 +51,19 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = lines[0]
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_backward_roofline_arithmetic():
+    import bench
+    peaks = {"hbm_gbs": 6791.7, "bf16_tflops": 1916.3}
+    c2 = S.CONFIGS["qwen3_30b_a3b"]
+    w = bench.backward_work(c2)
+    assert w["flops"] == 12 * 4096 * 8 * 2048 * 768
+    # BF16 weights read (E*3IH*2) and FP32 weight gradients written (E*3IH*4) dominate
+    assert 3.9e9 < w["bytes"] < 4.0e9
+    r = bench.backward_roofline(w, 1.6705, peaks, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"           # 0.58 ms of bytes vs 0.32 ms of FLOPs
+    assert r["frac"] == pytest.approx(w["bytes"] / 1.6705e-3 / 6791.7e9, abs=1e-4)
+    assert r["bound_ms"] == pytest.approx(1e3 * w["bytes"] / 6791.7e9, abs=1e-3)
+    big = bench.backward_roofline(bench.backward_work(S.CONFIGS["large"]), 20.0, peaks, "measured")
+    assert big["bound"] == "tensor" and big["unit"] == "TFLOP/s"
