@@ -376,8 +376,9 @@ size_t moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k);
  *  bwd_ws_dev, bwd_ws_bytes  scratch, moe_backward_workspace_bytes(T, H, I, E, k) bytes,
  *                       256-byte aligned
  * Nothing is allocated and nothing synchronises; every output is written in stream order.
- * T == 0 zeroes dW1 and dW2.  Argument errors as for moe_expert_forward_nvfp4; device error
- * NVFP4_ERR_DEVICE_TIMEOUT (a pipeline wait ran out). */
+ * T == 0 zeroes dW1 and dW2.  Argument errors as for moe_expert_forward_nvfp4, and
+ * NVFP4_ERR_UNSUPPORTED_SHAPE if rows_cap >= 2^30; device error NVFP4_ERR_DEVICE_TIMEOUT (a
+ * pipeline wait ran out). */
 nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int k, const void* x_dev,
                                      const void* dout_dev, const int32_t* expert_offsets_dev, const void* fwd_ws_dev,
                                      size_t fwd_ws_bytes, const float* fc1_pre_dev, void* dx_dev, float* dw1_dev,

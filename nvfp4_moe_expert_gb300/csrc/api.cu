@@ -519,6 +519,8 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
         return NVFP4_ERR_INVALID_ARG;
     moe_workspace_layout L;
     compute_layout(T, H, I, E, k, &L);
+    // the weight-gradient GEMMs address routed rows as byte coordinates (2 per row) in int32
+    if (L.rows_cap >= (int64_t(1) << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     moe_backward_layout B;
     compute_backward_layout(T, H, I, E, k, &B);
     if (fwd_ws_bytes < L.total || bwd_ws_bytes < B.total) return NVFP4_ERR_WORKSPACE_TOO_SMALL;

@@ -194,6 +194,10 @@ def test_backward_validation(lib):
     assert f(x=ctypes.c_void_p(p + 8)) == 1
     assert lib.moe_expert_backward_ste(ctypes.byref(M.moe_bf16_weights_t(0, p, 8, 256, 128)), 16, 2, q, q, q, q,
                                        fwd, q, q, q, q, q, q, bwd, None) == 1
+    # T*k just under 2^30 passes the shape check, but its rows_cap reaches 2^30
+    big_T = (1 << 30) // 2 - 1
+    assert lib.moe_expert_backward_ste(ctypes.byref(w), big_T, 2, q, q, q, q, 1 << 62, q, q, q, q, q, q, 1 << 62,
+                                       None) == 2
     t = lib.nvfp4_transpose_bf16
     assert t(q, 2, 100, 64, q, None) == 2 and t(q, 2, 64, 96, q, None) == 2 and t(q, 70000, 64, 64, q, None) == 2
     assert t(None, 2, 64, 64, q, None) == 1 and t(q, 2, 64, 64, ctypes.c_void_p(p + 2), None) == 1
