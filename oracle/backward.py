@@ -26,8 +26,8 @@ taken as the identity, every other op differentiated where it ran):
 
 Precision: FP64 on the given values (``bf16_stages=False``, the exact reading
 that the page's FP32 reference approximates).  ``bf16_stages=True`` also rounds
-to BF16 where a BF16 GEMM pipeline hands a tensor on (the readings listed in
-the design doc): dh (a BF16 GEMM output), [da, du] (the BF16 operand of the FC1
+to BF16 where a BF16 GEMM pipeline hands a tensor on (a reading: the page
+names no rounding points): dh (a BF16 GEMM output), [da, du] (the BF16 operand of the FC1
 dgrad and wgrad GEMMs), each slot's dx (a BF16 GEMM output), and dX, summed in
 FP32 in slot order and rounded once.  The weight gradients and dp stay FP64.
 

@@ -21,7 +21,7 @@ Sources:
   neighbours; section 4.5 "Cross-GPU reduction": expert outputs are summed in
   FP32 in top-k slot order.
 
-Readings where the pages are silent (all listed in the design doc): the GEMM
+Readings where the pages are silent: the GEMM
 accumulation is exact (FP64 on the exactly dequantised operands q*s, outer
 scales applied afterwards, (acc*g^x)*g^w, one rounding to BF16); W1's rows are
 gate rows 0..I-1 then up rows I..2I-1; SiLU(a) = a / (1 + exp(-a)) evaluated in

@@ -10,7 +10,7 @@ scale, elements get E2M1 codes; rounding is round-to-nearest-even; no Hadamard
 transform, no stochastic rounding.
 
 The page gives the outer scale but not how the block scale is derived from it
-nor the FP32 operation order.  Readings (each also listed in the design doc):
+nor the FP32 operation order.  Readings taken:
 
 1. block scale  s_b = e4m3( bmax / (g * 6) )  with bmax = max|x| over the block:
    the largest code magnitude 6 times s_b times g reaches bmax, and since

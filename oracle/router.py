@@ -14,7 +14,7 @@ performance, agent-driven" (spke.com/ko/ai/article/3192):
 * section 4.4 (the "R3 unnecessary" paragraph): with the single FP32-output
   router kernel the recomputed routing matches the rollout's.
 
-Readings (listed in the design doc): logits[t, e] = sum_h x[t, h] * W_r[e, h] on the
+Readings taken: logits[t, e] = sum_h x[t, h] * W_r[e, h] on the
 BF16 values, here exact (FP64 of exactly representable products); the k
 selected experts are the k largest logits, a larger logit first and, on equal
 logits, the lower expert id first (softmax is monotonic, so this is the order
