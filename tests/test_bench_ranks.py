@@ -67,3 +67,20 @@ def test_backward_roofline_arithmetic():
     assert r["bound_ms"] == pytest.approx(1e3 * w["bytes"] / 6791.7e9, abs=1e-3)
     big = bench.backward_roofline(bench.backward_work(S.CONFIGS["large"]), 20.0, peaks, "measured")
     assert big["bound"] == "tensor" and big["unit"] == "TFLOP/s"
+
+
+def test_forward_stage_roofline_arithmetic():
+    import bench
+    peaks = {"hbm_gbs": 6791.7, "bf16_tflops": 1916.3}
+    c2 = S.CONFIGS["qwen3_30b_a3b"]
+    w = bench.stage_work(c2)
+    # per token: X read once, k quantised copies (codes + scales + g), row maps
+    assert w["route_sort_quant"]["bytes"] == 4096 * 13504
+    # FC1 at 4096 tokens streams every expert's weights once: 201 MB of codes + 25 MB of scales
+    assert w["fc1_swiglu"]["bytes"] == 128 * 1536 * (1024 + 128 + 4) + 32768 * (1024 + 128 + 4) + 32768 * (1536 + 12)
+    assert w["fc1_swiglu"]["flops"] == 2 * 32768 * 2048 * 1536
+    r = bench.roofline_of("fc1_swiglu", w["fc1_swiglu"], 0.0953, peaks, "measured")
+    assert r["bound"] == "hbm" and r["frac"] == pytest.approx(w["fc1_swiglu"]["bytes"] / 95.3e-6 / 6791.7e9, abs=1e-4)
+    big = bench.stage_work(S.CONFIGS["large"])["fc1_swiglu"]
+    rb = bench.roofline_of("fc1_swiglu", big, 1.41, peaks, "measured")
+    assert rb["bound"] == "tensor" and rb["peak"] == pytest.approx(1916.3 * bench.FP4_OVER_BF16, abs=0.1)
