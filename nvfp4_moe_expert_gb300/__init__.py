@@ -386,15 +386,33 @@ class MoELayer:
 
     ``forward(..., save_for_backward=True)`` runs the forward stage by stage and keeps
     what the straight-through backward reads (the route, h, FC1's FP32 values);
-    ``backward(dout)`` then returns (dx, dw1, dw2, dprob)."""
+    ``backward(dout)`` then returns (dx, dw1, dw2, dprob).
+
+    The BF16 weights are the master copy: a forward after they were changed in place (an
+    optimizer step) quantises them again, and a backward refuses to run if they changed after
+    its forward, so one forward/backward pair never mixes two weight versions ("Finishing RL
+    training faster: bitwise consistency, high performance, agent-driven", section 3.1, the
+    inference kernels define the values and training adds the backward: each backward first
+    checks that the master weights are those of its forward)."""
 
     def __init__(self, w1, w2, stream=None):
-        self.weights = quantize_moe_weights(w1, w2, stream=stream)
-        self.E, self.H, self.I = self.weights.E, self.weights.H, self.weights.I
         self._w_bf16 = (w1, w2)
-        self._wt = None
         self._saved = None
         self._ws = {}
+        self._quantize(stream)
+
+    def _weight_version(self):
+        return tuple(t._version for t in self._w_bf16)
+
+    def _quantize(self, stream=None):
+        self.weights = quantize_moe_weights(*self._w_bf16, stream=stream)
+        self.E, self.H, self.I = self.weights.E, self.weights.H, self.weights.I
+        self._wt = None                      # transposed copies for the backward, made on demand
+        self._wver = self._weight_version()
+
+    def _refresh_if_changed(self, stream=None):
+        if self._weight_version() != self._wver:
+            self._quantize(stream)
 
     def workspace(self, T, k, device):
         key = (T, k)
@@ -404,6 +422,7 @@ class MoELayer:
         return self._ws[key]
 
     def forward(self, x, topk_ids, topk_w, out=None, stream=None, save_for_backward=False):
+        self._refresh_if_changed(stream)
         T, H = x.shape
         k = topk_ids.shape[1]
         ws = self.workspace(T, k, x.device)
@@ -421,7 +440,7 @@ class MoELayer:
         moe_requant_nvfp4(self.weights, T, k, offs, ws, stream=stream)
         moe_fc2_nvfp4(self.weights, T, k, offs, ws, stream=stream)
         moe_combine_bf16(self.weights, T, k, out, ws, stream=stream)
-        self._saved = (x, offs, ws, fc1_pre, T, k)
+        self._saved = (x, offs, ws, fc1_pre, T, k, self._wver)
         return out
 
     def backward(self, dout, stream=None):
@@ -429,7 +448,9 @@ class MoELayer:
         last forward run with save_for_backward=True."""
         if self._saved is None:
             raise RuntimeError("backward needs a forward with save_for_backward=True")
-        x, offs, ws, fc1_pre, T, k = self._saved
+        x, offs, ws, fc1_pre, T, k, wver = self._saved
+        if self._weight_version() != wver:
+            raise RuntimeError("the weights changed after the forward this backward belongs to")
         if self._wt is None:
             self._wt = MoEWeightsBF16T(*self._w_bf16, stream=stream)
         dev = x.device

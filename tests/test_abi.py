@@ -238,3 +238,29 @@ def test_backward_binding_checks_tensors(lib):
         call(pre=torch.zeros(4, dtype=f32))
     with pytest.raises(ValueError, match="CUDA"):      # right shapes, but host tensors: refused before any call
         call()
+
+
+def test_layer_weight_versions():
+    # host logic of MoELayer's weight-version checks, with the quantisation stubbed out
+    import torch
+    layer = M.MoELayer.__new__(M.MoELayer)
+    calls = []
+
+    def fake_quantize(stream=None):
+        calls.append(1)
+        layer._wt = None
+        layer._wver = layer._weight_version()
+
+    layer._quantize = fake_quantize
+    layer._w_bf16 = (torch.zeros(2, 4), torch.zeros(2, 4))
+    layer._quantize()
+    layer._refresh_if_changed()
+    assert len(calls) == 1                           # unchanged weights: nothing to do
+    layer._w_bf16[0].add_(1.0)                       # an optimizer step updates a weight in place
+    layer._refresh_if_changed()
+    assert len(calls) == 2 and layer._wver == layer._weight_version()
+    # a backward whose forward saw an older version refuses to run
+    layer._saved = (None, None, None, None, 0, 1, layer._wver)
+    layer._w_bf16[1].mul_(2.0)
+    with pytest.raises(RuntimeError, match="weights changed"):
+        layer.backward(None)
