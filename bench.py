@@ -149,6 +149,18 @@ def roofline_of(name, work, ms, peaks, peak_kind):
             "algorithmic": f"{b:.4g} bytes per launch"}
 
 
+def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
+    """The step's roofline: the sum over its stages of each stage's bound time (the larger of
+    algorithmic bytes / copy bandwidth and FLOPs / FP4 peak), against the measured step time."""
+    hbm = float(peaks["hbm_gbs"])
+    fp4 = float(peaks["bf16_tflops"]) * FP4_OVER_BF16
+    per = {n: max(w["bytes"] / (hbm * 1e9), w["flops"] / (fp4 * 1e12)) for n, w in stage_work(cfg).items()}
+    bound_ms = 1e3 * sum(per.values())
+    return {"bound_ms": round(bound_ms, 4), "measured_ms": round(ms_per_step, 4),
+            "frac": round(bound_ms / ms_per_step, 4), "stage_bound_us": {n: round(1e6 * t, 2) for n, t in per.items()},
+            "peak_note": "of " + peak_kind}
+
+
 def backward_work(cfg):
     """Algorithmic FLOPs and bytes of one moe_expert_backward_ste call: four BF16 GEMMs
     (2RHI, 2R(2I)H, 2RHI, 2R(2I)H FLOPs); the transposed BF16 weights read once, the FP32
@@ -572,6 +584,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "data": "synthetic (seeded; random-init weights of the layer's shape)",
         "config": describe(cfg) | {"parallelism": f"token shards x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
+        "layer_roofline": layer_roofline(cfg, peaks, peak_kind, total_ms / K),
         "kernels": kernels,
         "weight_quant_ms": round(wq_ms, 3),
         "router_step": router,

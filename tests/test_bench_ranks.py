@@ -84,3 +84,15 @@ def test_forward_stage_roofline_arithmetic():
     big = bench.stage_work(S.CONFIGS["large"])["fc1_swiglu"]
     rb = bench.roofline_of("fc1_swiglu", big, 1.41, peaks, "measured")
     assert rb["bound"] == "tensor" and rb["peak"] == pytest.approx(1916.3 * bench.FP4_OVER_BF16, abs=0.1)
+
+
+def test_layer_roofline_arithmetic():
+    import bench
+    peaks = {"hbm_gbs": 6791.7, "bf16_tflops": 1916.3}
+    r = bench.layer_roofline(S.CONFIGS["qwen3_30b_a3b"], peaks, "measured", 0.2554)
+    per = r["stage_bound_us"]
+    assert set(per) == {"route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"}
+    # at 4096 tokens every stage is bound by its bytes: FC1's weight stream is ~46 us
+    assert 45 < per["fc1_swiglu"] < 48 and 7 < per["route_sort_quant"] < 9
+    assert r["bound_ms"] == pytest.approx(sum(per.values()) / 1e3, abs=1e-3)
+    assert r["frac"] == pytest.approx(r["bound_ms"] / 0.2554, abs=1e-3)
