@@ -149,6 +149,29 @@ def roofline_of(name, work, ms, peaks, peak_kind):
             "algorithmic": f"{b:.4g} bytes per launch"}
 
 
+def batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev, sizes=(1, 7, 64), n_decode=32):
+    """Bitwise batch invariance of the step: the first n tokens run as a batch of their own, and
+    n_decode tokens spread over the batch run one at a time (decode-shaped calls), give the same
+    BF16 output bits as in the full batch `out`."""
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    offs_n = torch.empty(E + 1, dtype=torch.int32, device=dev)
+
+    def run(lo, hi):
+        n = hi - lo
+        ws_n = M.alloc_workspace(n, H, I, E, k, dev)
+        out_n = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+        M.moe_route_sort_amax(x[lo:hi], ids[lo:hi], pw[lo:hi], E, offs_n, ws_n)
+        M.moe_expert_forward_nvfp4(weights, n, k, offs_n, out_n, ws_n)
+        return bool(torch.equal(out_n.view(torch.int16), out[lo:hi].view(torch.int16)))
+
+    batches = {str(n): run(0, n) for n in sorted(set(tuple(sizes) + (T // 2,))) if 0 < n < T}
+    step = max(1, T // n_decode)
+    decode = [run(t, t + 1) for t in range(0, T, step)][:n_decode]
+    return {"bitwise_equal": all(batches.values()) and all(decode), "batches": batches,
+            "decode_tokens": len(decode), "decode_equal": sum(decode),
+            "note": "first n tokens as their own batch, and single-token calls, against the full batch"}
+
+
 def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
     """The step's roofline: the sum over its stages of each stage's bound time (the larger of
     algorithmic bytes / copy bandwidth and FLOPs / FP4 peak), against the measured step time."""
@@ -512,6 +535,9 @@ def run_ours(args, cfg, rank, world, local_rank):
     # the contiguous step's output is recomputed so `out` holds it again for the checks below
     M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
     M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+    invariance = batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev)
+    if M.nvfp4_get_device_error() != 0:
+        raise RuntimeError("device error in the batch-invariance check")
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region.
     # A serving loop: every step copies its own inputs in and its output back, on two copy
@@ -585,6 +611,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "config": describe(cfg) | {"parallelism": f"token shards x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "layer_roofline": layer_roofline(cfg, peaks, peak_kind, total_ms / K),
+        "batch_invariance": invariance,
         "kernels": kernels,
         "weight_quant_ms": round(wq_ms, 3),
         "router_step": router,

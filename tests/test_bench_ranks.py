@@ -96,3 +96,37 @@ def test_layer_roofline_arithmetic():
     assert 45 < per["fc1_swiglu"] < 48 and 7 < per["route_sort_quant"] < 9
     assert r["bound_ms"] == pytest.approx(sum(per.values()) / 1e3, abs=1e-3)
     assert r["frac"] == pytest.approx(r["bound_ms"] / 0.2554, abs=1e-3)
+
+
+def test_batch_invariance_glue_on_cpu():
+    # bench.batch_invariance driven by a stand-in library on host tensors: a per-token
+    # computation passes, one that depends on the batch size fails
+    import torch
+    import bench
+
+    class Lib:
+        def __init__(self, batch_dependent):
+            self.batch_dependent = batch_dependent
+
+        def alloc_workspace(self, T, H, I, E, k, dev):
+            return torch.empty(1)
+
+        def moe_route_sort_amax(self, x, ids, pw, E, offs, ws):
+            self.x = x
+
+        def moe_expert_forward_nvfp4(self, w, T, k, offs, out, ws):
+            scale = float(T) if self.batch_dependent else 2.0
+            out.copy_((self.x.float() * scale).to(torch.bfloat16))
+
+    cfg = S.CONFIGS["tiny"]
+    x = torch.randn(cfg.T, cfg.H).to(torch.bfloat16)
+    ids = torch.zeros(cfg.T, cfg.k, dtype=torch.int32)
+    pw = torch.ones(cfg.T, cfg.k)
+    ok = Lib(False)
+    out = (x.float() * 2.0).to(torch.bfloat16)
+    r = bench.batch_invariance(ok, torch, cfg, None, x, ids, pw, out, "cpu")
+    assert r["bitwise_equal"] and set(r["batches"]) == {"1", "7", "32"} and r["decode_tokens"] == 32
+    bad = Lib(True)
+    out = (x.float() * cfg.T).to(torch.bfloat16)
+    r = bench.batch_invariance(bad, torch, cfg, None, x, ids, pw, out, "cpu")
+    assert not r["bitwise_equal"] and r["decode_equal"] == 0
