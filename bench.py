@@ -52,6 +52,12 @@ def parse():
     ap.add_argument("--workload", default="qwen3_30b_a3b", choices=sorted(S.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="time only the headline workload (skip the 16384-token skewed and large layers)")
+    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-seconds", type=float, default=5.0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-tokens", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-experts", type=int, default=8, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -149,10 +155,12 @@ def roofline_of(name, work, ms, peaks, peak_kind):
             "algorithmic": f"{b:.4g} bytes per launch"}
 
 
-def batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev, sizes=(1, 7, 64), n_decode=32):
-    """Bitwise batch invariance of the step: the first n tokens run as a batch of their own, and
-    n_decode tokens spread over the batch run one at a time (decode-shaped calls), give the same
-    BF16 output bits as in the full batch `out`."""
+def batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev, sizes=(1, 7, 64), n_decode=32, n_windows=3):
+    """Spot check of bitwise batch invariance on this workload: the first n tokens and n_windows
+    random contiguous windows of each size n run as batches of their own, and n_decode tokens
+    spread over the batch run one at a time (decode-shaped calls); each must give the same BF16
+    output bits as in the full batch `out` (the full sweep over 256 sequences of 64-2048 tokens
+    is tests/test_gpu_invariance.py)."""
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
     offs_n = torch.empty(E + 1, dtype=torch.int32, device=dev)
 
@@ -164,12 +172,19 @@ def batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev, sizes=(1, 7, 
         M.moe_expert_forward_nvfp4(weights, n, k, offs_n, out_n, ws_n)
         return bool(torch.equal(out_n.view(torch.int16), out[lo:hi].view(torch.int16)))
 
-    batches = {str(n): run(0, n) for n in sorted(set(tuple(sizes) + (T // 2,))) if 0 < n < T}
+    rng = np.random.default_rng(T)
+    calls = []
+    for n in sorted(set(tuple(sizes) + (T // 2,))):
+        if 0 < n < T:
+            calls.append((0, n))
+            calls += [(int(lo), int(lo) + n) for lo in rng.integers(1, T - n + 1, n_windows)]
+    equal = [run(lo, hi) for lo, hi in calls]
     step = max(1, T // n_decode)
     decode = [run(t, t + 1) for t in range(0, T, step)][:n_decode]
-    return {"bitwise_equal": all(batches.values()) and all(decode), "batches": batches,
-            "decode_tokens": len(decode), "decode_equal": sum(decode),
-            "note": "first n tokens as their own batch, and single-token calls, against the full batch"}
+    return {"bitwise_equal": all(equal) and all(decode), "batches": len(calls), "batches_equal": sum(equal),
+            "decode_calls": len(decode), "decode_equal": sum(decode),
+            "what": f"{cfg.name}: prefix and random-window sub-batches of {sorted(set(sizes + (T // 2,)))} "
+                    f"tokens and single-token calls vs the full batch"}
 
 
 def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
@@ -179,9 +194,9 @@ def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
     fp4 = float(peaks["bf16_tflops"]) * FP4_OVER_BF16
     per = {n: max(w["bytes"] / (hbm * 1e9), w["flops"] / (fp4 * 1e12)) for n, w in stage_work(cfg).items()}
     bound_ms = 1e3 * sum(per.values())
-    return {"bound_ms": round(bound_ms, 4), "measured_ms": round(ms_per_step, 4),
-            "frac": round(bound_ms / ms_per_step, 4), "stage_bound_us": {n: round(1e6 * t, 2) for n, t in per.items()},
-            "peak_note": "of " + peak_kind}
+    return {"frac": round(bound_ms / ms_per_step, 4), "bound_ms": round(bound_ms, 4),
+            "measured_ms": round(ms_per_step, 4),
+            "stage_bound_us": {n: round(1e6 * t, 2) for n, t in per.items()}, "peak_note": "of " + peak_kind}
 
 
 def backward_work(cfg):
@@ -259,14 +274,14 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def oracle_sample_rate(cfg, seconds=12.0, n_experts=8):
+def oracle_sample_rate(cfg, seconds=12.0, n_experts=8, T=None):
     """Time the CPU oracle on a bounded sample of the workload: every (token, slot)
-    pair routed to the first n experts (their weights quantised beforehand,
-    untimed), repeated until about `seconds` of CPU work.  Returns (tokens/s,
-    sample description, host cores)."""
+    pair of the first T tokens routed to the first n experts (their weights quantised
+    beforehand, untimed), repeated until about `seconds` of CPU work (at least one pass).
+    Returns (tokens/s, sample description)."""
     from oracle import moe as OM
-    ids, w = S.make_routing(cfg)
-    x = S.make_x(cfg)
+    ids, w = S.make_routing(cfg, T)
+    x = S.make_x(cfg, T)
     n_experts = max(1, min(cfg.E, n_experts))
     w1, w2 = S.make_weights(cfg, experts=n_experts)
     wq = OM.quantize_weights(w1, w2)
@@ -275,7 +290,8 @@ def oracle_sample_rate(cfg, seconds=12.0, n_experts=8):
     groups = []
     for e in range(n_experts):
         t_e, s_e = np.nonzero(ids == e)
-        groups.append((x[t_e], np.zeros((len(t_e), 1), np.int32) + e, w[t_e, s_e][:, None]))
+        if len(t_e):
+            groups.append((x[t_e], np.zeros((len(t_e), 1), np.int32) + e, w[t_e, s_e][:, None]))
     pairs = sum(len(g[0]) for g in groups)
     reps = 0
     t0 = time.perf_counter()
@@ -287,10 +303,64 @@ def oracle_sample_rate(cfg, seconds=12.0, n_experts=8):
         if dt >= seconds or reps >= 1000:
             break
     tokens_per_s = pairs * reps / cfg.k / dt
-    desc = (f"oracle (numpy, FP64 GEMMs) on every routed (token, slot) pair of experts 0..{n_experts - 1} "
-            f"of the {cfg.name} workload ({pairs} pairs), {reps} passes in {dt:.1f} s; "
-            f"tokens/s = pairs/s / top-{cfg.k}")
-    return tokens_per_s, desc, os.cpu_count()
+    n_tok = cfg.T if T is None else T
+    desc = (f"{cfg.name}: every routed (token, slot) pair of experts 0..{n_experts - 1} among the first "
+            f"{n_tok} tokens ({pairs} pairs), {reps} passes in {dt:.1f} s; tokens/s = pairs/s / top-{cfg.k}")
+    return tokens_per_s, desc
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_sample_subprocess(name, seconds, tokens=0, experts=8, threads=None):
+    """oracle_sample_rate in a child process (threads=1: numpy's BLAS held to one thread)."""
+    env = dict(os.environ)
+    if threads is not None:
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[v] = str(threads)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", name, "--oracle-seconds", str(seconds),
+           "--oracle-tokens", str(tokens), "--oracle-experts", str(experts)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baselines(cfg):
+    """The oracle on the host cores: the headline workload (all cores, and one thread), the
+    small 64-token layer in full, and bounded samples of 2048-token slices of the skewed
+    16384-token workload and of the large layer."""
+    v, desc = oracle_sample_rate(cfg, seconds=10.0)
+    out = {"value": round(v, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle", "sample": desc,
+           "cpu_model": cpu_model()}
+    one = oracle_sample_subprocess(cfg.name, 5.0, threads=1)
+    if one:
+        out["single_thread"] = {"value": round(one["value"], 3), "cores": 1, "sample": one["sample"]}
+    extra = {}
+    for name, tokens, experts in (("tiny", 0, 8), ("qwen3_30b_a3b_skew", 2048, 4), ("large", 2048, 1)):
+        if name in S.CONFIGS:
+            r = oracle_sample_subprocess(name, 4.0, tokens=tokens, experts=experts)
+            if r:
+                extra[name] = {"value": round(r["value"], 3), "unit": "tokens/s", "sample": r["sample"]}
+    out["workloads"] = extra
+    return out
 
 
 def max_over_ranks(x, world, device=None):
@@ -372,6 +442,98 @@ def run_reference(args, cfg, rank, world):
 
 
 # ---------------------------------------------------------------- GPU arm
+STAGES = ["route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"]
+
+
+def stage_times(M, torch, cfg, weights, x, ids, pw, offs, ws, out, flush, stream, n):
+    """Mean CUDA-event time (ms) of each stage over n passes of the step called stage by
+    stage (events on the launching stream between the stages), L2 flushed between passes."""
+    T, E, k = cfg.T, cfg.E, cfg.k
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(n)]
+    for i in range(n):
+        e = evs[i]
+        e[0].record(stream)
+        M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+        e[1].record(stream)
+        M.moe_fc1_swiglu_nvfp4(weights, T, k, offs, ws)
+        e[2].record(stream)
+        M.moe_requant_nvfp4(weights, T, k, offs, ws)
+        e[3].record(stream)
+        M.moe_fc2_nvfp4(weights, T, k, offs, ws)
+        e[4].record(stream)
+        M.moe_combine_bf16(weights, T, k, out, ws)
+        e[5].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    return {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
+            for j, name in enumerate(STAGES)}
+
+
+def time_steps(M, torch, weights, cfg, x, ids, pw, offs, ws, out, flush, stream, K, W):
+    """CUDA-event time (ms) of each of K steps (route sort + expert forward), after W warm-up
+    steps, L2 flushed between steps outside the events."""
+    T, E, k = cfg.T, cfg.E, cfg.k
+
+    def step():
+        M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+        M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+
+    for _ in range(W):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def extra_workload(M, torch, name, dev, stream, flush, K, W, peaks, peak_kind, to_dev):
+    """Throughput of one of the compute-bound workloads (the 16384-token skewed layer, the
+    large 4096/1536 layer): step time, each stage's time against its roofline (FP4 tensor
+    peak for the GEMMs, copy bandwidth for the rest) and a batch-invariance spot check."""
+    cfg = S.CONFIGS[name]
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    w1, w2 = S.make_weights_device(cfg, dev)
+    weights = M.quantize_moe_weights(w1, w2)
+    del w1, w2
+    x = to_dev(S.make_x(cfg))
+    ids_np, w_np = S.make_routing(cfg)
+    ids = torch.from_numpy(ids_np).to(dev)
+    pw = torch.from_numpy(w_np).to(dev)
+    ws = M.alloc_workspace(T, H, I, E, k, dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ms = time_steps(M, torch, weights, cfg, x, ids, pw, offs, ws, out, flush, stream, K, W)
+    st = stage_times(M, torch, cfg, weights, x, ids, pw, offs, ws, out, flush, stream, min(K, 20))
+    if M.nvfp4_get_device_error() != 0:
+        raise RuntimeError(f"device error in the {name} workload")
+    work = stage_work(cfg)
+    stages = {}
+    for n in STAGES:
+        r = roofline_of(n, work[n], st[n], peaks, peak_kind)
+        stages[n] = {"ms": round(st[n], 4), "bound": r["bound"], "frac": r["frac"],
+                     "achieved": r["achieved"], "unit": r["unit"]}
+    step_ms = statistics.mean(ms)
+    M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+    M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+    inv = batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev, sizes=(1, 64), n_decode=8, n_windows=2)
+    res = {"tokens_per_s": round(T / (step_ms * 1e-3), 1), "ms_per_step": round(step_ms, 4), "steps": K,
+           "stages": stages, "layer_roofline_frac": layer_roofline(cfg, peaks, peak_kind, step_ms)["frac"],
+           "bitwise_invariant": inv["bitwise_equal"],
+           "config": f"H {H}, I {I}, E {E}, top-{k}, {T} tokens, {cfg.routing} routing"
+                     + (f", {cfg.outlier_frac:.0%} x20 outlier channels" if cfg.outlier_frac else "")
+                     + ", weights drawn on the GPU (seeded), L2 flushed between steps"}
+    del weights, ws, out, x
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, cfg, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -445,26 +607,9 @@ def run_ours(args, cfg, rank, world, local_rank):
     value = job_tokens_per_s(T, world, K, total_ms)
 
     # ---- per-stage attribution (separate pass, same launches, events between stages)
-    names = ["route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"]
+    names = STAGES
     n_attr = min(K, 100)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n_attr)]
-    for i in range(n_attr):
-        e = evs[i]
-        e[0].record(stream)
-        M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
-        e[1].record(stream)
-        M.moe_fc1_swiglu_nvfp4(weights, T, k, offs, ws)
-        e[2].record(stream)
-        M.moe_requant_nvfp4(weights, T, k, offs, ws)
-        e[3].record(stream)
-        M.moe_fc2_nvfp4(weights, T, k, offs, ws)
-        e[4].record(stream)
-        M.moe_combine_bf16(weights, T, k, out, ws)
-        e[5].record(stream)
-        flush.zero_()
-    torch.cuda.synchronize()
-    stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_attr))
-                for j, n in enumerate(names)}
+    stage_ms = stage_times(M, torch, cfg, weights, x, ids, pw, offs, ws, out, flush, stream, n_attr)
     peaks, peak_kind = load_peaks()
     work = stage_work(cfg)
     kernels = {n: roofline_of(n, work[n], stage_ms[n], peaks, peak_kind) | {"ms": round(stage_ms[n], 4)}
@@ -602,28 +747,39 @@ def run_ours(args, cfg, rank, world, local_rank):
                              min(K, 20), peaks, peak_kind)
     del w1, w2
 
+    # ---- the compute-bound workloads: 16384 tokens with skewed routing, and the large layer
+    workloads = {}
+    if not args.no_extra_workloads:
+        del ws, ws_m
+        torch.cuda.empty_cache()
+        for name in ("qwen3_30b_a3b_skew", "large"):
+            workloads[name] = extra_workload(M, torch, name, dev, stream, flush, min(K, 20), max(3, args.warmup),
+                                             peaks, peak_kind, to_dev)
+
     line = {
         "metric": "nvfp4_moe_expert_forward_tokens_per_s", "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x ue4m3 block-scaled) MMA, f32 accumulate/epilogue, bf16 in/out",
         "data": "synthetic (seeded; random-init weights of the layer's shape)",
-        "config": describe(cfg) | {"parallelism": f"token shards x{world}" if world > 1 else "single GPU"},
+        "config": describe(cfg),
         "roofline": roof,
-        "layer_roofline": layer_roofline(cfg, peaks, peak_kind, total_ms / K),
-        "batch_invariance": invariance,
+        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "pinned host X/ids/probs in and output out every step; two copy streams, "
+                        "double-buffered device buffers"},
+        "gpu_launches": kernels_per_step(cfg) * K,
+        "clocks": clocks,
         "kernels": kernels,
         "weight_quant_ms": round(wq_ms, 3),
         "router_step": router,
         "masked_step": masked,
         "backward_step": backward,
-        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "every step copies its pinned host X/ids/probs in and its output out; two copy "
-                        "streams and double-buffered device inputs/outputs overlap step i's copies with "
-                        "the compute of its neighbours"},
-        "gpu_launches": kernels_per_step(cfg) * K,
-        "clocks": clocks,
+        # last, where a tail of the output shows them: the compute-bound workloads' stage
+        # fractions, the headline layer's roofline and the invariance check
+        "workloads": workloads,
+        "layer_roofline": layer_roofline(cfg, peaks, peak_kind, total_ms / K),
+        "batch_invariance": invariance,
     }
     return line
 
@@ -677,6 +833,11 @@ def backward_step(M, torch, cfg, weights, w1, w2, x, ids, pw, ws, offs, flush, s
 
 def main():
     args = parse()
+    if args.oracle_sample:
+        c = S.CONFIGS[args.oracle_sample]
+        v, desc = oracle_sample_rate(c, args.oracle_seconds, args.oracle_experts, args.oracle_tokens or None)
+        print(json.dumps({"value": v, "sample": desc}), flush=True)
+        return
     cfg = S.CONFIGS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -691,9 +852,9 @@ def main():
     else:
         line = run_ours(args, cfg, rank, world, local_rank)
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            v, desc, cores = oracle_sample_rate(cfg)
-            line["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                    "sample": desc}
+            tail = {key: line.pop(key) for key in ("workloads", "layer_roofline", "batch_invariance")}
+            line["cpu_baseline"] = cpu_baselines(cfg)
+            line.update(tail)
     if rank == 0 and line is not None:
         print(json.dumps(line), flush=True)
     if world > 1 and args.impl == "ours":

@@ -215,8 +215,9 @@ nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int
  * errors as for moe_route_sort_amax.
  *
  * Set-up and sharing: the first call on a device looks up the array's device
- * address (host-side, once per device, with that device current); make that
- * first call before any stream capture.  Every call on a device shares the
+ * address (host-side, once per device, with that device current; again after a
+ * device reset gives the device a new context); make that first call before any
+ * stream capture.  Every call on a device shares the
  * one array and leaves its contents behind; no part of it needs to start at
  * zero.  Calls that can overlap on the GPU (on different streams without an
  * ordering between them) race on the array and must not be issued.
@@ -384,6 +385,16 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
                                      size_t fwd_ws_bytes, const float* fc1_pre_dev, void* dx_dev, float* dw1_dev,
                                      float* dw2_dev, float* dprob_dev, void* bwd_ws_dev, size_t bwd_ws_bytes,
                                      void* stream);
+
+/* nvfp4_silu_table -- copy the SiLU table that the FC1 epilogue applies to its BF16 gate
+ * values ([RL/4.4]: SiLU(gate)*up in FP32) into out_dev: float [65536], entry i = silu(a)
+ * for the BF16 value a whose bit pattern is i, where silu(a) = a / (1 + e^-a) rounded once
+ * (to nearest, ties to even) to FP32; silu(+-0) = +-0, silu(+inf) = +inf, silu(-inf) and
+ * silu(NaN) are NaN.  The table is part of the library's device image (computed when the
+ * library is built), so it exists as soon as the library is loaded and no call has to fill
+ * it first.  out_dev: device memory, 4-byte aligned, 262144 bytes, owned by the caller.
+ * Enqueued on `stream` (a device-to-device copy); returns NVFP4_ERR_CUDA if it cannot be. */
+nvfp4_status nvfp4_silu_table(float* out_dev, void* stream);
 
 /* Synchronise `stream`, then report and clear this device's error word:
  * *device_status receives NVFP4_OK or the first device error recorded since

@@ -16,7 +16,8 @@ of the same shapes stand in for them):
 * ``large``   hidden 4096, intermediate 1536, 128 experts, top-8, 32768
   tokens, Zipf routing, 1% outlier channels, weights N(0, 0.015)
 
-Recipe: numpy PCG64; sub-streams seed+0 (X), +1 (W1), +2 (W2), +3 (router
+Recipe: numpy PCG64 (throughput runs of the large layers may draw the
+weights on the GPU instead, make_weights_device); sub-streams seed+0 (X), +1 (W1), +2 (W2), +3 (router
 logits), +4 (outlier channels), +5 (sequence lengths), +6 (router weights for
 the router step, W_r ~ N(0, 1/H) so that logits of N(0,1) inputs are about
 N(0,1)), +7 (the output gradient of the backward, dOut ~ N(0, 1)).  Values are
@@ -62,8 +63,10 @@ def _rng(seed, sub):
 
 def f32_to_bf16_bits(a):
     """Round binary32 values to BF16 (RNE) and return the uint16 bit patterns."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    # 32-bit arithmetic: a carry past 2^32 (only from negative NaN patterns) is dropped by
+    # the final 16-bit truncation either way, so the bits equal a 64-bit computation's
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    rounded = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return rounded.astype(np.uint16)
 
 
@@ -104,6 +107,24 @@ def make_weights(cfg, experts=None):
         w1[e] = f32_to_bf16_bits(r1.standard_normal((2 * cfg.I, cfg.H), dtype=np.float32) * std)
         w2[e] = f32_to_bf16_bits(r2.standard_normal((cfg.H, cfg.I), dtype=np.float32) * std)
     return w1, w2
+
+
+def make_weights_device(cfg, device, seed_offset=0):
+    """BF16 expert weights drawn on the GPU (torch tensors W1 [E, 2I, H], W2 [E, H, I]),
+    N(0, w_std) rounded to BF16: the same distribution as make_weights from torch's seeded
+    device generator (sub-streams seed+1 and seed+2), for throughput runs of layers whose
+    host-side draw would take a minute.  The values differ from make_weights'."""
+    import torch
+    out = []
+    for sub, shape in ((1, (cfg.E, 2 * cfg.I, cfg.H)), (2, (cfg.E, cfg.H, cfg.I))):
+        g = torch.Generator(device=device)
+        g.manual_seed(cfg.seed + sub + seed_offset)
+        w = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        for e in range(cfg.E):   # one expert at a time keeps the float32 temporary small
+            w[e] = (torch.randn(shape[1:], generator=g, device=device, dtype=torch.float32)
+                    * cfg.w_std).to(torch.bfloat16)
+        out.append(w)
+    return tuple(out)
 
 
 def make_routing(cfg, T=None, stream=0):

@@ -7,7 +7,7 @@ entry points have the names of the C ABI in ``include/nvfp4_moe.h``:
     nvfp4_quantize_rows, moe_route_sort_amax, moe_expert_forward_nvfp4,
     moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16,
     moe_workspace_bytes, moe_workspace_layout_query, nvfp4_sf_bytes,
-    nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string,
+    nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string, nvfp4_silu_table,
     moe_router_topk, the fixed-capacity moe_*_masked calls, and the
     straight-through backward: nvfp4_transpose_bf16, moe_backward_layout_query,
     moe_backward_workspace_bytes, moe_expert_backward_ste
@@ -84,6 +84,7 @@ _SIGNATURES = {
     "moe_fc2_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_combine_bf16": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
     "nvfp4_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_int)]),
+    "nvfp4_silu_table": (_I32, [_P, _P]),
     "moe_route_sort_amax_noalloc": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_router_topk": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
     "moe_workspace_layout_query_masked": (_I32, [_I64, _I32, _I32, _I32, _I32, _I32,
@@ -181,6 +182,18 @@ def nvfp4_quantize_rows(x, codes=None, sf=None, g=None, stream=None):
     _check("nvfp4_quantize_rows", lib().nvfp4_quantize_rows(
         _ptr(x), rows, cols, x.stride(0), _ptr(codes), _ptr(sf), _ptr(g), _stream(stream)))
     return codes, sf, g
+
+
+def nvfp4_silu_table(out=None, stream=None):
+    """The FC1 epilogue's SiLU table: float32 [65536] on the current device, entry i =
+    silu of the BF16 value with bit pattern i, rounded once to FP32."""
+    if out is None:
+        out = torch.empty(65536, dtype=torch.float32, device="cuda")
+    _need_cuda(out)
+    if out.dtype != torch.float32 or out.numel() != 65536:
+        raise ValueError("out must be a float32 tensor of 65536 elements")
+    _check("nvfp4_silu_table", lib().nvfp4_silu_table(_ptr(out), _stream(stream)))
+    return out
 
 
 def nvfp4_get_device_error(stream=None):
@@ -388,31 +401,43 @@ class MoELayer:
     what the straight-through backward reads (the route, h, FC1's FP32 values);
     ``backward(dout)`` then returns (dx, dw1, dw2, dprob).
 
-    The BF16 weights are the master copy: a forward after they were changed in place (an
-    optimizer step) quantises them again, and a backward refuses to run if they changed after
-    its forward, so one forward/backward pair never mixes two weight versions ("Finishing RL
-    training faster: bitwise consistency, high performance, agent-driven", section 3.1, the
-    inference kernels define the values and training adds the backward: each backward first
-    checks that the master weights are those of its forward)."""
+    The BF16 weights are the master copy and the layer keeps their NVFP4 quantisation in
+    step with them ("Finishing RL training faster: bitwise consistency, high performance,
+    agent-driven", section 3.1: the inference kernels define the forward values and the
+    backward must belong to the same weights):
+
+    * a forward re-quantises the weights when they were changed through an in-place op on
+      the tensors themselves (``w.add_(...)``, ``w.copy_(...)``: torch's version counter) or
+      when a tensor's storage was swapped (``w.data = ...``: its data pointer);
+    * a write that bypasses the version counter, such as ``w.data.add_(...)`` in a
+      hand-written optimizer step, is not seen: call ``refresh_weights()`` after it;
+    * ``backward`` raises if the weights were changed or refreshed after the forward it
+      belongs to, so one forward/backward pair never mixes two weight versions."""
 
     def __init__(self, w1, w2, stream=None):
         self._w_bf16 = (w1, w2)
         self._saved = None
         self._ws = {}
+        self._gen = 0
         self._quantize(stream)
 
     def _weight_version(self):
-        return tuple(t._version for t in self._w_bf16)
+        return tuple((t._version, t.data_ptr()) for t in self._w_bf16)
 
     def _quantize(self, stream=None):
         self.weights = quantize_moe_weights(*self._w_bf16, stream=stream)
         self.E, self.H, self.I = self.weights.E, self.weights.H, self.weights.I
         self._wt = None                      # transposed copies for the backward, made on demand
         self._wver = self._weight_version()
+        self._gen += 1
 
     def _refresh_if_changed(self, stream=None):
         if self._weight_version() != self._wver:
             self._quantize(stream)
+
+    def refresh_weights(self, stream=None):
+        """Quantise the BF16 weights again (after a write the version counter cannot see)."""
+        self._quantize(stream)
 
     def workspace(self, T, k, device):
         key = (T, k)
@@ -440,7 +465,7 @@ class MoELayer:
         moe_requant_nvfp4(self.weights, T, k, offs, ws, stream=stream)
         moe_fc2_nvfp4(self.weights, T, k, offs, ws, stream=stream)
         moe_combine_bf16(self.weights, T, k, out, ws, stream=stream)
-        self._saved = (x, offs, ws, fc1_pre, T, k, self._wver)
+        self._saved = (x, offs, ws, fc1_pre, T, k, (self._wver, self._gen))
         return out
 
     def backward(self, dout, stream=None):
@@ -448,8 +473,8 @@ class MoELayer:
         last forward run with save_for_backward=True."""
         if self._saved is None:
             raise RuntimeError("backward needs a forward with save_for_backward=True")
-        x, offs, ws, fc1_pre, T, k, wver = self._saved
-        if self._weight_version() != wver:
+        x, offs, ws, fc1_pre, T, k, (wver, gen) = self._saved
+        if self._weight_version() != wver or self._gen != gen:
             raise RuntimeError("the weights changed after the forward this backward belongs to")
         if self._wt is None:
             self._wt = MoEWeightsBF16T(*self._w_bf16, stream=stream)

@@ -20,7 +20,9 @@ LIB_NAME = "libnvfp4moe.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["quant.cu", "gemm.cu", "combine.cu", "router.cu", "api.cu", "route_noalloc.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", BUILD_DIR]
+SILU_GEN = os.path.join(HERE, "silu_table.py")
+SILU_INC = os.path.join(BUILD_DIR, "silu_table.inc")
 
 
 def _nvcc():
@@ -31,7 +33,17 @@ def _nvcc():
 
 
 def _deps():
-    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "nvfp4_moe.h")]
+    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "nvfp4_moe.h"), SILU_GEN]
+
+
+def _silu_table():
+    """Generate the SiLU table initialiser gemm.cu compiles in (when missing or stale)."""
+    if os.path.exists(SILU_INC) and os.path.getmtime(SILU_INC) >= os.path.getmtime(SILU_GEN):
+        return
+    from . import silu_table
+    tmp = SILU_INC + ".tmp"
+    silu_table.write_inc(tmp)
+    os.replace(tmp, SILU_INC)
 
 
 def up_to_date():
@@ -47,6 +59,7 @@ def build(force=False, verbose=False):
         return LIB_PATH
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
+    _silu_table()
     extra = ["-Xptxas", "-v"] if verbose else []
 
     def compile_one(src):

@@ -17,7 +17,24 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
 int* g_err_ptr[kMaxDevices];
+void* g_err_ctx[kMaxDevices];
 int g_sm_count[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        }
+    });
+    return fn;
+}
 
 int current_device() {
     int d = -1;
@@ -25,15 +42,17 @@ int current_device() {
     return (d >= 0 && d < kMaxDevices) ? d : -1;
 }
 
-// Device address of this device's error word (looked up once per device).
+// Device address of this device's error word (looked up once per device and context).
 int* device_error_ptr() {
     const int d = current_device();
     if (d < 0) return nullptr;
+    void* ctx = current_context();
     std::lock_guard<std::mutex> lock(g_dev_mutex);
-    if (!g_err_ptr[d]) {
+    if (!g_err_ptr[d] || g_err_ctx[d] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
         g_err_ptr[d] = static_cast<int*>(p);
+        g_err_ctx[d] = ctx;
     }
     return g_err_ptr[d];
 }
@@ -199,6 +218,13 @@ GemmArgs fc2_args(const moe_nvfp4_weights* w, const int32_t* offsets, void* ws, 
 }  // namespace
 
 int* device_error_word() { return device_error_ptr(); }
+
+void* current_context() {
+    CtxGetCurrentFn fn = ctx_get_current_fn();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
 
 int device_sm_count() {
     const int d = current_device();
@@ -557,6 +583,11 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
     a.x_t = at<uint16_t>(bwd_ws_dev, B.x_t);
     a.err = err;
     return from_cuda(launch_moe_backward_ste(a, st));
+}
+
+nvfp4_status nvfp4_silu_table(float* out_dev, void* stream) {
+    if (!out_dev || !aligned(out_dev, 4)) return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(copy_silu_table(out_dev, static_cast<cudaStream_t>(stream)));
 }
 
 nvfp4_status nvfp4_get_device_error(void* stream, int* device_status) {

@@ -115,6 +115,8 @@ struct GemmArgs {
 
 cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st, bool pdl);
+// Copy the FC1 epilogue's 65536-entry SiLU table (FP32, by BF16 bit pattern) to `out`.
+cudaError_t copy_silu_table(float* out, cudaStream_t st);
 
 cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st, bool pdl);
 
@@ -122,5 +124,11 @@ int device_sm_count();
 
 // Device address of this device's error word (nullptr if it cannot be looked up).
 int* device_error_word();
+
+// The calling thread's current CUDA context (nullptr if it cannot be read).  Device
+// addresses of the library's __device__ variables are cached per device together with the
+// context they were looked up in, and looked up again when the context changes (a device
+// reset tears the old one down and loads the library's module again elsewhere).
+void* current_context();
 
 }  // namespace nvfp4

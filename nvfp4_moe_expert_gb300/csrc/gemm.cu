@@ -51,8 +51,13 @@
 
 namespace nvfp4 {
 
-// SiLU of every BF16 value, each computed in FP64 and rounded once to FP32.
-__device__ float g_silu_table[65536];
+// SiLU of every BF16 value, correctly rounded to FP32, indexed by the BF16 bit pattern.
+// The values are computed at build time (silu_table.py, exact to 60 digits before the one
+// rounding) and compiled in, so the table is in device memory as soon as the library loads:
+// no launch fills it and nothing waits for it.
+__device__ const uint32_t g_silu_bits[65536] = {
+#include "silu_table.inc"
+};
 
 namespace {
 
@@ -90,14 +95,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;                     // per stage: SFA 4, SFB 8 columns per MMA
 constexpr uint32_t kSfColsPerStage = 12 * kMmaPerStage;
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
-
-__global__ void init_silu_table_kernel() {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < 65536) {
-        const double a = static_cast<double>(__uint_as_float(static_cast<uint32_t>(i) << 16));
-        g_silu_table[i] = __double2float_rn(a / (1.0 + exp(-a)));
-    }
-}
 
 // Expert owning routed row `row`: largest e < E with off[e] <= row (off in shared memory).
 __device__ __forceinline__ int expert_of_row(const int32_t* off, int E, int row) {
@@ -227,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kFC1) {
         for (int i = threadIdx.x; i < 2 * static_cast<int>(kSiluSpan); i += blockDim.x) {
             const uint32_t bits = kSiluLo + (i % kSiluSpan) + (i >= static_cast<int>(kSiluSpan) ? 0x8000u : 0u);
-            s_silu[i] = __ldg(g_silu_table + bits);
+            s_silu[i] = __uint_as_float(__ldg(g_silu_bits + bits));
         }
     }
     tc_fence_before();
@@ -461,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t gbits = u ? gb >> 16 : gb & 0xFFFFu;
                         const uint32_t gi = (gbits & 0x7FFFu) - kSiluLo;
                         sl[u] = gi < kSiluSpan ? s_silu[gi + ((gbits >> 15) ? kSiluSpan : 0u)]
-                                               : __ldg(g_silu_table + gbits);
+                                               : __uint_as_float(__ldg(g_silu_bits + gbits));
                     }
                     // silu(gate) * up in FP32, then * p, one BF16 rounding
                     const uint64_t h2 = f2_mul(f2_mul(f2(__float_as_uint(sl[0]), __float_as_uint(sl[1])),
@@ -569,10 +566,10 @@ bool make_gateup_map(CUtensorMap* m, const void* base, int E, int I, int64_t row
 
 constexpr int kMaxDevices = 64;
 std::mutex g_init_mutex;
-bool g_silu_ready[kMaxDevices];
 bool g_attr_ready[kMaxDevices][2];
 
-cudaError_t prepare_device(bool fc1, cudaStream_t st) {
+// Host-side set-up of the kernel attributes, once per device (no launch, no synchronisation).
+cudaError_t prepare_device(bool fc1) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -587,27 +584,11 @@ cudaError_t prepare_device(bool fc1, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         g_attr_ready[dev][which] = true;
     }
-    if (fc1 && !g_silu_ready[dev]) {
-        // The table is filled once per device, in stream order before the first
-        // FC1 launch.  Outside stream capture the stream is also synchronised
-        // once, so FC1 launches on other streams see the finished table.
-        init_silu_table_kernel<<<256, 256, 0, st>>>();
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        e = cudaStreamIsCapturing(st, &cs);
-        if (e != cudaSuccess) return e;
-        if (cs == cudaStreamCaptureStatusNone) {
-            e = cudaStreamSynchronize(st);
-            if (e != cudaSuccess) return e;
-        }
-        g_silu_ready[dev] = true;
-    }
     return cudaSuccess;
 }
 
 cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st, bool pdl) {
-    cudaError_t e = prepare_device(fc1, st);
+    cudaError_t e = prepare_device(fc1);
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb;
     if (!make_code_map(&ma, a.a_codes, a.rows_cap, a.K / 2, kBM)) return cudaErrorInvalidValue;
@@ -623,5 +604,9 @@ cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st, bool pdl) 
 
 cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st, bool pdl) { return launch_gemm(true, a, st, pdl); }
 cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st, bool pdl) { return launch_gemm(false, a, st, pdl); }
+
+cudaError_t copy_silu_table(float* out, cudaStream_t st) {
+    return cudaMemcpyFromSymbolAsync(out, g_silu_bits, sizeof(g_silu_bits), 0, cudaMemcpyDeviceToDevice, st);
+}
 
 }  // namespace nvfp4

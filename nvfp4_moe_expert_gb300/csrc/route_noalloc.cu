@@ -28,16 +28,21 @@ static __device__ __align__(256) uint8_t g_route_scratch[kRouteScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 uint8_t* g_scratch_addr[kMaxDevices];
+void* g_scratch_ctx[kMaxDevices];
 
 // Device address of g_route_scratch on device `dev` (which must be current).
 // In host code the array's name is only a host-side stand-in, so the address
-// is looked up once per device and cached.
+// is looked up once per device and cached with the context it was looked up
+// in; after a device reset (a new context, the library's module loaded again)
+// it is looked up anew instead of reusing an address that no longer exists.
 uint8_t* scratch_address(int dev) {
+    void* ctx = current_context();
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return nullptr;
         g_scratch_addr[dev] = static_cast<uint8_t*>(p);
+        g_scratch_ctx[dev] = ctx;
     }
     return g_scratch_addr[dev];
 }

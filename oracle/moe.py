@@ -70,12 +70,18 @@ def epilogue_f64(acc, g_rows, g_cols):
     return (acc * np.asarray(g_rows, np.float64)[:, None]) * np.asarray(g_cols, np.float64)[None, :]
 
 
+def silu_f32(gate_bits):
+    """silu(a) = a / (1 + exp(-a)) of BF16 values (bits), evaluated in FP64 and rounded
+    once to FP32."""
+    with np.errstate(over="ignore", invalid="ignore"):
+        a = bf16_bits_to_f32(gate_bits).astype(np.float64)
+        return (a / (1.0 + np.exp(-a))).astype(np.float32)
+
+
 def swiglu_prob(gate_bits, up_bits, prob):
     """h = bf16( f32( f32(silu(gate) * up) * p ) ); gate/up BF16 bits, p FP32 per row."""
-    a = bf16_bits_to_f32(gate_bits).astype(np.float64)
+    silu = silu_f32(gate_bits)                                     # FP64, one rounding
     u = bf16_bits_to_f32(up_bits)
-    with np.errstate(over="ignore"):
-        silu = (a / (1.0 + np.exp(-a))).astype(np.float32)        # FP64, one rounding
     t1 = (silu * u).astype(np.float32)                             # FP32 product
     t2 = (t1 * np.asarray(prob, np.float32)[:, None]).astype(np.float32)
     return round_to_bf16_bits(t2)

@@ -250,8 +250,10 @@ def test_layer_weight_versions():
         calls.append(1)
         layer._wt = None
         layer._wver = layer._weight_version()
+        layer._gen += 1
 
     layer._quantize = fake_quantize
+    layer._gen = 0
     layer._w_bf16 = (torch.zeros(2, 4), torch.zeros(2, 4))
     layer._quantize()
     layer._refresh_if_changed()
@@ -259,8 +261,20 @@ def test_layer_weight_versions():
     layer._w_bf16[0].add_(1.0)                       # an optimizer step updates a weight in place
     layer._refresh_if_changed()
     assert len(calls) == 2 and layer._wver == layer._weight_version()
+    layer._w_bf16[1].data = torch.ones(2, 4)         # storage swapped: seen through the data pointer
+    layer._refresh_if_changed()
+    assert len(calls) == 3
+    # a write through .data bypasses the version counter: not seen until refresh_weights()
+    layer._w_bf16[0].data.add_(1.0)
+    layer._refresh_if_changed()
+    assert len(calls) == 3
+    layer._saved = (None, None, None, None, 0, 1, (layer._wver, layer._gen))
+    layer.refresh_weights()
+    assert len(calls) == 4
+    with pytest.raises(RuntimeError, match="weights changed"):   # refreshed after its forward
+        layer.backward(None)
     # a backward whose forward saw an older version refuses to run
-    layer._saved = (None, None, None, None, 0, 1, layer._wver)
+    layer._saved = (None, None, None, None, 0, 1, (layer._wver, layer._gen))
     layer._w_bf16[1].mul_(2.0)
     with pytest.raises(RuntimeError, match="weights changed"):
         layer.backward(None)

@@ -2,8 +2,9 @@
 
 * FC1 (tcgen05 block-scaled FP4 grouped GEMM + FP32 epilogue): pre-cast FP32
   values within relative L2 1e-5 of the oracle's exact FP64 values, BF16
-  gate/up within 1 ulp; SwiGLU x prob bit-exact wherever gate and up agree;
-  the row maxima equal max|h|.
+  gate/up within 1 ulp; SwiGLU x prob bit-exact wherever gate and up agree,
+  and elsewhere every element within the bound the gate/up difference
+  propagates to (tests/_helpers.h_bound); the row maxima equal max|h|.
 * requantisation of a seeded synthetic FC2 input: bit-exact.
 * FC2 on that input: pre-cast within 1e-5, BF16 y within 1 ulp.
 * combine of a seeded synthetic y: bit-exact.
@@ -22,7 +23,7 @@ from nvfp4_moe_expert_gb300 import build as B
 from oracle import formats as F
 from oracle import moe as OM
 from oracle import quant as Q
-from _helpers import (GEMM_BF16_ULP, GEMM_REL_L2, bf16_to_torch, bf16_ulp_distance, rel_l2,
+from _helpers import (GEMM_BF16_ULP, GEMM_REL_L2, bf16_to_torch, bf16_ulp_distance, h_bound, rel_l2,
                       torch_to_bf16_bits)
 
 pytestmark = pytest.mark.gpu
@@ -104,9 +105,15 @@ def test_fc1_stage(run):
     same = (gu_gpu[:, :c.I] == gu_ref[:, :c.I]) & (gu_gpu[:, c.I:] == gu_ref[:, c.I:])
     assert same.mean() > 0.9
     assert np.array_equal(h_gpu[same], h_ref[same])
-    # where gate or up differ by their 1-ulp cast difference, h moves by that times
-    # |d ln silu / d ln gate| = |1 + g (1 - sigmoid(g))| (about 4 at g = -5): stay loose
-    assert rel_l2(F.bf16_bits_to_f32(h_gpu), F.bf16_bits_to_f32(h_ref)) <= 1e-3
+    # where gate or up differ (by their 1-ulp cast difference), every element of h stays
+    # within the bound that difference propagates to through silu(gate)*up*p
+    diff = ~same
+    f = F.bf16_bits_to_f32
+    pr = np.broadcast_to(run.L["topk_w"][toks, slots][:, None], same.shape)
+    bound = h_bound(f(gu_gpu[:, :c.I])[diff], f(gu_gpu[:, c.I:])[diff], f(gu_ref[:, :c.I])[diff],
+                    f(gu_ref[:, c.I:])[diff], pr[diff], f(h_gpu)[diff], f(h_ref)[diff])
+    err = np.abs(f(h_gpu)[diff].astype(np.float64) - f(h_ref)[diff])
+    assert (err <= bound).all(), float((err / bound).max())
     # FC2 maxima: the producer's max|h| over each row
     hmax = np.abs(F.bf16_bits_to_f32(h_gpu)).max(axis=1)
     assert np.array_equal(amax2, hmax.view(np.uint32))
