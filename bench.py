@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--workload", default="qwen3_30b_a3b", choices=sorted(S.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--minimal", action="store_true",
+                    help="time the steps and their stages only (no e2e, router, masked, backward, invariance, "
+                         "extra workloads or CPU baseline): the command the ncu captures run")
     ap.add_argument("--no-extra-workloads", action="store_true",
                     help="time only the headline workload (skip the 16384-token skewed and large layers)")
     ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
@@ -621,6 +624,11 @@ def run_ours(args, cfg, rank, world, local_rank):
     dominant = max(names, key=lambda n: stage_ms[n])
     roof = dict(kernels[dominant])
     roof["peak_note"] = "of " + peak_kind
+    if args.minimal:
+        return {"metric": "nvfp4_moe_expert_forward_tokens_per_s", "value": round(value, 1), "unit": "tokens/s",
+                "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "config": describe(cfg),
+                "roofline": roof, "kernels": kernels, "clocks": clocks, "minimal": True}
 
     # ---- router step (produces the step's routing; timed on its own, not part of the step)
     router = None
@@ -851,7 +859,7 @@ def main():
         line = run_reference(args, cfg, rank, world)
     else:
         line = run_ours(args, cfg, rank, world, local_rank)
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.minimal:
             tail = {key: line.pop(key) for key in ("workloads", "layer_roofline", "batch_invariance")}
             line["cpu_baseline"] = cpu_baselines(cfg)
             line.update(tail)
