@@ -37,11 +37,25 @@ FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor ratio on GB300
 FLUSH_BYTES = 512 << 20         # > L2 (129 MB)
 
 
+FUSED_FC2_MAX_I = 768   # moe_fc2_requant_max_intermediate(): FC2 with the requantisation fused in
+
+
+def fused_fc2(cfg):
+    return cfg.I <= FUSED_FC2_MAX_I
+
+
 def kernels_per_step(cfg):
     """Launches of one step: the route sort is one block-sort kernel for up to 8192 (token,
     slot) pairs and E <= 256, else a histogram and a scan kernel; then quantise-scatter, FC1,
-    requant, FC2, combine."""
-    return (1 if cfg.T * cfg.k <= 8192 and cfg.E <= 256 else 2) + 5
+    FC2 with the requantisation fused in (or requant and FC2 where I > 768), combine."""
+    return (1 if cfg.T * cfg.k <= 8192 and cfg.E <= 256 else 2) + (4 if fused_fc2(cfg) else 5)
+
+
+def step_stages(cfg):
+    """The stages one step runs, in order."""
+    if fused_fc2(cfg):
+        return ["route_sort_quant", "fc1_swiglu", "fc2_requant", "combine"]
+    return ["route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"]
 
 
 def parse():
@@ -66,10 +80,11 @@ def parse():
 
 # Source files each stage's kernels are built from (for matching stored ncu captures).
 STAGE_SOURCES = {
-    "route_sort_quant": ["quant.cu", "ptx.cuh", "common.cuh"],
-    "fc1_swiglu": ["gemm.cu", "ptx.cuh", "common.cuh"],
-    "requant": ["quant.cu", "ptx.cuh", "common.cuh"],
-    "fc2": ["gemm.cu", "ptx.cuh", "common.cuh"],
+    "route_sort_quant": ["quant.cu", "nvfp4_quant.cuh", "ptx.cuh", "common.cuh"],
+    "fc1_swiglu": ["gemm.cu", "nvfp4_quant.cuh", "ptx.cuh", "common.cuh"],
+    "requant": ["quant.cu", "nvfp4_quant.cuh", "ptx.cuh", "common.cuh"],
+    "fc2": ["gemm.cu", "nvfp4_quant.cuh", "ptx.cuh", "common.cuh"],
+    "fc2_requant": ["gemm.cu", "nvfp4_quant.cuh", "ptx.cuh", "common.cuh"],
     "combine": ["combine.cu", "common.cuh"],
 }
 
@@ -136,6 +151,8 @@ def stage_work(cfg):
                        "flops": 2 * R * H * 2 * I},
         "requant": {"bytes": R * (2 * I + 4 + 4) + R * row_q(I), "flops": 0},
         "fc2": {"bytes": E * H * row_q(I) + R * row_q(I) + R * 2 * H, "flops": 2 * R * I * H},
+        # FC2 with the requantisation fused in: W2, h and its maxima/row map read, y written
+        "fc2_requant": {"bytes": E * H * row_q(I) + R * (2 * I + 8) + R * 2 * H, "flops": 2 * R * I * H},
         "combine": {"bytes": R * 2 * H + T * 2 * H, "flops": 0},
     }
 
@@ -195,7 +212,8 @@ def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
     algorithmic bytes / copy bandwidth and FLOPs / FP4 peak), against the measured step time."""
     hbm = float(peaks["hbm_gbs"])
     fp4 = float(peaks["bf16_tflops"]) * FP4_OVER_BF16
-    per = {n: max(w["bytes"] / (hbm * 1e9), w["flops"] / (fp4 * 1e12)) for n, w in stage_work(cfg).items()}
+    work = stage_work(cfg)
+    per = {n: max(work[n]["bytes"] / (hbm * 1e9), work[n]["flops"] / (fp4 * 1e12)) for n in step_stages(cfg)}
     bound_ms = 1e3 * sum(per.values())
     return {"frac": round(bound_ms / ms_per_step, 4), "bound_ms": round(bound_ms, 4),
             "measured_ms": round(ms_per_step, 4),
@@ -445,31 +463,30 @@ def run_reference(args, cfg, rank, world):
 
 
 # ---------------------------------------------------------------- GPU arm
-STAGES = ["route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"]
-
-
 def stage_times(M, torch, cfg, weights, x, ids, pw, offs, ws, out, flush, stream, n):
     """Mean CUDA-event time (ms) of each stage over n passes of the step called stage by
     stage (events on the launching stream between the stages), L2 flushed between passes."""
     T, E, k = cfg.T, cfg.E, cfg.k
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(n)]
+    calls = {
+        "route_sort_quant": lambda: M.moe_route_sort_amax(x, ids, pw, E, offs, ws),
+        "fc1_swiglu": lambda: M.moe_fc1_swiglu_nvfp4(weights, T, k, offs, ws),
+        "requant": lambda: M.moe_requant_nvfp4(weights, T, k, offs, ws),
+        "fc2": lambda: M.moe_fc2_nvfp4(weights, T, k, offs, ws),
+        "fc2_requant": lambda: M.moe_fc2_requant_nvfp4(weights, T, k, offs, ws),
+        "combine": lambda: M.moe_combine_bf16(weights, T, k, out, ws),
+    }
+    names = step_stages(cfg)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n)]
     for i in range(n):
         e = evs[i]
         e[0].record(stream)
-        M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
-        e[1].record(stream)
-        M.moe_fc1_swiglu_nvfp4(weights, T, k, offs, ws)
-        e[2].record(stream)
-        M.moe_requant_nvfp4(weights, T, k, offs, ws)
-        e[3].record(stream)
-        M.moe_fc2_nvfp4(weights, T, k, offs, ws)
-        e[4].record(stream)
-        M.moe_combine_bf16(weights, T, k, out, ws)
-        e[5].record(stream)
+        for j, name in enumerate(names):
+            calls[name]()
+            e[j + 1].record(stream)
         flush.zero_()
     torch.cuda.synchronize()
     return {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
-            for j, name in enumerate(STAGES)}
+            for j, name in enumerate(names)}
 
 
 def time_steps(M, torch, weights, cfg, x, ids, pw, offs, ws, out, flush, stream, K, W):
@@ -518,7 +535,7 @@ def extra_workload(M, torch, name, dev, stream, flush, K, W, peaks, peak_kind, t
         raise RuntimeError(f"device error in the {name} workload")
     work = stage_work(cfg)
     stages = {}
-    for n in STAGES:
+    for n in step_stages(cfg):
         r = roofline_of(n, work[n], st[n], peaks, peak_kind)
         stages[n] = {"ms": round(st[n], 4), "bound": r["bound"], "frac": r["frac"],
                      "achieved": r["achieved"], "unit": r["unit"]}
@@ -610,7 +627,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     value = job_tokens_per_s(T, world, K, total_ms)
 
     # ---- per-stage attribution (separate pass, same launches, events between stages)
-    names = STAGES
+    names = step_stages(cfg)
     n_attr = min(K, 100)
     stage_ms = stage_times(M, torch, cfg, weights, x, ids, pw, offs, ws, out, flush, stream, n_attr)
     peaks, peak_kind = load_peaks()

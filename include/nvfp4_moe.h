@@ -235,7 +235,8 @@ nvfp4_status moe_route_sort_amax_noalloc(const void* x_dev, int64_t T, int H, in
  * grouped GEMM with the same epilogue, BF16 y per (token, slot); and the
  * combine out[t] = bf16(sum over slots 0..k-1 in order, FP32)
  * [miniTE/differs, miniTE/use, RL/4.4, RL/4.5].  Equivalent to
- * moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16.
+ * moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16 (bitwise); it
+ * runs the requantisation fused into FC2 (moe_fc2_requant_nvfp4) when I <= 768.
  *
  *  w                   quantised weights (host struct, device pointers)
  *  T, k                as given to moe_route_sort_amax
@@ -266,6 +267,27 @@ nvfp4_status moe_fc2_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
                            size_t ws_bytes, float* fc2_debug_dev, void* stream);
 nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev,
                               void* ws_dev, size_t ws_bytes, void* stream);
+
+/* moe_fc2_requant_nvfp4 -- moe_requant_nvfp4 and moe_fc2_nvfp4 as one kernel: the FC2 input h
+ * is requantised inside the FC2 kernel and never goes back through memory as NVFP4
+ * ("miniTE diagnoses and narrows the cross-engine execution gap of NVFP4 RL", section
+ * "Assumptions and limits": the online amax-quantisation-GEMM fusion).  Each FC2 work unit
+ * quantises the 128 routed rows of its m-tile once into shared memory, with
+ * g2 = amax2 / 2688 from the maxima FC1 reduced, and keeps them there while the W2 tiles of
+ * its n-tiles stream through.  The codes, scales and outer scales are those
+ * moe_requant_nvfp4 writes and the MMAs walk K in the same order, so y (and fc2_debug_dev)
+ * are bitwise those of the two stages.  The workspace's requantised-operand buffers
+ * (a2_codes, a2_sf, a2_g) are not written.  Reads h, amax2 and the row map that
+ * moe_fc1_swiglu_nvfp4 and the route sort left in the workspace.
+ * Supported for I <= moe_fc2_requant_max_intermediate() (768: two A buffers of 128 rows must
+ * fit in shared memory beside the W2 stages); larger I returns NVFP4_ERR_UNSUPPORTED_SHAPE.
+ * moe_expert_forward_nvfp4 and moe_expert_forward_nvfp4_masked use it whenever I allows,
+ * and the two separate stages otherwise. */
+nvfp4_status moe_fc2_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
+                                   const int32_t* expert_offsets_dev, void* ws_dev,
+                                   size_t ws_bytes, float* fc2_debug_dev, void* stream);
+/* Largest expert intermediate size moe_fc2_requant_nvfp4 takes (host only). */
+int moe_fc2_requant_max_intermediate(void);
 
 /* Fixed-capacity ("masked") layout -- a second way to lay the routed rows out: expert e owns
  * rows [e*capacity, (e+1)*capacity) whatever the batch, its pairs first (token, slot order),
@@ -386,14 +408,15 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
                                      float* dw2_dev, float* dprob_dev, void* bwd_ws_dev, size_t bwd_ws_bytes,
                                      void* stream);
 
-/* nvfp4_silu_table -- copy the SiLU table that the FC1 epilogue applies to its BF16 gate
- * values ([RL/4.4]: SiLU(gate)*up in FP32) into out_dev: float [65536], entry i = silu(a)
- * for the BF16 value a whose bit pattern is i, where silu(a) = a / (1 + e^-a) rounded once
- * (to nearest, ties to even) to FP32; silu(+-0) = +-0, silu(+inf) = +inf, silu(-inf) and
- * silu(NaN) are NaN.  The table is part of the library's device image (computed when the
- * library is built), so it exists as soon as the library is loaded and no call has to fill
- * it first.  out_dev: device memory, 4-byte aligned, 262144 bytes, owned by the caller.
- * Enqueued on `stream` (a device-to-device copy); returns NVFP4_ERR_CUDA if it cannot be. */
+/* nvfp4_silu_table -- the SiLU that the FC1 epilogue applies to its BF16 gate values
+ * ([RL/4.4]: SiLU(gate)*up in FP32), evaluated by the epilogue's own code for every input:
+ * out_dev float [65536], entry i = silu(a) for the BF16 value a whose bit pattern is i, where
+ * silu(a) = a / (1 + e^-a) rounded once (to nearest, ties to even) to FP32; silu(+-0) = +-0,
+ * silu(+inf) = +inf, silu(-inf) and silu(NaN) are NaN.  The values come from a table that is
+ * part of the library's device image (computed when the library is built, so no call has to
+ * fill it first) and, outside 2^-24 <= |a| < 2^7, from closed forms that give the same bits.
+ * out_dev: device memory, 4-byte aligned, 262144 bytes, owned by the caller.  Enqueued on
+ * `stream` (one small kernel); returns NVFP4_ERR_CUDA if it cannot be. */
 nvfp4_status nvfp4_silu_table(float* out_dev, void* stream);
 
 /* Synchronise `stream`, then report and clear this device's error word:

@@ -5,7 +5,7 @@ CUDA kernels; PyTorch provides device memory and the current stream.  The
 entry points have the names of the C ABI in ``include/nvfp4_moe.h``:
 
     nvfp4_quantize_rows, moe_route_sort_amax, moe_expert_forward_nvfp4,
-    moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16,
+    moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_fc2_requant_nvfp4, moe_combine_bf16,
     moe_workspace_bytes, moe_workspace_layout_query, nvfp4_sf_bytes,
     nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string, nvfp4_silu_table,
     moe_router_topk, the fixed-capacity moe_*_masked calls, and the
@@ -83,6 +83,8 @@ _SIGNATURES = {
     "moe_requant_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
     "moe_fc2_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_combine_bf16": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
+    "moe_fc2_requant_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
+    "moe_fc2_requant_max_intermediate": (_I32, []),
     "nvfp4_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_int)]),
     "nvfp4_silu_table": (_I32, [_P, _P]),
     "moe_route_sort_amax_noalloc": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -185,8 +187,9 @@ def nvfp4_quantize_rows(x, codes=None, sf=None, g=None, stream=None):
 
 
 def nvfp4_silu_table(out=None, stream=None):
-    """The FC1 epilogue's SiLU table: float32 [65536] on the current device, entry i =
-    silu of the BF16 value with bit pattern i, rounded once to FP32."""
+    """The SiLU the FC1 epilogue applies, evaluated by its own code for every BF16 input:
+    float32 [65536] on the current device, entry i = silu of the BF16 value with bit pattern
+    i, rounded once to FP32."""
     if out is None:
         out = torch.empty(65536, dtype=torch.float32, device="cuda")
     _need_cuda(out)
@@ -325,6 +328,17 @@ def moe_fc2_nvfp4(weights, T, k, expert_offsets, ws, debug=None, stream=None):
     _need_cuda(expert_offsets, ws, debug)
     _check("moe_fc2_nvfp4", lib().moe_fc2_nvfp4(
         weights.ref(), T, k, _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(debug), _stream(stream)))
+
+
+def moe_fc2_requant_nvfp4(weights, T, k, expert_offsets, ws, debug=None, stream=None):
+    """Requantisation of h fused into FC2 (one kernel; y bitwise that of the two stages)."""
+    _need_cuda(expert_offsets, ws, debug)
+    _check("moe_fc2_requant_nvfp4", lib().moe_fc2_requant_nvfp4(
+        weights.ref(), T, k, _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(debug), _stream(stream)))
+
+
+def moe_fc2_requant_max_intermediate():
+    return lib().moe_fc2_requant_max_intermediate()
 
 
 def moe_combine_bf16(weights, T, k, out, ws, stream=None):

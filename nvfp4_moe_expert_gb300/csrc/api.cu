@@ -409,6 +409,23 @@ static nvfp4_status moe_fc2_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, in
                                 static_cast<cudaStream_t>(stream), pdl));
 }
 
+static nvfp4_status moe_fc2_requant_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k,
+                                               const int32_t* expert_offsets_dev, void* ws_dev, size_t ws_bytes,
+                                               float* fc2_debug_dev, void* stream, bool pdl, int capacity = 0) {
+    moe_workspace_layout L;
+    const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
+    if (s != NVFP4_OK) return s;
+    if (w->I > fc2_requant_max_i()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!expert_offsets_dev) return NVFP4_ERR_INVALID_ARG;
+    if (T == 0) return NVFP4_OK;
+    int* err = device_error_ptr();
+    if (!err) return NVFP4_ERR_CUDA;
+    GemmArgs a = fc2_args(w, expert_offsets_dev, ws_dev, L, fc2_debug_dev, err);
+    a.h = at<uint16_t>(ws_dev, L.h);             // the FC2 input before requantisation, and its maxima
+    a.amax2 = at<uint32_t>(ws_dev, L.amax2);
+    return from_cuda(launch_fc2_requant(a, static_cast<cudaStream_t>(stream), pdl));
+}
+
 static nvfp4_status moe_combine_bf16_impl(const moe_nvfp4_weights* w, int64_t T, int k, void* out_dev, void* ws_dev,
                               size_t ws_bytes, void* stream, bool pdl, int capacity = 0) {
     moe_workspace_layout L;
@@ -418,6 +435,24 @@ static nvfp4_status moe_combine_bf16_impl(const moe_nvfp4_weights* w, int64_t T,
     if (!out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
     return from_cuda(launch_combine(at<uint16_t>(ws_dev, L.y), T, k, w->H, static_cast<uint16_t*>(out_dev),
                                     static_cast<cudaStream_t>(stream), pdl));
+}
+
+// FC1, then the FC2 input's requantisation and FC2 (fused into one kernel where it fits, as
+// two launches otherwise), then the combine; every kernel after FC1 starts early
+// (programmatic dependent launch) and waits on its predecessor in the device.
+static nvfp4_status forward_stages(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* offs, void* out_dev,
+                                   void* ws_dev, size_t ws_bytes, void* stream, int capacity) {
+    nvfp4_status s = moe_fc1_swiglu_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, false, capacity);
+    if (s != NVFP4_OK) return s;
+    if (w->I <= fc2_requant_max_i()) {
+        s = moe_fc2_requant_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, true, capacity);
+    } else {
+        s = moe_requant_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, stream, true, capacity);
+        if (s != NVFP4_OK) return s;
+        s = moe_fc2_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, true, capacity);
+    }
+    if (s != NVFP4_OK) return s;
+    return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, true, capacity);
 }
 
 // The stage entry points: each one's kernel is ordered after all earlier work on the stream.
@@ -441,6 +476,13 @@ nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void
     return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, false);
 }
 
+nvfp4_status moe_fc2_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                                   void* ws_dev, size_t ws_bytes, float* fc2_debug_dev, void* stream) {
+    return moe_fc2_requant_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, fc2_debug_dev, stream, false);
+}
+
+int moe_fc2_requant_max_intermediate(void) { return fc2_requant_max_i(); }
+
 nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
                                       void* out_dev, void* ws_dev, size_t ws_bytes, void* stream) {
     moe_workspace_layout L;
@@ -448,15 +490,7 @@ nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int
     if (s != NVFP4_OK) return s;
     if (T == 0) return NVFP4_OK;
     if (!expert_offsets_dev || !out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
-    // FC1 is ordered after everything queued before; the three kernels after it start
-    // early (programmatic dependent launch) and wait on their predecessor in the device
-    s = moe_fc1_swiglu_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, false);
-    if (s != NVFP4_OK) return s;
-    s = moe_requant_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, stream, true);
-    if (s != NVFP4_OK) return s;
-    s = moe_fc2_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, true);
-    if (s != NVFP4_OK) return s;
-    return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, true);
+    return forward_stages(w, T, k, expert_offsets_dev, out_dev, ws_dev, ws_bytes, stream, 0);
 }
 
 nvfp4_status moe_router_topk(const void* x_dev, int64_t T, int H, const void* w_router_dev, int E, int k,
@@ -485,13 +519,7 @@ nvfp4_status moe_expert_forward_nvfp4_masked(const moe_nvfp4_weights* w, int64_t
     if (s != NVFP4_OK) return s;
     if (T == 0) return NVFP4_OK;
     if (!expert_offsets_dev || !out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
-    s = moe_fc1_swiglu_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, false, capacity);
-    if (s != NVFP4_OK) return s;
-    s = moe_requant_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, stream, true, capacity);
-    if (s != NVFP4_OK) return s;
-    s = moe_fc2_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, true, capacity);
-    if (s != NVFP4_OK) return s;
-    return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, true, capacity);
+    return forward_stages(w, T, k, expert_offsets_dev, out_dev, ws_dev, ws_bytes, stream, capacity);
 }
 
 nvfp4_status nvfp4_transpose_bf16(const void* in_dev, int64_t batch, int64_t rows, int64_t cols, void* out_dev,

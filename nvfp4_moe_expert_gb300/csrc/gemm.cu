@@ -47,6 +47,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "nvfp4_quant.cuh"
 #include "ptx.cuh"
 
 namespace nvfp4 {
@@ -81,20 +82,58 @@ static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 constexpr int kStagePitch = 144;                      // 128 B of BF16 per row + 16 B pad (no bank conflicts)
 constexpr int kStageWarpBytes = 32 * kStagePitch;     // one warp's 32 rows (FC2 output transpose)
 constexpr int kEpiStageOff = kStages * kStageBytes;
-constexpr int kScaleOff = kEpiStageOff + kEpiWarps * kStageWarpBytes;   // 128 floats per epilogue warp
-constexpr int kOffsetsOff = kScaleOff + kEpiWarps * 128 * 4;             // expert offsets, up to 1025 ints
-constexpr int kSiluOff = kOffsetsOff + 4352;
-// SiLU of the BF16 values with 2^-8 <= |a| < 2^4 (bit patterns 0x3B80..0x417F and their
-// negatives): 3072 entries copied from the global table into shared memory per CTA
-constexpr uint32_t kSiluLo = 0x3B80u, kSiluSpan = 0x4180u - 0x3B80u;
-constexpr int kBarOff = kSiluOff + 2 * kSiluSpan * 4;
+// SiLU of the BF16 values with 2^-24 <= |a| < 2^7 (bit patterns 0x3380..0x42FF and their
+// negatives): 7936 entries copied from the global table into shared memory per FC1 CTA.
+// Outside that range silu has a closed form (silu_bf16), so no lookup leaves the SM.
+constexpr uint32_t kSiluLo = 0x3380u, kSiluSpan = 0x4300u - 0x3380u;
 constexpr int kBarrierBytes = 256;
-constexpr int kSmemBytes = kBarOff + kBarrierBytes + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+// Shared-memory layout after the stages: FC2 has the output transpose buffers, FC1 (whose
+// lanes store their own rows) the SiLU range instead.
+template <bool kFC1>
+struct Smem {
+    static constexpr int scale = kEpiStageOff + (kFC1 ? 0 : kEpiWarps * kStageWarpBytes);   // 128 floats per warp
+    static constexpr int offsets = scale + kEpiWarps * 128 * 4;                             // up to 1025 ints
+    static constexpr int silu = offsets + 4352;
+    static constexpr int bar = silu + (kFC1 ? 2 * kSiluSpan * 4 : 0);
+    static constexpr int bytes = bar + kBarrierBytes + 1024;
+    static_assert(bytes <= 232448, "shared memory budget");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;                     // per stage: SFA 4, SFB 8 columns per MMA
 constexpr uint32_t kSfColsPerStage = 12 * kMmaPerStage;
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+
+// silu of the BF16 value with bit pattern `bits` (low 16 bits), as the FC1 epilogue applies it:
+// from the shared-memory copy of the table for 2^-24 <= |a| < 2^7; a/2 below (the correctly
+// rounded silu there, a*sigma(a) = a/2 + a^2/4 - ... differing from a/2 by under half an ulp;
+// also +-0); a for a >= 2^7 and -0 for a <= -2^7 (e^-128 is far below the rounding); the
+// global table for infinities and NaN.  Every value equals the table's (checked over all
+// 65536 inputs by the tests through nvfp4_silu_table).
+__device__ __forceinline__ float silu_bf16(uint32_t bits, const float* s_silu) {
+    const uint32_t mag = bits & 0x7FFFu;
+    const uint32_t idx = mag - kSiluLo;
+    if (idx < kSiluSpan) return s_silu[idx + ((bits >> 15) ? kSiluSpan : 0u)];
+    const float a = __uint_as_float(bits << 16);
+    if (mag < kSiluLo) return a * 0.5f;
+    if (mag < 0x7F80u) return (bits >> 15) ? -0.0f : a;
+    return __uint_as_float(__ldg(g_silu_bits + bits));
+}
+
+// Copy the table's SiLU range into shared memory (2 * kSiluSpan floats).
+__device__ __forceinline__ void load_silu_range(float* s_silu) {
+    for (int i = threadIdx.x; i < 2 * static_cast<int>(kSiluSpan); i += blockDim.x) {
+        const uint32_t bits = kSiluLo + (i % kSiluSpan) + (i >= static_cast<int>(kSiluSpan) ? 0x8000u : 0u);
+        s_silu[i] = __uint_as_float(__ldg(g_silu_bits + bits));
+    }
+}
+
+// Every BF16 input through silu_bf16, as the FC1 epilogue evaluates it (one block).
+__global__ void __launch_bounds__(1024) silu_eval_kernel(float* out) {
+    extern __shared__ float s_silu_eval[];
+    load_silu_range(s_silu_eval);
+    __syncthreads();
+    for (int i = threadIdx.x; i < 65536; i += blockDim.x) out[i] = silu_bf16(static_cast<uint32_t>(i), s_silu_eval);
+}
 
 // Expert owning routed row `row`: largest e < E with off[e] <= row (off in shared memory).
 __device__ __forceinline__ int expert_of_row(const int32_t* off, int E, int row) {
@@ -184,16 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+    using L = Smem<kFC1>;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bar);
     uint64_t* empty = full + kStages;
     uint64_t* tmem_full = empty + kStages;
     uint64_t* tmem_empty = tmem_full + 1;
     uint64_t* drain = tmem_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* scale_buf = reinterpret_cast<float*>(smem + kScaleOff);
-    int32_t* s_off = reinterpret_cast<int32_t*>(smem + kOffsetsOff);
-    float* s_silu = reinterpret_cast<float*>(smem + kSiluOff);
+    float* scale_buf = reinterpret_cast<float*>(smem + L::scale);
+    int32_t* s_off = reinterpret_cast<int32_t*>(smem + L::offsets);
+    float* s_silu = reinterpret_cast<float*>(smem + L::silu);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -221,12 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
     pdl_launch_dependents();
     for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
-    if (kFC1) {
-        for (int i = threadIdx.x; i < 2 * static_cast<int>(kSiluSpan); i += blockDim.x) {
-            const uint32_t bits = kSiluLo + (i % kSiluSpan) + (i >= static_cast<int>(kSiluSpan) ? 0x8000u : 0u);
-            s_silu[i] = __uint_as_float(__ldg(g_silu_bits + bits));
-        }
-    }
+    if (kFC1) load_silu_range(s_silu);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -452,14 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dbg[I + j + 1] = vu[1];
                     }
                     const uint32_t gb = bf16x2_rn(vg[0], vg[1]), ub = bf16x2_rn(vu[0], vu[1]);
-                    float sl[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t gbits = u ? gb >> 16 : gb & 0xFFFFu;
-                        const uint32_t gi = (gbits & 0x7FFFu) - kSiluLo;
-                        sl[u] = gi < kSiluSpan ? s_silu[gi + ((gbits >> 15) ? kSiluSpan : 0u)]
-                                               : __uint_as_float(__ldg(g_silu_bits + gbits));
-                    }
+                    const float sl[2] = {silu_bf16(gb & 0xFFFFu, s_silu), silu_bf16(gb >> 16, s_silu)};
                     // silu(gate) * up in FP32, then * p, one BF16 rounding
                     const uint64_t h2 = f2_mul(f2_mul(f2(__float_as_uint(sl[0]), __float_as_uint(sl[1])),
                                                       f2(ub << 16, ub & 0xFFFF0000u)),
@@ -510,6 +538,388 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
 }
+
+// ---------------------------------------------------------------- FC2 with the requantisation fused
+// The FC2 input h is requantised inside the FC2 kernel, so the requantised operand never goes
+// through HBM ("miniTE diagnoses and narrows the cross-engine execution gap of NVFP4 RL",
+// section "Assumptions and limits": online amax-quantisation-GEMM fusion).  FC2's A operand of
+// one m-tile (its 128 routed rows, all I columns) is quantised once into shared memory, in the
+// K-major 128B-swizzled layout a TMA load would give, with its block scales in the 512-byte
+// scale-tile layout and its outer scales g2 = amax2 / 2688 taken from the maxima FC1 reduced;
+// it then stays resident while the W2 tiles of the unit's n-tiles stream through a 2-stage
+// ring.  The quantiser is the one the requant kernel runs (nvfp4_quant.cuh) and the MMA walks
+// K in the same order over the same codes and scales, so y is bitwise what the staged
+// requant + FC2 give.
+//
+// Work unit: (m-tile, group of n-tiles); the number of groups per m-tile is chosen on the
+// device from the number of m-tiles so that the units spread over the SMs with a short tail.
+// A is double-buffered: the epilogue warps quantise the next unit's A one row chunk before each
+// of the current unit's tile epilogues, so the MMA warp finds it ready when the unit changes.
+// Fits I <= 768 (two 54 KB A buffers beside two 36 KB B stages and the output transpose).
+namespace fused {
+constexpr int kMaxI = 768;
+constexpr int kStagesB = 2;
+constexpr int kThreadsF = 64 + kEpiThreads;                       // producer B, MMA, 8 epilogue warps
+constexpr int kABlockBytes = kBM * kBKBytes;                      // one K=256 block of 128 rows: 16 KB
+constexpr int kACodesBytes = (kMaxI / 256) * kABlockBytes;        // 48 KB
+constexpr int kASfBytes = (kMaxI / 64) * kSfAtomBytes;            // 6 KB
+constexpr int kABufBytes = kACodesBytes + kASfBytes;
+static_assert(kABufBytes % 1024 == 0, "A buffers keep 1024-byte alignment");
+constexpr int kBStageBytes = kBBytes + 2 * kMmaPerStage * kSfAtomBytes;
+constexpr int kBOff = 2 * kABufBytes;
+constexpr int kEpiOff = kBOff + kStagesB * kBStageBytes;
+constexpr int kScaleOffF = kEpiOff + kEpiWarps * kStageWarpBytes;
+constexpr int kRowOff = kScaleOffF + kEpiWarps * 128 * 4;         // per A buffer: g2[128]
+constexpr int kOffsetsOffF = kRowOff + 2 * 128 * 4;
+constexpr int kBarOffF = kOffsetsOffF + 4352;
+constexpr int kSmemBytesF = kBarOffF + kBarrierBytes + 1024;
+static_assert(kSmemBytesF <= 232448, "shared memory budget");
+constexpr uint32_t kSfColsPerStageF = 12 * kMmaPerStage;
+static_assert(kSfCol0 + kStagesB * kSfColsPerStageF <= kTmemCols, "TMEM budget");
+
+// Work units of one launch: n-tile groups per m-tile, the smallest estimated makespan
+// (rounds of units over the grid, each unit costing its n-tiles plus one for quantising A).
+struct Units {
+    int groups, per, count;
+    __device__ Units(int num_m, int n_tiles, int grid) {
+        groups = 1;
+        long long best = -1;
+        for (int g = 1; g <= n_tiles && n_tiles % g == 0; g *= 2) {
+            const long long rounds = (static_cast<long long>(num_m) * g + grid - 1) / grid;
+            const long long cost = rounds * (n_tiles / g + 1);
+            if (best < 0 || cost < best) {
+                best = cost;
+                groups = g;
+            }
+            if (g > n_tiles / 2) break;
+        }
+        per = n_tiles / groups;
+        count = num_m * groups;
+    }
+};
+
+// Quantise rows [r0, r1) of m-tile mt's h into A buffer `abuf` (codes, scales) and their
+// outer scales g2s: the epilogue warps share the rows, each row over G = I/64 lanes.
+__device__ __forceinline__ void quantize_a_rows(const GemmArgs& args, int mt, int r0, int r1, uint8_t* abuf,
+                                                float* g2s, int ew) {
+    const int I = args.I;
+    const int G = I / 64;
+    const RowLanes rl(G);
+    const int lane = threadIdx.x & 31;
+    uint8_t* sfb = abuf + kACodesBytes;
+    for (int base = r0 + ew * rl.RPW; base < r1; base += kEpiWarps * rl.RPW) {
+        const int r = base + rl.slot;
+        const bool row_ok = rl.active && r < r1;
+        const int64_t grow = static_cast<int64_t>(mt) * kBM + r;
+        const int32_t pair = row_ok ? __ldg(args.row_pair + grow) : -1;
+        const uint32_t amax_bits = row_ok ? __ldg(args.amax2 + grow) : 0u;
+        uint4 v[1][8];
+        if (pair >= 0) load_row_lanes<1>(args.h + grow * I, rl, G, v);
+        // every lane of the warp takes part in the row maximum's reduction
+        GroupQ q[1];
+        bool finite = true;
+        float gr = 0.0f;
+        if (rl.active) {
+            if (pair < 0) {   // pad row (or past the chunk): zero codes are not needed, zero scales are
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[0][i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            gr = quantize_loaded<1>(v, rl, G, __uint_as_float(amax_bits), q, finite);
+        }
+        if (!row_ok) continue;
+        if (pair < 0) {
+            q[0].sfw = 0u;
+            gr = 0.0f;
+        } else if (!finite && rl.li == 0) {
+            set_device_error(args.err, NVFP4_ERR_NONFINITE);
+        }
+        const int grp = rl.li;
+        if (grp < G) {
+            // codes: K block grp/4, 32 bytes at (grp%4)*32 of the row, as two swizzled 16-byte chunks
+            uint8_t* rowp = abuf + (grp >> 2) * kABlockBytes + r * kBKBytes;
+            const int c0 = 2 * (grp & 3);
+            *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) =
+                make_uint4(q[0].code[0], q[0].code[1], q[0].code[2], q[0].code[3]);
+            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) =
+                make_uint4(q[0].code[4], q[0].code[5], q[0].code[6], q[0].code[7]);
+            *reinterpret_cast<uint32_t*>(sfb + grp * kSfAtomBytes + (r & 31) * 16 + (r >> 5) * 4) = q[0].sfw;
+        }
+        if (rl.li == 0) g2s[r] = gr;
+    }
+    (void)lane;
+}
+
+__global__ void __maxnreg__(200)
+    fc2_requant_kernel(const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffF);
+    uint64_t* empty = full + kStagesB;
+    uint64_t* a_full = empty + kStagesB;          // [2]
+    uint64_t* tmem_full = a_full + 2;
+    uint64_t* tmem_empty = tmem_full + 1;
+    uint64_t* drain = tmem_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* scale_buf = reinterpret_cast<float*>(smem + kScaleOffF);
+    int32_t* s_off = reinterpret_cast<int32_t*>(smem + kOffsetsOffF);
+    float* g2_s = reinterpret_cast<float*>(smem + kRowOff);                 // [2][128]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesB; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&a_full[0], kEpiThreads);
+        mbar_init(&a_full[1], kEpiThreads);
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, kEpiThreads);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) prefetch_tensormap(&tmB);
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int E = args.E;
+    const int num_m = s_off[E] / kBM;
+    const int n_tiles = args.H / kBN;
+    const Units U(num_m, n_tiles, gridDim.x);
+    const int num_k64 = args.I / 64;
+    const int num_ks = (num_k64 + kMmaPerStage - 1) / kMmaPerStage;
+    bool failed = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer of B (W2 tiles)
+        const uint64_t pol = policy_evict_normal();
+        int stage = 0;
+        uint32_t phase = 0, issued = 0, issued_parity = 0;
+        for (int u = blockIdx.x; u < U.count && !failed; u += gridDim.x) {
+            const int mt = u / U.groups, nt0 = (u % U.groups) * U.per;
+            const int e = expert_of_row(s_off, E, mt * kBM);
+            for (int nt = nt0; nt < nt0 + U.per && !failed; ++nt) {
+                const int row0 = e * args.Nw + nt * kBN;
+                for (int ks = 0; ks < num_ks; ++ks) {
+                    const bool ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetCycles);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) {
+                        failed = true;
+                        break;
+                    }
+                    const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
+                    const uint32_t sf_bytes = static_cast<uint32_t>(nk) * kSfAtomBytes;
+                    uint8_t* st = smem + kBOff + stage * kBStageBytes;
+                    mbar_arrive_expect_tx_elect(&full[stage], kBBytes + 2 * sf_bytes);
+                    tma_load_2d_elect(st, &tmB, &full[stage], ks * kBKBytes, row0, pol);
+                    bulk_load_elect(st + kBBytes,
+                                    args.b_sf + (static_cast<int64_t>(row0 / 128) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
+                                    sf_bytes, &full[stage], pol);
+                    bulk_load_elect(st + kBBytes + kMmaPerStage * kSfAtomBytes,
+                                    args.b_sf + (static_cast<int64_t>(row0 / 128 + 1) * num_k64 + kMmaPerStage * ks) * kSfAtomBytes,
+                                    sf_bytes, &full[stage], pol);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStagesB) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        if (failed) {
+            if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            for (int s = 0; s < kStagesB; ++s) {
+                if (issued & (1u << s)) mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, kWaitBudgetCycles);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t idesc = idesc_nvf4(kBM, kBN);
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool issued_any = false;
+        int local = 0;
+        for (int u = blockIdx.x; u < U.count && !failed; u += gridDim.x, ++local) {
+            const int ab = local & 1;
+            const bool oka = mbar_wait_bounded(&a_full[ab], (local >> 1) & 1, abort_flag, kWaitBudgetCycles);
+            if (!__all_sync(0xFFFFFFFFu, oka)) {
+                failed = true;
+                break;
+            }
+            const uint32_t a_base = smem_u32(smem + ab * kABufBytes);
+            const uint32_t a_sf = a_base + kACodesBytes;
+            for (int j = 0; j < U.per && !failed; ++j) {
+                const bool ok = mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, kWaitBudgetCycles);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    failed = true;
+                    break;
+                }
+                acc_phase ^= 1u;
+                tc_fence_after();
+                for (int ks = 0; ks < num_ks; ++ks) {
+                    const bool okf = mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetCycles);
+                    if (!__all_sync(0xFFFFFFFFu, okf)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(kMmaPerStage, num_k64 - kMmaPerStage * ks);
+                    const uint32_t st = smem_u32(smem + kBOff + stage * kBStageBytes);
+                    const uint32_t sf_col = tmem + kSfCol0 + kSfColsPerStageF * stage;
+                    const uint64_t adesc = sdesc_k_swizzled<kSwizzleBytes>(a_base + ks * kABlockBytes);
+                    const uint64_t bdesc = sdesc_k_swizzled<kSwizzleBytes>(st);
+                    const uint32_t sfa = a_sf + kMmaPerStage * ks * kSfAtomBytes;
+                    const uint32_t sfb = st + kBBytes;
+                    if (kMmaPerStage == 4 && nk == 4) {
+                        tc_stage4_nvf4_elect(tmem, adesc, bdesc, idesc, sdesc_sf(sfa), sdesc_sf(sfb),
+                                             sdesc_sf(sfb + kMmaPerStage * kSfAtomBytes), sf_col, ks != 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < kMmaPerStage; ++jj) {
+                            if (jj < nk) {
+                                tc_cp_32x128b_warpx4_elect(sf_col + 4 * jj, sdesc_sf(sfa + kSfAtomBytes * jj));
+                                tc_cp_32x128b_warpx4_elect(sf_col + 4 * kMmaPerStage + 8 * jj,
+                                                           sdesc_sf(sfb + kSfAtomBytes * jj));
+                                tc_cp_32x128b_warpx4_elect(sf_col + 4 * kMmaPerStage + 8 * jj + 4,
+                                                           sdesc_sf(sfb + kMmaPerStage * kSfAtomBytes + kSfAtomBytes * jj));
+                                tc_mma_nvf4_elect(tmem, adesc + 2 * jj, bdesc + 2 * jj, idesc, sf_col + 4 * jj,
+                                                  sf_col + 4 * kMmaPerStage + 8 * jj, (ks | jj) != 0 ? 1u : 0u);
+                            }
+                        }
+                    }
+                    issued_any = true;
+                    tc_commit_elect(&empty[stage]);
+                    if (++stage == kStagesB) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (failed) break;
+                tc_commit_elect(tmem_full);
+            }
+        }
+        if (failed) {
+            if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            if (issued_any) {
+                tc_commit_elect(drain);
+                mbar_wait_bounded(drain, 0, nullptr, kWaitBudgetCycles);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue + A quantisers
+        const int ew = warp - 2;                             // 0..7
+        const int q = warp & 3;                              // TMEM lane quarter of this warp
+        const int half = ew >> 2;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        float* sc = scale_buf + ew * 128;
+        uint8_t* stage_buf = smem + kEpiOff + ew * kStageWarpBytes;
+        uint32_t acc_phase = 0;
+        const int H = args.H;
+        // the first unit's A, whole
+        if (static_cast<int>(blockIdx.x) < U.count) {
+            quantize_a_rows(args, blockIdx.x / U.groups, 0, kBM, smem, g2_s, ew);
+            fence_proxy_async_shared();
+            mbar_arrive(&a_full[0]);
+        }
+        int local = 0;
+        for (int u = blockIdx.x; u < U.count; u += gridDim.x, ++local) {
+            const int ab = local & 1;
+            const int mt = u / U.groups, nt0 = (u % U.groups) * U.per;
+            const int e = expert_of_row(s_off, E, mt * kBM);
+            const int un = u + gridDim.x;                    // the next unit, whose A is quantised now
+            // this unit's row data: written by all epilogue warps before they arrived on a_full
+            if (!mbar_wait_bounded(&a_full[ab], (local >> 1) & 1, abort_flag, kWaitBudgetCycles)) {
+                if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            const int row = q * 32 + lane;
+            const int pair = __ldg(args.row_pair + static_cast<int64_t>(mt) * kBM + row);
+            const float gr = pair >= 0 ? g2_s[ab * 128 + row] : 0.0f;
+            const bool live = pair >= 0;
+            const float* gw = args.b_g + static_cast<int64_t>(e) * args.Nw;
+            bool stop = false;
+            for (int j = 0; j < U.per; ++j) {
+                const int nt = nt0 + j;
+                if (un < U.count) {
+                    const int r0 = j * kBM / U.per, r1 = (j + 1) * kBM / U.per;
+                    quantize_a_rows(args, un / U.groups, r0, r1, smem + (ab ^ 1) * kABufBytes, g2_s + (ab ^ 1) * 128,
+                                    ew);
+                    if (j == U.per - 1) {
+                        fence_proxy_async_shared();
+                        mbar_arrive(&a_full[ab ^ 1]);
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[lane + 32 * i] = __ldg(gw + nt * kBN + 128 * half + lane + 32 * i);
+                __syncwarp();
+                if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
+                    if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                    stop = true;
+                    break;
+                }
+                acc_phase ^= 1u;
+                tc_fence_after();
+                uint32_t acc[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 128 * half + 32 * c, acc[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(tmem_empty);
+
+                const float* sw = sc;
+                const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
+                const int64_t grow = static_cast<int64_t>(mt) * kBM + row;
+                float* dbg = args.debug ? args.debug + grow * H + nt * kBN + 128 * half : nullptr;
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t packed[32];
+#pragma unroll
+                    for (int jj = 0; jj < 64; jj += 2) {
+                        const int c = 64 * c2 + jj;
+                        const uint64_t v2 = f2_mul(f2_mul(f2(acc[c >> 5][c & 31], acc[c >> 5][(c & 31) + 1]), gr2),
+                                                   *reinterpret_cast<const uint64_t*>(sw + c));
+                        float v0, v1;
+                        f2_unpack(v2, v0, v1);
+                        if (dbg && live) {
+                            dbg[c] = v0;
+                            dbg[c + 1] = v1;
+                        }
+                        packed[jj >> 1] = bf16x2_rn(v0, v1);
+                    }
+                    uint16_t* ybase = args.y + nt * kBN + 128 * half + 64 * c2;
+                    store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
+                        const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
+                        return pr >= 0 ? ybase + static_cast<int64_t>(pr) * H : nullptr;
+                    });
+                }
+            }
+            if (stop) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+}  // namespace fused
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -566,21 +976,23 @@ bool make_gateup_map(CUtensorMap* m, const void* base, int E, int I, int64_t row
 
 constexpr int kMaxDevices = 64;
 std::mutex g_init_mutex;
-bool g_attr_ready[kMaxDevices][2];
+bool g_attr_ready[kMaxDevices][3];
 
 // Host-side set-up of the kernel attributes, once per device (no launch, no synchronisation).
-cudaError_t prepare_device(bool fc1) {
+// which: 0 FC1, 1 FC2, 2 FC2 with the requantisation fused.
+cudaError_t prepare_device(int which) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_init_mutex);
-    const int which = fc1 ? 0 : 1;
     if (!g_attr_ready[dev][which]) {
-        e = fc1 ? cudaFuncSetAttribute(grouped_gemm_nvf4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes)
-                : cudaFuncSetAttribute(grouped_gemm_nvf4_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = which == 0 ? cudaFuncSetAttribute(grouped_gemm_nvf4_kernel<true>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<true>::bytes)
+            : which == 1 ? cudaFuncSetAttribute(grouped_gemm_nvf4_kernel<false>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<false>::bytes)
+                         : cudaFuncSetAttribute(fused::fc2_requant_kernel,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, fused::kSmemBytesF);
         if (e != cudaSuccess) return e;
         g_attr_ready[dev][which] = true;
     }
@@ -588,7 +1000,7 @@ cudaError_t prepare_device(bool fc1) {
 }
 
 cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st, bool pdl) {
-    cudaError_t e = prepare_device(fc1);
+    cudaError_t e = prepare_device(fc1 ? 0 : 1);
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb;
     if (!make_code_map(&ma, a.a_codes, a.rows_cap, a.K / 2, kBM)) return cudaErrorInvalidValue;
@@ -596,17 +1008,41 @@ cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st, bool pdl) 
             : !make_code_map(&mb, a.b_codes, static_cast<int64_t>(a.E) * a.Nw, a.K / 2, kBN))
         return cudaErrorInvalidValue;
     const int grid = device_sm_count();
-    if (fc1) return launch_pdl(pdl, grouped_gemm_nvf4_kernel<true>, grid, kThreads, kSmemBytes, st, ma, mb, a);
-    return launch_pdl(pdl, grouped_gemm_nvf4_kernel<false>, grid, kThreads, kSmemBytes, st, ma, mb, a);
+    if (fc1) return launch_pdl(pdl, grouped_gemm_nvf4_kernel<true>, grid, kThreads, Smem<true>::bytes, st, ma, mb, a);
+    return launch_pdl(pdl, grouped_gemm_nvf4_kernel<false>, grid, kThreads, Smem<false>::bytes, st, ma, mb, a);
+}
+
+cudaError_t launch_fc2_requant_impl(const GemmArgs& a, cudaStream_t st, bool pdl) {
+    if (a.I > fused::kMaxI || a.I % 128 != 0) return cudaErrorInvalidValue;
+    cudaError_t e = prepare_device(2);
+    if (e != cudaSuccess) return e;
+    CUtensorMap mb;
+    if (!make_code_map(&mb, a.b_codes, static_cast<int64_t>(a.E) * a.Nw, a.K / 2, kBN)) return cudaErrorInvalidValue;
+    return launch_pdl(pdl, fused::fc2_requant_kernel, device_sm_count(), fused::kThreadsF, fused::kSmemBytesF, st, mb,
+                      a);
 }
 
 }  // namespace
+
+cudaError_t launch_fc2_requant(const GemmArgs& a, cudaStream_t st, bool pdl) {
+    return launch_fc2_requant_impl(a, st, pdl);
+}
+int fc2_requant_max_i() { return fused::kMaxI; }
 
 cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st, bool pdl) { return launch_gemm(true, a, st, pdl); }
 cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st, bool pdl) { return launch_gemm(false, a, st, pdl); }
 
 cudaError_t copy_silu_table(float* out, cudaStream_t st) {
-    return cudaMemcpyFromSymbolAsync(out, g_silu_bits, sizeof(g_silu_bits), 0, cudaMemcpyDeviceToDevice, st);
+    const size_t smem = 2 * kSiluSpan * sizeof(float);
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [smem] {
+        attr = cudaFuncSetAttribute(silu_eval_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+    });
+    if (attr != cudaSuccess) return attr;
+    silu_eval_kernel<<<1, 1024, smem, st>>>(out);
+    return cudaGetLastError();
 }
 
 }  // namespace nvfp4

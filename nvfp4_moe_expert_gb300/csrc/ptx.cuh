@@ -57,6 +57,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Order this thread's generic-proxy writes to shared memory before later async-proxy reads
+// of it (TMA, tcgen05.mma / tcgen05.cp operands) that another thread issues after a barrier.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                             uint64_t policy) {

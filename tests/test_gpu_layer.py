@@ -1,6 +1,7 @@
 """End-to-end parity of the GPU layer (moe_route_sort_amax + moe_expert_forward_nvfp4)
 with the oracle: output relative L2 <= 1e-2, FC2 requantisation code flips
-<= 0.1%, and the fused call identical to the four stages called one by one.
+<= 0.1%, and the fused call (FC2 with the requantisation fused in) identical to
+the four stages called one by one.
 At the full 2048/768/128/top-8 size with 4096 tokens the oracle checks a
 sample of routed rows and tokens."""
 
@@ -66,23 +67,74 @@ def a2_codes_by_pair(ws, lay, offs, T, k, I):
 ], ids=lambda c: c.name)
 def test_layer_vs_oracle(cfg):
     L = S.make_layer(cfg)
-    out, ws, offs, lay = gpu_layer(L, cfg.E)
+    out, _, _, _ = gpu_layer(L, cfg.E)
     wq = OM.quantize_weights(L["w1"], L["w2"])
     ref, inter = OM.moe_forward(L["x"], L["topk_ids"], L["topk_w"], wq, keep=True)
     got = torch_to_bf16_bits(out)
     assert rel_l2(F.bf16_bits_to_f32(got), F.bf16_bits_to_f32(ref)) <= LAYER_REL_L2
+    # the requantised FC2 operand: written to the workspace by the staged path (the fused FC2
+    # keeps it in shared memory), whose output is bitwise the fused one
+    out_s, ws, offs, lay = gpu_layer(L, cfg.E, stages=True)
+    assert np.array_equal(torch_to_bf16_bits(out_s), got)
     ref_codes = Q.pack_nibbles(inter["hq"][0])
     gpu_codes = a2_codes_by_pair(ws, lay, offs, cfg.T, cfg.k, cfg.I)
     flips = (Q.unpack_nibbles(ref_codes) != Q.unpack_nibbles(gpu_codes)).mean()
     assert flips <= FC2_CODE_FLIP_RATE, flips
 
 
-def test_fused_equals_stages():
-    cfg = S.LayerConfig("mid", H=1024, I=384, E=16, k=4, T=300)
+@pytest.mark.parametrize("cfg", [
+    S.LayerConfig("mid", H=1024, I=384, E=16, k=4, T=300),
+    S.LayerConfig("one_ntile", H=256, I=128, E=8, k=2, T=700),
+    S.LayerConfig("narrow_i", H=512, I=256, E=4, k=2, T=2000, routing="zipf"),
+    S.LayerConfig("qwen_many_mtiles", H=2048, I=768, E=128, k=8, T=3000, routing="zipf", outlier_frac=0.01),
+    S.LayerConfig("qwen_few_mtiles", H=2048, I=768, E=128, k=8, T=40),
+], ids=lambda c: c.name)
+def test_fused_equals_stages(cfg):
+    """moe_expert_forward_nvfp4 (FC2 with the requantisation fused in) against the four stages
+    called one by one (requant writes A2 to memory, FC2 reads it back): bitwise equal, over
+    shapes whose m-tile counts make the fused kernel group n-tiles differently and that take
+    partial K blocks (I = 384) and a single n-tile (H = 256)."""
     L = S.make_layer(cfg)
     a = torch_to_bf16_bits(gpu_layer(L, cfg.E)[0])
     b = torch_to_bf16_bits(gpu_layer(L, cfg.E, stages=True)[0])
     assert np.array_equal(a, b)
+
+
+def test_fused_fc2_stage_equals_requant_then_fc2():
+    """The fused stage entry point against the two stages it replaces, with the FP32 pre-cast
+    values of FC2 compared too (bit for bit), and y for every (token, slot)."""
+    cfg = S.LayerConfig("skew", H=2048, I=768, E=32, k=4, T=900, routing="zipf", outlier_frac=0.01)
+    L = S.make_layer(cfg)
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    w = M.quantize_moe_weights(bf16_to_torch(L["w1"]), bf16_to_torch(L["w2"]))
+    ws = M.alloc_workspace(T, H, I, E, k)
+    lay = M.moe_workspace_layout_query(T, H, I, E, k)
+    offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    M.moe_route_sort_amax(bf16_to_torch(L["x"]), torch.from_numpy(L["topk_ids"]).cuda(),
+                          torch.from_numpy(L["topk_w"]).cuda(), E, offs, ws)
+    M.moe_fc1_swiglu_nvfp4(w, T, k, offs, ws)
+    y_view = ws[lay.y:lay.y + 2 * T * k * H]
+    d1 = torch.full((lay.rows_cap, H), float("nan"), device="cuda")
+    d2 = torch.full((lay.rows_cap, H), float("nan"), device="cuda")
+    M.moe_requant_nvfp4(w, T, k, offs, ws)
+    M.moe_fc2_nvfp4(w, T, k, offs, ws, debug=d1)
+    y1 = y_view.clone()
+    y_view.zero_()
+    M.moe_fc2_requant_nvfp4(w, T, k, offs, ws, debug=d2)
+    assert M.nvfp4_get_device_error() == 0
+    assert torch.equal(y1, y_view)
+    assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))     # NaN-filled pad rows alike
+
+
+def test_fused_fc2_rejects_wide_intermediate():
+    cfg = S.LayerConfig("wide", H=256, I=1024, E=2, k=1, T=8)
+    assert M.moe_fc2_requant_max_intermediate() == 768
+    w = M.quantize_moe_weights(torch.zeros((2, 2048, 256), dtype=torch.bfloat16, device="cuda"),
+                               torch.zeros((2, 256, 1024), dtype=torch.bfloat16, device="cuda"))
+    ws = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    offs = torch.zeros(cfg.E + 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(M.NVFP4Error, match="UNSUPPORTED_SHAPE"):
+        M.moe_fc2_requant_nvfp4(w, cfg.T, cfg.k, offs, ws)
 
 
 def test_run_to_run_deterministic():

@@ -1,5 +1,6 @@
-"""The SiLU table in device memory (what the FC1 epilogue reads) equals the oracle's SiLU,
-FP64 then one rounding to FP32, bit for bit at all 65,536 BF16 gate values ("Finishing RL
+"""The SiLU the FC1 epilogue applies (its shared-memory range of the table and its closed
+forms outside it, run by the epilogue's own device function) equals the oracle's SiLU, FP64
+then one rounding to FP32, bit for bit at all 65,536 BF16 gate values ("Finishing RL
 training faster: bitwise consistency, high performance, agent-driven", section 4.4)."""
 
 import numpy as np
