@@ -419,6 +419,13 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
  * `stream` (one small kernel); returns NVFP4_ERR_CUDA if it cannot be. */
 nvfp4_status nvfp4_silu_table(float* out_dev, void* stream);
 
+/* The CUDA runtime error (a cudaError_t value) behind the calling thread's most recent
+ * NVFP4_ERR_CUDA, or 0 if no call of this thread has returned NVFP4_ERR_CUDA.  Host only; it
+ * neither synchronises nor clears anything. */
+int nvfp4_last_cuda_error(void);
+/* cudaGetErrorName of a cudaError_t value (static string, never NULL).  Host only. */
+const char* nvfp4_cuda_error_name(int error);
+
 /* Synchronise `stream`, then report and clear this device's error word:
  * *device_status receives NVFP4_OK or the first device error recorded since
  * the last call.  Returns NVFP4_ERR_CUDA if the synchronisation failed. */

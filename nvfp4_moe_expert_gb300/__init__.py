@@ -33,9 +33,9 @@ STATUS_NAMES = {
 
 
 class NVFP4Error(RuntimeError):
-    def __init__(self, fn, status):
+    def __init__(self, fn, status, detail=""):
         self.status = status
-        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}{detail}")
 
 
 class moe_nvfp4_weights(ctypes.Structure):
@@ -87,6 +87,8 @@ _SIGNATURES = {
     "moe_fc2_requant_max_intermediate": (_I32, []),
     "nvfp4_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_int)]),
     "nvfp4_silu_table": (_I32, [_P, _P]),
+    "nvfp4_last_cuda_error": (_I32, []),
+    "nvfp4_cuda_error_name": (ctypes.c_char_p, [_I32]),
     "moe_route_sort_amax_noalloc": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_router_topk": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
     "moe_workspace_layout_query_masked": (_I32, [_I64, _I32, _I32, _I32, _I32, _I32,
@@ -124,7 +126,11 @@ def lib():
 
 def _check(fn, status):
     if status != NVFP4_OK:
-        raise NVFP4Error(fn, status)
+        detail = ""
+        if status == 4 and _lib is not None:          # NVFP4_ERR_CUDA: name the CUDA error behind it
+            code = _lib.nvfp4_last_cuda_error()
+            detail = f" ({_lib.nvfp4_cuda_error_name(code).decode()}, {code})"
+        raise NVFP4Error(fn, status, detail)
 
 
 def _ptr(t):

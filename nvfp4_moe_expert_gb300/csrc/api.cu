@@ -137,7 +137,14 @@ void compute_backward_layout(int64_t T, int H, int I, int E, int k, moe_backward
     B->total = o;
 }
 
-nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+// The CUDA error behind the calling thread's last NVFP4_ERR_CUDA (cudaSuccess if none yet).
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+nvfp4_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return NVFP4_OK;
+    t_last_cuda_error = e;
+    return NVFP4_ERR_CUDA;
+}
 
 template <typename T>
 T* at(void* ws, size_t off) {
@@ -613,6 +620,10 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
     return from_cuda(launch_moe_backward_ste(a, st));
 }
 
+int nvfp4_last_cuda_error(void) { return static_cast<int>(t_last_cuda_error); }
+
+const char* nvfp4_cuda_error_name(int error) { return cudaGetErrorName(static_cast<cudaError_t>(error)); }
+
 nvfp4_status nvfp4_silu_table(float* out_dev, void* stream) {
     if (!out_dev || !aligned(out_dev, 4)) return NVFP4_ERR_INVALID_ARG;
     return from_cuda(copy_silu_table(out_dev, static_cast<cudaStream_t>(stream)));
@@ -621,12 +632,12 @@ nvfp4_status nvfp4_silu_table(float* out_dev, void* stream) {
 nvfp4_status nvfp4_get_device_error(void* stream, int* device_status) {
     if (!device_status) return NVFP4_ERR_INVALID_ARG;
     *device_status = NVFP4_OK;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (from_cuda(cudaStreamSynchronize(static_cast<cudaStream_t>(stream))) != NVFP4_OK) return NVFP4_ERR_CUDA;
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (from_cuda(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int))) != NVFP4_OK) return NVFP4_ERR_CUDA;
     if (v != 0) {
         const int zero = 0;
-        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+        if (from_cuda(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int))) != NVFP4_OK) return NVFP4_ERR_CUDA;
     }
     *device_status = v;
     return NVFP4_OK;

@@ -649,7 +649,65 @@ __device__ __forceinline__ void quantize_a_rows(const GemmArgs& args, int mt, in
     (void)lane;
 }
 
-__global__ void __maxnreg__(200)
+// One n-tile's epilogue for this warp's 32 rows and 128 columns: the column scales of W2 into
+// shared memory, the accumulator out of TMEM (handed back at once), y = bf16((acc*g2)*g^w2)
+// stored to the rows' (token, slot) places.  Out of line, so that the 128 accumulator
+// registers do not compete with the caller's loop state.  Returns false if the wait for the
+// accumulator ran out (the error is recorded).
+__device__ __noinline__ bool fc2_tile_epilogue(const GemmArgs& args, uint64_t* tmem_full, uint64_t* tmem_empty,
+                                               volatile int* abort_flag, uint32_t& acc_phase, uint32_t taddr,
+                                               float* sc, uint8_t* stage_buf, const float* gw, int mt, int nt, int row,
+                                               int pair, float gr, int half) {
+    const int lane = threadIdx.x & 31;
+    const int H = args.H;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[lane + 32 * i] = __ldg(gw + nt * kBN + 128 * half + lane + 32 * i);
+    __syncwarp();
+    if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
+        if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+    }
+    acc_phase ^= 1u;
+    tc_fence_after();
+    uint32_t acc[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 128 * half + 32 * c, acc[c]);
+    tmem_ld_wait();
+    tc_fence_before();
+    mbar_arrive(tmem_empty);
+
+    const bool live = pair >= 0;
+    const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
+    const int64_t grow = static_cast<int64_t>(mt) * kBM + row;
+    float* dbg = args.debug ? args.debug + grow * H + nt * kBN + 128 * half : nullptr;
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t packed[32];
+#pragma unroll
+        for (int jj = 0; jj < 64; jj += 2) {
+            const int c = 64 * c2 + jj;
+            const uint64_t v2 = f2_mul(f2_mul(f2(acc[c >> 5][c & 31], acc[c >> 5][(c & 31) + 1]), gr2),
+                                       *reinterpret_cast<const uint64_t*>(sc + c));
+            float v0, v1;
+            f2_unpack(v2, v0, v1);
+            if (dbg && live) {
+                dbg[c] = v0;
+                dbg[c + 1] = v1;
+            }
+            packed[jj >> 1] = bf16x2_rn(v0, v1);
+        }
+        uint16_t* ybase = args.y + nt * kBN + 128 * half + 64 * c2;
+        store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
+            const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
+            return pr >= 0 ? ybase + static_cast<int64_t>(pr) * H : nullptr;
+        });
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kThreadsF, 1)
     fc2_requant_kernel(const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -826,7 +884,6 @@ __global__ void __maxnreg__(200)
         float* sc = scale_buf + ew * 128;
         uint8_t* stage_buf = smem + kEpiOff + ew * kStageWarpBytes;
         uint32_t acc_phase = 0;
-        const int H = args.H;
         // the first unit's A, whole
         if (static_cast<int>(blockIdx.x) < U.count) {
             quantize_a_rows(args, blockIdx.x / U.groups, 0, kBM, smem, g2_s, ew);
@@ -848,7 +905,6 @@ __global__ void __maxnreg__(200)
             const int row = q * 32 + lane;
             const int pair = __ldg(args.row_pair + static_cast<int64_t>(mt) * kBM + row);
             const float gr = pair >= 0 ? g2_s[ab * 128 + row] : 0.0f;
-            const bool live = pair >= 0;
             const float* gw = args.b_g + static_cast<int64_t>(e) * args.Nw;
             bool stop = false;
             for (int j = 0; j < U.per; ++j) {
@@ -862,50 +918,10 @@ __global__ void __maxnreg__(200)
                         mbar_arrive(&a_full[ab ^ 1]);
                     }
                 }
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < 4; ++i) sc[lane + 32 * i] = __ldg(gw + nt * kBN + 128 * half + lane + 32 * i);
-                __syncwarp();
-                if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
-                    if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
-                    *abort_flag = 1;
+                if (!fc2_tile_epilogue(args, tmem_full, tmem_empty, abort_flag, acc_phase, taddr, sc, stage_buf, gw,
+                                       mt, nt, row, pair, gr, half)) {
                     stop = true;
                     break;
-                }
-                acc_phase ^= 1u;
-                tc_fence_after();
-                uint32_t acc[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 128 * half + 32 * c, acc[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(tmem_empty);
-
-                const float* sw = sc;
-                const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
-                const int64_t grow = static_cast<int64_t>(mt) * kBM + row;
-                float* dbg = args.debug ? args.debug + grow * H + nt * kBN + 128 * half : nullptr;
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t packed[32];
-#pragma unroll
-                    for (int jj = 0; jj < 64; jj += 2) {
-                        const int c = 64 * c2 + jj;
-                        const uint64_t v2 = f2_mul(f2_mul(f2(acc[c >> 5][c & 31], acc[c >> 5][(c & 31) + 1]), gr2),
-                                                   *reinterpret_cast<const uint64_t*>(sw + c));
-                        float v0, v1;
-                        f2_unpack(v2, v0, v1);
-                        if (dbg && live) {
-                            dbg[c] = v0;
-                            dbg[c + 1] = v1;
-                        }
-                        packed[jj >> 1] = bf16x2_rn(v0, v1);
-                    }
-                    uint16_t* ybase = args.y + nt * kBN + 128 * half + 64 * c2;
-                    store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
-                        const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
-                        return pr >= 0 ? ybase + static_cast<int64_t>(pr) * H : nullptr;
-                    });
                 }
             }
             if (stop) break;

@@ -61,7 +61,7 @@ __device__ __forceinline__ float quantize_row_lanes(const uint16_t* src, const R
 
 // ------------------------------------------------------------------ plain rows
 template <int GPL>
-__global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(256, GPL == 1 ? 3 : (GPL == 2 ? 2 : 1)) quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int cols, int64_t ld, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf, float* __restrict__ g,
                                                             int* err) {
@@ -368,7 +368,7 @@ __device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* 
 // [offsets[e] + count_e, offsets[e+1]): zero scales, g = 0, row_pair = -1.
 // The remaining blocks quantise tokens (X read once) and write the k copies.
 template <int GPL>
-__global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_kernel(
+__global__ void __launch_bounds__(256, GPL == 1 ? 3 : (GPL == 2 ? 2 : 1)) route_quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int E, int k, const int32_t* __restrict__ ids,
     const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int pad_blocks, int capacity,
     int* err) {
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) route_quant_scatter_ker
 
 // ------------------------------------------------------------------ requant
 template <int GPL>
-__global__ void __launch_bounds__(256, GPL == 1 ? 3 : 1) requant_kernel(const uint16_t* __restrict__ h,
+__global__ void __launch_bounds__(256, GPL == 1 ? 3 : (GPL == 2 ? 2 : 1)) requant_kernel(const uint16_t* __restrict__ h,
                                                       const uint32_t* __restrict__ amax2,
                                                       const int32_t* __restrict__ row_pair,
                                                       const int32_t* __restrict__ offsets, int E, int I,
