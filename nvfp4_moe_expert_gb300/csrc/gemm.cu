@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- FC2 with the requantisation fused
 // The FC2 input h is requantised inside the FC2 kernel, so the requantised operand never goes
-// through HBM ("miniTE diagnoses and narrows the cross-engine execution gap of NVFP4 RL",
+// through memory ("miniTE diagnoses and narrows the cross-engine execution gap of NVFP4 RL",
 // section "Assumptions and limits": online amax-quantisation-GEMM fusion).  FC2's A operand of
 // one m-tile (its 128 routed rows, all I columns) is quantised once into shared memory, in the
 // K-major 128B-swizzled layout a TMA load would give, with its block scales in the 512-byte
@@ -553,13 +553,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // Work unit: (m-tile, group of n-tiles); the number of groups per m-tile is chosen on the
 // device from the number of m-tiles so that the units spread over the SMs with a short tail.
-// A is double-buffered: the epilogue warps quantise the next unit's A one row chunk before each
-// of the current unit's tile epilogues, so the MMA warp finds it ready when the unit changes.
-// Fits I <= 768 (two 54 KB A buffers beside two 36 KB B stages and the output transpose).
+// Warp roles (12 warps, three per SM sub-partition so 168 registers each fit its register
+// file): warp 0 loads W2 tiles (TMA), warp 1 issues the MMAs, warps 2-9 run the epilogue,
+// warps 10-11 quantise A one unit ahead into the other of two A buffers (three rows in flight
+// per lane).  Fits I <= 768 (two 54 KB A buffers beside two 36 KB B stages and the output
+// transpose).
 namespace fused {
 constexpr int kMaxI = 768;
 constexpr int kStagesB = 2;
-constexpr int kThreadsF = 64 + kEpiThreads;                       // producer B, MMA, 8 epilogue warps
+constexpr int kQuantWarps = 2;
+constexpr int kQuantWarp0 = 2 + kEpiWarps;
+constexpr int kThreadsF = 32 * (kQuantWarp0 + kQuantWarps);       // 384
 constexpr int kABlockBytes = kBM * kBKBytes;                      // one K=256 block of 128 rows: 16 KB
 constexpr int kACodesBytes = (kMaxI / 256) * kABlockBytes;        // 48 KB
 constexpr int kASfBytes = (kMaxI / 64) * kSfAtomBytes;            // 6 KB
@@ -576,9 +580,10 @@ constexpr int kSmemBytesF = kBarOffF + kBarrierBytes + 1024;
 static_assert(kSmemBytesF <= 232448, "shared memory budget");
 constexpr uint32_t kSfColsPerStageF = 12 * kMmaPerStage;
 static_assert(kSfCol0 + kStagesB * kSfColsPerStageF <= kTmemCols, "TMEM budget");
+constexpr int kRowsInFlight = 3;                                  // rows per quantiser lane loaded ahead
 
 // Work units of one launch: n-tile groups per m-tile, the smallest estimated makespan
-// (rounds of units over the grid, each unit costing its n-tiles plus one for quantising A).
+// (rounds of units over the grid, each unit costing its n-tiles plus one).
 struct Units {
     int groups, per, count;
     __device__ Units(int num_m, int n_tiles, int grid) {
@@ -598,113 +603,52 @@ struct Units {
     }
 };
 
-// Quantise rows [r0, r1) of m-tile mt's h into A buffer `abuf` (codes, scales) and their
-// outer scales g2s: the epilogue warps share the rows, each row over G = I/64 lanes.
-__device__ __forceinline__ void quantize_a_rows(const GemmArgs& args, int mt, int r0, int r1, uint8_t* abuf,
-                                                float* g2s, int ew) {
-    const int I = args.I;
-    const int G = I / 64;
-    const RowLanes rl(G);
-    const int lane = threadIdx.x & 31;
-    uint8_t* sfb = abuf + kACodesBytes;
-    for (int base = r0 + ew * rl.RPW; base < r1; base += kEpiWarps * rl.RPW) {
-        const int r = base + rl.slot;
-        const bool row_ok = rl.active && r < r1;
-        const int64_t grow = static_cast<int64_t>(mt) * kBM + r;
-        const int32_t pair = row_ok ? __ldg(args.row_pair + grow) : -1;
-        const uint32_t amax_bits = row_ok ? __ldg(args.amax2 + grow) : 0u;
-        uint4 v[1][8];
-        if (pair >= 0) load_row_lanes<1>(args.h + grow * I, rl, G, v);
-        // every lane of the warp takes part in the row maximum's reduction
-        GroupQ q[1];
-        bool finite = true;
-        float gr = 0.0f;
-        if (rl.active) {
-            if (pair < 0) {   // pad row (or past the chunk): zero codes are not needed, zero scales are
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[0][i] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            gr = quantize_loaded<1>(v, rl, G, __uint_as_float(amax_bits), q, finite);
-        }
-        if (!row_ok) continue;
-        if (pair < 0) {
-            q[0].sfw = 0u;
-            gr = 0.0f;
-        } else if (!finite && rl.li == 0) {
-            set_device_error(args.err, NVFP4_ERR_NONFINITE);
-        }
-        const int grp = rl.li;
-        if (grp < G) {
-            // codes: K block grp/4, 32 bytes at (grp%4)*32 of the row, as two swizzled 16-byte chunks
-            uint8_t* rowp = abuf + (grp >> 2) * kABlockBytes + r * kBKBytes;
-            const int c0 = 2 * (grp & 3);
-            *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) =
-                make_uint4(q[0].code[0], q[0].code[1], q[0].code[2], q[0].code[3]);
-            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) =
-                make_uint4(q[0].code[4], q[0].code[5], q[0].code[6], q[0].code[7]);
-            *reinterpret_cast<uint32_t*>(sfb + grp * kSfAtomBytes + (r & 31) * 16 + (r >> 5) * 4) = q[0].sfw;
-        }
-        if (rl.li == 0) g2s[r] = gr;
-    }
-    (void)lane;
+// One row of h as a quantiser lane holds it: its 64-element group (G = I/64 lanes per row),
+// the row's pair (-1: pad row) and FC1's max|h| of the row.
+struct HRow {
+    uint4 v[1][8];
+    int32_t pair;
+    uint32_t amax_bits;
+};
+
+__device__ __forceinline__ void load_h_row(const GemmArgs& args, int mt, int r, const RowLanes& rl, int G, HRow& x) {
+    x.pair = -1;
+    x.amax_bits = 0u;
+    if (!rl.active || r >= kBM) return;
+    const int64_t grow = static_cast<int64_t>(mt) * kBM + r;
+    x.pair = __ldg(args.row_pair + grow);
+    x.amax_bits = __ldg(args.amax2 + grow);
+    if (x.pair >= 0) load_row_lanes<1>(args.h + grow * args.I, rl, G, x.v);
 }
 
-// One n-tile's epilogue for this warp's 32 rows and 128 columns: the column scales of W2 into
-// shared memory, the accumulator out of TMEM (handed back at once), y = bf16((acc*g2)*g^w2)
-// stored to the rows' (token, slot) places.  Out of line, so that the 128 accumulator
-// registers do not compete with the caller's loop state.  Returns false if the wait for the
-// accumulator ran out (the error is recorded).
-__device__ __noinline__ bool fc2_tile_epilogue(const GemmArgs& args, uint64_t* tmem_full, uint64_t* tmem_empty,
-                                               volatile int* abort_flag, uint32_t& acc_phase, uint32_t taddr,
-                                               float* sc, uint8_t* stage_buf, const float* gw, int mt, int nt, int row,
-                                               int pair, float gr, int half) {
-    const int lane = threadIdx.x & 31;
-    const int H = args.H;
-    __syncwarp();
+// Quantise a loaded row into A buffer `abuf` (codes in the swizzled K-major layout, scales in
+// the scale-tile layout) and its outer scale into g2s[r].
+__device__ __forceinline__ void store_a_row(const GemmArgs& args, HRow& x, int r, const RowLanes& rl, int G,
+                                            uint8_t* abuf, float* g2s) {
+    if (!rl.active) return;
+    if (x.pair < 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) sc[lane + 32 * i] = __ldg(gw + nt * kBN + 128 * half + lane + 32 * i);
-    __syncwarp();
-    if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
-        if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
-        *abort_flag = 1;
-        return false;
+        for (int i = 0; i < 8; ++i) x.v[0][i] = make_uint4(0u, 0u, 0u, 0u);
     }
-    acc_phase ^= 1u;
-    tc_fence_after();
-    uint32_t acc[4][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 128 * half + 32 * c, acc[c]);
-    tmem_ld_wait();
-    tc_fence_before();
-    mbar_arrive(tmem_empty);
-
-    const bool live = pair >= 0;
-    const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
-    const int64_t grow = static_cast<int64_t>(mt) * kBM + row;
-    float* dbg = args.debug ? args.debug + grow * H + nt * kBN + 128 * half : nullptr;
-#pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t packed[32];
-#pragma unroll
-        for (int jj = 0; jj < 64; jj += 2) {
-            const int c = 64 * c2 + jj;
-            const uint64_t v2 = f2_mul(f2_mul(f2(acc[c >> 5][c & 31], acc[c >> 5][(c & 31) + 1]), gr2),
-                                       *reinterpret_cast<const uint64_t*>(sc + c));
-            float v0, v1;
-            f2_unpack(v2, v0, v1);
-            if (dbg && live) {
-                dbg[c] = v0;
-                dbg[c + 1] = v1;
-            }
-            packed[jj >> 1] = bf16x2_rn(v0, v1);
-        }
-        uint16_t* ybase = args.y + nt * kBN + 128 * half + 64 * c2;
-        store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
-            const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
-            return pr >= 0 ? ybase + static_cast<int64_t>(pr) * H : nullptr;
-        });
+    GroupQ q[1];
+    bool finite = true;
+    float gr = quantize_loaded<1>(x.v, rl, G, __uint_as_float(x.amax_bits), q, finite);
+    if (r >= kBM) return;
+    if (x.pair < 0) {
+        q[0].sfw = 0u;
+        gr = 0.0f;
+    } else if (!finite && rl.li == 0) {
+        set_device_error(args.err, NVFP4_ERR_NONFINITE);
     }
-    return true;
+    const int grp = rl.li;
+    uint8_t* rowp = abuf + (grp >> 2) * kABlockBytes + r * kBKBytes;
+    const int c0 = 2 * (grp & 3);
+    *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) =
+        make_uint4(q[0].code[0], q[0].code[1], q[0].code[2], q[0].code[3]);
+    *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) =
+        make_uint4(q[0].code[4], q[0].code[5], q[0].code[6], q[0].code[7]);
+    *reinterpret_cast<uint32_t*>(abuf + kACodesBytes + grp * kSfAtomBytes + (r & 31) * 16 + (r >> 5) * 4) = q[0].sfw;
+    if (rl.li == 0) g2s[r] = gr;
 }
 
 __global__ void __launch_bounds__(kThreadsF, 1)
@@ -713,8 +657,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffF);
     uint64_t* empty = full + kStagesB;
-    uint64_t* a_full = empty + kStagesB;          // [2]
-    uint64_t* tmem_full = a_full + 2;
+    uint64_t* a_full = empty + kStagesB;          // [2]: quantisers -> MMA and epilogue
+    uint64_t* a_empty = a_full + 2;               // [2]: MMA (a unit's MMAs done) + epilogue (its g2 read) -> quantisers
+    uint64_t* tmem_full = a_empty + 2;
     uint64_t* tmem_empty = tmem_full + 1;
     uint64_t* drain = tmem_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -729,8 +674,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(&a_full[0], kEpiThreads);
-        mbar_init(&a_full[1], kEpiThreads);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&a_full[b], 32 * kQuantWarps);
+            mbar_init(&a_empty[b], 1 + kEpiThreads);
+        }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, kEpiThreads);
         mbar_init(drain, 1);
@@ -815,6 +762,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 failed = true;
                 break;
             }
+            tc_fence_after();
             const uint32_t a_base = smem_u32(smem + ab * kABufBytes);
             const uint32_t a_sf = a_base + kACodesBytes;
             for (int j = 0; j < U.per && !failed; ++j) {
@@ -866,6 +814,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 if (failed) break;
                 tc_commit_elect(tmem_full);
             }
+            if (failed) break;
+            tc_commit_elect(&a_empty[ab]);        // this unit's A is free once its MMAs are done
         }
         if (failed) {
             if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
@@ -875,56 +825,133 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 mbar_wait_bounded(drain, 0, nullptr, kWaitBudgetCycles);
             }
         }
+    } else if (warp >= kQuantWarp0) {
+        // ------------------------------------------------------------ A quantisers
+        const int qw = warp - kQuantWarp0;
+        const int G = args.I / 64;
+        const RowLanes rl(G);
+        const int step = kQuantWarps * rl.RPW;             // rows per pass of all quantiser warps
+        const int passes = (kBM + step - 1) / step;
+        int local = 0;
+        for (int u = blockIdx.x; u < U.count; u += gridDim.x, ++local) {
+            const int ab = local & 1;
+            if (local >= 2) {   // the unit that last used this buffer: its MMAs done, its g2 read
+                if (!mbar_wait_bounded(&a_empty[ab], ((local - 2) >> 1) & 1, abort_flag, kWaitBudgetCycles)) {
+                    if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            const int mt = u / U.groups;
+            uint8_t* abuf = smem + ab * kABufBytes;
+            float* g2b = g2_s + ab * 128;
+            // rows qw*RPW + slot + p*step for passes p; kRowsInFlight passes loaded ahead
+            HRow x[kRowsInFlight];
+#pragma unroll
+            for (int i = 0; i < kRowsInFlight; ++i) load_h_row(args, mt, qw * rl.RPW + rl.slot + i * step, rl, G, x[i]);
+            for (int p = 0; p < passes; p += kRowsInFlight) {
+#pragma unroll
+                for (int i = 0; i < kRowsInFlight; ++i) {
+                    if (p + i < passes) {
+                        store_a_row(args, x[i], qw * rl.RPW + rl.slot + (p + i) * step, rl, G, abuf, g2b);
+                        if (p + i + kRowsInFlight < passes)
+                            load_h_row(args, mt, qw * rl.RPW + rl.slot + (p + i + kRowsInFlight) * step, rl, G, x[i]);
+                    }
+                }
+            }
+            fence_proxy_async_shared();
+            mbar_arrive(&a_full[ab]);
+        }
     } else {
-        // ------------------------------------------------------------ epilogue + A quantisers
+        // ------------------------------------------------------------ epilogue
         const int ew = warp - 2;                             // 0..7
         const int q = warp & 3;                              // TMEM lane quarter of this warp
         const int half = ew >> 2;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
         float* sc = scale_buf + ew * 128;
         uint8_t* stage_buf = smem + kEpiOff + ew * kStageWarpBytes;
+        const int H = args.H;
+        const int row = q * 32 + lane;
         uint32_t acc_phase = 0;
-        // the first unit's A, whole
-        if (static_cast<int>(blockIdx.x) < U.count) {
-            quantize_a_rows(args, blockIdx.x / U.groups, 0, kBM, smem, g2_s, ew);
-            fence_proxy_async_shared();
-            mbar_arrive(&a_full[0]);
-        }
         int local = 0;
-        for (int u = blockIdx.x; u < U.count; u += gridDim.x, ++local) {
+        // the W2 column scales of this warp's 128 columns, loaded one tile ahead
+        auto tile_of = [&](int uu, int jj, int& mt_, int& nt_, int& e_) {
+            mt_ = uu / U.groups;
+            nt_ = (uu % U.groups) * U.per + jj;
+            e_ = expert_of_row(s_off, E, mt_ * kBM);
+        };
+        float n_sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        auto prefetch_sc = [&](int uu, int jj) {
+            int mt_, nt_, e_;
+            tile_of(uu, jj, mt_, nt_, e_);
+            const float* gw = args.b_g + static_cast<int64_t>(e_) * args.Nw + nt_ * kBN + 128 * half;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) n_sc[i] = __ldg(gw + lane + 32 * i);
+        };
+        if (static_cast<int>(blockIdx.x) < U.count) prefetch_sc(blockIdx.x, 0);
+        bool stop = false;
+        for (int u = blockIdx.x; u < U.count && !stop; u += gridDim.x, ++local) {
             const int ab = local & 1;
             const int mt = u / U.groups, nt0 = (u % U.groups) * U.per;
-            const int e = expert_of_row(s_off, E, mt * kBM);
-            const int un = u + gridDim.x;                    // the next unit, whose A is quantised now
-            // this unit's row data: written by all epilogue warps before they arrived on a_full
+            // this unit's outer scales g2: written by the quantisers before they arrived on a_full
             if (!mbar_wait_bounded(&a_full[ab], (local >> 1) & 1, abort_flag, kWaitBudgetCycles)) {
                 if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
                 break;
             }
-            const int row = q * 32 + lane;
             const int pair = __ldg(args.row_pair + static_cast<int64_t>(mt) * kBM + row);
-            const float gr = pair >= 0 ? g2_s[ab * 128 + row] : 0.0f;
-            const float* gw = args.b_g + static_cast<int64_t>(e) * args.Nw;
-            bool stop = false;
+            const bool live = pair >= 0;
+            const float gr = live ? g2_s[ab * 128 + row] : 0.0f;
+            mbar_arrive(&a_empty[ab]);                       // g2 read: the buffer may be refilled
+            const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
             for (int j = 0; j < U.per; ++j) {
                 const int nt = nt0 + j;
-                if (un < U.count) {
-                    const int r0 = j * kBM / U.per, r1 = (j + 1) * kBM / U.per;
-                    quantize_a_rows(args, un / U.groups, r0, r1, smem + (ab ^ 1) * kABufBytes, g2_s + (ab ^ 1) * 128,
-                                    ew);
-                    if (j == U.per - 1) {
-                        fence_proxy_async_shared();
-                        mbar_arrive(&a_full[ab ^ 1]);
-                    }
-                }
-                if (!fc2_tile_epilogue(args, tmem_full, tmem_empty, abort_flag, acc_phase, taddr, sc, stage_buf, gw,
-                                       mt, nt, row, pair, gr, half)) {
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[lane + 32 * i] = n_sc[i];
+                __syncwarp();
+                if (j + 1 < U.per) prefetch_sc(u, j + 1);
+                else if (u + static_cast<int>(gridDim.x) < U.count) prefetch_sc(u + gridDim.x, 0);
+                if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
+                    if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
                     stop = true;
                     break;
                 }
+                acc_phase ^= 1u;
+                tc_fence_after();
+                uint32_t acc[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 128 * half + 32 * c, acc[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(tmem_empty);
+
+                const int64_t grow = static_cast<int64_t>(mt) * kBM + row;
+                float* dbg = args.debug ? args.debug + grow * H + nt * kBN + 128 * half : nullptr;
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t packed[32];
+#pragma unroll
+                    for (int jj = 0; jj < 64; jj += 2) {
+                        const int c = 64 * c2 + jj;
+                        const uint64_t v2 = f2_mul(f2_mul(f2(acc[c >> 5][c & 31], acc[c >> 5][(c & 31) + 1]), gr2),
+                                                   *reinterpret_cast<const uint64_t*>(sc + c));
+                        float v0, v1;
+                        f2_unpack(v2, v0, v1);
+                        if (dbg && live) {
+                            dbg[c] = v0;
+                            dbg[c + 1] = v1;
+                        }
+                        packed[jj >> 1] = bf16x2_rn(v0, v1);
+                    }
+                    uint16_t* ybase = args.y + nt * kBN + 128 * half + 64 * c2;
+                    store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
+                        const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
+                        return pr >= 0 ? ybase + static_cast<int64_t>(pr) * H : nullptr;
+                    });
+                }
             }
-            if (stop) break;
         }
     }
 
