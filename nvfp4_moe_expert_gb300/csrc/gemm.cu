@@ -553,17 +553,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // Work unit: (m-tile, group of n-tiles); the number of groups per m-tile is chosen on the
 // device from the number of m-tiles so that the units spread over the SMs with a short tail.
-// Warp roles (12 warps, three per SM sub-partition so 168 registers each fit its register
-// file): warp 0 loads W2 tiles (TMA), warp 1 issues the MMAs, warps 2-9 run the epilogue,
-// warps 10-11 quantise A one unit ahead into the other of two A buffers (three rows in flight
-// per lane).  Fits I <= 768 (two 54 KB A buffers beside two 36 KB B stages and the output
+// Warp roles (16 warps, four per SM sub-partition at 128 registers each, which fills its
+// 16K-register file): warp 0 loads W2 tiles (TMA), warp 1 issues the MMAs, warps 2-9 run the
+// epilogue (reading the accumulator in two halves of 64 columns, so that it fits), warps 10-15
+// quantise A one unit ahead into the other of two A buffers, two rows in flight per lane: the
+// quantisation costs about twice the epilogue's instructions per m-tile, so it needs the
+// warps.  Fits I <= 768 (two 54 KB A buffers beside two 36 KB B stages and the output
 // transpose).
 namespace fused {
 constexpr int kMaxI = 768;
 constexpr int kStagesB = 2;
-constexpr int kQuantWarps = 2;
+constexpr int kQuantWarps = 6;
 constexpr int kQuantWarp0 = 2 + kEpiWarps;
-constexpr int kThreadsF = 32 * (kQuantWarp0 + kQuantWarps);       // 384
+constexpr int kThreadsF = 32 * (kQuantWarp0 + kQuantWarps);       // 512
 constexpr int kABlockBytes = kBM * kBKBytes;                      // one K=256 block of 128 rows: 16 KB
 constexpr int kACodesBytes = (kMaxI / 256) * kABlockBytes;        // 48 KB
 constexpr int kASfBytes = (kMaxI / 64) * kSfAtomBytes;            // 6 KB
@@ -580,7 +582,7 @@ constexpr int kSmemBytesF = kBarOffF + kBarrierBytes + 1024;
 static_assert(kSmemBytesF <= 232448, "shared memory budget");
 constexpr uint32_t kSfColsPerStageF = 12 * kMmaPerStage;
 static_assert(kSfCol0 + kStagesB * kSfColsPerStageF <= kTmemCols, "TMEM budget");
-constexpr int kRowsInFlight = 3;                                  // rows per quantiser lane loaded ahead
+constexpr int kRowsInFlight = 2;                                  // rows per quantiser lane loaded ahead
 
 // Work units of one launch: n-tile groups per m-tile, the smallest estimated makespan
 // (rounds of units over the grid, each unit costing its n-tiles plus one).
@@ -920,22 +922,25 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 }
                 acc_phase ^= 1u;
                 tc_fence_after();
-                uint32_t acc[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 128 * half + 32 * c, acc[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(tmem_empty);
-
                 const int64_t grow = static_cast<int64_t>(mt) * kBM + row;
                 float* dbg = args.debug ? args.debug + grow * H + nt * kBN + 128 * half : nullptr;
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
+                    // 64 of the warp's 128 accumulator columns at a time; TMEM goes back after the
+                    // second half is in registers
+                    uint32_t acc[2][32];
+                    tmem_ld_32x32b_x32(taddr + 128 * half + 64 * c2, acc[0]);
+                    tmem_ld_32x32b_x32(taddr + 128 * half + 64 * c2 + 32, acc[1]);
+                    tmem_ld_wait();
+                    if (c2 == 1) {
+                        tc_fence_before();
+                        mbar_arrive(tmem_empty);
+                    }
                     uint32_t packed[32];
 #pragma unroll
                     for (int jj = 0; jj < 64; jj += 2) {
                         const int c = 64 * c2 + jj;
-                        const uint64_t v2 = f2_mul(f2_mul(f2(acc[c >> 5][c & 31], acc[c >> 5][(c & 31) + 1]), gr2),
+                        const uint64_t v2 = f2_mul(f2_mul(f2(acc[jj >> 5][jj & 31], acc[jj >> 5][(jj & 31) + 1]), gr2),
                                                    *reinterpret_cast<const uint64_t*>(sc + c));
                         float v0, v1;
                         f2_unpack(v2, v0, v1);
