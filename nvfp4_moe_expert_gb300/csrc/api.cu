@@ -422,7 +422,7 @@ static nvfp4_status moe_fc2_requant_nvfp4_impl(const moe_nvfp4_weights* w, int64
     moe_workspace_layout L;
     const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
     if (s != NVFP4_OK) return s;
-    if (w->I > fc2_requant_max_i()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (w->I > fc2_requant_max_i() || w->E > fc2_requant_max_e()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!expert_offsets_dev) return NVFP4_ERR_INVALID_ARG;
     if (T == 0) return NVFP4_OK;
     int* err = device_error_ptr();
@@ -451,7 +451,7 @@ static nvfp4_status forward_stages(const moe_nvfp4_weights* w, int64_t T, int k,
                                    void* ws_dev, size_t ws_bytes, void* stream, int capacity) {
     nvfp4_status s = moe_fc1_swiglu_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, false, capacity);
     if (s != NVFP4_OK) return s;
-    if (w->I <= fc2_requant_max_i()) {
+    if (w->I <= fc2_requant_max_i() && w->E <= fc2_requant_max_e()) {
         s = moe_fc2_requant_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, true, capacity);
     } else {
         s = moe_requant_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, stream, true, capacity);

@@ -116,9 +116,10 @@ struct GemmArgs {
 cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st, bool pdl);
 // FC2 with the requantisation of h fused in (reads h, amax2 and row_pair; a_codes/a_sf/a_g
-// unused); supports I <= fc2_requant_max_i().
+// unused); supports I <= fc2_requant_max_i() and E <= fc2_requant_max_e().
 cudaError_t launch_fc2_requant(const GemmArgs& a, cudaStream_t st, bool pdl);
 int fc2_requant_max_i();
+int fc2_requant_max_e();
 // Copy the FC1 epilogue's 65536-entry SiLU table (FP32, by BF16 bit pattern) to `out`.
 cudaError_t copy_silu_table(float* out, cudaStream_t st);
 

@@ -555,16 +555,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // device from the number of m-tiles so that the units spread over the SMs with a short tail.
 // Warp roles (16 warps, four per SM sub-partition at 128 registers each, which fills its
 // 16K-register file): warp 0 loads W2 tiles (TMA), warp 1 issues the MMAs, warps 2-9 run the
-// epilogue (reading the accumulator in two halves of 64 columns, so that it fits), warps 10-15
-// quantise A one unit ahead into the other of two A buffers, two rows in flight per lane: the
-// quantisation costs about twice the epilogue's instructions per m-tile, so it needs the
-// warps.  Fits I <= 768 (two 54 KB A buffers beside two 36 KB B stages and the output
-// transpose).
+// epilogue (reading the accumulator in two halves of 64 columns, so that it fits, and storing
+// each lane's row with 32-byte stores), warp 10 copies h into shared memory in chunks of
+// consecutive rows (cp.async.bulk, two slots) together with each unit's row map and maxima,
+// and warps 11-15 quantise from there into the other of two A buffers, one unit ahead of the
+// MMAs.  Fits I <= 768 and E <= 512 (two 54 KB A buffers, two 36 KB W2 stages, two 18 KB h
+// slots).
 namespace fused {
 constexpr int kMaxI = 768;
+constexpr int kMaxE = 512;
 constexpr int kStagesB = 2;
-constexpr int kQuantWarps = 6;
-constexpr int kQuantWarp0 = 2 + kEpiWarps;
+constexpr int kHWarp = 2 + kEpiWarps;                              // 10
+constexpr int kQuantWarp0 = kHWarp + 1;                           // 11
+constexpr int kQuantWarps = 5;
 constexpr int kThreadsF = 32 * (kQuantWarp0 + kQuantWarps);       // 512
 constexpr int kABlockBytes = kBM * kBKBytes;                      // one K=256 block of 128 rows: 16 KB
 constexpr int kACodesBytes = (kMaxI / 256) * kABlockBytes;        // 48 KB
@@ -572,17 +575,18 @@ constexpr int kASfBytes = (kMaxI / 64) * kSfAtomBytes;            // 6 KB
 constexpr int kABufBytes = kACodesBytes + kASfBytes;
 static_assert(kABufBytes % 1024 == 0, "A buffers keep 1024-byte alignment");
 constexpr int kBStageBytes = kBBytes + 2 * kMmaPerStage * kSfAtomBytes;
+constexpr int kHSlotBytes = 12 * 2 * kMaxI;                       // 12 rows of h at I = 768
 constexpr int kBOff = 2 * kABufBytes;
-constexpr int kEpiOff = kBOff + kStagesB * kBStageBytes;
-constexpr int kScaleOffF = kEpiOff + kEpiWarps * kStageWarpBytes;
-constexpr int kRowOff = kScaleOffF + kEpiWarps * 128 * 4;         // per A buffer: g2[128]
-constexpr int kOffsetsOffF = kRowOff + 2 * 128 * 4;
-constexpr int kBarOffF = kOffsetsOffF + 4352;
+constexpr int kHOff = kBOff + kStagesB * kBStageBytes;
+constexpr int kRowDataOff = kHOff + 2 * kHSlotBytes;              // per A buffer: pair[128], amax2[128]
+constexpr int kScaleOffF = kRowDataOff + 2 * 2 * 128 * 4;
+constexpr int kG2Off = kScaleOffF + kEpiWarps * 128 * 4;          // per A buffer: g2[128]
+constexpr int kOffsetsOffF = kG2Off + 2 * 128 * 4;
+constexpr int kBarOffF = kOffsetsOffF + (kMaxE + 64) * 4;
 constexpr int kSmemBytesF = kBarOffF + kBarrierBytes + 1024;
 static_assert(kSmemBytesF <= 232448, "shared memory budget");
 constexpr uint32_t kSfColsPerStageF = 12 * kMmaPerStage;
 static_assert(kSfCol0 + kStagesB * kSfColsPerStageF <= kTmemCols, "TMEM budget");
-constexpr int kRowsInFlight = 2;                                  // rows per quantiser lane loaded ahead
 
 // Work units of one launch: n-tile groups per m-tile, the smallest estimated makespan
 // (rounds of units over the grid, each unit costing its n-tiles plus one).
@@ -605,52 +609,11 @@ struct Units {
     }
 };
 
-// One row of h as a quantiser lane holds it: its 64-element group (G = I/64 lanes per row),
-// the row's pair (-1: pad row) and FC1's max|h| of the row.
-struct HRow {
-    uint4 v[1][8];
-    int32_t pair;
-    uint32_t amax_bits;
-};
-
-__device__ __forceinline__ void load_h_row(const GemmArgs& args, int mt, int r, const RowLanes& rl, int G, HRow& x) {
-    x.pair = -1;
-    x.amax_bits = 0u;
-    if (!rl.active || r >= kBM) return;
-    const int64_t grow = static_cast<int64_t>(mt) * kBM + r;
-    x.pair = __ldg(args.row_pair + grow);
-    x.amax_bits = __ldg(args.amax2 + grow);
-    if (x.pair >= 0) load_row_lanes<1>(args.h + grow * args.I, rl, G, x.v);
-}
-
-// Quantise a loaded row into A buffer `abuf` (codes in the swizzled K-major layout, scales in
-// the scale-tile layout) and its outer scale into g2s[r].
-__device__ __forceinline__ void store_a_row(const GemmArgs& args, HRow& x, int r, const RowLanes& rl, int G,
-                                            uint8_t* abuf, float* g2s) {
-    if (!rl.active) return;
-    if (x.pair < 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x.v[0][i] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    GroupQ q[1];
-    bool finite = true;
-    float gr = quantize_loaded<1>(x.v, rl, G, __uint_as_float(x.amax_bits), q, finite);
-    if (r >= kBM) return;
-    if (x.pair < 0) {
-        q[0].sfw = 0u;
-        gr = 0.0f;
-    } else if (!finite && rl.li == 0) {
-        set_device_error(args.err, NVFP4_ERR_NONFINITE);
-    }
-    const int grp = rl.li;
-    uint8_t* rowp = abuf + (grp >> 2) * kABlockBytes + r * kBKBytes;
-    const int c0 = 2 * (grp & 3);
-    *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) =
-        make_uint4(q[0].code[0], q[0].code[1], q[0].code[2], q[0].code[3]);
-    *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) =
-        make_uint4(q[0].code[4], q[0].code[5], q[0].code[6], q[0].code[7]);
-    *reinterpret_cast<uint32_t*>(abuf + kACodesBytes + grp * kSfAtomBytes + (r & 31) * 16 + (r >> 5) * 4) = q[0].sfw;
-    if (rl.li == 0) g2s[r] = gr;
+// Rows of h per staging slot: every quantiser warp's rows of one pass, capped by the slot.
+__device__ __forceinline__ int rows_per_chunk(int I) {
+    const int G = I / 64;
+    const int rpw = G <= 32 ? 32 / G : 1;
+    return min(kQuantWarps * rpw, kHSlotBytes / (2 * I));
 }
 
 __global__ void __launch_bounds__(kThreadsF, 1)
@@ -661,14 +624,16 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     uint64_t* empty = full + kStagesB;
     uint64_t* a_full = empty + kStagesB;          // [2]: quantisers -> MMA and epilogue
     uint64_t* a_empty = a_full + 2;               // [2]: MMA (a unit's MMAs done) + epilogue (its g2 read) -> quantisers
-    uint64_t* tmem_full = a_empty + 2;
+    uint64_t* h_full = a_empty + 2;               // [2]: h chunk (and, with a unit's first chunk, its row data) landed
+    uint64_t* h_empty = h_full + 2;               // [2]: quantisers done with the slot
+    uint64_t* tmem_full = h_empty + 2;
     uint64_t* tmem_empty = tmem_full + 1;
     uint64_t* drain = tmem_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* scale_buf = reinterpret_cast<float*>(smem + kScaleOffF);
     int32_t* s_off = reinterpret_cast<int32_t*>(smem + kOffsetsOffF);
-    float* g2_s = reinterpret_cast<float*>(smem + kRowOff);                 // [2][128]
+    float* g2_s = reinterpret_cast<float*>(smem + kG2Off);                  // [2][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -679,6 +644,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&a_full[b], 32 * kQuantWarps);
             mbar_init(&a_empty[b], 1 + kEpiThreads);
+            mbar_init(&h_full[b], 1);
+            mbar_init(&h_empty[b], 32 * kQuantWarps);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, kEpiThreads);
@@ -705,6 +672,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     const Units U(num_m, n_tiles, gridDim.x);
     const int num_k64 = args.I / 64;
     const int num_ks = (num_k64 + kMmaPerStage - 1) / kMmaPerStage;
+    const int rpc = rows_per_chunk(args.I);
+    const int nchunks = (kBM + rpc - 1) / rpc;
     bool failed = false;
 
     if (warp == 0) {
@@ -827,15 +796,55 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 mbar_wait_bounded(drain, 0, nullptr, kWaitBudgetCycles);
             }
         }
+    } else if (warp == kHWarp) {
+        // ------------------------------------------------------------ producer of h chunks
+        // Rows [c*rpc, c*rpc + rpc) of each unit's m-tile are consecutive in h: one bulk copy
+        // per chunk.  A unit's first chunk also brings its 128 row-map entries and maxima.
+        const uint64_t pol = policy_evict_first();   // last use of h
+        int gc = 0;                                  // chunks issued so far (slot gc & 1)
+        uint32_t issued = 0, issued_parity = 0;
+        int local = 0;
+        for (int u = blockIdx.x; u < U.count && !failed; u += gridDim.x, ++local) {
+            const int mt = u / U.groups;
+            const int ab = local & 1;
+            const int64_t row0 = static_cast<int64_t>(mt) * kBM;
+            for (int c = 0; c < nchunks; ++c, ++gc) {
+                const int slot = gc & 1;
+                const bool ok = mbar_wait_bounded(&h_empty[slot], ((gc >> 1) & 1) ^ 1u, abort_flag, kWaitBudgetCycles);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    failed = true;
+                    break;
+                }
+                const int r0 = c * rpc, nr = min(rpc, kBM - r0);
+                const uint32_t hbytes = static_cast<uint32_t>(nr) * 2 * args.I;
+                uint8_t* rd = smem + kRowDataOff + ab * 1024;
+                mbar_arrive_expect_tx_elect(&h_full[slot], hbytes + (c == 0 ? 1024u : 0u));
+                bulk_load_elect(smem + kHOff + slot * kHSlotBytes, args.h + (row0 + r0) * args.I, hbytes, &h_full[slot],
+                                pol);
+                if (c == 0) {
+                    bulk_load_elect(rd, args.row_pair + row0, 512, &h_full[slot], pol);
+                    bulk_load_elect(rd + 512, args.amax2 + row0, 512, &h_full[slot], pol);
+                }
+                issued |= 1u << slot;
+                issued_parity = (issued_parity & ~(1u << slot)) | (static_cast<uint32_t>((gc >> 1) & 1) << slot);
+            }
+        }
+        if (failed) {
+            if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            for (int s = 0; s < 2; ++s) {
+                if (issued & (1u << s)) mbar_wait_bounded(&h_full[s], (issued_parity >> s) & 1u, nullptr, kWaitBudgetCycles);
+            }
+        }
     } else if (warp >= kQuantWarp0) {
         // ------------------------------------------------------------ A quantisers
         const int qw = warp - kQuantWarp0;
         const int G = args.I / 64;
         const RowLanes rl(G);
-        const int step = kQuantWarps * rl.RPW;             // rows per pass of all quantiser warps
-        const int passes = (kBM + step - 1) / step;
+        int gc = 0;
         int local = 0;
-        for (int u = blockIdx.x; u < U.count; u += gridDim.x, ++local) {
+        bool stop = false;
+        for (int u = blockIdx.x; u < U.count && !stop; u += gridDim.x, ++local) {
             const int ab = local & 1;
             if (local >= 2) {   // the unit that last used this buffer: its MMAs done, its g2 read
                 if (!mbar_wait_bounded(&a_empty[ab], ((local - 2) >> 1) & 1, abort_flag, kWaitBudgetCycles)) {
@@ -844,23 +853,60 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     break;
                 }
             }
-            const int mt = u / U.groups;
             uint8_t* abuf = smem + ab * kABufBytes;
             float* g2b = g2_s + ab * 128;
-            // rows qw*RPW + slot + p*step for passes p; kRowsInFlight passes loaded ahead
-            HRow x[kRowsInFlight];
+            const int32_t* rpair = reinterpret_cast<const int32_t*>(smem + kRowDataOff + ab * 1024);
+            const uint32_t* ramax = reinterpret_cast<const uint32_t*>(smem + kRowDataOff + ab * 1024 + 512);
+            for (int c = 0; c < nchunks; ++c, ++gc) {
+                const int slot = gc & 1;
+                if (!mbar_wait_bounded(&h_full[slot], (gc >> 1) & 1, abort_flag, kWaitBudgetCycles)) {
+                    if (lane == 0) set_device_error(args.err, NVFP4_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                    stop = true;
+                    break;
+                }
+                const int r0 = c * rpc, nr = min(rpc, kBM - r0);
+                const int rr = qw * rl.RPW + rl.slot;            // this lane's row within the chunk
+                const bool row_ok = rl.active && rr < nr;
+                const int r = r0 + rr;
+                const int32_t pair = row_ok ? rpair[r] : -1;
+                const uint32_t amax_bits = row_ok ? ramax[r] : 0u;
+                uint4 v[1][8];
+                if (pair >= 0) {
+                    const uint4* src = reinterpret_cast<const uint4*>(smem + kHOff + slot * kHSlotBytes +
+                                                                      static_cast<int64_t>(rr) * 2 * args.I + rl.li * 128);
 #pragma unroll
-            for (int i = 0; i < kRowsInFlight; ++i) load_h_row(args, mt, qw * rl.RPW + rl.slot + i * step, rl, G, x[i]);
-            for (int p = 0; p < passes; p += kRowsInFlight) {
+                    for (int i = 0; i < 8; ++i) v[0][i] = src[i];
+                } else {
 #pragma unroll
-                for (int i = 0; i < kRowsInFlight; ++i) {
-                    if (p + i < passes) {
-                        store_a_row(args, x[i], qw * rl.RPW + rl.slot + (p + i) * step, rl, G, abuf, g2b);
-                        if (p + i + kRowsInFlight < passes)
-                            load_h_row(args, mt, qw * rl.RPW + rl.slot + (p + i + kRowsInFlight) * step, rl, G, x[i]);
+                    for (int i = 0; i < 8; ++i) v[0][i] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                mbar_arrive(&h_empty[slot]);                 // the slot's data is in registers
+                if (rl.active) {
+                    GroupQ q[1];
+                    bool finite = true;
+                    float gr = quantize_loaded<1>(v, rl, G, __uint_as_float(amax_bits), q, finite);
+                    if (row_ok) {
+                        if (pair < 0) {
+                            q[0].sfw = 0u;
+                            gr = 0.0f;
+                        } else if (!finite && rl.li == 0) {
+                            set_device_error(args.err, NVFP4_ERR_NONFINITE);
+                        }
+                        const int grp = rl.li;
+                        uint8_t* rowp = abuf + (grp >> 2) * kABlockBytes + r * kBKBytes;
+                        const int c0 = 2 * (grp & 3);
+                        *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) =
+                            make_uint4(q[0].code[0], q[0].code[1], q[0].code[2], q[0].code[3]);
+                        *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) =
+                            make_uint4(q[0].code[4], q[0].code[5], q[0].code[6], q[0].code[7]);
+                        *reinterpret_cast<uint32_t*>(abuf + kACodesBytes + grp * kSfAtomBytes + (r & 31) * 16 +
+                                                     (r >> 5) * 4) = q[0].sfw;
+                        if (rl.li == 0) g2b[r] = gr;
                     }
                 }
             }
+            if (stop) break;
             fence_proxy_async_shared();
             mbar_arrive(&a_full[ab]);
         }
@@ -871,21 +917,16 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const int half = ew >> 2;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
         float* sc = scale_buf + ew * 128;
-        uint8_t* stage_buf = smem + kEpiOff + ew * kStageWarpBytes;
         const int H = args.H;
         const int row = q * 32 + lane;
         uint32_t acc_phase = 0;
         int local = 0;
         // the W2 column scales of this warp's 128 columns, loaded one tile ahead
-        auto tile_of = [&](int uu, int jj, int& mt_, int& nt_, int& e_) {
-            mt_ = uu / U.groups;
-            nt_ = (uu % U.groups) * U.per + jj;
-            e_ = expert_of_row(s_off, E, mt_ * kBM);
-        };
         float n_sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         auto prefetch_sc = [&](int uu, int jj) {
-            int mt_, nt_, e_;
-            tile_of(uu, jj, mt_, nt_, e_);
+            const int mt_ = uu / U.groups;
+            const int nt_ = (uu % U.groups) * U.per + jj;
+            const int e_ = expert_of_row(s_off, E, mt_ * kBM);
             const float* gw = args.b_g + static_cast<int64_t>(e_) * args.Nw + nt_ * kBN + 128 * half;
 #pragma unroll
             for (int i = 0; i < 4; ++i) n_sc[i] = __ldg(gw + lane + 32 * i);
@@ -924,6 +965,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 tc_fence_after();
                 const int64_t grow = static_cast<int64_t>(mt) * kBM + row;
                 float* dbg = args.debug ? args.debug + grow * H + nt * kBN + 128 * half : nullptr;
+                uint16_t* yrow = live ? args.y + static_cast<int64_t>(pair) * H + nt * kBN + 128 * half : nullptr;
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
                     // 64 of the warp's 128 accumulator columns at a time; TMEM goes back after the
@@ -950,11 +992,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                         }
                         packed[jj >> 1] = bf16x2_rn(v0, v1);
                     }
-                    uint16_t* ybase = args.y + nt * kBN + 128 * half + 64 * c2;
-                    store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
-                        const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
-                        return pr >= 0 ? ybase + static_cast<int64_t>(pr) * H : nullptr;
-                    });
+                    if (live) store_row_64(yrow + 64 * c2, packed);
                 }
             }
         }
@@ -1061,7 +1099,7 @@ cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st, bool pdl) 
 }
 
 cudaError_t launch_fc2_requant_impl(const GemmArgs& a, cudaStream_t st, bool pdl) {
-    if (a.I > fused::kMaxI || a.I % 128 != 0) return cudaErrorInvalidValue;
+    if (a.I > fused::kMaxI || a.I % 128 != 0 || a.E > fused::kMaxE) return cudaErrorInvalidValue;
     cudaError_t e = prepare_device(2);
     if (e != cudaSuccess) return e;
     CUtensorMap mb;
@@ -1076,6 +1114,7 @@ cudaError_t launch_fc2_requant(const GemmArgs& a, cudaStream_t st, bool pdl) {
     return launch_fc2_requant_impl(a, st, pdl);
 }
 int fc2_requant_max_i() { return fused::kMaxI; }
+int fc2_requant_max_e() { return fused::kMaxE; }
 
 cudaError_t launch_fc1(const GemmArgs& a, cudaStream_t st, bool pdl) { return launch_gemm(true, a, st, pdl); }
 cudaError_t launch_fc2(const GemmArgs& a, cudaStream_t st, bool pdl) { return launch_gemm(false, a, st, pdl); }
