@@ -881,7 +881,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) v[0][i] = make_uint4(0u, 0u, 0u, 0u);
                 }
-                mbar_arrive(&h_empty[slot]);                 // the slot's data is in registers
+                // the slot's data is in registers; the next bulk copy into the slot (async proxy)
+                // must not overtake these generic-proxy reads
+                fence_proxy_async_shared();
+                mbar_arrive(&h_empty[slot]);
                 if (rl.active) {
                     GroupQ q[1];
                     bool finite = true;
