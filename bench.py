@@ -40,21 +40,19 @@ FLUSH_BYTES = 512 << 20         # > L2 (129 MB)
 FUSED_FC2_MAX_I = 768   # moe_fc2_requant_max_intermediate(): FC2 with the requantisation fused in
 
 
-def fused_fc2(cfg):
-    return cfg.I <= FUSED_FC2_MAX_I
+def fused_fc2_supported(cfg):
+    return cfg.I <= FUSED_FC2_MAX_I and cfg.E <= 512
 
 
 def kernels_per_step(cfg):
     """Launches of one step: the route sort is one block-sort kernel for up to 8192 (token,
     slot) pairs and E <= 256, else a histogram and a scan kernel; then quantise-scatter, FC1,
-    FC2 with the requantisation fused in (or requant and FC2 where I > 768), combine."""
-    return (1 if cfg.T * cfg.k <= 8192 and cfg.E <= 256 else 2) + (4 if fused_fc2(cfg) else 5)
+    requant, FC2, combine."""
+    return (1 if cfg.T * cfg.k <= 8192 and cfg.E <= 256 else 2) + 5
 
 
 def step_stages(cfg):
     """The stages one step runs, in order."""
-    if fused_fc2(cfg):
-        return ["route_sort_quant", "fc1_swiglu", "fc2_requant", "combine"]
     return ["route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"]
 
 
@@ -489,6 +487,31 @@ def stage_times(M, torch, cfg, weights, x, ids, pw, offs, ws, out, flush, stream
             for j, name in enumerate(names)}
 
 
+def fused_fc2_timing(M, torch, cfg, weights, x, ids, pw, offs, ws, flush, stream, n, stage_ms, peaks, peak_kind):
+    """moe_fc2_requant_nvfp4 (the FC2 input's requantisation fused into FC2, same bits as the
+    requant and FC2 stages) timed on its own after a route sort and FC1, L2 flushed between
+    calls, against the two stages' times."""
+    if not fused_fc2_supported(cfg):
+        return None
+    T, E, k = cfg.T, cfg.E, cfg.k
+    M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+    M.moe_fc1_swiglu_nvfp4(weights, T, k, offs, ws)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        M.moe_fc2_requant_nvfp4(weights, T, k, offs, ws)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if M.nvfp4_get_device_error() != 0:
+        raise RuntimeError("device error in the fused FC2")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    r = roofline_of("fc2_requant", stage_work(cfg)["fc2_requant"], ms, peaks, peak_kind)
+    return {"ms": round(ms, 4), "bound": r["bound"], "frac": r["frac"],
+            "requant_plus_fc2_ms": round(stage_ms["requant"] + stage_ms["fc2"], 4),
+            "note": "moe_fc2_requant_nvfp4, not used by the step: slower than the two stages here"}
+
+
 def time_steps(M, torch, weights, cfg, x, ids, pw, offs, ws, out, flush, stream, K, W):
     """CUDA-event time (ms) of each of K steps (route sort + expert forward), after W warm-up
     steps, L2 flushed between steps outside the events."""
@@ -542,9 +565,14 @@ def extra_workload(M, torch, name, dev, stream, flush, K, W, peaks, peak_kind, t
     step_ms = statistics.mean(ms)
     M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
     M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+    fused = fused_fc2_timing(M, torch, cfg, weights, x, ids, pw, offs, ws, flush, stream, min(K, 20), st, peaks,
+                             peak_kind)
+    M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
+    M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
     inv = batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev, sizes=(1, 64), n_decode=8, n_windows=2)
     res = {"tokens_per_s": round(T / (step_ms * 1e-3), 1), "ms_per_step": round(step_ms, 4), "steps": K,
            "stages": stages, "layer_roofline_frac": layer_roofline(cfg, peaks, peak_kind, step_ms)["frac"],
+           "fused_fc2_requant": fused,
            "bitwise_invariant": inv["bitwise_equal"],
            "config": f"H {H}, I {I}, E {E}, top-{k}, {T} tokens, {cfg.routing} routing"
                      + (f", {cfg.outlier_frac:.0%} x20 outlier channels" if cfg.outlier_frac else "")
@@ -638,6 +666,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     for n in names:
         if n in traffic:
             kernels[n]["traffic"] = traffic[n]
+    fused = fused_fc2_timing(M, torch, cfg, weights, x, ids, pw, offs, ws, flush, stream, min(K, 50), stage_ms,
+                             peaks, peak_kind)
     dominant = max(names, key=lambda n: stage_ms[n])
     roof = dict(kernels[dominant])
     roof["peak_note"] = "of " + peak_kind
@@ -796,6 +826,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "gpu_launches": kernels_per_step(cfg) * K,
         "clocks": clocks,
         "kernels": kernels,
+        "fused_fc2_requant": fused,
         "weight_quant_ms": round(wq_ms, 3),
         "router_step": router,
         "masked_step": masked,

@@ -235,8 +235,7 @@ nvfp4_status moe_route_sort_amax_noalloc(const void* x_dev, int64_t T, int H, in
  * grouped GEMM with the same epilogue, BF16 y per (token, slot); and the
  * combine out[t] = bf16(sum over slots 0..k-1 in order, FP32)
  * [miniTE/differs, miniTE/use, RL/4.4, RL/4.5].  Equivalent to
- * moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16 (bitwise); it
- * runs the requantisation fused into FC2 (moe_fc2_requant_nvfp4) when I <= 768.
+ * moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16 (bitwise).
  *
  *  w                   quantised weights (host struct, device pointers)
  *  T, k                as given to moe_route_sort_amax
@@ -280,9 +279,10 @@ nvfp4_status moe_combine_bf16(const moe_nvfp4_weights* w, int64_t T, int k, void
  * (a2_codes, a2_sf, a2_g) are not written.  Reads h, amax2 and the row map that
  * moe_fc1_swiglu_nvfp4 and the route sort left in the workspace.
  * Supported for I <= moe_fc2_requant_max_intermediate() (768: two A buffers of 128 rows must
- * fit in shared memory beside the W2 stages); larger I returns NVFP4_ERR_UNSUPPORTED_SHAPE.
- * moe_expert_forward_nvfp4 and moe_expert_forward_nvfp4_masked use it whenever I allows,
- * and the two separate stages otherwise. */
+ * fit in shared memory beside the W2 stages and the staging of h) and E <= 512; other shapes
+ * return NVFP4_ERR_UNSUPPORTED_SHAPE.  moe_expert_forward_nvfp4 runs the two separate stages,
+ * which are faster on GB300 at the sizes measured (the quantisation inside FC2 is issue-bound
+ * on the warps left beside FC2's own); this call gives the same bits with one launch less. */
 nvfp4_status moe_fc2_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
                                    const int32_t* expert_offsets_dev, void* ws_dev,
                                    size_t ws_bytes, float* fc2_debug_dev, void* stream);

@@ -444,20 +444,18 @@ static nvfp4_status moe_combine_bf16_impl(const moe_nvfp4_weights* w, int64_t T,
                                     static_cast<cudaStream_t>(stream), pdl));
 }
 
-// FC1, then the FC2 input's requantisation and FC2 (fused into one kernel where it fits, as
-// two launches otherwise), then the combine; every kernel after FC1 starts early
-// (programmatic dependent launch) and waits on its predecessor in the device.
+// FC1, the FC2 input's requantisation, FC2, the combine; every kernel after FC1 starts early
+// (programmatic dependent launch) and waits on its predecessor in the device.  The forward runs
+// requant and FC2 as two kernels: on GB300 at the measured sizes that is faster than the fused
+// moe_fc2_requant_nvfp4 (same bits), whose in-kernel quantisation is issue-bound on the few
+// warps the FC2 kernel's registers and shared memory leave for it.
 static nvfp4_status forward_stages(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* offs, void* out_dev,
                                    void* ws_dev, size_t ws_bytes, void* stream, int capacity) {
     nvfp4_status s = moe_fc1_swiglu_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, false, capacity);
     if (s != NVFP4_OK) return s;
-    if (w->I <= fc2_requant_max_i() && w->E <= fc2_requant_max_e()) {
-        s = moe_fc2_requant_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, true, capacity);
-    } else {
-        s = moe_requant_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, stream, true, capacity);
-        if (s != NVFP4_OK) return s;
-        s = moe_fc2_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, true, capacity);
-    }
+    s = moe_requant_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, stream, true, capacity);
+    if (s != NVFP4_OK) return s;
+    s = moe_fc2_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, true, capacity);
     if (s != NVFP4_OK) return s;
     return moe_combine_bf16_impl(w, T, k, out_dev, ws_dev, ws_bytes, stream, true, capacity);
 }

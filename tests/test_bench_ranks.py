@@ -91,11 +91,10 @@ def test_layer_roofline_arithmetic():
     peaks = {"hbm_gbs": 6791.7, "bf16_tflops": 1916.3}
     r = bench.layer_roofline(S.CONFIGS["qwen3_30b_a3b"], peaks, "measured", 0.2554)
     per = r["stage_bound_us"]
-    # I = 768: FC2 runs with the requantisation fused in, so the step has four stages
-    assert set(per) == {"route_sort_quant", "fc1_swiglu", "fc2_requant", "combine"}
+    assert set(per) == {"route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"}
     assert list(per) == bench.step_stages(S.CONFIGS["qwen3_30b_a3b"])
-    # the large layer (I = 1536) keeps requant and FC2 as two stages
-    assert bench.step_stages(S.CONFIGS["large"]) == ["route_sort_quant", "fc1_swiglu", "requant", "fc2", "combine"]
+    # the fused FC2 (timed beside the step) takes I <= 768 and E <= 512
+    assert bench.fused_fc2_supported(S.CONFIGS["qwen3_30b_a3b"]) and not bench.fused_fc2_supported(S.CONFIGS["large"])
     # at 4096 tokens every stage is bound by its bytes: FC1's weight stream is ~46 us
     assert 45 < per["fc1_swiglu"] < 48 and 7 < per["route_sort_quant"] < 9
     assert r["bound_ms"] == pytest.approx(sum(per.values()) / 1e3, abs=1e-3)
