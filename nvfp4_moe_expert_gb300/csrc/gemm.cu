@@ -16,12 +16,12 @@
 // fixed order, independent of its neighbours).
 //
 // Kernel design (sm_103a):
-//  * persistent: one 352-thread CTA per SM walks the (m-tile, n-tile) list;
+//  * persistent: one 608-thread CTA per SM walks the (m-tile, n-tile) list;
 //    the list length comes from the device-side expert offsets, so nothing
 //    is read back to the host;
 //  * two TMA producers, because one issuing thread caps what an SM pulls from
 //    L2 well below what it can take in: warp 0 loads the A tile (128 rows x
-//    256 K, 16 KB, 128B swizzle) and its scale-factor tiles, warp 10 the B
+//    256 K, 16 KB, 128B swizzle) and its scale-factor tiles, warp 18 the B
 //    tile (256 rows x 256 K in one box: FC2 256 consecutive weight rows, FC1
 //    through a 4D map the 128 gate rows and the matching 128 up rows, so one
 //    tile holds both halves of SwiGLU) and its scale-factor tiles; 3-stage
@@ -32,13 +32,16 @@
 //  * warp 1 = MMA issuer: tcgen05.cp moves the stage's scale factors into
 //    TMEM, then 4 x tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //    (M=128, N=256, K=64) accumulate in a 256-column FP32 TMEM tile;
-//  * warps 2-9 = epilogue, two warps per 32-lane TMEM quarter, each taking
-//    half of the tile's columns.  They copy their accumulator columns to
-//    registers and release TMEM at once, so the next tile's MMAs run while
+//  * warps 2-17 = epilogue, four warps per 32-lane TMEM quarter, each taking
+//    64 accumulator columns (FC1: 32 gate columns and the matching 32 up
+//    columns; FC2: 64 output columns), so four epilogue warps share each
+//    scheduler to hide their latencies.  They copy their accumulator columns
+//    to registers and release TMEM at once, so the next tile's MMAs run while
 //    they apply the FP32 scales (staged in shared memory per tile), BF16
-//    casts and the fused SwiGLU x prob; FC1 lanes write their own h rows
-//    with 32-byte stores, FC2 rows (scattered to (token, slot) places) go
-//    through a per-warp shared-memory transpose as whole 128-byte lines.
+//    casts and the fused SwiGLU x prob; every lane writes its own row's
+//    values with 32-byte stores (FC2 rows to their (token, slot) places).
+//    19 warps leave a thread 96 registers (five warps share three of the
+//    SM's sub-partitions, each with 16K registers).
 //  Every row's arithmetic is the same whatever tile, expert or batch it is
 //  in: one tile shape, no split-K, K always walked 0..K-1 in 64-wide steps.
 //  All waits are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
@@ -63,10 +66,16 @@ __device__ const uint32_t g_silu_bits[65536] = {
 namespace {
 
 constexpr int kStages = 3;
+// The grouped GEMM kernel: producer A, MMA, 16 epilogue warps (four per TMEM lane quarter,
+// each owning 64 accumulator columns), producer B.  19 warps put five on three of the SM's
+// sub-partitions, so a thread gets at most 96 registers (5 x 32 x 96 <= 16384 per partition).
+constexpr int kMainEpiWarps = 16;
+constexpr int kMainEpiThreads = kMainEpiWarps * 32;
+constexpr int kMainThreads = 96 + kMainEpiThreads;
+constexpr int kMainProducerBWarp = 2 + kMainEpiWarps;
+// The fused FC2 kernel's epilogue warps.
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 96 + kEpiThreads;            // + producer A, MMA, producer B warps
-constexpr int kProducerBWarp = 2 + kEpiWarps;
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBKBytes = 128;                         // bytes of K per row per stage (256 FP4 values)
@@ -87,12 +96,12 @@ constexpr int kEpiStageOff = kStages * kStageBytes;
 // Outside that range silu has a closed form (silu_bf16), so no lookup leaves the SM.
 constexpr uint32_t kSiluLo = 0x3380u, kSiluSpan = 0x4300u - 0x3380u;
 constexpr int kBarrierBytes = 256;
-// Shared-memory layout after the stages: FC2 has the output transpose buffers, FC1 (whose
-// lanes store their own rows) the SiLU range instead.
+// Shared-memory layout after the stages: the epilogue warps' column scales, the expert offsets
+// and, for FC1, the SiLU range.
 template <bool kFC1>
 struct Smem {
-    static constexpr int scale = kEpiStageOff + (kFC1 ? 0 : kEpiWarps * kStageWarpBytes);   // 128 floats per warp
-    static constexpr int offsets = scale + kEpiWarps * 128 * 4;                             // up to 1025 ints
+    static constexpr int scale = kEpiStageOff;                                              // 64 floats per warp
+    static constexpr int offsets = scale + kMainEpiWarps * 64 * 4;                          // up to 1025 ints
     static constexpr int silu = offsets + 4352;
     static constexpr int bar = silu + (kFC1 ? 2 * kSiluSpan * 4 : 0);
     static constexpr int bytes = bar + kBarrierBytes + 1024;
@@ -109,14 +118,17 @@ static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 // also +-0); a for a >= 2^7 and -0 for a <= -2^7 (e^-128 is far below the rounding); the
 // global table for infinities and NaN.  Every value equals the table's (checked over all
 // 65536 inputs by the tests through nvfp4_silu_table).
-__device__ __forceinline__ float silu_bf16(uint32_t bits, const float* s_silu) {
+__device__ __noinline__ float silu_bf16_outside(uint32_t bits) {
     const uint32_t mag = bits & 0x7FFFu;
-    const uint32_t idx = mag - kSiluLo;
-    if (idx < kSiluSpan) return s_silu[idx + ((bits >> 15) ? kSiluSpan : 0u)];
     const float a = __uint_as_float(bits << 16);
     if (mag < kSiluLo) return a * 0.5f;
     if (mag < 0x7F80u) return (bits >> 15) ? -0.0f : a;
     return __uint_as_float(__ldg(g_silu_bits + bits));
+}
+__device__ __forceinline__ float silu_bf16(uint32_t bits, const float* s_silu) {
+    const uint32_t idx = (bits & 0x7FFFu) - kSiluLo;
+    if (__builtin_expect(idx < kSiluSpan, 1)) return s_silu[idx + ((bits >> 15) ? kSiluSpan : 0u)];
+    return silu_bf16_outside(bits);
 }
 
 // Copy the table's SiLU range into shared memory (2 * kSiluSpan floats).
@@ -217,8 +229,77 @@ __device__ __forceinline__ void store_rows_64(uint8_t* stage, const uint32_t (&p
     __syncwarp();
 }
 
+// 32 BF16 values (packed[0..15], column pairs) of this lane's row at dst (32-byte aligned) as
+// two 32-byte stores.
+__device__ __forceinline__ void store_row_32(uint16_t* dst, const uint32_t (&packed)[16]) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * k),
+                     "r"(packed[8 * k]), "r"(packed[8 * k + 1]), "r"(packed[8 * k + 2]), "r"(packed[8 * k + 3]),
+                     "r"(packed[8 * k + 4]), "r"(packed[8 * k + 5]), "r"(packed[8 * k + 6]), "r"(packed[8 * k + 7])
+                     : "memory");
+    }
+}
+
+// FC1 epilogue of one lane's row over the warp's 32 gate columns (acc[0]) and the matching 32
+// up columns (acc[1]): gate/up = bf16((acc*g^x)*g^w) with the column scales sc[0..31] (gate)
+// and sc[32..63] (up), h = bf16(f32(f32(silu(gate)*up)*p)) into packed[0..15]; returns the
+// running max of |h| as a BF16 pair.  kDbg: also write the FP32 gate/up values to dbg
+// (gate at dbg[j], up at dbg[I + j]).
+template <bool kDbg>
+__device__ __forceinline__ uint32_t fc1_rows(const uint32_t (&acc)[2][32], const float* sc, float gr, float p,
+                                             const float* s_silu, float* dbg, int I, uint32_t (&packed)[16]) {
+    const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
+    const uint64_t p2 = f2(__float_as_uint(p), __float_as_uint(p));
+    uint32_t hmax2 = 0u;
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const uint64_t vg2 = f2_mul(f2_mul(f2(acc[0][j], acc[0][j + 1]), gr2), *reinterpret_cast<const uint64_t*>(sc + j));
+        const uint64_t vu2 =
+            f2_mul(f2_mul(f2(acc[1][j], acc[1][j + 1]), gr2), *reinterpret_cast<const uint64_t*>(sc + 32 + j));
+        float vg[2], vu[2];
+        f2_unpack(vg2, vg[0], vg[1]);
+        f2_unpack(vu2, vu[0], vu[1]);
+        if (kDbg) {
+            dbg[j] = vg[0];
+            dbg[j + 1] = vg[1];
+            dbg[I + j] = vu[0];
+            dbg[I + j + 1] = vu[1];
+        }
+        const uint32_t gb = bf16x2_rn(vg[0], vg[1]), ub = bf16x2_rn(vu[0], vu[1]);
+        const float sl0 = silu_bf16(gb & 0xFFFFu, s_silu), sl1 = silu_bf16(gb >> 16, s_silu);
+        // silu(gate) * up in FP32, then * p, one BF16 rounding
+        const uint64_t h2 =
+            f2_mul(f2_mul(f2(__float_as_uint(sl0), __float_as_uint(sl1)), f2(ub << 16, ub & 0xFFFF0000u)), p2);
+        float h[2];
+        f2_unpack(h2, h[0], h[1]);
+        packed[j >> 1] = bf16x2_rn(h[0], h[1]);
+        hmax2 = bf16x2_max(hmax2, packed[j >> 1] & 0x7FFF7FFFu);
+    }
+    return hmax2;
+}
+
+// FC2 epilogue of one lane's row over 32 columns: y = bf16((acc*g2)*g^w2) with the column
+// scales sc[0..31] into packed[0..15].  kDbg: also write the FP32 values to dbg[0..31].
+template <bool kDbg>
+__device__ __forceinline__ void fc2_cols(const uint32_t (&acc)[32], const float* sc, float gr, float* dbg,
+                                         uint32_t (&packed)[16]) {
+    const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const uint64_t v2 = f2_mul(f2_mul(f2(acc[j], acc[j + 1]), gr2), *reinterpret_cast<const uint64_t*>(sc + j));
+        float v0, v1;
+        f2_unpack(v2, v0, v1);
+        if (kDbg) {
+            dbg[j] = v0;
+            dbg[j + 1] = v1;
+        }
+        packed[j >> 1] = bf16x2_rn(v0, v1);
+    }
+}
+
 template <bool kFC1>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(96)
     grouped_gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
@@ -243,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, kEpiThreads);
+        mbar_init(tmem_empty, kMainEpiThreads);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -279,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The producer and MMA warps run their loops with all 32 lanes in step (every value
     // warp-uniform, waits taken by all lanes and agreed with a vote); the TMA and tcgen05
     // instructions are issued by the lane elect.sync picks.
-    if (warp == 0 || warp == kProducerBWarp) {
+    if (warp == 0 || warp == kMainProducerBWarp) {
         // ------------------------------------------------------------ producers
         const bool is_a = warp == 0;
         const uint64_t pol = is_a ? policy_evict_last() : policy_evict_normal();
@@ -400,18 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 2;                             // 0..7
+        const int ew = warp - 2;                             // 0..15
         const int q = warp & 3;                              // TMEM lane quarter of this warp
-        const int half = ew >> 2;                            // which half of the tile's columns
+        const int sub = ew >> 2;                             // which quarter of the tile's columns
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        float* sc = scale_buf + ew * 128;                    // this warp's 128 column scales
-        uint8_t* stage_buf = smem + kEpiStageOff + ew * kStageWarpBytes;
+        float* sc = scale_buf + ew * 64;                     // this warp's 64 column scales
         uint32_t acc_phase = 0;
-        // this tile's row data and the weight scales of this warp's 128 columns
-        // (FC1: 64 gate then 64 up) are loaded one tile ahead, so their latency
-        // hides behind the previous tile's epilogue
+        // this tile's row data and the weight scales of this warp's 64 columns (FC1: 32 gate
+        // then the 32 matching up columns) are loaded one tile ahead, so their latency hides
+        // behind the previous tile's epilogue
         int n_pair = -1;
-        float n_gr = 0.0f, n_p = 0.0f, n_sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float n_gr = 0.0f, n_p = 0.0f, n_sc[2] = {0.0f, 0.0f};
         auto prefetch = [&](int tt) {
             const int mt_ = tt / n_tiles, nt_ = tt % n_tiles;
             const int e_ = expert_of_row(s_off, E, mt_ * kBM);
@@ -420,11 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             n_gr = __ldg(args.a_g + row_);
             n_p = kFC1 ? __ldg(args.row_prob + row_) : 0.0f;
             const float* gw = args.b_g + static_cast<int64_t>(e_) * args.Nw;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = lane + 32 * i;
-                n_sc[i] = kFC1 ? __ldg(gw + (c < 64 ? nt_ * 128 + 64 * half + c : args.I + nt_ * 128 + 64 * half + c - 64))
-                               : __ldg(gw + nt_ * kBN + 128 * half + c);
+            if (kFC1) {
+                n_sc[0] = __ldg(gw + nt_ * 128 + 32 * sub + lane);
+                n_sc[1] = __ldg(gw + args.I + nt_ * 128 + 32 * sub + lane);
+            } else {
+                n_sc[0] = __ldg(gw + nt_ * kBN + 64 * sub + lane);
+                n_sc[1] = __ldg(gw + nt_ * kBN + 64 * sub + 32 + lane);
             }
         };
         if (static_cast<int>(blockIdx.x) < num_tiles) prefetch(blockIdx.x);
@@ -436,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float gr = live ? n_gr : 0.0f;
             const float p = live ? n_p : 0.0f;
             __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) sc[lane + 32 * i] = n_sc[i];
+            sc[lane] = n_sc[0];
+            sc[lane + 32] = n_sc[1];
             __syncwarp();
             if (t + static_cast<int>(gridDim.x) < num_tiles) prefetch(t + gridDim.x);
             if (!mbar_wait_bounded(tmem_full, acc_phase, abort_flag, kWaitBudgetCycles)) {
@@ -447,16 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             acc_phase ^= 1u;
             tc_fence_after();
-            // copy this warp's 128 accumulator columns to registers, then hand TMEM back
-            uint32_t acc[4][32];
+            // copy this warp's 64 accumulator columns to registers, then hand TMEM back
+            uint32_t acc[2][32];
             if (kFC1) {
-                tmem_ld_32x32b_x32(taddr + 64 * half, acc[0]);
-                tmem_ld_32x32b_x32(taddr + 64 * half + 32, acc[1]);
-                tmem_ld_32x32b_x32(taddr + 128 + 64 * half, acc[2]);
-                tmem_ld_32x32b_x32(taddr + 128 + 64 * half + 32, acc[3]);
+                tmem_ld_32x32b_x32(taddr + 32 * sub, acc[0]);          // gate columns
+                tmem_ld_32x32b_x32(taddr + 128 + 32 * sub, acc[1]);    // the matching up columns
             } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 128 * half + 32 * c, acc[c]);
+                tmem_ld_32x32b_x32(taddr + 64 * sub, acc[0]);
+                tmem_ld_32x32b_x32(taddr + 64 * sub + 32, acc[1]);
             }
             tmem_ld_wait();
             tc_fence_before();
@@ -464,68 +543,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (kFC1) {
                 const int I = args.I;
-                const float* sg = sc;                        // gate scales of my columns
-                const float* su = sc + 64;                   // up scales
-                float* dbg = args.debug ? args.debug + row * (2 * I) + nt * 128 + 64 * half : nullptr;
-                uint32_t packed[32];
-                uint32_t hmax2 = 0u;                         // running max of |h| as a BF16 pair
-                const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
-                const uint64_t p2 = f2(__float_as_uint(p), __float_as_uint(p));
-#pragma unroll
-                for (int j = 0; j < 64; j += 2) {       // columns j, j+1: ((acc*g^x)*g^w), both halves
-                    const uint64_t vg2 = f2_mul(f2_mul(f2(acc[j >> 5][j & 31], acc[j >> 5][(j & 31) + 1]), gr2),
-                                                *reinterpret_cast<const uint64_t*>(sg + j));
-                    const uint64_t vu2 = f2_mul(f2_mul(f2(acc[2 + (j >> 5)][j & 31], acc[2 + (j >> 5)][(j & 31) + 1]), gr2),
-                                                *reinterpret_cast<const uint64_t*>(su + j));
-                    float vg[2], vu[2];
-                    f2_unpack(vg2, vg[0], vg[1]);
-                    f2_unpack(vu2, vu[0], vu[1]);
-                    if (dbg && live) {
-                        dbg[j] = vg[0];
-                        dbg[j + 1] = vg[1];
-                        dbg[I + j] = vu[0];
-                        dbg[I + j + 1] = vu[1];
-                    }
-                    const uint32_t gb = bf16x2_rn(vg[0], vg[1]), ub = bf16x2_rn(vu[0], vu[1]);
-                    const float sl[2] = {silu_bf16(gb & 0xFFFFu, s_silu), silu_bf16(gb >> 16, s_silu)};
-                    // silu(gate) * up in FP32, then * p, one BF16 rounding
-                    const uint64_t h2 = f2_mul(f2_mul(f2(__float_as_uint(sl[0]), __float_as_uint(sl[1])),
-                                                      f2(ub << 16, ub & 0xFFFF0000u)),
-                                               p2);
-                    float h[2];
-                    f2_unpack(h2, h[0], h[1]);
-                    packed[j >> 1] = bf16x2_rn(h[0], h[1]);
-                    hmax2 = bf16x2_max(hmax2, packed[j >> 1] & 0x7FFF7FFFu);
-                }
+                float* dbg = args.debug && live ? args.debug + row * (2 * I) + nt * 128 + 32 * sub : nullptr;
+                uint32_t packed[16];
+                uint32_t hmax2;
+                if (dbg) hmax2 = fc1_rows<true>(acc, sc, gr, p, s_silu, dbg, I, packed);
+                else hmax2 = fc1_rows<false>(acc, sc, gr, p, s_silu, nullptr, I, packed);
                 const float hmax = __uint_as_float((bf16x2_max(hmax2, hmax2 >> 16) & 0xFFFFu) << 16);
-                if (live) atomicMax(args.amax2 + row, __float_as_uint(hmax));
-                if (live) store_row_64(args.h + row * I + nt * 128 + 64 * half, packed);
+                if (live) {
+                    atomicMax(args.amax2 + row, __float_as_uint(hmax));
+                    store_row_32(args.h + row * I + nt * 128 + 32 * sub, packed);
+                }
             } else {
                 const int H = args.H;
-                const float* sw = sc;
-                const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
-                float* dbg = args.debug ? args.debug + row * H + nt * kBN + 128 * half : nullptr;
+                float* dbg = args.debug && live ? args.debug + row * H + nt * kBN + 64 * sub : nullptr;
+                uint16_t* yrow = live ? args.y + static_cast<int64_t>(pair) * H + nt * kBN + 64 * sub : nullptr;
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {            // two 64-column chunks
-                    uint32_t packed[32];
-#pragma unroll
-                    for (int j = 0; j < 64; j += 2) {
-                        const int c = 64 * c2 + j;
-                        const uint64_t v2 = f2_mul(f2_mul(f2(acc[c >> 5][c & 31], acc[c >> 5][(c & 31) + 1]), gr2),
-                                                   *reinterpret_cast<const uint64_t*>(sw + c));
-                        float v0, v1;
-                        f2_unpack(v2, v0, v1);
-                        if (dbg && live) {
-                            dbg[c] = v0;
-                            dbg[c + 1] = v1;
-                        }
-                        packed[j >> 1] = bf16x2_rn(v0, v1);
-                    }
-                    uint16_t* ybase = args.y + nt * kBN + 128 * half + 64 * c2;
-                    store_rows_64(stage_buf, packed, [&](int r) -> uint16_t* {
-                        const int pr = __shfl_sync(0xFFFFFFFFu, pair, r);
-                        return pr >= 0 ? ybase + static_cast<int64_t>(pr) * H : nullptr;
-                    });
+                for (int c2 = 0; c2 < 2; ++c2) {            // two 32-column halves, 64 bytes of y each
+                    uint32_t packed[16];
+                    if (dbg) fc2_cols<true>(acc[c2], sc + 32 * c2, gr, dbg + 32 * c2, packed);
+                    else fc2_cols<false>(acc[c2], sc + 32 * c2, gr, nullptr, packed);
+                    if (live) store_row_32(yrow + 32 * c2, packed);
                 }
             }
         }
@@ -1097,8 +1134,9 @@ cudaError_t launch_gemm(bool fc1, const GemmArgs& a, cudaStream_t st, bool pdl) 
             : !make_code_map(&mb, a.b_codes, static_cast<int64_t>(a.E) * a.Nw, a.K / 2, kBN))
         return cudaErrorInvalidValue;
     const int grid = device_sm_count();
-    if (fc1) return launch_pdl(pdl, grouped_gemm_nvf4_kernel<true>, grid, kThreads, Smem<true>::bytes, st, ma, mb, a);
-    return launch_pdl(pdl, grouped_gemm_nvf4_kernel<false>, grid, kThreads, Smem<false>::bytes, st, ma, mb, a);
+    if (fc1)
+        return launch_pdl(pdl, grouped_gemm_nvf4_kernel<true>, grid, kMainThreads, Smem<true>::bytes, st, ma, mb, a);
+    return launch_pdl(pdl, grouped_gemm_nvf4_kernel<false>, grid, kMainThreads, Smem<false>::bytes, st, ma, mb, a);
 }
 
 cudaError_t launch_fc2_requant_impl(const GemmArgs& a, cudaStream_t st, bool pdl) {
