@@ -364,80 +364,11 @@ __device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* 
     return (capacity > 0 && row - e * capacity >= capacity) ? -1 : row;
 }
 
-// One token as the quantise-scatter holds it: its row (this lane's groups) and, on lanes
-// li < k, the destination row and router probability of slot li.
-template <int GPL>
-struct TokIn {
-    uint4 v[GPL][8];
-    int32_t dst;
-    float prob;
-    bool has;
-};
-
-template <int GPL>
-__device__ __forceinline__ void route_load(const uint16_t* __restrict__ x, int64_t T, int H, int E, int k,
-                                           const int32_t* __restrict__ ids, const float* __restrict__ probs,
-                                           const RouteBufs& b, int capacity, int64_t base, const RowLanes& rl, int G,
-                                           TokIn<GPL>& tk) {
-    const int64_t t = base + rl.slot;
-    tk.has = rl.active && t < T;
-    tk.dst = -1;
-    tk.prob = 0.0f;
-    if (!tk.has) return;
-    load_row_lanes<GPL>(x + t * H, rl, G, tk.v);
-    if (rl.LPR >= k && rl.li < k) {
-        const int64_t p = t * k + rl.li;
-        tk.prob = __ldg(probs + p);
-        tk.dst = pair_dest(b, ids, E, p, t / kRouteChunk, capacity);
-    }
-}
-
-template <int GPL>
-__device__ __forceinline__ void route_store(const TokIn<GPL>& tk, int64_t base, int64_t T, int H, int E, int k,
-                                            const int32_t* __restrict__ ids, const float* __restrict__ probs,
-                                            const RouteBufs& b, int capacity, const RowLanes& rl, int G, int* err) {
-    if (!tk.has) return;
-    const int64_t t = base + rl.slot;
-    GroupQ q[GPL];
-    bool finite;
-    const float gr = quantize_loaded<GPL>(tk.v, rl, G, -1.0f, q, finite);
-    if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
-    const bool slot_lane = rl.LPR >= k && rl.li < k;
-    if (slot_lane && tk.dst >= 0) {   // the routed row's per-row data, one slot per lane
-        b.a_g[tk.dst] = gr;
-        b.row_pair[tk.dst] = static_cast<int32_t>(t * k + rl.li);
-        b.row_prob[tk.dst] = tk.prob;
-        b.amax2[tk.dst] = 0u;
-    }
-    const int src0 = rl.slot * rl.LPR;
-    for (int j = 0; j < k; ++j) {
-        const int64_t p = t * k + j;
-        int64_t r;
-        if (rl.LPR >= k) {
-            r = __shfl_sync(rl.mask, tk.dst, src0 + j);
-        } else {                 // rows narrower than k lanes: look the slot up directly
-            r = pair_dest(b, ids, E, p, t / kRouteChunk, capacity);
-            if (r >= 0 && rl.li == 0) {
-                b.a_g[r] = gr;
-                b.row_pair[r] = static_cast<int32_t>(p);
-                b.row_prob[r] = __ldg(probs + p);
-                b.amax2[r] = 0u;
-            }
-        }
-        if (r < 0) continue;
-#pragma unroll
-        for (int i = 0; i < GPL; ++i) {
-            const int grp = rl.li + rl.LPR * i;
-            if (grp < G) store_group(q[i], r, grp, H, b.a_codes, b.a_sf);
-        }
-    }
-}
-
 // Blocks [0, pad_blocks) give one warp per expert for its pad rows
 // [offsets[e] + count_e, offsets[e+1]): zero scales, g = 0, row_pair = -1.
 // The remaining blocks quantise tokens (X read once) and write the k copies.
 template <int GPL>
-__global__ void __launch_bounds__(256, GPL <= 2 ? 2 : 1) route_quant_scatter_kernel(
+__global__ void __launch_bounds__(256, GPL == 1 ? 3 : (GPL == 2 ? 2 : 1)) route_quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int E, int k, const int32_t* __restrict__ ids,
     const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int pad_blocks, int capacity,
     int* err) {
@@ -465,84 +396,60 @@ __global__ void __launch_bounds__(256, GPL <= 2 ? 2 : 1) route_quant_scatter_ker
     const RowLanes rl(G);
     const int64_t warp = (static_cast<int64_t>(blockIdx.x - pad_blocks) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x - pad_blocks) * blockDim.x) >> 5;
-    const int64_t stride = nwarps * rl.RPW;
-    if (GPL == 1) {
-        // one wave of warps, each with two tokens in flight: the next token's row and slot
-        // lookups are loaded before the current token is quantised and scattered
-        TokIn<GPL> a, c;
-        int64_t b0 = warp * rl.RPW;
-        route_load<GPL>(x, T, H, E, k, ids, probs, b, capacity, b0, rl, G, a);
-        for (; b0 < T; b0 += 2 * stride) {
-            const int64_t b1 = b0 + stride;
-            route_load<GPL>(x, T, H, E, k, ids, probs, b, capacity, b1, rl, G, c);
-            route_store<GPL>(a, b0, T, H, E, k, ids, probs, b, capacity, rl, G, err);
-            if (b1 >= T) break;
-            route_load<GPL>(x, T, H, E, k, ids, probs, b, capacity, b1 + stride, rl, G, a);
-            route_store<GPL>(c, b1, T, H, E, k, ids, probs, b, capacity, rl, G, err);
+    for (int64_t base = warp * rl.RPW; base < T; base += nwarps * rl.RPW) {
+        const int64_t t = base + rl.slot;
+        if (!rl.active || t >= T) continue;
+        const int64_t chunk = t / kRouteChunk;
+        // lane li < k of the row looks up slot li's destination and probability; these
+        // loads and the row's are all in flight together
+        uint4 v[GPL][8];
+        load_row_lanes<GPL>(x + t * H, rl, G, v);
+        const bool slot_lane = rl.LPR >= k && rl.li < k;
+        int32_t my_dst = -1;
+        float my_prob = 0.0f;
+        if (slot_lane) {
+            const int64_t p = t * k + rl.li;
+            my_prob = __ldg(probs + p);
+            my_dst = pair_dest(b, ids, E, p, chunk, capacity);
         }
-    } else {
-        for (int64_t b0 = warp * rl.RPW; b0 < T; b0 += stride) {
-            TokIn<GPL> a;
-            route_load<GPL>(x, T, H, E, k, ids, probs, b, capacity, b0, rl, G, a);
-            route_store<GPL>(a, b0, T, H, E, k, ids, probs, b, capacity, rl, G, err);
+        GroupQ q[GPL];
+        bool finite;
+        const float gr = quantize_loaded<GPL>(v, rl, G, -1.0f, q, finite);
+        if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
+        if (slot_lane && my_dst >= 0) {   // the routed row's per-row data, one slot per lane
+            b.a_g[my_dst] = gr;
+            b.row_pair[my_dst] = static_cast<int32_t>(t * k + rl.li);
+            b.row_prob[my_dst] = my_prob;
+            b.amax2[my_dst] = 0u;
+        }
+        const int src0 = rl.slot * rl.LPR;
+        for (int j = 0; j < k; ++j) {
+            const int64_t p = t * k + j;
+            int64_t r;
+            if (rl.LPR >= k) {
+                r = __shfl_sync(rl.mask, my_dst, src0 + j);
+            } else {                 // rows narrower than k lanes: look the slot up directly
+                r = pair_dest(b, ids, E, p, chunk, capacity);
+                if (r >= 0 && rl.li == 0) {
+                    b.a_g[r] = gr;
+                    b.row_pair[r] = static_cast<int32_t>(p);
+                    b.row_prob[r] = __ldg(probs + p);
+                    b.amax2[r] = 0u;
+                }
+            }
+            if (r < 0) continue;
+#pragma unroll
+            for (int i = 0; i < GPL; ++i) {
+                const int grp = rl.li + rl.LPR * i;
+                if (grp < G) store_group(q[i], r, grp, H, b.a_codes, b.a_sf);
+            }
         }
     }
 }
 
 // ------------------------------------------------------------------ requant
-// One row of h as a quantiser lane holds it (its GPL 64-element groups), with the row's pair
-// (-1: pad row; kNoRow: past the last row) and FC1's max|h| of the row.
-constexpr int32_t kNoRow = -2;
 template <int GPL>
-struct HRowIn {
-    uint4 v[GPL][8];
-    int32_t pair;
-    uint32_t amax_bits;
-};
-
-template <int GPL>
-__device__ __forceinline__ void requant_load(const uint16_t* __restrict__ h, const uint32_t* __restrict__ amax2,
-                                             const int32_t* __restrict__ row_pair, int64_t base, int64_t rows, int I,
-                                             const RowLanes& rl, int G, HRowIn<GPL>& x) {
-    const int64_t r = base + rl.slot;
-    x.pair = kNoRow;
-    if (!rl.active || r >= rows) return;
-    x.pair = __ldg(row_pair + r);
-    x.amax_bits = __ldg(amax2 + r);
-    if (x.pair >= 0) load_row_lanes<GPL>(h + r * I, rl, G, x.v);   // a pad row's h is never used
-}
-
-template <int GPL>
-__device__ __forceinline__ void requant_store(const HRowIn<GPL>& x, int64_t base, int I, const RowLanes& rl, int G,
-                                              uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-                                              float* __restrict__ g, int* err) {
-    if (x.pair == kNoRow) return;
-    const int64_t r = base + rl.slot;
-    if (x.pair < 0) {       // pad row: zero scales, g = 0 (codes are never read)
-        for (int i = 0; i < GPL; ++i) {
-            const int grp = rl.li + rl.LPR * i;
-            if (grp < G) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, I)) = 0u;
-        }
-        if (rl.li == 0) g[r] = 0.0f;
-        return;
-    }
-    GroupQ q[GPL];
-    bool finite;
-    const float gr = quantize_loaded<GPL>(x.v, rl, G, __uint_as_float(x.amax_bits), q, finite);
-    if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
-#pragma unroll
-    for (int i = 0; i < GPL; ++i) {
-        const int grp = rl.li + rl.LPR * i;
-        if (grp < G) store_group(q[i], r, grp, I, codes, sf);
-    }
-    if (rl.li == 0) g[r] = gr;
-}
-
-// A grid of one wave walks the rows; each warp holds two row passes in flight (the loads of
-// the next pass are issued before the current one is quantised), so the load latency is
-// hidden by the pipeline instead of by waves of short-lived warps.
-template <int GPL>
-__global__ void __launch_bounds__(256, GPL <= 2 ? 2 : 1) requant_kernel(const uint16_t* __restrict__ h,
+__global__ void __launch_bounds__(256, GPL == 1 ? 3 : (GPL == 2 ? 2 : 1)) requant_kernel(const uint16_t* __restrict__ h,
                                                       const uint32_t* __restrict__ amax2,
                                                       const int32_t* __restrict__ row_pair,
                                                       const int32_t* __restrict__ offsets, int E, int I,
@@ -555,25 +462,32 @@ __global__ void __launch_bounds__(256, GPL <= 2 ? 2 : 1) requant_kernel(const ui
     const int64_t rows = offsets[E];
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t stride = nwarps * rl.RPW;
-    if (GPL == 1) {
-        HRowIn<GPL> a, b;
-        int64_t b0 = warp * rl.RPW;
-        requant_load<GPL>(h, amax2, row_pair, b0, rows, I, rl, G, a);
-        for (; b0 < rows; b0 += 2 * stride) {
-            const int64_t b1 = b0 + stride;
-            requant_load<GPL>(h, amax2, row_pair, b1, rows, I, rl, G, b);
-            requant_store<GPL>(a, b0, I, rl, G, codes, sf, g, err);
-            if (b1 >= rows) break;
-            requant_load<GPL>(h, amax2, row_pair, b1 + stride, rows, I, rl, G, a);
-            requant_store<GPL>(b, b1, I, rl, G, codes, sf, g, err);
+    for (int64_t base = warp * rl.RPW; base < rows; base += nwarps * rl.RPW) {
+        const int64_t r = base + rl.slot;
+        if (!rl.active || r >= rows) continue;
+        // the row's flags and values are loaded together (a pad row's h is never used)
+        const int32_t pair = __ldg(row_pair + r);
+        const uint32_t amax_bits = __ldg(amax2 + r);
+        uint4 v[GPL][8];
+        load_row_lanes<GPL>(h + r * I, rl, G, v);
+        if (pair < 0) {       // pad row: zero scales, g = 0 (codes are never read)
+            for (int i = 0; i < GPL; ++i) {
+                const int grp = rl.li + rl.LPR * i;
+                if (grp < G) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, I)) = 0u;
+            }
+            if (rl.li == 0) g[r] = 0.0f;
+            continue;
         }
-    } else {   // wider rows: one pass in flight (two would not fit the registers)
-        for (int64_t b0 = warp * rl.RPW; b0 < rows; b0 += stride) {
-            HRowIn<GPL> a;
-            requant_load<GPL>(h, amax2, row_pair, b0, rows, I, rl, G, a);
-            requant_store<GPL>(a, b0, I, rl, G, codes, sf, g, err);
+        GroupQ q[GPL];
+        bool finite;
+        const float gr = quantize_loaded<GPL>(v, rl, G, __uint_as_float(amax_bits), q, finite);
+        if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
+#pragma unroll
+        for (int i = 0; i < GPL; ++i) {
+            const int grp = rl.li + rl.LPR * i;
+            if (grp < G) store_group(q[i], r, grp, I, codes, sf);
         }
+        if (rl.li == 0) g[r] = gr;
     }
 }
 
@@ -631,18 +545,7 @@ cudaError_t launch_route_sort_quant_cap(const uint16_t* x, int64_t T, int H, int
         if (e != cudaSuccess) return e;
     }
     const int pad_blocks = (E + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    // tokens: narrow rows (one group per lane) run one wave of warps with two tokens in flight
-    // each; wider rows one token per warp pass
-    const int G = H / 64;
-    int token_blocks;
-    if (G <= 32) {
-        const int64_t blocks = (warps_for_rows(T, G) + 2 * kWarpsPerBlock - 1) / (2 * kWarpsPerBlock);
-        const int64_t cap = static_cast<int64_t>(device_sm_count()) * 2;
-        token_blocks = static_cast<int>(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
-    } else {
-        token_blocks = grid_for_warps(warps_for_rows(T, G));
-    }
-    const int grid = pad_blocks + token_blocks;
+    const int grid = pad_blocks + grid_for_warps(warps_for_rows(T, H / 64));
     return NVFP4_GPL_LAUNCH(true, H / 64, route_quant_scatter_kernel, grid, st, x, T, H, E, k, ids, probs, offsets, b,
                             pad_blocks, capacity, err);
 }
@@ -656,11 +559,7 @@ cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, 
 cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32_t* row_pair,
                            const int32_t* offsets, int E, int64_t rows_cap, int I, uint8_t* codes, uint8_t* sf,
                            float* g, int* err, cudaStream_t st, bool pdl) {
-    // one wave: two 256-thread blocks per SM (the kernel's register budget; one for the
-    // widest rows), or fewer if the rows need fewer warps at two passes each
-    const int64_t blocks = (warps_for_rows(rows_cap, I / 64) + 2 * kWarpsPerBlock - 1) / (2 * kWarpsPerBlock);
-    const int64_t cap = static_cast<int64_t>(device_sm_count()) * (I / 64 <= 64 ? 2 : 1);
-    const int grid = static_cast<int>(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
+    const int grid = grid_for_warps(warps_for_rows(rows_cap, I / 64));
     return NVFP4_GPL_LAUNCH(pdl, I / 64, requant_kernel, grid, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
 }
 
