@@ -491,6 +491,98 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : (GPL == 2 ? 2 : 1)) requan
     }
 }
 
+// ------------------------------------------------------------------ requant, coalesced
+// The same quantisation with a warp per row and the row's bytes spread over the lanes in
+// 16-byte chunks: lane l holds elements 256 j + 8 l .. +7 for chunks j = 0..C-1 (C = I/256
+// rounded up; the last chunk may cover only the first lanes).  Every load and every code
+// store of a warp covers whole 128-byte lines, which takes an eighth of the L1 wavefronts of
+// the lane-owns-a-group layout.  A 16-element block is the lane pair (2m, 2m+1) of a chunk:
+// its maximum is one shuffle, both lanes derive the same block scale, and each lane divides
+// its own 8 elements; the 4-byte scale word of a 64-element group is gathered to the group's
+// first lane.  Arithmetic and results are those of quantize_group.
+constexpr int kCoalescedMaxChunks = 8;   // I <= 2048
+
+template <int C>
+__global__ void __launch_bounds__(256) requant_coalesced_kernel(const uint16_t* __restrict__ h,
+                                                                const uint32_t* __restrict__ amax2,
+                                                                const int32_t* __restrict__ row_pair,
+                                                                const int32_t* __restrict__ offsets, int E, int I,
+                                                                uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                                float* __restrict__ g, int* err) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = offsets[E];
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int last_lanes = (I - 256 * (C - 1)) / 8;          // lanes holding data in the last chunk
+    for (int64_t r = warp; r < rows; r += nwarps) {
+        const int32_t pair = __ldg(row_pair + r);
+        const uint32_t amax_bits = __ldg(amax2 + r);
+        uint4 v[C];
+        if (pair >= 0) {
+#pragma unroll
+            for (int j = 0; j < C; ++j)
+                v[j] = (j < C - 1 || lane < last_lanes)
+                           ? __ldg(reinterpret_cast<const uint4*>(h + r * I + 256 * j + 8 * lane))
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (pair < 0) {       // pad row: zero scales, g = 0 (codes are never read)
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                const int grp = 4 * j + (lane >> 3);
+                if ((lane & 7) == 0 && (j < C - 1 || lane < last_lanes))
+                    *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, I)) = 0u;
+            }
+            if (lane == 0) g[r] = 0.0f;
+            continue;
+        }
+        // block maxima (this lane's 8 elements, then its pair lane's) and the row's finiteness
+        uint32_t bm[C];
+        uint32_t m_all = 0u;
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+            constexpr uint32_t kAbs = 0x7FFF7FFFu;
+            uint32_t m = bf16x2_max_nan(bf16x2_max_nan(v[j].x & kAbs, v[j].y & kAbs),
+                                        bf16x2_max_nan(v[j].z & kAbs, v[j].w & kAbs));
+            m = bf16x2_max_nan(m, m >> 16);
+            m = bf16x2_max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1)) << 16;
+            bm[j] = m;
+            m_all = max(m_all, m);
+        }
+        m_all = __reduce_max_sync(0xFFFFFFFFu, m_all);
+        const bool finite = m_all < 0x7F800000u;
+        if (!finite && lane == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
+        const float amax = __uint_as_float(amax_bits);
+        const float gr = finite ? __fdiv_rn(amax, kOuterDivisor) : 0.0f;
+        const float d1 = __fmul_rn(gr, 6.0f);
+        const float rc1 = d1 >= kMarksteinMinDivisor ? __frcp_rn(d1) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+            const bool have = j < C - 1 || lane < last_lanes;
+            const float bmx = __uint_as_float(bm[j]);
+            const float q1 = rc1 != 0.0f ? div_markstein(bmx, d1, rc1) : div_rn_slow(bmx, d1);
+            const uint32_t s_code = d1 > 0.0f ? cvt_e4m3(q1) : 0u;
+            const float d2 = __fmul_rn(gr, e4m3_value(s_code));
+            uint32_t cw = 0u;
+            if (d2 > 0.0f) {
+                const bool mk = d2 >= kMarksteinMinDivisor;
+                cw = codes8(v[j], d2, mk ? __frcp_rn(d2) : 0.0f, mk);
+            }
+            if (have) *reinterpret_cast<uint32_t*>(codes + r * (I / 2) + 128 * j + 4 * lane) = cw;
+            // the group's four block scales (lanes 8m, 8m+2, 8m+4, 8m+6) into one word on lane 8m
+            const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, s_code, 2);
+            const uint32_t s4 = __shfl_down_sync(0xFFFFFFFFu, s_code, 4);
+            const uint32_t s6 = __shfl_down_sync(0xFFFFFFFFu, s_code, 6);
+            if ((lane & 7) == 0 && have) {
+                const int grp = 4 * j + (lane >> 3);
+                *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, I)) = s_code | (s2 << 8) | (s4 << 16) | (s6 << 24);
+            }
+        }
+        if (lane == 0) g[r] = gr;
+    }
+}
+
 int grid_for_warps(int64_t warps) {
     const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
@@ -559,6 +651,18 @@ cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, 
 cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32_t* row_pair,
                            const int32_t* offsets, int E, int64_t rows_cap, int I, uint8_t* codes, uint8_t* sf,
                            float* g, int* err, cudaStream_t st, bool pdl) {
+    const int C = (I + 255) / 256;
+    if (C <= kCoalescedMaxChunks) {
+        const int grid = grid_for_warps(rows_cap);
+#define NVFP4_REQUANT_C(CC) \
+    case CC: return launch_pdl(pdl, requant_coalesced_kernel<CC>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
+        switch (C) {
+            NVFP4_REQUANT_C(1) NVFP4_REQUANT_C(2) NVFP4_REQUANT_C(3) NVFP4_REQUANT_C(4)
+            NVFP4_REQUANT_C(5) NVFP4_REQUANT_C(6) NVFP4_REQUANT_C(7) NVFP4_REQUANT_C(8)
+            default: break;
+        }
+#undef NVFP4_REQUANT_C
+    }
     const int grid = grid_for_warps(warps_for_rows(rows_cap, I / 64));
     return NVFP4_GPL_LAUNCH(pdl, I / 64, requant_kernel, grid, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
 }
