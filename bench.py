@@ -201,8 +201,7 @@ def batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev, sizes=(1, 7, 
     decode = [run(t, t + 1) for t in range(0, T, step)][:n_decode]
     return {"bitwise_equal": all(equal) and all(decode), "batches": len(calls), "batches_equal": sum(equal),
             "decode_calls": len(decode), "decode_equal": sum(decode),
-            "what": f"{cfg.name}: prefix and random-window sub-batches of {sorted(set(sizes + (T // 2,)))} "
-                    f"tokens and single-token calls vs the full batch"}
+            "what": f"prefix + random-window sub-batches of {sorted(set(sizes + (T // 2,)))} tokens, 1-token calls"}
 
 
 def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
@@ -215,7 +214,7 @@ def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
     bound_ms = 1e3 * sum(per.values())
     return {"frac": round(bound_ms / ms_per_step, 4), "bound_ms": round(bound_ms, 4),
             "measured_ms": round(ms_per_step, 4),
-            "stage_bound_us": {n: round(1e6 * t, 2) for n, t in per.items()}, "peak_note": "of " + peak_kind}
+            "stage_bound_us": {n: round(1e6 * t, 1) for n, t in per.items()}, "peak_note": "of " + peak_kind}
 
 
 def backward_work(cfg):
@@ -560,8 +559,8 @@ def extra_workload(M, torch, name, dev, stream, flush, K, W, peaks, peak_kind, t
     stages = {}
     for n in step_stages(cfg):
         r = roofline_of(n, work[n], st[n], peaks, peak_kind)
-        stages[n] = {"ms": round(st[n], 4), "bound": r["bound"], "frac": r["frac"],
-                     "achieved": r["achieved"], "unit": r["unit"]}
+        # [ms, roofline fraction, bound]: "tensor" = of the FP4 peak, "hbm" = of the copy bandwidth
+        stages[n] = [round(st[n], 4), r["frac"], r["bound"]]
     step_ms = statistics.mean(ms)
     M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
     M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
@@ -571,12 +570,11 @@ def extra_workload(M, torch, name, dev, stream, flush, K, W, peaks, peak_kind, t
     M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
     inv = batch_invariance(M, torch, cfg, weights, x, ids, pw, out, dev, sizes=(1, 64), n_decode=8, n_windows=2)
     res = {"tokens_per_s": round(T / (step_ms * 1e-3), 1), "ms_per_step": round(step_ms, 4), "steps": K,
-           "stages": stages, "layer_roofline_frac": layer_roofline(cfg, peaks, peak_kind, step_ms)["frac"],
-           "fused_fc2_requant": fused,
+           "layer_roofline_frac": layer_roofline(cfg, peaks, peak_kind, step_ms)["frac"],
            "bitwise_invariant": inv["bitwise_equal"],
-           "config": f"H {H}, I {I}, E {E}, top-{k}, {T} tokens, {cfg.routing} routing"
-                     + (f", {cfg.outlier_frac:.0%} x20 outlier channels" if cfg.outlier_frac else "")
-                     + ", weights drawn on the GPU (seeded), L2 flushed between steps"}
+           "stages_ms_frac_bound": stages}
+    if fused:
+        res["fused_fc2_requant_ms"] = [fused["ms"], fused["frac"], fused["requant_plus_fc2_ms"]]
     del weights, ws, out, x
     torch.cuda.empty_cache()
     return res
