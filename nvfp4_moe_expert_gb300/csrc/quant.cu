@@ -367,8 +367,10 @@ __device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* 
 // Blocks [0, pad_blocks) give one warp per expert for its pad rows
 // [offsets[e] + count_e, offsets[e+1]): zero scales, g = 0, row_pair = -1.
 // The remaining blocks quantise tokens (X read once) and write the k copies.
+// Narrow rows (one group per lane) run in 128-thread blocks held to 72 registers, seven
+// blocks (28 warps) per SM, so that 4096 tokens at one token per warp fit in one wave.
 template <int GPL>
-__global__ void __launch_bounds__(256, GPL == 1 ? 3 : (GPL == 2 ? 2 : 1)) route_quant_scatter_kernel(
+__global__ void __launch_bounds__(GPL == 1 ? 128 : 256, GPL == 1 ? 7 : (GPL == 2 ? 2 : 1)) route_quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int E, int k, const int32_t* __restrict__ ids,
     const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int pad_blocks, int capacity,
     int* err) {
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(256, GPL == 1 ? 3 : (GPL == 2 ? 2 : 1)) route_
     const int G = H / 64;
     const int lane = threadIdx.x & 31;
     if (static_cast<int>(blockIdx.x) < pad_blocks) {
-        const int e = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+        const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
         if (e >= E) return;
         const int64_t r0 = static_cast<int64_t>(__ldg(offsets + e)) + __ldg(b.expert_count + e);
         const int64_t r1 = __ldg(offsets + e + 1);
@@ -636,9 +638,18 @@ cudaError_t launch_route_sort_quant_cap(const uint16_t* x, int64_t T, int H, int
                        b.expert_count, offsets, capacity, err);
         if (e != cudaSuccess) return e;
     }
+    const int G = H / 64;
+    if (G <= 32) {   // 128-thread blocks (4 warps), one warp per token
+        const int pad_blocks = (E + 3) / 4;
+        const int64_t wanted = (warps_for_rows(T, G) + 3) / 4;
+        const int64_t cap = static_cast<int64_t>(device_sm_count()) * 32;
+        const int grid = pad_blocks + static_cast<int>(wanted < 1 ? 1 : (wanted < cap ? wanted : cap));
+        return launch_pdl(true, route_quant_scatter_kernel<1>, grid, 128, 0, st, x, T, H, E, k, ids, probs, offsets, b,
+                          pad_blocks, capacity, err);
+    }
     const int pad_blocks = (E + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const int grid = pad_blocks + grid_for_warps(warps_for_rows(T, H / 64));
-    return NVFP4_GPL_LAUNCH(true, H / 64, route_quant_scatter_kernel, grid, st, x, T, H, E, k, ids, probs, offsets, b,
+    const int grid = pad_blocks + grid_for_warps(warps_for_rows(T, G));
+    return NVFP4_GPL_LAUNCH(true, G, route_quant_scatter_kernel, grid, st, x, T, H, E, k, ids, probs, offsets, b,
                             pad_blocks, capacity, err);
 }
 
