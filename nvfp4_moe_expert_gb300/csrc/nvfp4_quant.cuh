@@ -98,30 +98,31 @@ __device__ __forceinline__ uint64_t f32x2_splat(float a) {
     return x;
 }
 
-// IEEE quotients for the divisors below the Markstein range; kept out of line so the
-// common path stays short (it is taken only for rows whose maximum is below ~2^-48).
-__device__ __noinline__ void quotients_fdiv(const uint32_t (&w)[4], float d, float (&q)[8]) {
+// Codes by IEEE division for the divisors below the Markstein range; kept out of line so
+// the common path stays short (it is taken only for rows whose maximum is below ~2^-48).
+// Its arguments and result are scalars, so the call keeps everything in registers.
+__device__ __noinline__ uint32_t codes8_fdiv(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, float d) {
+    const uint32_t w[4] = {w0, w1, w2, w3};
+    float q[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         q[2 * j] = __fdiv_rn(__uint_as_float(w[j] << 16), d);
         q[2 * j + 1] = __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), d);
     }
+    return e2m1x8(q);   // IEEE division keeps the sign of a zero quotient
 }
 
 __device__ __noinline__ float div_rn_slow(float a, float b) { return __fdiv_rn(a, b); }
 
 // Eight E2M1 codes of one 16-byte vector of BF16 values, quotient by d (rc = RN(1/d)).
 __device__ __forceinline__ uint32_t codes8(const uint4& v, float d, float rc, bool markstein) {
+    if (!markstein) return codes8_fdiv(v.x, v.y, v.z, v.w, d);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float q[8];
-    if (markstein) {
-        const uint64_t nrc2 = f32x2_splat(-rc), d2 = f32x2_splat(d);
+    const uint64_t nrc2 = f32x2_splat(-rc), d2 = f32x2_splat(d);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            div_markstein_neg_x2(bf16x2_to_f32x2(w[j] ^ 0x80008000u), nrc2, d2, q[2 * j], q[2 * j + 1]);
-    } else {
-        quotients_fdiv(w, d, q);   // IEEE division keeps the sign of a zero quotient
-    }
+    for (int j = 0; j < 4; ++j)
+        div_markstein_neg_x2(bf16x2_to_f32x2(w[j] ^ 0x80008000u), nrc2, d2, q[2 * j], q[2 * j + 1]);
     // The conversion keeps the quotient's sign, also of a zero (-0.0 and tiny negatives
     // give code 8), and every quotient above carries x's sign: the code's sign is x's.
     return e2m1x8(q);

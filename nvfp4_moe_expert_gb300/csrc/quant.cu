@@ -202,8 +202,11 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int64_t n_chunk
     __shared__ int32_t seg_sum[1024];
     __shared__ int32_t e_off[1024];
     __shared__ int32_t warp_tot[33];
-    pdl_wait();
+    // The quantise-scatter that follows may start at once: it reads only inputs written
+    // before the histogram kernel (which starts after all earlier work has finished) until
+    // its own wait, which covers this kernel and, through this kernel's wait, the histogram.
     pdl_launch_dependents();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int S = blockDim.x / E;                  // threads per expert (>= 1)
     const int e = tid / S, seg = tid % S;
@@ -366,7 +369,10 @@ __device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* 
 
 // Blocks [0, pad_blocks) give one warp per expert for its pad rows
 // [offsets[e] + count_e, offsets[e+1]): zero scales, g = 0, row_pair = -1.
-// The remaining blocks quantise tokens (X read once) and write the k copies.
+// The remaining blocks quantise tokens (X read once) and write the k copies.  A token's
+// row and routing probabilities are inputs of the route stage, so they are loaded and the
+// row quantised before the wait on the sorting kernels; only the destination rows (and
+// the stores) come after it.
 // Narrow rows (one group per lane) run in 128-thread blocks held to 72 registers, seven
 // blocks (28 warps) per SM, so that 4096 tokens at one token per warp fit in one wave.
 template <int GPL>
@@ -374,11 +380,11 @@ __global__ void __launch_bounds__(GPL == 1 ? 128 : 256, GPL == 1 ? 7 : (GPL == 2
     const uint16_t* __restrict__ x, int64_t T, int H, int E, int k, const int32_t* __restrict__ ids,
     const float* __restrict__ probs, const int32_t* __restrict__ offsets, RouteBufs b, int pad_blocks, int capacity,
     int* err) {
-    pdl_wait();
     pdl_launch_dependents();
     const int G = H / 64;
     const int lane = threadIdx.x & 31;
     if (static_cast<int>(blockIdx.x) < pad_blocks) {
+        pdl_wait();
         const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
         if (e >= E) return;
         const int64_t r0 = static_cast<int64_t>(__ldg(offsets + e)) + __ldg(b.expert_count + e);
@@ -402,22 +408,20 @@ __global__ void __launch_bounds__(GPL == 1 ? 128 : 256, GPL == 1 ? 7 : (GPL == 2
         const int64_t t = base + rl.slot;
         if (!rl.active || t >= T) continue;
         const int64_t chunk = t / kRouteChunk;
-        // lane li < k of the row looks up slot li's destination and probability; these
-        // loads and the row's are all in flight together
+        // lane li < k of the row holds slot li's probability and, after the wait, its
+        // destination row
         uint4 v[GPL][8];
         load_row_lanes<GPL>(x + t * H, rl, G, v);
         const bool slot_lane = rl.LPR >= k && rl.li < k;
-        int32_t my_dst = -1;
         float my_prob = 0.0f;
-        if (slot_lane) {
-            const int64_t p = t * k + rl.li;
-            my_prob = __ldg(probs + p);
-            my_dst = pair_dest(b, ids, E, p, chunk, capacity);
-        }
+        if (slot_lane) my_prob = __ldg(probs + t * k + rl.li);
         GroupQ q[GPL];
         bool finite;
         const float gr = quantize_loaded<GPL>(v, rl, G, -1.0f, q, finite);
         if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
+        pdl_wait();
+        int32_t my_dst = -1;
+        if (slot_lane) my_dst = pair_dest(b, ids, E, t * k + rl.li, chunk, capacity);
         if (slot_lane && my_dst >= 0) {   // the routed row's per-row data, one slot per lane
             b.a_g[my_dst] = gr;
             b.row_pair[my_dst] = static_cast<int32_t>(t * k + rl.li);
