@@ -31,11 +31,15 @@ __device__ __forceinline__ void set_device_error(int* err, int code) {
 // Programmatic dependent launch.  Inside one library call, every kernel after
 // the first is launched with programmatic stream serialisation, so its CTAs may
 // be scheduled while the previous kernel (also this library's) is finishing.
-// Every kernel calls pdl_wait() before its first access to global memory (it
-// returns once the previous kernel has completed and its writes are visible;
-// at once for a normal launch) and then pdl_launch_dependents() so that the
-// next kernel can be scheduled early too.  The first kernel of a call is
-// launched normally, so it is ordered after whatever the caller queued before.
+// Every kernel calls pdl_wait() before its first access to global memory that
+// an earlier kernel may still be writing (it returns once the previous kernel
+// has completed and its writes are visible; at once for a normal launch) and
+// then pdl_launch_dependents() so that the next kernel can be scheduled early
+// too.  The first kernel of a call is launched normally, so it is ordered after
+// whatever the caller queued before; the route sort's first kernel is the one
+// exception: it is launched early as well, and since it triggers its dependents
+// only after its own wait has returned, every later kernel of the call still
+// starts after the caller's work is complete.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -357,14 +357,19 @@ __global__ void __launch_bounds__(1024) route_block_sort_kernel(const int32_t* _
 // by route_block_sort_kernel, or chunk base + rank from the chunked kernels.
 // With a fixed capacity C (> 0), a pair whose row falls past its expert's C rows is dropped
 // (-1; reported by the counting kernels).
-__device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* ids, int E, int64_t p, int64_t chunk,
-                                             int capacity) {
+// The same given the pair's expert id e (already loaded): its rank and chunk base are loaded
+// together.
+__device__ __forceinline__ int32_t pair_dest_e(const RouteBufs& b, int e, int E, int64_t p, int64_t chunk,
+                                               int capacity) {
     if (b.direct_rows) return __ldg(b.pair_rank + p);
-    const int e = __ldg(ids + p);
-    const int32_t rank = __ldg(b.pair_rank + p);
     if (e < 0 || e >= E) return -1;   // reported by the counting kernels
+    const int32_t rank = __ldg(b.pair_rank + p);
     const int32_t row = __ldg(b.chunk_base + static_cast<int64_t>(e) * b.n_chunks + chunk) + rank;
     return (capacity > 0 && row - e * capacity >= capacity) ? -1 : row;
+}
+__device__ __forceinline__ int32_t pair_dest(const RouteBufs& b, const int32_t* ids, int E, int64_t p, int64_t chunk,
+                                             int capacity) {
+    return pair_dest_e(b, b.direct_rows ? 0 : __ldg(ids + p), E, p, chunk, capacity);
 }
 
 // Blocks [0, pad_blocks) give one warp per expert for its pad rows
@@ -408,20 +413,24 @@ __global__ void __launch_bounds__(GPL == 1 ? 128 : 256, GPL == 1 ? 7 : (GPL == 2
         const int64_t t = base + rl.slot;
         if (!rl.active || t >= T) continue;
         const int64_t chunk = t / kRouteChunk;
-        // lane li < k of the row holds slot li's probability and, after the wait, its
-        // destination row
+        // lane li < k of the row holds slot li's probability and expert id (inputs) and,
+        // after the wait, its destination row
         uint4 v[GPL][8];
         load_row_lanes<GPL>(x + t * H, rl, G, v);
         const bool slot_lane = rl.LPR >= k && rl.li < k;
         float my_prob = 0.0f;
-        if (slot_lane) my_prob = __ldg(probs + t * k + rl.li);
+        int my_e = -1;
+        if (slot_lane) {
+            my_prob = __ldg(probs + t * k + rl.li);
+            my_e = __ldg(ids + t * k + rl.li);
+        }
         GroupQ q[GPL];
         bool finite;
         const float gr = quantize_loaded<GPL>(v, rl, G, -1.0f, q, finite);
         if (!finite && rl.li == 0) set_device_error(err, NVFP4_ERR_NONFINITE);
         pdl_wait();
         int32_t my_dst = -1;
-        if (slot_lane) my_dst = pair_dest(b, ids, E, t * k + rl.li, chunk, capacity);
+        if (slot_lane) my_dst = pair_dest_e(b, my_e, E, t * k + rl.li, chunk, capacity);
         if (slot_lane && my_dst >= 0) {   // the routed row's per-row data, one slot per lane
             b.a_g[my_dst] = gr;
             b.row_pair[my_dst] = static_cast<int32_t>(t * k + rl.li);
@@ -589,6 +598,140 @@ __global__ void __launch_bounds__(256) requant_coalesced_kernel(const uint16_t* 
     }
 }
 
+// ------------------------------------------------------------------ requant, a block per lane
+// The same quantisation with every lane owning whole 16-element blocks.  A warp takes R
+// consecutive rows at a time, R the smallest count for which the batch's R*B blocks (B = I/16)
+// fill whole passes of 32 lanes, in P = R*B/32 passes: in pass p lane l quantises block
+// f = 32 p + l of the batch (row f / B, block f % B).  Consecutive rows are contiguous in h, so
+// each pass reads 1 KB (one 32-byte load per lane) and writes 256 contiguous bytes of codes.
+// Each block's scale, reciprocal and codes are computed once, by its own lane; per row, the
+// finiteness is one ballot per pass and the outer scale is computed by lane rho for row rho
+// and shuffled.  Arithmetic and results are those of quantize_group.
+constexpr int kBlockLanesMaxPasses = 4;
+
+__device__ __forceinline__ void load32_nc(const uint16_t* p, uint4& a, uint4& b) {
+    asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+        : "l"(p));
+}
+
+// Passes per batch for rows of I columns (0 when the batch would need more than
+// kBlockLanesMaxPasses).
+int block_lanes_passes(int I) {
+    if (I % 16 != 0 || I <= 0) return 0;
+    const int B = I / 16;
+    int gcd = B, b = 32;
+    while (b) {
+        const int t = gcd % b;
+        gcd = b;
+        b = t;
+    }
+    const int R = 32 / gcd;
+    const int P = R * B / 32;
+    return P <= kBlockLanesMaxPasses ? P : 0;
+}
+
+template <int P>
+__global__ void __launch_bounds__(256, P <= 3 ? 4 : 2) requant_blocks_kernel(const uint16_t* __restrict__ h,
+                                                             const uint32_t* __restrict__ amax2,
+                                                             const int32_t* __restrict__ row_pair,
+                                                             const int32_t* __restrict__ offsets, int E, int I,
+                                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                             float* __restrict__ g, int* err) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int B = I / 16;
+    const int R = 32 * P / B;
+    const int64_t rows = offsets[E];
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    int rho[P], blk[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        const int f = 32 * p + lane;
+        rho[p] = f / B;
+        blk[p] = f - rho[p] * B;
+    }
+    for (int64_t r0 = warp * R; r0 < rows; r0 += nwarps * R) {
+        // row data on lane rho for row r0 + rho
+        int32_t pair_l = -1;
+        uint32_t amax_l = 0u;
+        const bool row_lane = lane < R && r0 + lane < rows;
+        if (row_lane) {
+            pair_l = __ldg(row_pair + r0 + lane);
+            amax_l = __ldg(amax2 + r0 + lane);
+        }
+        // h is loaded for every row below the used count, pad rows included, so that these
+        // loads need not wait for the row map; a pad row's (stale) values are never used
+        uint4 v[P][2];
+        bool in_range[P], live[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            in_range[p] = r0 + rho[p] < rows;
+            if (in_range[p]) {
+                load32_nc(h + (r0 + rho[p]) * I + 16 * blk[p], v[p][0], v[p][1]);
+            } else {
+                v[p][0] = make_uint4(0u, 0u, 0u, 0u);
+                v[p][1] = v[p][0];
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < P; ++p) live[p] = in_range[p] && __shfl_sync(0xFFFFFFFFu, pair_l, rho[p]) >= 0;
+        // block maxima; a row is finite when none of its blocks holds an infinity or NaN
+        uint32_t bm[P];
+        unsigned nonfinite_mask[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            bm[p] = block_absmax_bits(v[p][0], v[p][1]);
+            nonfinite_mask[p] = __ballot_sync(0xFFFFFFFFu, bm[p] >= 0x7F800000u);
+        }
+        float g_l = 0.0f, d1_l = 0.0f, rc1_l = 0.0f;
+        if (row_lane) {
+            bool finite = true;
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const int lo = max(lane * B - 32 * p, 0), hi = min(lane * B + B - 32 * p, 32);
+                if (lo < hi) {
+                    const unsigned m = (hi - lo == 32 ? 0xFFFFFFFFu : ((1u << (hi - lo)) - 1u)) << lo;
+                    if (nonfinite_mask[p] & m) finite = false;
+                }
+            }
+            if (pair_l >= 0) {
+                if (!finite) set_device_error(err, NVFP4_ERR_NONFINITE);
+                g_l = finite ? __fdiv_rn(__uint_as_float(amax_l), kOuterDivisor) : 0.0f;
+                d1_l = __fmul_rn(g_l, 6.0f);
+                rc1_l = d1_l >= kMarksteinMinDivisor ? __frcp_rn(d1_l) : 0.0f;
+            }
+            g[r0 + lane] = g_l;                  // pad rows: g = 0
+        }
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const float gr = __shfl_sync(0xFFFFFFFFu, g_l, rho[p]);
+            const float d1 = __shfl_sync(0xFFFFFFFFu, d1_l, rho[p]);
+            const float rc1 = __shfl_sync(0xFFFFFFFFu, rc1_l, rho[p]);
+            if (!in_range[p]) continue;
+            const int64_t r = r0 + rho[p];
+            uint32_t s_code = 0u;
+            if (live[p]) {
+                const float bmx = __uint_as_float(bm[p]);
+                const float q1 = rc1 != 0.0f ? div_markstein(bmx, d1, rc1) : div_rn_slow(bmx, d1);
+                s_code = d1 > 0.0f ? cvt_e4m3(q1) : 0u;
+                const float d2 = __fmul_rn(gr, e4m3_value(s_code));
+                uint32_t c0 = 0u, c1 = 0u;
+                if (d2 > 0.0f) {
+                    const bool mk = d2 >= kMarksteinMinDivisor;
+                    const float rc = mk ? __frcp_rn(d2) : 0.0f;
+                    c0 = codes8(v[p][0], d2, rc, mk);
+                    c1 = codes8(v[p][1], d2, rc, mk);
+                }
+                *reinterpret_cast<uint2*>(codes + r * (I / 2) + 8 * blk[p]) = make_uint2(c0, c1);
+            }
+            sf[sf_offset(r, blk[p], I)] = static_cast<uint8_t>(s_code);   // pad rows: zero scales
+        }
+    }
+}
+
 int grid_for_warps(int64_t warps) {
     const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
@@ -629,13 +772,13 @@ cudaError_t launch_route_sort_quant_cap(const uint16_t* x, int64_t T, int H, int
     if (E <= kBlockSortMaxE && T * k <= kBlockSortMaxPairs) {
         b.direct_rows = 1;
         const size_t smem = sizeof(int32_t) * kBlockSortWarps * E;
-        e = launch_pdl(false, route_block_sort_kernel, 1, kBlockSortWarps * 32, smem, st, ids, T, E, k, b.pair_rank,
+        e = launch_pdl(true, route_block_sort_kernel, 1, kBlockSortWarps * 32, smem, st, ids, T, E, k, b.pair_rank,
                        b.expert_count, offsets, capacity, err);
         if (e != cudaSuccess) return e;
     } else {
         b.direct_rows = 0;
         const size_t smem = sizeof(int32_t) * kWarpsPerBlock * E;
-        e = launch_pdl(false, route_hist_rank_kernel, static_cast<unsigned>(b.n_chunks), 256, smem, st, ids, T, E, k,
+        e = launch_pdl(true, route_hist_rank_kernel, static_cast<unsigned>(b.n_chunks), 256, smem, st, ids, T, E, k,
                        b.n_chunks, b.chunk_count, b.pair_rank, err);
         if (e != cudaSuccess) return e;
         e = launch_pdl(true, route_scan_kernel, 1, 1024, 0, st, E, b.n_chunks, b.chunk_count, b.chunk_base,
@@ -666,6 +809,18 @@ cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, 
 cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32_t* row_pair,
                            const int32_t* offsets, int E, int64_t rows_cap, int I, uint8_t* codes, uint8_t* sf,
                            float* g, int* err, cudaStream_t st, bool pdl) {
+    const int P = block_lanes_passes(I);
+    if (P > 0) {
+        const int B = I / 16, R = 32 * P / B;
+        const int grid = grid_for_warps((rows_cap + R - 1) / R);
+        switch (P) {
+            case 1: return launch_pdl(pdl, requant_blocks_kernel<1>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
+            case 2: return launch_pdl(pdl, requant_blocks_kernel<2>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
+            case 3: return launch_pdl(pdl, requant_blocks_kernel<3>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
+            case 4: return launch_pdl(pdl, requant_blocks_kernel<4>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
+            default: break;
+        }
+    }
     const int C = (I + 255) / 256;
     if (C <= kCoalescedMaxChunks) {
         const int grid = grid_for_warps(rows_cap);

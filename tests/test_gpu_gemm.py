@@ -168,6 +168,56 @@ def test_requant_and_fc2_stage(run):
     assert bf16_ulp_distance(y_rows, F.round_to_bf16_bits(v_ref)).max() <= GEMM_BF16_ULP
 
 
+# Requant lane mappings: a batch of R rows per warp in P passes of 32 blocks (I = 128: R 4,
+# P 1; 256: R 2, P 1; 384: R 4, P 3; 1024: P 2; 1536: P 3; 2048: P 4), the coalesced
+# warp-per-row kernel (640: five passes would be needed) and the lane-owns-groups kernel
+# (2304 > 2048).  Rows include zeros, values whose divisors fall below the Markstein range
+# (the IEEE-division fallback) and one row each with an infinity and a NaN (zero codes,
+# scales and g, flagged as non-finite).
+@pytest.mark.parametrize("I", [128, 256, 384, 640, 1024, 1536, 2048, 2304])
+def test_requant_lane_mappings(I):
+    c = S.LayerConfig(f"rq{I}", H=256, I=I, E=4, k=2, T=150)
+    run = Run(c)
+    rc = run.lay.rows_cap
+    rng = np.random.default_rng(I)
+    n = len(run.real)
+    h = rng.standard_normal((n, I)).astype(np.float32)
+    h *= np.exp2(rng.uniform(-8, 2, (n, 1))).astype(np.float32)
+    h[0] = 0.0
+    h[1] *= np.float32(2.0 ** -110)                  # g*6 and g*s below 2^-60
+    h[2, : I // 2] *= np.float32(2.0 ** -120)       # BF16 subnormals beside normal values
+    bits = S.f32_to_bf16_bits(h)
+    bad = {3: 0x7F80, 4: 0x7FC0}                      # +inf, NaN
+    for row, b in bad.items():
+        bits[row, 7] = b
+    full = np.zeros((rc, I), np.uint16)
+    full[run.real] = bits
+    run.view("h", rc * I, torch.int16).copy_(torch.from_numpy(full.view(np.int16).ravel()).cuda())
+    f = F.bf16_bits_to_f32(bits)
+    amax = np.zeros(rc, np.float32)
+    with np.errstate(invalid="ignore"):
+        amax[run.real] = np.where(np.isnan(f).any(axis=1), np.float32(np.nan), np.abs(f).max(axis=1))
+    run.view("amax2", rc, torch.int32).copy_(torch.from_numpy(amax.view(np.int32)).cuda())
+    assert M.nvfp4_get_device_error() == 0
+    M.moe_requant_nvfp4(run.w, c.T, c.k, run.offs, run.ws)
+    assert M.nvfp4_get_device_error() == 6            # NVFP4_ERR_NONFINITE
+
+    a2c = run.view("a2_codes", rc * I // 2, torch.uint8).cpu().numpy().reshape(rc, I // 2)
+    a2s = M.sf_to_rows(run.view("a2_sf", rc * I // 16, torch.uint8).cpu().numpy(), rc, I)
+    a2g = run.view("a2_g", rc, torch.float32).cpu().numpy()
+    good = np.array([i for i in range(n) if i not in bad])
+    hc, hs, hg = Q.quantize_rows(f[good])
+    rows = run.real[good]
+    assert np.array_equal(a2c[rows], Q.pack_nibbles(hc))
+    assert np.array_equal(a2s[rows], hs)
+    assert np.array_equal(a2g[rows].view(np.uint32), hg.view(np.uint32))
+    for row in bad:
+        r = run.real[row]
+        assert not a2c[r].any() and not a2s[r].any() and a2g[r] == 0
+    pads = np.nonzero(run.pair[:run.off_np[-1]] < 0)[0]
+    assert len(pads) and not a2s[pads].any() and not a2g[pads].any()
+
+
 def test_combine_stage(run):
     c = run.cfg
     rng = np.random.default_rng(c.T + 1)
