@@ -36,10 +36,9 @@ __device__ __forceinline__ void set_device_error(int* err, int code) {
 // has completed and its writes are visible; at once for a normal launch) and
 // then pdl_launch_dependents() so that the next kernel can be scheduled early
 // too.  The first kernel of a call is launched normally, so it is ordered after
-// whatever the caller queued before; the route sort's first kernel is the one
-// exception: it is launched early as well, and since it triggers its dependents
-// only after its own wait has returned, every later kernel of the call still
-// starts after the caller's work is complete.
+// whatever the caller queued before (a programmatic launch is not ordered after a
+// host-to-device copy); a later kernel may therefore read the call's inputs
+// before its own wait once the kernel before it has passed its wait.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

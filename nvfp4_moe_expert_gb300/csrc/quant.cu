@@ -772,13 +772,13 @@ cudaError_t launch_route_sort_quant_cap(const uint16_t* x, int64_t T, int H, int
     if (E <= kBlockSortMaxE && T * k <= kBlockSortMaxPairs) {
         b.direct_rows = 1;
         const size_t smem = sizeof(int32_t) * kBlockSortWarps * E;
-        e = launch_pdl(true, route_block_sort_kernel, 1, kBlockSortWarps * 32, smem, st, ids, T, E, k, b.pair_rank,
+        e = launch_pdl(false, route_block_sort_kernel, 1, kBlockSortWarps * 32, smem, st, ids, T, E, k, b.pair_rank,
                        b.expert_count, offsets, capacity, err);
         if (e != cudaSuccess) return e;
     } else {
         b.direct_rows = 0;
         const size_t smem = sizeof(int32_t) * kWarpsPerBlock * E;
-        e = launch_pdl(true, route_hist_rank_kernel, static_cast<unsigned>(b.n_chunks), 256, smem, st, ids, T, E, k,
+        e = launch_pdl(false, route_hist_rank_kernel, static_cast<unsigned>(b.n_chunks), 256, smem, st, ids, T, E, k,
                        b.n_chunks, b.chunk_count, b.pair_rank, err);
         if (e != cudaSuccess) return e;
         e = launch_pdl(true, route_scan_kernel, 1, 1024, 0, st, E, b.n_chunks, b.chunk_count, b.chunk_base,
