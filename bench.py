@@ -144,14 +144,16 @@ def stage_work(cfg):
     R = T * k
     row_q = lambda C: C // 2 + C // 16 + 4          # codes + block scales + g of one NVFP4 row
     return {
-        "route_sort_quant": {"bytes": T * (2 * H + k * row_q(H) + 8 * k + 12 * k), "flops": 0},
+        # X read, k routed copies written, ids/probs read, row map/probability/maxima and each
+        # pair's row written
+        "route_sort_quant": {"bytes": T * (2 * H + k * row_q(H) + 8 * k + 16 * k), "flops": 0},
         "fc1_swiglu": {"bytes": E * 2 * I * row_q(H) + R * row_q(H) + R * (2 * I + 4 + 8),
                        "flops": 2 * R * H * 2 * I},
         "requant": {"bytes": R * (2 * I + 4 + 4) + R * row_q(I), "flops": 0},
         "fc2": {"bytes": E * H * row_q(I) + R * row_q(I) + R * 2 * H, "flops": 2 * R * I * H},
         # FC2 with the requantisation fused in: W2, h and its maxima/row map read, y written
         "fc2_requant": {"bytes": E * H * row_q(I) + R * (2 * I + 8) + R * 2 * H, "flops": 2 * R * I * H},
-        "combine": {"bytes": R * 2 * H + T * 2 * H, "flops": 0},
+        "combine": {"bytes": R * (2 * H + 4) + T * 2 * H, "flops": 0},
     }
 
 

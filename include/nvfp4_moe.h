@@ -135,6 +135,8 @@ typedef struct {
     size_t row_pair;      /* int32 [rows_cap]        token*k + slot, -1 for a pad row */
     size_t row_prob;      /* float [rows_cap]        router probability of the row */
     size_t amax2;         /* uint32 [rows_cap]       bits of max|h| of the row (FC2 maxima) */
+    size_t pair_row;      /* int32 [T*k]             routed row of each (token, slot), -1 if
+                                                     the fixed-capacity layout dropped it */
     size_t chunk_count;   /* int32 [E][n_chunks]     route-sort scratch */
     size_t chunk_base;    /* int32 [E][n_chunks]     route-sort scratch */
     size_t pair_rank;     /* int32 [T*k]             route-sort scratch */
@@ -144,7 +146,7 @@ typedef struct {
     size_t a2_codes;      /* uint8 [rows_cap][I/2]   requantised h (FC2 A operand) */
     size_t a2_sf;         /* nvfp4_sf_bytes(rows_cap, I) */
     size_t a2_g;          /* float [rows_cap] */
-    size_t y;             /* bf16 [T][k][H]          FC2 output per (token, slot) */
+    size_t y;             /* bf16 [rows_cap][H]      FC2 output per routed row (pad rows unwritten) */
     size_t total;         /* == moe_workspace_bytes(T, H, I, E, k) */
 } moe_workspace_layout;
 
@@ -163,8 +165,9 @@ size_t moe_workspace_bytes(int64_t T, int H, int I, int E, int k);
  * expert, stable in token-then-slot order; each expert's rows padded to a
  * multiple of 128; each token row read once, its max|x| taken in the same
  * pass, quantised once (as nvfp4_quantize_rows) and written to its k routed
- * rows.  Also records each row's (token, slot) and router probability, and
- * zeroes the FC2 maxima.  Pad rows get zero scales and g = 0.
+ * rows.  Also records each row's (token, slot) and router probability, each
+ * (token, slot)'s row (pair_row), and zeroes the FC2 maxima.  Pad rows get
+ * zero scales and g = 0.
  *
  *  x_dev           BF16 [T][H], 16-byte aligned
  *  topk_ids_dev    int32 [T][k], slot order = top-k order
@@ -203,8 +206,9 @@ nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int
  *  out_dev          the routed-row outputs: the first
  *                   moe_workspace_layout.chunk_count bytes of a workspace laid
  *                   out as moe_workspace_layout_query(T, H, I, E, k) describes
- *                   (codes, scales, g^x, row pair, row probability, FC2 maxima;
- *                   these offsets do not depend on I), 256-byte aligned.  A full
+ *                   (codes, scales, g^x, row pair, row probability, FC2 maxima,
+ *                   pair rows; these offsets do not depend on I), 256-byte
+ *                   aligned.  A full
  *                   workspace can be passed; its scratch part is not touched.
  *  out_bytes        size of out_dev; at least layout.chunk_count
  *
@@ -232,8 +236,9 @@ nvfp4_status moe_route_sort_amax_noalloc(const void* x_dev, int64_t T, int H, in
  * FC1 grouped GEMM (tcgen05 block-scaled FP4, FP32 accumulate) with the
  * epilogue v = (acc*g^x)*g^w, BF16 gate/up, h = bf16(f32(silu(gate)*up)*p)
  * and the row maxima of h; requantisation of h with those maxima; FC2
- * grouped GEMM with the same epilogue, BF16 y per (token, slot); and the
- * combine out[t] = bf16(sum over slots 0..k-1 in order, FP32)
+ * grouped GEMM with the same epilogue, BF16 y per routed row (each tile's
+ * rows written contiguously); and the combine out[t] = bf16(sum over slots
+ * 0..k-1 in order, FP32) of the rows pair_row names
  * [miniTE/differs, miniTE/use, RL/4.4, RL/4.5].  Equivalent to
  * moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_combine_bf16 (bitwise).
  *

@@ -95,6 +95,7 @@ void compute_layout(int64_t T, int H, int I, int E, int k, moe_workspace_layout*
     L->row_pair = take(rc * 4);
     L->row_prob = take(rc * 4);
     L->amax2 = take(rc * 4);
+    L->pair_row = take(R * 4);
     L->chunk_count = take(static_cast<size_t>(E) * L->n_chunks * 4);
     L->chunk_base = take(static_cast<size_t>(E) * L->n_chunks * 4);
     L->pair_rank = take(R * 4);
@@ -104,7 +105,7 @@ void compute_layout(int64_t T, int H, int I, int E, int k, moe_workspace_layout*
     L->a2_codes = take(rc * I / 2);
     L->a2_sf = take(rc * I / 16);
     L->a2_g = take(rc * 4);
-    L->y = take(R * H * 2);
+    L->y = take(rc * H * 2);
     L->total = o;
 }
 
@@ -336,6 +337,7 @@ static nvfp4_status route_impl(const void* x_dev, int64_t T, int H, int E, int k
     b.row_pair = at<int32_t>(ws_dev, L.row_pair);
     b.row_prob = at<float>(ws_dev, L.row_prob);
     b.amax2 = at<uint32_t>(ws_dev, L.amax2);
+    b.pair_row = at<int32_t>(ws_dev, L.pair_row);
     b.chunk_count = at<int32_t>(ws_dev, L.chunk_count);
     b.chunk_base = at<int32_t>(ws_dev, L.chunk_base);
     b.pair_rank = at<int32_t>(ws_dev, L.pair_rank);
@@ -440,7 +442,8 @@ static nvfp4_status moe_combine_bf16_impl(const moe_nvfp4_weights* w, int64_t T,
     if (s != NVFP4_OK) return s;
     if (T == 0) return NVFP4_OK;
     if (!out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
-    return from_cuda(launch_combine(at<uint16_t>(ws_dev, L.y), T, k, w->H, static_cast<uint16_t*>(out_dev),
+    return from_cuda(launch_combine(at<uint16_t>(ws_dev, L.y), at<int32_t>(ws_dev, L.pair_row), T, k, w->H,
+                                    static_cast<uint16_t*>(out_dev),
                                     static_cast<cudaStream_t>(stream), pdl));
 }
 

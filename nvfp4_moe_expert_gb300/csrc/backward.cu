@@ -569,7 +569,7 @@ cudaError_t launch_moe_backward_ste(const BackwardArgs& a, cudaStream_t st) {
     // FC1 dgrad per (token, slot), then the slot-order sum
     e = launch_dgrad(a.dgu, a.w1t, rc, 2 * a.I, a.H, a.E, a.offsets, a.row_pair, kModePairs, a.dx_pairs, a.err, st);
     if (e != cudaSuccess) return e;
-    e = launch_combine(a.dx_pairs, a.T, a.k, a.H, a.dx, st, false);
+    e = launch_combine(a.dx_pairs, nullptr, a.T, a.k, a.H, a.dx, st, false);
     if (e != cudaSuccess) return e;
     // FC2 wgrad: dW2[e] = dy^T h over the expert's rows
     e = launch_transpose<kSrcToken>(a.dout, a.H, 0, a.row_pair, a.k, a.offsets, a.E, rc, a.H, 1, a.dy_t, rc, 0, st);

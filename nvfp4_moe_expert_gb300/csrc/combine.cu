@@ -9,6 +9,11 @@
 // padding, quantisation and cast.  The router probability was already
 // applied before FC2, so the combine is a plain sum.
 //
+// The forward's y holds one row per routed row (FC2 writes each tile's rows contiguously);
+// rows[t*k + s] names the row of token t's slot s (-1 for a pair the fixed-capacity layout
+// dropped, which adds nothing).  The backward's dX pairs are in (token, slot) order (rows =
+// nullptr).
+//
 // HBM-bound: each thread owns 8 consecutive columns of one token (16-byte
 // loads of the k slot rows, all issued before the adds, one 16-byte store);
 // a grid-stride loop over T*H/8 such vectors keeps every access coalesced.
@@ -25,28 +30,45 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 
 // kMaxK > 0: k <= kMaxK slots, all loads issued before the adds (more bytes in flight).
 template <int kMaxK>
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, int64_t T, int k, int H,
-                                                      uint16_t* __restrict__ out) {
-    pdl_wait();
-    pdl_launch_dependents();
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ rows,
+                                                      int64_t T, int k, int H, uint16_t* __restrict__ out) {
     const int vec_per_row = H / 8;
     const int64_t nvec = T * vec_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    // the row numbers of the next vector are loaded while this vector's rows are in flight
+    int32_t rn[kMaxK];
+    auto load_rows = [&](int64_t i) {
+        const int64_t t = i / vec_per_row;
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s) {
+            if (s < k) rn[s] = rows ? __ldg(rows + t * k + s) : static_cast<int32_t>(t * k + s);
+        }
+    };
+    // The first ones even before the wait: the row map comes from the route sort, which is
+    // complete once the kernel before this one (FC2, which triggers after its own wait) has
+    // started; y is read only after the wait.
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < nvec) load_rows(i);
+    pdl_wait();
+    pdl_launch_dependents();
+    for (; i < nvec; i += stride) {
         const int64_t t = i / vec_per_row;
         const int v = static_cast<int>(i - t * vec_per_row);
-        const uint4* src = reinterpret_cast<const uint4*>(y + t * k * H) + v;
+        int32_t r[kMaxK];
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s) r[s] = rn[s];
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
         uint4 w[kMaxK];
 #pragma unroll
         for (int s = 0; s < kMaxK; ++s) {
-            if (s < k) w[s] = __ldcs(src + static_cast<int64_t>(s) * vec_per_row);
+            if (s < k && r[s] >= 0) w[s] = __ldcs(reinterpret_cast<const uint4*>(y + static_cast<int64_t>(r[s]) * H) + v);
         }
+        if (i + stride < nvec) load_rows(i + stride);
 #pragma unroll
         for (int s = 0; s < kMaxK; ++s) {          // slots in top-k order
-            if (s < k) {
+            if (s < k && r[s] >= 0) {
                 const uint32_t ws[4] = {w[s].x, w[s].y, w[s].z, w[s].w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -66,18 +88,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
 }  // namespace
 
-cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st, bool pdl) {
+cudaError_t launch_combine(const uint16_t* y, const int32_t* rows, int64_t T, int k, int H, uint16_t* out,
+                           cudaStream_t st, bool pdl) {
     const int64_t nvec = T * (H / 8);
     if (nvec == 0) return cudaSuccess;
     int64_t blocks = (nvec + 255) / 256;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     const dim3 g(static_cast<unsigned>(blocks));
-    if (k <= 2) return launch_pdl(pdl, combine_kernel<2>, g, 256, 0, st, y, T, k, H, out);
-    if (k <= 4) return launch_pdl(pdl, combine_kernel<4>, g, 256, 0, st, y, T, k, H, out);
-    if (k <= 8) return launch_pdl(pdl, combine_kernel<8>, g, 256, 0, st, y, T, k, H, out);
-    if (k <= 16) return launch_pdl(pdl, combine_kernel<16>, g, 256, 0, st, y, T, k, H, out);
-    return launch_pdl(pdl, combine_kernel<32>, g, 256, 0, st, y, T, k, H, out);
+    if (k <= 2) return launch_pdl(pdl, combine_kernel<2>, g, 256, 0, st, y, rows, T, k, H, out);
+    if (k <= 4) return launch_pdl(pdl, combine_kernel<4>, g, 256, 0, st, y, rows, T, k, H, out);
+    if (k <= 8) return launch_pdl(pdl, combine_kernel<8>, g, 256, 0, st, y, rows, T, k, H, out);
+    if (k <= 16) return launch_pdl(pdl, combine_kernel<16>, g, 256, 0, st, y, rows, T, k, H, out);
+    return launch_pdl(pdl, combine_kernel<32>, g, 256, 0, st, y, rows, T, k, H, out);
 }
 
 }  // namespace nvfp4

@@ -71,6 +71,7 @@ struct RouteBufs {
     int32_t* row_pair;
     float* row_prob;
     uint32_t* amax2;
+    int32_t* pair_row;   // [T*k] routed row of each (token, slot), -1 if dropped
     int32_t* chunk_count;
     int32_t* chunk_base;
     int32_t* pair_rank;
@@ -111,7 +112,7 @@ struct GemmArgs {
     uint32_t* amax2;          // [rows_cap]
     // FC2 outputs
     int H;
-    uint16_t* y;              // [T*k][H]
+    uint16_t* y;              // [rows_cap][H], per routed row
     float* debug;             // optional pre-cast FP32 values
     int* err;
 };
@@ -126,7 +127,10 @@ int fc2_requant_max_e();
 // Copy the FC1 epilogue's 65536-entry SiLU table (FP32, by BF16 bit pattern) to `out`.
 cudaError_t copy_silu_table(float* out, cudaStream_t st);
 
-cudaError_t launch_combine(const uint16_t* y, int64_t T, int k, int H, uint16_t* out, cudaStream_t st, bool pdl);
+// rows: the y row of each (token, slot) (rows[t*k+s], -1 for none), or nullptr for y in
+// (token, slot) order.
+cudaError_t launch_combine(const uint16_t* y, const int32_t* rows, int64_t T, int k, int H, uint16_t* out,
+                           cudaStream_t st, bool pdl);
 
 int device_sm_count();
 

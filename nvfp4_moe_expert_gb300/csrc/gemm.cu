@@ -556,7 +556,7 @@ __global__ void __maxnreg__(96)
             } else {
                 const int H = args.H;
                 float* dbg = args.debug && live ? args.debug + row * H + nt * kBN + 64 * sub : nullptr;
-                uint16_t* yrow = live ? args.y + static_cast<int64_t>(pair) * H + nt * kBN + 64 * sub : nullptr;
+                uint16_t* yrow = live ? args.y + row * H + nt * kBN + 64 * sub : nullptr;
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {            // two 32-column halves, 64 bytes of y each
                     uint32_t packed[16];
@@ -1005,7 +1005,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 tc_fence_after();
                 const int64_t grow = static_cast<int64_t>(mt) * kBM + row;
                 float* dbg = args.debug ? args.debug + grow * H + nt * kBN + 128 * half : nullptr;
-                uint16_t* yrow = live ? args.y + static_cast<int64_t>(pair) * H + nt * kBN + 128 * half : nullptr;
+                uint16_t* yrow = live ? args.y + grow * H + nt * kBN + 128 * half : nullptr;
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
                     // 64 of the warp's 128 accumulator columns at a time; TMEM goes back after the

@@ -431,6 +431,7 @@ __global__ void __launch_bounds__(GPL == 1 ? 128 : 256, GPL == 1 ? 7 : (GPL == 2
         pdl_wait();
         int32_t my_dst = -1;
         if (slot_lane) my_dst = pair_dest_e(b, my_e, E, t * k + rl.li, chunk, capacity);
+        if (slot_lane) b.pair_row[t * k + rl.li] = my_dst;
         if (slot_lane && my_dst >= 0) {   // the routed row's per-row data, one slot per lane
             b.a_g[my_dst] = gr;
             b.row_pair[my_dst] = static_cast<int32_t>(t * k + rl.li);
@@ -445,6 +446,7 @@ __global__ void __launch_bounds__(GPL == 1 ? 128 : 256, GPL == 1 ? 7 : (GPL == 2
                 r = __shfl_sync(rl.mask, my_dst, src0 + j);
             } else {                 // rows narrower than k lanes: look the slot up directly
                 r = pair_dest(b, ids, E, p, chunk, capacity);
+                if (rl.li == 0) b.pair_row[p] = static_cast<int32_t>(r);
                 if (r >= 0 && rl.li == 0) {
                     b.a_g[r] = gr;
                     b.row_pair[r] = static_cast<int32_t>(p);

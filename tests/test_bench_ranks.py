@@ -74,8 +74,10 @@ def test_forward_stage_roofline_arithmetic():
     peaks = {"hbm_gbs": 6791.7, "bf16_tflops": 1916.3}
     c2 = S.CONFIGS["qwen3_30b_a3b"]
     w = bench.stage_work(c2)
-    # per token: X read once, k quantised copies (codes + scales + g), row maps
-    assert w["route_sort_quant"]["bytes"] == 4096 * 13504
+    # per token: X read once, k quantised copies (codes + scales + g), row maps, pair rows
+    assert w["route_sort_quant"]["bytes"] == 4096 * 13536
+    # the combine: k rows of y read (gathered through the pair rows), one output row written
+    assert w["combine"]["bytes"] == 32768 * (4096 + 4) + 4096 * 4096
     # FC1 at 4096 tokens streams every expert's weights once: 201 MB of codes + 25 MB of scales
     assert w["fc1_swiglu"]["bytes"] == 128 * 1536 * (1024 + 128 + 4) + 32768 * (1024 + 128 + 4) + 32768 * (1536 + 12)
     assert w["fc1_swiglu"]["flops"] == 2 * 32768 * 2048 * 1536

@@ -162,8 +162,8 @@ def test_requant_and_fc2_stage(run):
         _, (c2, s2, g2) = run.wq.expert(int(e))
         v_ref[sel] = OM.epilogue_f64(OM.qgemm_f64(hc[sel], hs[sel], c2, s2), hg[sel], g2)
     assert rel_l2(v_gpu, v_ref) <= GEMM_REL_L2
-    y = run.view("y", c.T * c.k * c.H, torch.int16).cpu().numpy().view(np.uint16).reshape(c.T * c.k, c.H)
-    y_rows = y[run.pair[run.real]]
+    y = run.view("y", rc * c.H, torch.int16).cpu().numpy().view(np.uint16).reshape(rc, c.H)
+    y_rows = y[run.real]                                               # y is per routed row
     assert np.array_equal(y_rows, F.round_to_bf16_bits(v_gpu))        # the kernel's own cast
     assert bf16_ulp_distance(y_rows, F.round_to_bf16_bits(v_ref)).max() <= GEMM_BF16_ULP
 
@@ -219,11 +219,19 @@ def test_requant_lane_mappings(I):
 
 
 def test_combine_stage(run):
+    """The combine reads token t's slot s from the routed row the route sort recorded for
+    (t, s); a seeded y is placed at those rows (every other row holds NaN, which must not
+    leak into the output)."""
     c = run.cfg
+    rc = run.lay.rows_cap
     rng = np.random.default_rng(c.T + 1)
     y = S.f32_to_bf16_bits(rng.standard_normal((c.T, c.k, c.H)).astype(np.float32)
                            * np.exp2(rng.uniform(-20, 20, (c.T, c.k, 1))).astype(np.float32))
-    run.view("y", c.T * c.k * c.H, torch.int16).copy_(torch.from_numpy(y.view(np.int16).ravel()).cuda())
+    pair_row = run.view("pair_row", c.T * c.k, torch.int32).cpu().numpy()
+    assert np.array_equal(pair_row[run.pair[run.real]], run.real)      # the inverse of the row map
+    full = np.full((rc, c.H), 0x7FC0, np.uint16)
+    full[pair_row] = y.reshape(c.T * c.k, c.H)
+    run.view("y", rc * c.H, torch.int16).copy_(torch.from_numpy(full.view(np.int16).ravel()).cuda())
     out = torch.empty((c.T, c.H), dtype=torch.bfloat16, device="cuda")
     M.moe_combine_bf16(run.w, c.T, c.k, out, run.ws)
     assert np.array_equal(torch_to_bf16_bits(out), OM.combine_slots(y))

@@ -153,7 +153,7 @@ def test_fc1_and_swiglu(big):
 def test_requant_and_fc2(big):
     c, lay = big.cfg, big.lay
     rc = lay.rows_cap
-    y = big.ws[lay.y:lay.y + 2 * c.T * c.k * c.H].view(torch.int16).view(c.T * c.k, c.H)
+    y = big.ws[lay.y:lay.y + 2 * rc * c.H].view(torch.int16).view(rc, c.H)      # per routed row
     for e in big.experts:
         r, t, s = big.expert_rows(e)
         h_gpu = F.bf16_bits_to_f32(_rows(big.ws, lay.h, rc, 2 * c.I, r).view(np.uint16))
@@ -166,7 +166,7 @@ def test_requant_and_fc2(big):
         _, (c2, s2, gw2) = big.wq.expert(e)
         v_ref = OM.epilogue_f64(OM.qgemm_f64(hc, hs, c2, s2), hg, gw2)
         assert rel_l2(v_gpu, v_ref) <= GEMM_REL_L2, e
-        y_rows = y[torch.from_numpy(t * c.k + s).cuda()].cpu().numpy().view(np.uint16)
+        y_rows = y[torch.from_numpy(r).cuda()].cpu().numpy().view(np.uint16)
         assert np.array_equal(y_rows, F.round_to_bf16_bits(v_gpu)), e
         assert bf16_ulp_distance(y_rows, F.round_to_bf16_bits(v_ref)).max() <= GEMM_BF16_ULP, e
 
@@ -174,8 +174,11 @@ def test_requant_and_fc2(big):
 def test_combine_on_gpu_y(big):
     c, lay = big.cfg, big.lay
     toks = np.sort(np.random.default_rng(1).choice(c.T, 64, replace=False))
-    y = big.ws[lay.y:lay.y + 2 * c.T * c.k * c.H].view(torch.int16).view(c.T, c.k, c.H)
-    y_t = y[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
+    rc = lay.rows_cap
+    y = big.ws[lay.y:lay.y + 2 * rc * c.H].view(torch.int16).view(rc, c.H)
+    pair_row = big.ws[lay.pair_row:lay.pair_row + 4 * c.T * c.k].view(torch.int32).view(c.T, c.k)
+    rows_t = pair_row[torch.from_numpy(toks).cuda()]
+    y_t = y[rows_t.reshape(-1)].view(len(toks), c.k, c.H).cpu().numpy().view(np.uint16)
     got = torch_to_bf16_bits(big.out)[toks]
     assert np.array_equal(got, OM.combine_slots(y_t))
 
@@ -185,13 +188,13 @@ def test_chain_from_x(big):
     sampled experts' (token, slot) rows against the GPU's per-slot outputs."""
     c, lay = big.cfg, big.lay
     rc = lay.rows_cap
-    y = big.ws[lay.y:lay.y + 2 * c.T * c.k * c.H].view(torch.int16).view(c.T * c.k, c.H)
+    y = big.ws[lay.y:lay.y + 2 * rc * c.H].view(torch.int16).view(rc, c.H)
     flips = n = 0
     for e in big.experts:
         r, t, s = big.expert_rows(e)
         ids = np.full((len(t), 1), e, np.int32)
         _, inter = OM.moe_forward(big.L["x"][t], ids, big.L["topk_w"][t, s][:, None], big.wq, keep=True)
-        y_rows = y[torch.from_numpy(t * c.k + s).cuda()].cpu().numpy().view(np.uint16)
+        y_rows = y[torch.from_numpy(r).cuda()].cpu().numpy().view(np.uint16)
         assert rel_l2(F.bf16_bits_to_f32(y_rows), F.bf16_bits_to_f32(inter["y"][:, 0])) <= LAYER_REL_L2, e
         gpu_codes = Q.unpack_nibbles(_rows(big.ws, lay.a2_codes, rc, c.I // 2, r))
         flips += int((gpu_codes != inter["hq"][0]).sum())

@@ -110,10 +110,11 @@ def test_fused_fc2_stage_equals_requant_then_fc2(cfg):
     M.moe_route_sort_amax(bf16_to_torch(L["x"]), torch.from_numpy(L["topk_ids"]).cuda(),
                           torch.from_numpy(L["topk_w"]).cuda(), E, offs, ws)
     M.moe_fc1_swiglu_nvfp4(w, T, k, offs, ws)
-    y_view = ws[lay.y:lay.y + 2 * T * k * H]
+    y_view = ws[lay.y:lay.y + 2 * lay.rows_cap * H]          # per routed row; pad rows unwritten
     d1 = torch.full((lay.rows_cap, H), float("nan"), device="cuda")
     d2 = torch.full((lay.rows_cap, H), float("nan"), device="cuda")
     M.moe_requant_nvfp4(w, T, k, offs, ws)
+    y_view.zero_()
     M.moe_fc2_nvfp4(w, T, k, offs, ws, debug=d1)
     y1 = y_view.clone()
     for _ in range(2):                  # twice: the second call starts from the first one's leftovers
@@ -172,11 +173,14 @@ def test_qwen3_30b_a3b_full_size_sampled():
     ref = OM.moe_forward(L["x"][toks], L["topk_ids"][toks], L["topk_w"][toks], wq)
     assert rel_l2(F.bf16_bits_to_f32(got[toks]), F.bf16_bits_to_f32(ref)) <= LAYER_REL_L2
     # per-slot FC2 outputs of every pair routed to experts {0, 77, 127}
-    y = ws[lay.y:lay.y + cfg.T * cfg.k * cfg.H * 2].view(torch.int16).cpu().numpy().view(np.uint16)
-    y = y.reshape(cfg.T, cfg.k, cfg.H)
+    rc = lay.rows_cap
+    y = ws[lay.y:lay.y + rc * cfg.H * 2].view(torch.int16).cpu().numpy().view(np.uint16).reshape(rc, cfg.H)
+    pair_row = ws[lay.pair_row:lay.pair_row + 4 * cfg.T * cfg.k].view(torch.int32).cpu().numpy()
+    pair_row = pair_row.reshape(cfg.T, cfg.k)
     for e in (0, 77, 127):
         t_e, s_e = np.nonzero(L["topk_ids"] == e)
         sub_ids = np.zeros((len(t_e), 1), np.int32) + e
         sub_w = L["topk_w"][t_e, s_e][:, None]
         _, inter = OM.moe_forward(L["x"][t_e], sub_ids, sub_w, wq, keep=True)
-        assert rel_l2(F.bf16_bits_to_f32(y[t_e, s_e]), F.bf16_bits_to_f32(inter["y"][:, 0])) <= LAYER_REL_L2
+        y_e = y[pair_row[t_e, s_e]]
+        assert rel_l2(F.bf16_bits_to_f32(y_e), F.bf16_bits_to_f32(inter["y"][:, 0])) <= LAYER_REL_L2

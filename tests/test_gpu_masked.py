@@ -98,3 +98,11 @@ def test_masked_capacity_overflow_is_reported(T):
     assert status == (8 if over else 0)
     assert not guard.any()
     assert np.array_equal(off_m.cpu().numpy(), np.arange(cfg.E + 1) * C)
+    # dropped pairs have no row (the combine adds nothing for them); the others name a row of
+    # their expert
+    lay = M.moe_workspace_layout_query_masked(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, C)
+    pair_row = ws_m[lay.pair_row:lay.pair_row + 4 * cfg.T * cfg.k].view(torch.int32).cpu().numpy()
+    flat = ids_np.ravel()
+    kept = pair_row >= 0
+    assert np.all(pair_row[kept] // C == flat[kept])
+    assert (~kept).sum() == np.maximum(np.bincount(flat, minlength=cfg.E) - C, 0).sum()

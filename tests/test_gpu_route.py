@@ -46,6 +46,7 @@ def run_route(x_bits, ids, probs, E, I=128):
         pair=ws_view(ws, L.row_pair, rc, torch.int32).cpu().numpy(),
         prob=ws_view(ws, L.row_prob, rc, torch.float32).cpu().numpy(),
         amax2=ws_view(ws, L.amax2, rc, torch.int32).cpu().numpy(),
+        pair_row=ws_view(ws, L.pair_row, T * k, torch.int32).cpu().numpy(),
     )
     return out
 
@@ -75,6 +76,8 @@ def check_route(x_bits, ids, probs, E):
         assert not r["amax2"][rows].any()
         assert np.all(r["pair"][pads] == -1) and not r["g"][pads].any() and not r["prob"][pads].any()
         assert not sf_rows[pads].any() and not r["amax2"][pads].any()
+        # each (token, slot) knows its row: the inverse of the row map
+        assert np.array_equal(r["pair_row"][want_pairs], rows), f"pair rows of expert {e}"
 
 
 @pytest.mark.parametrize("name,T,H,E,k,routing", [

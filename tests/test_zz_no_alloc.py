@@ -32,7 +32,8 @@ def _lib():
 
 
 def _outputs(buf, offs, lay, H):
-    """Expert offsets and every routed-row output below expert_offsets[E]."""
+    """Expert offsets, every routed-row output below expert_offsets[E] and the row of every
+    (token, slot)."""
     o = offs.cpu().numpy()
     n = int(o[-1])
     b = buf.cpu().numpy()
@@ -51,6 +52,7 @@ def _outputs(buf, offs, lay, H):
         "prob": rows(lay.row_prob, 4),
         "amax2": rows(lay.amax2, 4),
         "sf": b[lay.a_sf:lay.a_sf + n * H // 16],
+        "pair_row": b[lay.pair_row:lay.pair_row + 4 * lay.T * lay.k],
     }
 
 
