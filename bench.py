@@ -46,9 +46,9 @@ def fused_fc2_supported(cfg):
 
 def kernels_per_step(cfg):
     """Launches of one step: the route sort is one block-sort kernel for up to 8192 (token,
-    slot) pairs and E <= 256, else a histogram and a scan kernel; then quantise-scatter, FC1,
-    requant, FC2, combine."""
-    return (1 if cfg.T * cfg.k <= 8192 and cfg.E <= 256 else 2) + 5
+    slot) pairs and E <= 256, else a histogram and a scan kernel; then quantise-scatter, the
+    scale-tile kernel, FC1, requant, FC2, combine."""
+    return (1 if cfg.T * cfg.k <= 8192 and cfg.E <= 256 else 2) + 6
 
 
 def step_stages(cfg):
@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="qwen3_30b_a3b", choices=sorted(S.CONFIGS))
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload's layer with this many tokens instead (small profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--minimal", action="store_true",
@@ -108,7 +110,7 @@ def stored_traffic(cfg):
         return {}
     with open(p) as f:
         d = json.load(f)
-    if d.get("workload") != cfg.name:
+    if d.get("workload") != cfg.name or d.get("tokens", cfg.T) != cfg.T:
         return {}
     out = {}
     for stage, rec in d.get("kernels", {}).items():
@@ -895,6 +897,8 @@ def main():
         print(json.dumps({"value": v, "sample": desc}), flush=True)
         return
     cfg = S.CONFIGS[args.workload]
+    if args.tokens > 0:
+        cfg = S.shrink(cfg, T=args.tokens)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

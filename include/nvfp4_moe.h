@@ -137,6 +137,9 @@ typedef struct {
     size_t amax2;         /* uint32 [rows_cap]       bits of max|h| of the row (FC2 maxima) */
     size_t pair_row;      /* int32 [T*k]             routed row of each (token, slot), -1 if
                                                      the fixed-capacity layout dropped it */
+    size_t a_sf_rows;     /* uint8 [rows_cap][H/16]  route-sort scratch: the routed rows' block
+                                                     scales row-major, before they are arranged
+                                                     into a_sf's tiles */
     size_t chunk_count;   /* int32 [E][n_chunks]     route-sort scratch */
     size_t chunk_base;    /* int32 [E][n_chunks]     route-sort scratch */
     size_t pair_rank;     /* int32 [T*k]             route-sort scratch */
@@ -207,8 +210,8 @@ nvfp4_status moe_route_sort_amax(const void* x_dev, int64_t T, int H, int E, int
  *                   moe_workspace_layout.chunk_count bytes of a workspace laid
  *                   out as moe_workspace_layout_query(T, H, I, E, k) describes
  *                   (codes, scales, g^x, row pair, row probability, FC2 maxima,
- *                   pair rows; these offsets do not depend on I), 256-byte
- *                   aligned.  A full
+ *                   pair rows, row-major scales; these offsets do not depend on
+ *                   I), 256-byte aligned.  A full
  *                   workspace can be passed; its scratch part is not touched.
  *  out_bytes        size of out_dev; at least layout.chunk_count
  *

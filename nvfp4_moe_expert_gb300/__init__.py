@@ -52,7 +52,7 @@ class moe_workspace_layout(ctypes.Structure):
         ("E", ctypes.c_int32), ("k", ctypes.c_int32),
         ("rows_cap", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
     ] + [(n, ctypes.c_size_t) for n in (
-        "a_codes", "a_sf", "a_g", "row_pair", "row_prob", "amax2", "pair_row", "chunk_count", "chunk_base",
+        "a_codes", "a_sf", "a_g", "row_pair", "row_prob", "amax2", "pair_row", "a_sf_rows", "chunk_count", "chunk_base",
         "pair_rank", "expert_count", "route_end", "h", "a2_codes", "a2_sf", "a2_g", "y", "total")]
 
 

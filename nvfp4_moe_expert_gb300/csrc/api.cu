@@ -96,6 +96,7 @@ void compute_layout(int64_t T, int H, int I, int E, int k, moe_workspace_layout*
     L->row_prob = take(rc * 4);
     L->amax2 = take(rc * 4);
     L->pair_row = take(R * 4);
+    L->a_sf_rows = take(rc * H / 16);
     L->chunk_count = take(static_cast<size_t>(E) * L->n_chunks * 4);
     L->chunk_base = take(static_cast<size_t>(E) * L->n_chunks * 4);
     L->pair_rank = take(R * 4);
@@ -338,6 +339,8 @@ static nvfp4_status route_impl(const void* x_dev, int64_t T, int H, int E, int k
     b.row_prob = at<float>(ws_dev, L.row_prob);
     b.amax2 = at<uint32_t>(ws_dev, L.amax2);
     b.pair_row = at<int32_t>(ws_dev, L.pair_row);
+    b.a_sf_rows = at<uint8_t>(ws_dev, L.a_sf_rows);
+    b.rows_cap = L.rows_cap;
     b.chunk_count = at<int32_t>(ws_dev, L.chunk_count);
     b.chunk_base = at<int32_t>(ws_dev, L.chunk_base);
     b.pair_rank = at<int32_t>(ws_dev, L.pair_rank);

@@ -23,6 +23,12 @@ __host__ __device__ inline size_t sf_offset(int64_t r, int64_t b, int64_t cols) 
                                ((r & 127) >> 5) * 4 + (b & 3));
 }
 
+// Byte of block scale (row r, 16-element block b) in the row-major scale layout of the routed
+// activation operands: [rows][cols/16].
+__host__ __device__ inline size_t sf_row_offset(int64_t r, int64_t b, int64_t cols) {
+    return static_cast<size_t>(r * (cols / 16) + b);
+}
+
 // Record a device-side error (first one wins).
 __device__ __forceinline__ void set_device_error(int* err, int code) {
     if (err) atomicCAS(err, 0, code);
@@ -67,6 +73,7 @@ constexpr long long kWaitBudgetCycles = 4000000000LL;
 struct RouteBufs {
     uint8_t* a_codes;
     uint8_t* a_sf;
+    uint8_t* a_sf_rows;  // [rows_cap][H/16] the scatter's scales, row-major, before the tile step
     float* a_g;
     int32_t* row_pair;
     float* row_prob;
@@ -77,6 +84,7 @@ struct RouteBufs {
     int32_t* pair_rank;
     int32_t* expert_count;
     int64_t n_chunks;
+    int64_t rows_cap;
     int direct_rows;   // set by the route launcher: pair_rank holds destination rows
 };
 

@@ -42,13 +42,24 @@ __host__ __device__ __forceinline__ int expert_id_bits(int E) {
 
 // The group's 32 bytes of codes go out in one 32-byte store (a whole sector: fewer,
 // fuller L2 write transactions than two 16-byte halves), its scale word in one 4-byte store.
-__device__ __forceinline__ void store_group(const GroupQ& q, int64_t r, int grp, int cols, uint8_t* codes,
-                                            uint8_t* sf) {
+__device__ __forceinline__ void store_codes(const GroupQ& q, int64_t r, int grp, int cols, uint8_t* codes) {
     uint8_t* c = codes + r * static_cast<int64_t>(cols / 2) + grp * 32;
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(c), "r"(q.code[0]), "r"(q.code[1]),
                  "r"(q.code[2]), "r"(q.code[3]), "r"(q.code[4]), "r"(q.code[5]), "r"(q.code[6]), "r"(q.code[7])
                  : "memory");
+}
+// Scales in the 512-byte scale tiles (weights: the GEMM copies their tiles as they are).
+__device__ __forceinline__ void store_group(const GroupQ& q, int64_t r, int grp, int cols, uint8_t* codes,
+                                            uint8_t* sf) {
+    store_codes(q, r, grp, cols, codes);
     *reinterpret_cast<uint32_t*>(sf + sf_offset(r, 4 * grp, cols)) = q.sfw;
+}
+// Scales row-major (routed activations: a row's scale words are contiguous, so a warp's k
+// copies of a token write whole lines; the GEMM rearranges them into tiles per stage).
+__device__ __forceinline__ void store_group_rows(const GroupQ& q, int64_t r, int grp, int cols, uint8_t* codes,
+                                                 uint8_t* sf) {
+    store_codes(q, r, grp, cols, codes);
+    *reinterpret_cast<uint32_t*>(sf + sf_row_offset(r, 4 * grp, cols)) = q.sfw;
 }
 
 template <int GPL>
@@ -402,7 +413,7 @@ __global__ void __launch_bounds__(GPL == 1 ? 128 : 256, GPL == 1 ? 7 : (GPL == 2
         }
         for (int64_t r = r0; r < r1; ++r) {
             for (int grp = lane; grp < G; grp += 32)
-                *reinterpret_cast<uint32_t*>(b.a_sf + sf_offset(r, 4 * grp, H)) = 0u;
+                *reinterpret_cast<uint32_t*>(b.a_sf_rows + sf_row_offset(r, 4 * grp, H)) = 0u;
         }
         return;
     }
@@ -458,9 +469,58 @@ __global__ void __launch_bounds__(GPL == 1 ? 128 : 256, GPL == 1 ? 7 : (GPL == 2
 #pragma unroll
             for (int i = 0; i < GPL; ++i) {
                 const int grp = rl.li + rl.LPR * i;
-                if (grp < G) store_group(q[i], r, grp, H, b.a_codes, b.a_sf);
+                if (grp < G) store_group_rows(q[i], r, grp, H, b.a_codes, b.a_sf_rows);
             }
         }
+    }
+}
+
+// ------------------------------------------------------------------ scale tiles
+// The scatter writes each routed copy's block scales row-major (a copy's scale words are one
+// contiguous line instead of 32 words in 32 different 512-byte tiles); this kernel rearranges
+// them into the tiles FC1 copies into TMEM.  A block takes one m-tile (128 rows) and `chunk`
+// K=64 blocks (4 to 32, chosen on the host for about 4096 blocks): each thread loads its row's
+// 4 * chunk bytes (16-byte loads, all in flight), and after a barrier the block writes the
+// chunk's tiles contiguously, one 16-byte slot per thread and step (slot s of tile j: the
+// K-block j words of rows s, s + 32, s + 64, s + 96).  Only rows below expert_offsets[E] are
+// touched (FC1 reads no others).
+constexpr int kTileMaxChunk = 32;
+
+__global__ void __launch_bounds__(128) route_scale_tiles_kernel(const uint8_t* __restrict__ rows_sf,
+                                                                 uint8_t* __restrict__ sf, int H, int chunk,
+                                                                 const int32_t* __restrict__ offsets, int E) {
+    extern __shared__ uint32_t s_rows[];                    // [kTileM][chunk + 1]: odd pitch, conflict-free column reads
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t mt = blockIdx.x;
+    if (mt * kTileM >= __ldg(offsets + E)) return;
+    const int tid = threadIdx.x;
+    const int W = H / 64;                                   // scale words per row
+    const int j0 = static_cast<int>(blockIdx.y) * chunk;
+    const int n = min(chunk, W - j0);                      // a multiple of 4 (H % 256 == 0)
+    const uint4* row =
+        reinterpret_cast<const uint4*>(rows_sf + (mt * kTileM + tid) * static_cast<int64_t>(H / 16)) + j0 / 4;
+    uint4 v[kTileMaxChunk / 4];
+#pragma unroll
+    for (int c = 0; c < kTileMaxChunk / 4; ++c)
+        if (4 * c < n) v[c] = __ldg(row + c);
+#pragma unroll
+    for (int c = 0; c < kTileMaxChunk / 4; ++c) {
+        if (4 * c < n) {
+            uint32_t* dst = s_rows + tid * (chunk + 1) + 4 * c;
+            dst[0] = v[c].x;
+            dst[1] = v[c].y;
+            dst[2] = v[c].z;
+            dst[3] = v[c].w;
+        }
+    }
+    __syncthreads();
+    uint4* tiles = reinterpret_cast<uint4*>(sf + (mt * W + j0) * kSfAtomBytes);
+    for (int i = tid; i < 32 * n; i += kTileM) {
+        const int j = i >> 5, slot = i & 31;
+        tiles[j * (kSfAtomBytes / 16) + slot] =
+            make_uint4(s_rows[slot * (chunk + 1) + j], s_rows[(slot + 32) * (chunk + 1) + j],
+                       s_rows[(slot + 64) * (chunk + 1) + j], s_rows[(slot + 96) * (chunk + 1) + j]);
     }
 }
 
@@ -793,13 +853,25 @@ cudaError_t launch_route_sort_quant_cap(const uint16_t* x, int64_t T, int H, int
         const int64_t wanted = (warps_for_rows(T, G) + 3) / 4;
         const int64_t cap = static_cast<int64_t>(device_sm_count()) * 32;
         const int grid = pad_blocks + static_cast<int>(wanted < 1 ? 1 : (wanted < cap ? wanted : cap));
-        return launch_pdl(true, route_quant_scatter_kernel<1>, grid, 128, 0, st, x, T, H, E, k, ids, probs, offsets, b,
-                          pad_blocks, capacity, err);
+        e = launch_pdl(true, route_quant_scatter_kernel<1>, grid, 128, 0, st, x, T, H, E, k, ids, probs, offsets, b,
+                       pad_blocks, capacity, err);
+    } else {
+        const int pad_blocks = (E + kWarpsPerBlock - 1) / kWarpsPerBlock;
+        const int grid = pad_blocks + grid_for_warps(warps_for_rows(T, G));
+        e = NVFP4_GPL_LAUNCH(true, G, route_quant_scatter_kernel, grid, st, x, T, H, E, k, ids, probs, offsets, b,
+                             pad_blocks, capacity, err);
     }
-    const int pad_blocks = (E + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const int grid = pad_blocks + grid_for_warps(warps_for_rows(T, G));
-    return NVFP4_GPL_LAUNCH(true, G, route_quant_scatter_kernel, grid, st, x, T, H, E, k, ids, probs, offsets, b,
-                            pad_blocks, capacity, err);
+    if (e != cudaSuccess) return e;
+    // one block per (m-tile, chunk of K-blocks) of the capacity, about 4096 blocks in all (few
+    // m-tiles: short blocks, many of them; many m-tiles: longer blocks); blocks past the used
+    // rows return at once
+    const int64_t m_tiles = b.rows_cap / kTileM;
+    const int W = H / 64;
+    int chunk = 4;
+    while (chunk < kTileMaxChunk && chunk < W && m_tiles * W / chunk > 4096) chunk *= 2;
+    const dim3 tg(static_cast<unsigned>(m_tiles), static_cast<unsigned>((W + chunk - 1) / chunk));
+    const size_t smem = sizeof(uint32_t) * kTileM * (chunk + 1);
+    return launch_pdl(true, route_scale_tiles_kernel, tg, kTileM, smem, st, b.a_sf_rows, b.a_sf, H, chunk, offsets, E);
 }
 
 cudaError_t launch_route_sort_quant(const uint16_t* x, int64_t T, int H, int E, int k, const int32_t* ids,

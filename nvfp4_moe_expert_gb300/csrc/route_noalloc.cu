@@ -89,6 +89,8 @@ extern "C" nvfp4_status moe_route_sort_amax_noalloc(const void* x_dev, int64_t T
     b.row_prob = reinterpret_cast<float*>(ws + L.row_prob);
     b.amax2 = reinterpret_cast<uint32_t*>(ws + L.amax2);
     b.pair_row = reinterpret_cast<int32_t*>(ws + L.pair_row);
+    b.a_sf_rows = ws + L.a_sf_rows;
+    b.rows_cap = L.rows_cap;
     b.chunk_count = reinterpret_cast<int32_t*>(scratch);
     b.chunk_base = reinterpret_cast<int32_t*>(scratch + cc_bytes);
     b.pair_rank = reinterpret_cast<int32_t*>(scratch + 2 * cc_bytes);

@@ -12,12 +12,17 @@
 // over all experts renormalised over the k chosen, computed as the softmax over the chosen,
 // p_j = exp(l_j - l_1) / sum_i exp(l_i - l_1) in FP32, the sum in slot order.
 //
-// Kernel (sm_103a): one CTA per 128-token tile.  Warp 0 loads the tile's X rows and all of W_r
-// through TMA (128 bytes of K per row per stage, 128B swizzle, 4-stage ring); warp 1 issues
-// tcgen05.mma.kind::f16 (M=128, N=E, K=16) into an FP32 TMEM accumulator, walking K from 0 to
-// H-1 in one fixed order whatever T is; warps 2-5, one token per thread, copy the token's E
-// logits from TMEM into registers (E <= 128) or into the (then idle) stage buffers, select the
-// top k in k passes and write ids and probabilities.  All waits are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
+// Kernel (sm_103a): a cluster of four CTAs per 128-token tile, one per quarter of H.  In each
+// CTA warp 0 loads the tile's X rows and W_r over its K quarter through TMA (128 bytes of K
+// per row per stage, 128B swizzle, 4-stage ring) and warp 1 issues tcgen05.mma.kind::f16
+// (M=128, N=E, K=16) into an FP32 TMEM accumulator, walking its quarter in one fixed order;
+// warps 2-5 copy the partial logits into shared memory.  After a cluster barrier, CTA c sums
+// rows 32c..32c+31 over the four partials in quarter order, reading the peers' shared memory
+// (distributed shared memory), so a logit is ((q0 + q1) + q2) + q3 whatever T is; one warp per
+// token then picks the top k (k rounds of a warp-wide arg-max) and writes ids and
+// probabilities.  A second cluster barrier keeps every CTA's shared memory alive until its
+// peers have read it; every thread reaches both barriers on every path.  All pipeline waits
+// are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
 #include <cmath>
 #include <mutex>
 
@@ -28,7 +33,8 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kRStages = 4;
-constexpr int kRBM = 128;                               // tokens per CTA
+constexpr int kRSplit = 4;                              // K quarters: the CTAs of one cluster
+constexpr int kRBM = 128;                               // tokens per cluster
 constexpr int kRRowBytes = 128;                         // bytes of K per row per stage (64 BF16)
 constexpr int kRMaxE = 256;
 constexpr int kRABytes = kRBM * kRRowBytes;             // 16 KB
@@ -38,12 +44,34 @@ constexpr int kRBarOff = kRStages * kRStageBytes;
 constexpr int kRSmemBytes = kRBarOff + 128 + 1024;
 constexpr int kRThreads = 192;                          // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr uint32_t kRTmemCols = 256;
-// epilogue staging in the stage buffers: 128 rows of E logits (stride E+1 floats: no bank
-// conflicts when the threads read one column), then 128 rows of 32 selected ids
-constexpr int kRIdsOff = kRBM * (kRMaxE + 1) * 4;
-constexpr int kRSelVOff = kRIdsOff + kRBM * 32 * 4;      // then 128 rows of 32 selected logits
-static_assert(kRSelVOff + kRBM * 32 * 4 <= kRBarOff, "epilogue staging fits in the stage buffers");
-constexpr int kRRegE = 128;                               // up to this many experts: logits in registers
+// after the MMAs, the partial logits sit in the idle stage buffers: 128 rows of E floats at a
+// stride of E + 1 (odd: the row-per-thread stores and the column reads are conflict-free)
+static_assert(kRBM * (kRMaxE + 1) * 4 <= kRBarOff, "partial logits fit in the stage buffers");
+// then each token's picks (32 values, 32 ids) for this CTA's 32 tokens
+constexpr int kRPickOff = kRBM * (kRMaxE + 1) * 4;
+static_assert(kRPickOff + 32 * 32 * 8 <= kRBarOff, "picks fit in the stage buffers");
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster arrives; shared-memory writes before it are visible
+// to the cluster's reads after it.
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address in CTA `rank`'s shared memory of the variable at local shared address `addr`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 // Instruction descriptor of tcgen05.mma kind::f16 with BF16 A and B (both K-major) and an FP32
 // accumulator.
@@ -73,7 +101,7 @@ __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
-__global__ void __launch_bounds__(kRThreads, 1)
+__global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
     router_topk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, int64_t T,
                        int H, int E, int k, int32_t* __restrict__ ids, float* __restrict__ probs,
                        float* __restrict__ logits, int* err) {
@@ -84,7 +112,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
     uint64_t* tmem_full = empty + kRStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* part = reinterpret_cast<float*>(smem);       // [kRBM][E + 1], valid after the MMAs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t split = cluster_ctarank();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRStages; ++s) {
@@ -109,9 +139,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // this CTA's K-blocks of 64: quarter `split` of H / 64 (empty for H < 256 and split 0..)
     const int num_ks = H / 64;
-    const int m0 = static_cast<int>(blockIdx.x) * kRBM;
+    const int ks0 = static_cast<int>(split) * num_ks / kRSplit;
+    const int ks_per = (static_cast<int>(split) + 1) * num_ks / kRSplit - ks0;
+    const int m0 = static_cast<int>(blockIdx.x / kRSplit) * kRBM;
     const uint32_t b_bytes = static_cast<uint32_t>(E) * kRRowBytes;
+    const int row_stride = E + 1;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (warp-uniform)
@@ -120,7 +154,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         int stage = 0;
         uint32_t phase = 0, issued = 0, issued_parity = 0;
         bool failed = false;
-        for (int ks = 0; ks < num_ks; ++ks) {
+        for (int ks = ks0; ks < ks0 + ks_per; ++ks) {
             const bool ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetCycles);
             if (!__all_sync(0xFFFFFFFFu, ok)) {
                 failed = true;
@@ -150,7 +184,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool failed = false, issued_any = false;
-        for (int ks = 0; ks < num_ks; ++ks) {
+        for (int ks = ks0; ks < ks0 + ks_per; ++ks) {
             const bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetCycles);
             if (!__all_sync(0xFFFFFFFFu, ok)) {
                 failed = true;
@@ -162,7 +196,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
             const uint64_t bdesc = sdesc_k_swizzled<128>(st + kRABytes);
 #pragma unroll
             for (int j = 0; j < 4; ++j)   // K = 16 BF16 (32 bytes) per MMA
-                tc_mma_bf16_elect(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (ks | j) != 0 ? 1u : 0u);
+                tc_mma_bf16_elect(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (ks != ks0 || j != 0) ? 1u : 0u);
             issued_any = true;
             tc_commit_elect(&empty[stage]);
             if (++stage == kRStages) {
@@ -181,147 +215,133 @@ __global__ void __launch_bounds__(kRThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue: one token per thread
+        // ------------------------------------------------------------ partial logits to shared memory
         const int q = warp & 3;                             // TMEM lane quarter
         const int r = q * 32 + lane;                        // row of the tile
-        const int64_t t = m0 + r;
         const bool ok = mbar_wait_bounded(tmem_full, 0, abort_flag, kWaitBudgetCycles);
-        if (!__all_sync(0xFFFFFFFFu, ok)) {
+        if (ks_per == 0) {                                  // an empty quarter adds zeros
+            for (int c = 0; c < E; ++c) part[r * row_stride + c] = 0.0f;
+        } else if (!__all_sync(0xFFFFFFFFu, ok)) {
             if (lane == 0) set_device_error(err, NVFP4_ERR_DEVICE_TIMEOUT);
             *abort_flag = 1;
         } else {
             tc_fence_after();
             // every MMA has completed, so no copy or MMA touches the stage buffers any more
-            int32_t* sel = reinterpret_cast<int32_t*>(smem + kRIdsOff) + r * 32;
-            float* selv = reinterpret_cast<float*>(smem + kRSelVOff) + r * 32;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            bool finite = true;
-            // one 16-column chunk of the token's logits from TMEM (E % 16 == 0: every column
-            // read is a logit), optionally stored to the logits output
-            auto load16 = [&](int c, uint32_t (&v)[16]) {
+            float* row = part + r * row_stride;
+            for (int c = 0; c < E; c += 16) {                // E % 16 == 0
+                uint32_t v[16];
                 tmem_ld_32x32b_x16(taddr + c, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) finite = finite && (v[i] & 0x7F800000u) != 0x7F800000u;
-                if (logits != nullptr && t < T) {
-                    float* dst = logits + t * E + c;    // 64-byte aligned (E % 16 == 0, base 32-aligned)
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * u),
-                                     "r"(v[8 * u]), "r"(v[8 * u + 1]), "r"(v[8 * u + 2]), "r"(v[8 * u + 3]),
-                                     "r"(v[8 * u + 4]), "r"(v[8 * u + 5]), "r"(v[8 * u + 6]), "r"(v[8 * u + 7])
-                                     : "memory");
-                    }
-                }
-            };
-            // k passes; each takes the first entry (in selection order) after the previous
-            // pick, scanning in eight independent chains (columns e = 8m + u) merged at the
-            // end: the same pick as one chain over all columns, with 8x shorter dependencies
-            auto merge = [&](const float (&bv)[8], const int (&bid)[8], float& best_v, int& best_id) {
-                best_v = bv[0];
-                best_id = bid[0];
-#pragma unroll
-                for (int u = 1; u < 8; ++u) {
-                    if (bid[u] >= 0 && (best_id < 0 || before(bv[u], bid[u], best_v, best_id))) {
-                        best_v = bv[u];
-                        best_id = bid[u];
-                    }
-                }
-            };
-            if (E <= kRRegE) {
-                // logits in registers (E <= 128)
-                float lv[kRRegE];
-#pragma unroll
-                for (int c = 0; c < kRRegE / 16; ++c) {
-                    if (16 * c < E) {
-                        uint32_t v[16];
-                        load16(16 * c, v);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) lv[16 * c + i] = __uint_as_float(v[i]);
-                    }
-                }
-                if (t < T) {
-                    float pv = INFINITY;
-                    int pid = -1;
-                    for (int j = 0; j < k; ++j) {
-                        float bv[8];
-                        int bid[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            bv[u] = -INFINITY;
-                            bid[u] = -1;
-                        }
-#pragma unroll
-                        for (int e = 0; e < kRRegE; ++e) {
-                            if (e < E) {
-                                const int u = e & 7;
-                                const float v = lv[e];
-                                const bool after = v < pv || (v == pv && e > pid);
-                                if (after && (bid[u] < 0 || before(v, e, bv[u], bid[u]))) {
-                                    bv[u] = v;
-                                    bid[u] = e;
-                                }
-                            }
-                        }
-                        merge(bv, bid, pv, pid);
-                        sel[j] = pid;
-                        selv[j] = pv;
-                    }
-                }
-            } else {
-                // logits staged in shared memory (rows of stride E+1 floats: no bank conflicts)
-                float* row = reinterpret_cast<float*>(smem) + r * (kRMaxE + 1);
-                for (int c = 0; c < E; c += 16) {
-                    uint32_t v[16];
-                    load16(c, v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) row[c + i] = __uint_as_float(v[i]);
-                }
-                if (t < T) {
-                    float pv = INFINITY;
-                    int pid = -1;
-                    for (int j = 0; j < k; ++j) {
-                        float bv[8];
-                        int bid[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            bv[u] = -INFINITY;
-                            bid[u] = -1;
-                        }
-                        for (int e0 = 0; e0 < E; e0 += 8) {   // E % 16 == 0
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const int e = e0 + u;
-                                const float v = row[e];
-                                const bool after = v < pv || (v == pv && e > pid);
-                                if (after && (bid[u] < 0 || before(v, e, bv[u], bid[u]))) {
-                                    bv[u] = v;
-                                    bid[u] = e;
-                                }
-                            }
-                        }
-                        merge(bv, bid, pv, pid);
-                        sel[j] = pid;
-                        selv[j] = pv;
-                    }
-                }
-            }
-            if (t < T) {
-                if (!finite) set_device_error(err, NVFP4_ERR_NONFINITE);
-                const float l1 = sel[0] < 0 ? 0.0f : selv[0];
-                float sum = 0.0f;
-                for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, sel[j] < 0 ? 0.0f : expf(__fsub_rn(selv[j], l1)));
-                for (int j = 0; j < k; ++j) {
-                    const int id = sel[j];
-                    ids[t * k + j] = id < 0 ? 0 : id;
-                    probs[t * k + j] = id < 0 ? 0.0f : __fdiv_rn(expf(__fsub_rn(selv[j], l1)), sum);
-                }
+                for (int i = 0; i < 16; ++i) row[c + i] = __uint_as_float(v[i]);
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    cluster_barrier();                                      // every CTA's partial logits are in place
+
+    if (warp >= 2) {
+        // ------------------------------------------------------------ sum, top-k, probabilities
+        // This CTA's rows 32*split .. +31 of the tile, four threads per token: thread q of a
+        // token holds the logits of experts q, q + 4, q + 8, ... (each the four quarters'
+        // partials added in quarter order), scans them itself each round and the four
+        // candidates are merged by two shuffles, so every thread knows every pick.
+        constexpr int kPer = kRMaxE / 4;
+        const int tid = threadIdx.x - 64;                   // 0..127
+        const int ti = tid >> 2, q = tid & 3;
+        const int r = 32 * static_cast<int>(split) + ti;
+        const int64_t t = m0 + r;
+        uint32_t peer[kRSplit];
+#pragma unroll
+        for (int s = 0; s < kRSplit; ++s) peer[s] = cluster_map(smem_u32(part), static_cast<uint32_t>(s));
+        float v[kPer];
+        bool finite = true;
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+            const int e = q + 4 * m;
+            v[m] = -INFINITY;
+            if (e < E) {
+                const uint32_t off = static_cast<uint32_t>(r * row_stride + e) * 4u;
+                float a = ld_cluster_f32(peer[0] + off);
+#pragma unroll
+                for (int s = 1; s < kRSplit; ++s) a = __fadd_rn(a, ld_cluster_f32(peer[s] + off));
+                v[m] = a;
+                if (t < T) {
+                    finite = finite && (__float_as_uint(a) & 0x7F800000u) != 0x7F800000u;
+                    if (logits != nullptr) logits[t * E + e] = a;
+                }
+            }
+        }
+        if (!finite) set_device_error(err, NVFP4_ERR_NONFINITE);
+        // k rounds: each takes the first entry, in (logit desc, id asc) order, after the
+        // previous pick; four independent chains per thread, merged, then over the four threads
+        float* pick_v = reinterpret_cast<float*>(smem + kRPickOff) + ti * 32;
+        int* pick_id = reinterpret_cast<int*>(smem + kRPickOff + 32 * 32 * 4) + ti * 32;
+        float pv = INFINITY;
+        int pid = -1;
+        for (int j = 0; j < k; ++j) {
+            float cv[4];
+            int cid[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                cv[u] = -INFINITY;
+                cid[u] = -1;
+            }
+#pragma unroll
+            for (int m = 0; m < kPer; ++m) {
+                const int e = q + 4 * m, u = m & 3;
+                if (e < E) {
+                    const bool after = v[m] < pv || (v[m] == pv && e > pid);
+                    if (after && (cid[u] < 0 || before(v[m], e, cv[u], cid[u]))) {
+                        cv[u] = v[m];
+                        cid[u] = e;
+                    }
+                }
+            }
+            float bv = cv[0];
+            int bid = cid[0];
+#pragma unroll
+            for (int u = 1; u < 4; ++u) {
+                if (cid[u] >= 0 && (bid < 0 || before(cv[u], cid[u], bv, bid))) {
+                    bv = cv[u];
+                    bid = cid[u];
+                }
+            }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+                const int oid = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
+                if (oid >= 0 && (bid < 0 || before(ov, oid, bv, bid))) {
+                    bv = ov;
+                    bid = oid;
+                }
+            }
+            pv = bv;
+            pid = bid;
+            if (q == 0) {
+                pick_v[j] = bv;
+                pick_id[j] = bid;
+            }
+        }
+        __syncwarp();
+        // p_j = exp(l_j - l_1) / sum over the picks in slot order, in FP32 (each of the token's
+        // threads sums the same terms in the same order); thread q writes slots q, q + 4, ...
+        const float l1 = pick_id[0] < 0 ? 0.0f : pick_v[0];
+        float sum = 0.0f;
+        for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, pick_id[j] < 0 ? 0.0f : expf(__fsub_rn(pick_v[j], l1)));
+        if (t < T) {
+            for (int j = q; j < k; j += 4) {
+                const int id = pick_id[j];
+                ids[t * k + j] = id < 0 ? 0 : id;
+                probs[t * k + j] = id < 0 ? 0.0f : __fdiv_rn(expf(__fsub_rn(pick_v[j], l1)), sum);
+            }
+        }
+    }
+
+    cluster_barrier();                                      // the peers are done reading this CTA's shared memory
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kRTmemCols);
@@ -383,7 +403,7 @@ cudaError_t launch_router_topk(const uint16_t* x, int64_t T, int H, const uint16
     }
     CUtensorMap mx, mw;
     if (!make_bf16_map(&mx, x, T, H, kRBM) || !make_bf16_map(&mw, w, E, H, E)) return cudaErrorInvalidValue;
-    const unsigned grid = static_cast<unsigned>((T + kRBM - 1) / kRBM);
+    const unsigned grid = static_cast<unsigned>((T + kRBM - 1) / kRBM * kRSplit);   // whole clusters
     return launch_pdl(false, router_topk_kernel, grid, kRThreads, kRSmemBytes, st, mx, mw, T, H, E, k, ids, probs,
                       logits, err);
 }

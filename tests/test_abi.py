@@ -69,7 +69,8 @@ def test_workspace_layout(lib):
     L = M.moe_workspace_layout_query(4096, 2048, 768, 128, 8)
     assert L.rows_cap % 128 == 0 and L.rows_cap >= 4096 * 8
     assert L.rows_cap <= 4096 * 8 + 128 * 128
-    offs = [L.a_codes, L.a_sf, L.a_g, L.row_pair, L.row_prob, L.amax2, L.pair_row, L.chunk_count, L.chunk_base,
+    offs = [L.a_codes, L.a_sf, L.a_g, L.row_pair, L.row_prob, L.amax2, L.pair_row, L.a_sf_rows, L.chunk_count,
+            L.chunk_base,
             L.pair_rank, L.expert_count, L.route_end, L.h, L.a2_codes, L.a2_sf, L.a2_g, L.y, L.total]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs)

@@ -65,8 +65,10 @@ def check(x_bits, w_bits, k):
     return ids, p, lg, len(bad)
 
 
+# H = 192 and 320 split H/64 unevenly over the four K quarters (192: the first quarter is
+# empty); E = 48 leaves the upper half of the lanes with one logit each
 @pytest.mark.parametrize("T,H,E,k", [(1, 256, 16, 4), (77, 256, 16, 4), (128, 512, 32, 8), (300, 1024, 64, 8),
-                                     (129, 256, 256, 32)])
+                                     (129, 256, 256, 32), (50, 192, 16, 4), (200, 320, 48, 5)])
 def test_router_small_shapes(T, H, E, k):
     cfg = S.LayerConfig("router_test", H=H, I=128, E=E, k=k, T=T, seed=T + H + E)
     check(S.make_x(cfg), S.make_router_weights(cfg), k)
