@@ -106,3 +106,37 @@ def test_masked_capacity_overflow_is_reported(T):
     kept = pair_row >= 0
     assert np.all(pair_row[kept] // C == flat[kept])
     assert (~kept).sum() == np.maximum(np.bincount(flat, minlength=cfg.E) - C, 0).sum()
+
+
+def test_masked_dropped_pairs_add_nothing():
+    """With experts over capacity, each dropped (token, slot) pair has no row and the combine adds
+    nothing for it: the output equals the contiguous layout's with those pairs' router
+    probabilities set to zero (their h, and so their y, are zero rows), compared as values
+    (+0 and -0 alike)."""
+    cfg = S.shrink(S.CONFIGS["qwen3_30b_a3b"], T=1024)
+    L, w, x, ids, pw = layer_inputs(cfg)
+    ids[:, 0] = 5                              # experts 5 and 6 get over 1024 pairs each
+    ids[:, 1] = 6
+    C = 256
+    dev = x.device
+    ws_m = M.alloc_workspace_masked(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, C)
+    off_m = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    out_m = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    M.moe_route_sort_amax_masked(x, ids, pw, cfg.E, C, off_m, ws_m)
+    assert M.nvfp4_get_device_error() == 8     # NVFP4_ERR_CAPACITY
+    M.moe_expert_forward_nvfp4_masked(w, cfg.T, cfg.k, C, off_m, out_m, ws_m)
+    assert M.nvfp4_get_device_error() == 0
+    lay = M.moe_workspace_layout_query_masked(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, C)
+    pair_row = ws_m[lay.pair_row:lay.pair_row + 4 * cfg.T * cfg.k].view(torch.int32).view(cfg.T, cfg.k)
+    dropped = pair_row < 0
+    counts = np.bincount(ids.cpu().numpy().ravel(), minlength=cfg.E)
+    assert int(dropped.sum()) == np.maximum(counts - C, 0).sum() > 0
+    pw0 = pw.clone()
+    pw0[dropped] = 0.0
+    ws_c = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    off_c = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    out_c = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    M.moe_route_sort_amax(x, ids, pw0, cfg.E, off_c, ws_c)
+    M.moe_expert_forward_nvfp4(w, cfg.T, cfg.k, off_c, out_c, ws_c)
+    assert M.nvfp4_get_device_error() == 0
+    assert torch.equal(out_m.float(), out_c.float())
