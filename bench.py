@@ -223,7 +223,7 @@ def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
 
 def backward_work(cfg):
     """Algorithmic FLOPs and bytes of one moe_expert_backward_ste call: four BF16 GEMMs
-    (2RHI, 2R(2I)H, 2RHI, 2R(2I)H FLOPs); the transposed BF16 weights read once, the FP32
+    (2RHI, 2R(2I)H, 2RHI, 2R(2I)H FLOPs); the BF16 weights read once, the FP32
     weight gradients written once, x, dOut, the saved h (BF16) and FC1 values (FP32) read,
     dX and dprob written."""
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
@@ -845,9 +845,9 @@ def run_ours(args, cfg, rank, world, local_rank):
 def backward_step(M, torch, cfg, weights, w1, w2, x, ids, pw, ws, offs, flush, stream, dev, to_dev, n, peaks,
                   peak_kind):
     """CUDA-event time of moe_expert_backward_ste (four BF16 grouped GEMMs, the SwiGLU x prob
-    derivative, transposes and the slot-order sum) on this workload, L2 flushed between calls."""
+    derivative, two row gathers and the slot-order sum) on this workload, L2 flushed between calls."""
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
-    wt = M.MoEWeightsBF16T(w1, w2)
+    wt = M.MoEWeightsBF16(w1, w2)
     lay = M.moe_workspace_layout_query(T, H, I, E, k)
     fc1_pre = torch.empty((lay.rows_cap, 2 * I), dtype=torch.float32, device=dev)
     dout = to_dev(S.make_grad_out(cfg))

@@ -357,20 +357,15 @@ nvfp4_status moe_router_topk(const void* x_dev, int64_t T, int H, const void* w_
  *   dW1[e]       = sum over e's rows of [dgate, dup][r]^T x[t(r)]        FP32
  * A token's dX and dprob do not depend on the other tokens of the batch. */
 
-/* The BF16 original weights, transposed per expert (nvfp4_transpose_bf16), so that the
- * backward GEMMs read them K-major:
- *   w1t  BF16 [E][H][2I], w1t[e][h][j] = W1[e][j][h]  (16-byte aligned)
- *   w2t  BF16 [E][I][H],  w2t[e][i][h] = W2[e][h][i]  (16-byte aligned) */
+/* The BF16 original weights, as given to the weight quantiser; the backward GEMMs read them in
+ * place (MN-major operands):
+ *   w1  BF16 [E][2I][H], gate rows then up rows per expert  (16-byte aligned)
+ *   w2  BF16 [E][H][I]                                      (16-byte aligned) */
 typedef struct {
-    const void* w1t;
-    const void* w2t;
+    const void* w1;
+    const void* w2;
     int32_t E, H, I;
 } moe_bf16_weights_t;
-
-/* out[b][c][r] = in[b][r][c] for BF16 matrices; rows % 64 == 0, cols % 64 == 0,
- * batch <= 65535, rows and cols <= 2^26; in and out 16-byte aligned and not overlapping. */
-nvfp4_status nvfp4_transpose_bf16(const void* in_dev, int64_t batch, int64_t rows, int64_t cols, void* out_dev,
-                                  void* stream);
 
 /* Byte offsets of the backward workspace's scratch buffers (256-byte aligned); rows_cap is
  * the forward layout's. */
@@ -381,10 +376,8 @@ typedef struct {
     size_t dh;        /* bf16 [rows_cap][I] */
     size_t dgu;       /* bf16 [rows_cap][2I] dgate then dup */
     size_t dx_pairs;  /* bf16 [T*k][H]       dX per (token, slot) */
-    size_t dy_t;      /* bf16 [H][rows_cap] */
-    size_t h_t;       /* bf16 [I][rows_cap] */
-    size_t dgu_t;     /* bf16 [2I][rows_cap] */
-    size_t x_t;       /* bf16 [H][rows_cap] */
+    size_t x_rows;    /* bf16 [rows_cap][H]  x gathered per routed row */
+    size_t real_end;  /* int32 [E]           end of each expert's real routed rows */
     size_t total;
 } moe_backward_layout;
 
@@ -392,7 +385,7 @@ nvfp4_status moe_backward_layout_query(int64_t T, int H, int I, int E, int k, mo
 size_t moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k);
 
 /* moe_expert_backward_ste -- the gradients of one forward, from what it saved.
- *  w                    transposed BF16 originals (host struct, device pointers)
+ *  w                    the BF16 originals (host struct, device pointers)
  *  T, k                 as given to the forward
  *  x_dev                BF16 [T][H], the forward's input; 16-byte aligned
  *  dout_dev             BF16 [T][H], the gradient of the forward's output; 16-byte aligned

@@ -9,7 +9,7 @@ entry points have the names of the C ABI in ``include/nvfp4_moe.h``:
     moe_workspace_bytes, moe_workspace_layout_query, nvfp4_sf_bytes,
     nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string, nvfp4_silu_table,
     moe_router_topk, the fixed-capacity moe_*_masked calls, and the
-    straight-through backward: nvfp4_transpose_bf16, moe_backward_layout_query,
+    straight-through backward: moe_backward_layout_query,
     moe_backward_workspace_bytes, moe_expert_backward_ste
 
 There is no CPU fallback: if the library is missing or a call fails, an
@@ -57,7 +57,7 @@ class moe_workspace_layout(ctypes.Structure):
 
 
 class moe_bf16_weights_t(ctypes.Structure):
-    _fields_ = [("w1t", ctypes.c_void_p), ("w2t", ctypes.c_void_p),
+    _fields_ = [("w1", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32)]
 
 
@@ -66,7 +66,7 @@ class moe_backward_layout(ctypes.Structure):
         ("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
         ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("rows_cap", ctypes.c_int64),
     ] + [(n, ctypes.c_size_t) for n in (
-        "dy_rows", "dh", "dgu", "dx_pairs", "dy_t", "h_t", "dgu_t", "x_t", "total")]
+        "dy_rows", "dh", "dgu", "dx_pairs", "x_rows", "real_end", "total")]
 
 
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
@@ -97,7 +97,6 @@ _SIGNATURES = {
     "moe_route_sort_amax_masked": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _SZ, _P]),
     "moe_expert_forward_nvfp4_masked": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _I32, _P, _P, _P,
                                                _SZ, _P]),
-    "nvfp4_transpose_bf16": (_I32, [_P, _I64, _I64, _I64, _P, _P]),
     "moe_backward_layout_query": (_I32, [_I64, _I32, _I32, _I32, _I32, ctypes.POINTER(moe_backward_layout)]),
     "moe_backward_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
     "moe_expert_backward_ste": (_I32, [ctypes.POINTER(moe_bf16_weights_t), _I64, _I32, _P, _P, _P, _P, _SZ, _P,
@@ -354,28 +353,22 @@ def moe_combine_bf16(weights, T, k, out, ws, stream=None):
 
 
 # ---------------------------------------------------------------- straight-through backward
-def nvfp4_transpose_bf16(x, out=None, stream=None):
-    """BF16 [B, R, C] (or [R, C]) -> its per-matrix transpose [B, C, R] ([C, R])."""
-    _need_cuda(x, out)
-    if x.dtype != torch.bfloat16 or x.dim() not in (2, 3):
-        raise ValueError("x must be a 2-D or 3-D bfloat16 tensor")
-    b, r, c = (1,) + tuple(x.shape) if x.dim() == 2 else tuple(x.shape)
-    if out is None:
-        out = torch.empty(tuple(x.shape[:-2]) + (c, r), dtype=torch.bfloat16, device=x.device)
-    _check("nvfp4_transpose_bf16", lib().nvfp4_transpose_bf16(_ptr(x), b, r, c, _ptr(out), _stream(stream)))
-    return out
+class MoEWeightsBF16:
+    """The BF16 original expert weights for the backward (w1 [E, 2I, H], w2 [E, H, I], as
+    given to quantize_moe_weights; the backward's GEMMs read them in place) and the C struct
+    pointing at them."""
 
-
-class MoEWeightsBF16T:
-    """The BF16 original expert weights transposed per expert for the backward
-    (w1t [E, H, 2I], w2t [E, I, H]) and the C struct pointing at them."""
-
-    def __init__(self, w1, w2, stream=None):
+    def __init__(self, w1, w2):
+        if w1.dtype != torch.bfloat16 or w2.dtype != torch.bfloat16 or w1.dim() != 3 or w2.dim() != 3:
+            raise ValueError("w1, w2 must be 3-D bfloat16 tensors")
         self.E, two_i, self.H = w1.shape
         self.I = two_i // 2
-        self.w1t = nvfp4_transpose_bf16(w1.contiguous(), stream=stream)
-        self.w2t = nvfp4_transpose_bf16(w2.contiguous(), stream=stream)
-        self.struct = moe_bf16_weights_t(self.w1t.data_ptr(), self.w2t.data_ptr(), self.E, self.H, self.I)
+        if tuple(w2.shape) != (self.E, self.H, self.I):
+            raise ValueError(f"w2 must be [E, H, I] = {(self.E, self.H, self.I)}, got {tuple(w2.shape)}")
+        self.w1 = w1.contiguous()
+        self.w2 = w2.contiguous()
+        _need_cuda(self.w1, self.w2)
+        self.struct = moe_bf16_weights_t(self.w1.data_ptr(), self.w2.data_ptr(), self.E, self.H, self.I)
 
     def ref(self):
         return ctypes.byref(self.struct)
@@ -447,7 +440,6 @@ class MoELayer:
     def _quantize(self, stream=None):
         self.weights = quantize_moe_weights(*self._w_bf16, stream=stream)
         self.E, self.H, self.I = self.weights.E, self.weights.H, self.weights.I
-        self._wt = None                      # transposed copies for the backward, made on demand
         self._wver = self._weight_version()
         self._gen += 1
 
@@ -496,15 +488,14 @@ class MoELayer:
         x, offs, ws, fc1_pre, T, k, (wver, gen) = self._saved
         if self._weight_version() != wver or self._gen != gen:
             raise RuntimeError("the weights changed after the forward this backward belongs to")
-        if self._wt is None:
-            self._wt = MoEWeightsBF16T(*self._w_bf16, stream=stream)
+        wt = MoEWeightsBF16(*self._w_bf16)
         dev = x.device
         dx = torch.empty((T, self.H), dtype=torch.bfloat16, device=dev)
         dw1 = torch.empty((self.E, 2 * self.I, self.H), dtype=torch.float32, device=dev)
         dw2 = torch.empty((self.E, self.H, self.I), dtype=torch.float32, device=dev)
         dprob = torch.empty((T, k), dtype=torch.float32, device=dev)
         bws = alloc_backward_workspace(T, self.H, self.I, self.E, k, dev)
-        moe_expert_backward_ste(self._wt, T, k, x, dout, offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws,
+        moe_expert_backward_ste(wt, T, k, x, dout, offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws,
                                 stream=stream)
         return dx, dw1, dw2, dprob
 

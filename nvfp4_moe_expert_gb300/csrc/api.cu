@@ -132,10 +132,8 @@ void compute_backward_layout(int64_t T, int H, int I, int E, int k, moe_backward
     B->dh = take(rc * I * 2);
     B->dgu = take(rc * 2 * I * 2);
     B->dx_pairs = take(T * k * H * 2);
-    B->dy_t = take(rc * H * 2);
-    B->h_t = take(rc * I * 2);
-    B->dgu_t = take(rc * 2 * I * 2);
-    B->x_t = take(rc * H * 2);
+    B->x_rows = take(rc * H * 2);
+    B->real_end = take(static_cast<size_t>(E) * 4);
     B->total = o;
 }
 
@@ -533,18 +531,6 @@ nvfp4_status moe_expert_forward_nvfp4_masked(const moe_nvfp4_weights* w, int64_t
     return forward_stages(w, T, k, expert_offsets_dev, out_dev, ws_dev, ws_bytes, stream, capacity);
 }
 
-nvfp4_status nvfp4_transpose_bf16(const void* in_dev, int64_t batch, int64_t rows, int64_t cols, void* out_dev,
-                                  void* stream) {
-    if (batch < 0 || batch > 65535 || rows < 0 || cols < 0 || rows % 64 || cols % 64 || rows > (int64_t(1) << 26) ||
-        cols > (int64_t(1) << 26))
-        return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (batch == 0 || rows == 0 || cols == 0) return NVFP4_OK;
-    if (!in_dev || !out_dev) return NVFP4_ERR_INVALID_ARG;
-    if (!aligned(in_dev, 16) || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
-    return from_cuda(launch_transpose_bf16(static_cast<const uint16_t*>(in_dev), batch, rows, cols,
-                                           static_cast<uint16_t*>(out_dev), static_cast<cudaStream_t>(stream)));
-}
-
 nvfp4_status moe_backward_layout_query(int64_t T, int H, int I, int E, int k, moe_backward_layout* out) {
     if (!out) return NVFP4_ERR_INVALID_ARG;
     if (!moe_shape_ok(T, H, I, E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -566,8 +552,8 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
                                      void* stream) {
     if (!w) return NVFP4_ERR_INVALID_ARG;
     if (!moe_shape_ok(T, w->H, w->I, w->E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (!w->w1t || !w->w2t || !dw1_dev || !dw2_dev) return NVFP4_ERR_INVALID_ARG;
-    if (!aligned(w->w1t, 16) || !aligned(w->w2t, 16) || !aligned(dw1_dev, 32) || !aligned(dw2_dev, 32))
+    if (!w->w1 || !w->w2 || !dw1_dev || !dw2_dev) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(w->w1, 16) || !aligned(w->w2, 16) || !aligned(dw1_dev, 32) || !aligned(dw2_dev, 32))
         return NVFP4_ERR_INVALID_ARG;
     const int H = w->H, I = w->I, E = w->E;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -584,7 +570,7 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
         return NVFP4_ERR_INVALID_ARG;
     moe_workspace_layout L;
     compute_layout(T, H, I, E, k, &L);
-    // the weight-gradient GEMMs address routed rows as byte coordinates (2 per row) in int32
+    // the backward's GEMMs address routed rows as int32 tensor-map coordinates
     if (L.rows_cap >= (int64_t(1) << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     moe_backward_layout B;
     compute_backward_layout(T, H, I, E, k, &B);
@@ -599,8 +585,8 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
     a.E = E;
     a.k = k;
     a.rows_cap = L.rows_cap;
-    a.w1t = static_cast<const uint16_t*>(w->w1t);
-    a.w2t = static_cast<const uint16_t*>(w->w2t);
+    a.w1 = static_cast<const uint16_t*>(w->w1);
+    a.w2 = static_cast<const uint16_t*>(w->w2);
     a.x = static_cast<const uint16_t*>(x_dev);
     a.dout = static_cast<const uint16_t*>(dout_dev);
     a.offsets = expert_offsets_dev;
@@ -616,10 +602,8 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
     a.dh = at<uint16_t>(bwd_ws_dev, B.dh);
     a.dgu = at<uint16_t>(bwd_ws_dev, B.dgu);
     a.dx_pairs = at<uint16_t>(bwd_ws_dev, B.dx_pairs);
-    a.dy_t = at<uint16_t>(bwd_ws_dev, B.dy_t);
-    a.h_t = at<uint16_t>(bwd_ws_dev, B.h_t);
-    a.dgu_t = at<uint16_t>(bwd_ws_dev, B.dgu_t);
-    a.x_t = at<uint16_t>(bwd_ws_dev, B.x_t);
+    a.x_rows = at<uint16_t>(bwd_ws_dev, B.x_rows);
+    a.real_end = at<int32_t>(bwd_ws_dev, B.real_end);
     a.err = err;
     return from_cuda(launch_moe_backward_ste(a, st));
 }

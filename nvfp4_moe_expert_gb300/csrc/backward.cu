@@ -20,14 +20,23 @@
 //   FC2 wgrad  dW2[e] = sum_r dy[r]^T h[r]                  FP32 output
 //   FC1 wgrad  dW1[e] = sum_r [da, du][r]^T x[t(r)]         FP32 output
 //
-// Every GEMM reads both operands K-major through TMA (128B swizzle, 64 BF16 of K per stage)
-// and runs tcgen05.mma.kind::f16 (M=128, N=128 or 256, FP32 accumulator in TMEM): the
-// weights come as per-expert transposed copies made once per weight version
-// (nvfp4_transpose_bf16); for the weight gradients, whose K runs over one expert's routed
-// rows, dy, h, [da, du] and the gathered x are transposed into [feature][routed row] copies
-// first.  One CTA per 128 x N output tile: warp 0 issues the TMA loads, warp 1 the MMAs,
-// warps 2-5 read the accumulator (one row per thread) and store it.  Each tile walks K in
-// one fixed order, so a token's dX and dprob do not depend on the other tokens.
+// The GEMMs read every operand where it lies, without transposed copies: an operand whose
+// reduction index K runs along its rows (the weights W1[e] [2I][H] and W2[e] [H][I] in the
+// activation gradients; dy, h, [da, du] and the gathered x in the weight gradients, whose K is
+// the expert's routed rows) is loaded as 64-row x 128-byte TMA boxes (128B swizzle) and handed
+// to tcgen05.mma.kind::f16 through MN-major shared-memory descriptors; dy and [da, du] in the
+// activation gradients are K-major as stored.  One persistent CTA per SM walks a static tile
+// list: warp 0 issues the TMA loads into a four-stage ring, warp 1 the MMAs (M=128, N=128 or
+// 256) into one of two TMEM accumulators, and warps 2-9 read the other accumulator (two warps
+// per TMEM lane quarter, each half of the columns) and store it, so a tile's stores overlap
+// the next tile's loads and MMAs.  Each tile walks K in one fixed order, so a token's dX and
+// dprob do not depend on the other tokens.
+//
+// Pad rows: the forward's h holds whatever was there before in an expert's pad rows (FC1 does
+// not store them), so the weight gradients stop at each expert's last real row (found once per
+// call from the row map): stages past it are not loaded, and the rows past it in the last
+// stage are zeroed in shared memory before the MMAs read them.
+#include <algorithm>
 #include <mutex>
 
 #include "backward.cuh"
@@ -45,21 +54,26 @@ constexpr int kBMaxN = 256;
 constexpr int kBABytes = kBM * kBRowBytes;              // 16 KB
 constexpr int kBBBytes = kBMaxN * kBRowBytes;           // 32 KB
 constexpr int kBStageBytes = kBABytes + kBBBytes;       // 48 KB
+constexpr int kBMnBox = kBK * kBRowBytes;               // 8 KB: 64 K-rows x 64 MN elements
+constexpr int kBEpiWarps = 8;
+constexpr int kBThreads = 64 + 32 * kBEpiWarps;         // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr uint32_t kBTmemCols = 2 * kBMaxN;             // two accumulators
+constexpr int kBMaxE = 1024;
 constexpr int kBBarOff = kBStages * kBStageBytes;
-constexpr int kBSmemBytes = kBBarOff + 128 + 1024;
-constexpr int kBThreads = 192;                          // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr uint32_t kBTmemCols = 256;
+constexpr int kBOffOff = kBBarOff + 256;                // offsets[0..E] then real_end[0..E)
+constexpr int kBSmemBytes = kBOffOff + 2 * (kBMaxE + 1) * 4 + 1024;
 
 enum : int { kModeRows = 0, kModePairs = 1, kModeWgrad = 2 };
 
-// One launch of the grouped GEMM C = A B^T (A [.][K], B [.][K], both BF16 K-major).
-//  kModeRows  (dgrad): tile (m, n) -> routed rows m*128.., expert e owning them; A rows there,
-//             B rows e*N + n0..; K = num_ks*64 from 0; out_bf16[row][n], row stride N.
-//  kModePairs (dgrad): as kModeRows, but row r goes to out_bf16[row_pair[r]][n] (pad rows
-//             are not stored).
-//  kModeWgrad: tile (e, m, n) -> A rows m*128.. and B rows n0.. of [feature][routed row]
-//             copies, K over expert e's routed rows [offsets[e], offsets[e+1]);
-//             out_f32[e][m][n] (an expert without rows gets zeros).
+// One launch of the grouped GEMM D = A B (FP32 accumulation), K in 64-wide stages.
+//  kModeRows  (dgrad): tile (m, n) -> routed rows m*128.. of expert e (the one owning them);
+//             A = routed rows [rows_cap][K] (K-major), B = weight rows e*K + k, columns n0..
+//             ([E*K][N], MN-major); out_bf16[row][n], row stride N.
+//  kModePairs (dgrad): as kModeRows, but row r goes to out_bf16[row_pair[r]][n] (pad rows are
+//             not stored).
+//  kModeWgrad: tile (e, m, n) -> K over expert e's routed rows offsets[e] .. real_end[e];
+//             A = [rows_cap][M] columns m0.. (MN-major), B = [rows_cap][N] columns n0..
+//             (MN-major); out_f32[e][m][n] (an expert without rows gets zeros).
 struct BgemmJob {
     int mode;
     int BN;             // 128 or 256
@@ -68,24 +82,43 @@ struct BgemmJob {
     int N;              // output columns
     int M;              // wgrad: output rows per expert
     int num_ks;         // dgrad: K / 64
+    int K;              // dgrad: weight rows per expert
     int E;
     const int32_t* offsets;
+    const int32_t* real_end;   // wgrad: end of each expert's real rows
     const int32_t* row_pair;
     uint16_t* out_bf16;
     float* out_f32;
     int* err;
 };
 
-// Instruction descriptor of tcgen05.mma kind::f16: BF16 A and B, both K-major, FP32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_bf16_kmajor(int M, int N) {
+// Instruction descriptor of tcgen05.mma kind::f16: BF16 A and B, FP32 accumulator; a_mn / b_mn
+// select MN-major ("transposed") operands.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
     return (1u << 4)                                  // D format: F32
            | (1u << 7)                                // A format: BF16
            | (1u << 10)                               // B format: BF16
+           | (a_mn ? 1u << 15 : 0u)                   // A major-ness
+           | (b_mn ? 1u << 16 : 0u)                   // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
-// D(tmem, FP32) (+)= A(smem, BF16) x B(smem, BF16)^T, M=128, K=16, issued by the lane
+// Shared-memory descriptor of an MN-major BF16 operand laid out as consecutive 8 KB TMA boxes
+// (each 64 K-rows of 128 bytes = 64 MN elements, 128B swizzle): 8-row groups along K are
+// 1024 bytes apart (stride byte offset), 64-element blocks along MN one box (8 KB) apart
+// (leading byte offset).  Base 1024-byte aligned; a K step of 16 rows advances it 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);        // start address >> 4
+    d |= static_cast<uint64_t>(kBMnBox >> 4) << 16;              // leading byte offset: next MN block
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                 // stride byte offset: next 8 K-rows
+    d |= static_cast<uint64_t>(1) << 46;                         // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                         // 128B swizzle
+    return d;
+}
+
+// D(tmem, FP32) (+)= A(smem, BF16) x B(smem, BF16), M=128, K=16, issued by the lane
 // elect.sync picks while the whole warp executes it in step.
 __device__ __forceinline__ void mma_bf16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                uint32_t accumulate) {
@@ -114,52 +147,84 @@ __device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
                  : "memory");
 }
 
+// Expert owning routed row `row`: largest e < E with off[e] <= row (off in shared memory).
+__device__ __forceinline__ int bwd_expert_of_row(const int32_t* off, int E, int row) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= row) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// The work of tile t (identical in every thread; s_off / s_end in shared memory).
+struct BTile {
+    int e, m0, n0;
+    int a_x;        // A box coordinates: K-major (x = K bytes, y = m0) or MN-major (x = m0 bytes)
+    int b_row;      // first B row of the tile's K range
+    int k0;         // wgrad: first routed row
+    int num_ks;     // stages with real rows
+    int tail;       // real K-rows in the last stage (1..64)
+};
+
+__device__ __forceinline__ BTile bgemm_tile(const BgemmJob& job, const int32_t* s_off, const int32_t* s_end, int t) {
+    BTile T;
+    const int nt = t % job.n_tiles, rest = t / job.n_tiles;
+    T.n0 = nt * job.BN;
+    if (job.mode == kModeWgrad) {
+        const int mt = rest % job.m_tiles;
+        T.e = rest / job.m_tiles;
+        T.m0 = mt * kBM;
+        T.k0 = s_off[T.e];
+        const int rows = s_end[T.e] - T.k0;
+        T.num_ks = (rows + kBK - 1) / kBK;
+        T.tail = rows - (T.num_ks - 1) * kBK;
+        T.b_row = T.k0;
+        T.a_x = 2 * T.m0;
+    } else {
+        T.m0 = rest * kBM;
+        T.e = bwd_expert_of_row(s_off, job.E, T.m0);
+        T.k0 = 0;
+        T.num_ks = job.num_ks;
+        T.tail = kBK;
+        T.b_row = T.e * job.K;
+        T.a_x = 0;
+    }
+    return T;
+}
+
 __global__ void __launch_bounds__(kBThreads, 1)
     bgemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const BgemmJob job) {
-    // ---- the tile of this CTA (identical in every thread)
-    const int nt = static_cast<int>(blockIdx.x % static_cast<unsigned>(job.n_tiles));
-    const int rest = static_cast<int>(blockIdx.x / static_cast<unsigned>(job.n_tiles));
-    const int n0 = nt * job.BN;
-    int e, m0, a_row, b_row, k0, num_ks;
-    if (job.mode == kModeWgrad) {
-        const int mt = rest % job.m_tiles;
-        e = rest / job.m_tiles;
-        m0 = mt * kBM;
-        a_row = m0;
-        b_row = n0;
-        k0 = job.offsets[e];
-        num_ks = (job.offsets[e + 1] - k0) / kBK;
-    } else {
-        m0 = rest * kBM;
-        if (m0 >= job.offsets[job.E]) return;          // past the last expert's rows
-        int lo = 0, hi = job.E - 1;                     // the last e with offsets[e] <= m0
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (job.offsets[mid] <= m0) lo = mid; else hi = mid - 1;
-        }
-        e = lo;
-        a_row = m0;
-        b_row = e * job.N + n0;
-        k0 = 0;
-        num_ks = job.num_ks;
-    }
-
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBBarOff);
     uint64_t* empty = full + kBStages;
-    uint64_t* tmem_full = empty + kBStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+    uint64_t* tmem_full = empty + kBStages;           // [2]
+    uint64_t* tmem_empty = tmem_full + 2;             // [2]
+    uint64_t* drain = tmem_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int32_t* s_off = reinterpret_cast<int32_t*>(smem + kBOffOff);
+    int32_t* s_end = s_off + kBMaxE + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool wgrad = job.mode == kModeWgrad;
 
+    for (int i = threadIdx.x; i <= job.E; i += kBThreads) {
+        s_off[i] = job.offsets[i];
+        if (wgrad && i < job.E) s_end[i] = job.real_end[i];
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(tmem_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tmem_full[b], 1);
+            mbar_init(&tmem_empty[b], kBEpiWarps);
+        }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -175,6 +240,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int num_tiles = wgrad ? job.E * job.m_tiles * job.n_tiles : (s_off[job.E] / kBM) * job.n_tiles;
+    const int b_boxes = job.BN / 64;
     const uint32_t b_bytes = static_cast<uint32_t>(job.BN) * kBRowBytes;
 
     if (warp == 0) {
@@ -183,22 +250,32 @@ __global__ void __launch_bounds__(kBThreads, 1)
         int stage = 0;
         uint32_t phase = 0, issued = 0, issued_parity = 0;
         bool failed = false;
-        for (int ks = 0; ks < num_ks; ++ks) {
-            const bool ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetCycles);
-            if (!__all_sync(0xFFFFFFFFu, ok)) {
-                failed = true;
-                break;
-            }
-            uint8_t* st = smem + stage * kBStageBytes;
-            const int x = (k0 + ks * kBK) * 2;          // byte coordinate along K
-            mbar_arrive_expect_tx_elect(&full[stage], kBABytes + b_bytes);
-            tma_load_2d_elect(st, &tmA, &full[stage], x, a_row, pol);
-            tma_load_2d_elect(st + kBABytes, &tmB, &full[stage], x, b_row, pol);
-            issued |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-            if (++stage == kBStages) {
-                stage = 0;
-                phase ^= 1u;
+        for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
+            const BTile T = bgemm_tile(job, s_off, s_end, t);
+            for (int ks = 0; ks < T.num_ks; ++ks) {
+                const bool ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetCycles);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    failed = true;
+                    break;
+                }
+                uint8_t* st = smem + stage * kBStageBytes;
+                const int k = ks * kBK;
+                mbar_arrive_expect_tx_elect(&full[stage], kBABytes + b_bytes);
+                if (wgrad) {
+                    tma_load_2d_elect(st, &tmA, &full[stage], T.a_x, T.k0 + k, pol);
+                    tma_load_2d_elect(st + kBMnBox, &tmA, &full[stage], T.a_x + 128, T.k0 + k, pol);
+                } else {
+                    tma_load_2d_elect(st, &tmA, &full[stage], 2 * k, T.m0, pol);
+                }
+                for (int c = 0; c < b_boxes; ++c)
+                    tma_load_2d_elect(st + kBABytes + c * kBMnBox, &tmB, &full[stage], 2 * (T.n0 + 64 * c),
+                                      T.b_row + k, pol);
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == kBStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
         if (failed) {
@@ -210,91 +287,127 @@ __global__ void __launch_bounds__(kBThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (warp-uniform)
-        const uint32_t idesc = idesc_bf16_kmajor(kBM, job.BN);
+        const uint32_t idesc = idesc_bf16(kBM, job.BN, wgrad, true);
         int stage = 0;
-        uint32_t phase = 0;
+        uint32_t phase = 0, acc_iter = 0;
         bool failed = false, issued_any = false;
-        for (int ks = 0; ks < num_ks; ++ks) {
-            const bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetCycles);
-            if (!__all_sync(0xFFFFFFFFu, ok)) {
+        for (int t = blockIdx.x; t < num_tiles && !failed; t += gridDim.x) {
+            const BTile T = bgemm_tile(job, s_off, s_end, t);
+            if (T.num_ks == 0) continue;
+            const uint32_t buf = acc_iter & 1u;
+            const bool ok_acc =
+                mbar_wait_bounded(&tmem_empty[buf], ((acc_iter >> 1) & 1u) ^ 1u, abort_flag, kWaitBudgetCycles);
+            if (!__all_sync(0xFFFFFFFFu, ok_acc)) {
                 failed = true;
                 break;
             }
             tc_fence_after();
-            const uint32_t st = smem_u32(smem + stage * kBStageBytes);
-            const uint64_t adesc = sdesc_k_swizzled<128>(st);
-            const uint64_t bdesc = sdesc_k_swizzled<128>(st + kBABytes);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)   // K = 16 BF16 (32 bytes) per MMA
-                mma_bf16_elect(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (ks | j) != 0 ? 1u : 0u);
-            issued_any = true;
-            tc_commit_elect(&empty[stage]);
-            if (++stage == kBStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-        if (num_ks > 0) {
-            if (!failed) {
-                tc_commit_elect(tmem_full);
-            } else {
-                if (lane == 0) set_device_error(job.err, NVFP4_ERR_DEVICE_TIMEOUT);
-                *abort_flag = 1;
-                if (issued_any) {   // let the issued MMAs finish before TMEM is released
-                    tc_commit_elect(tmem_full);
-                    mbar_wait_bounded(tmem_full, 0, nullptr, kWaitBudgetCycles);
+            const uint32_t d_tmem = tmem + buf * kBMaxN;
+            for (int ks = 0; ks < T.num_ks; ++ks) {
+                const bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetCycles);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    failed = true;
+                    break;
                 }
+                tc_fence_after();
+                uint8_t* stp = smem + stage * kBStageBytes;
+                if (ks == T.num_ks - 1 && T.tail < kBK) {
+                    // rows past the expert's real rows: zero B's K-rows tail..63 in every box
+                    const int chunks = (kBK - T.tail) * (kBRowBytes / 16);
+                    for (int c = 0; c < b_boxes; ++c) {
+                        uint4* z = reinterpret_cast<uint4*>(stp + kBABytes + c * kBMnBox + T.tail * kBRowBytes);
+                        for (int i = lane; i < chunks; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                }
+                const uint32_t st = smem_u32(stp);
+                const uint64_t adesc = wgrad ? sdesc_mn_sw128(st) : sdesc_k_swizzled<128>(st);
+                const uint64_t bdesc = sdesc_mn_sw128(st + kBABytes);
+                const uint64_t a_step = wgrad ? 2048 >> 4 : 32 >> 4;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)   // K = 16 BF16 per MMA
+                    mma_bf16_elect(d_tmem, adesc + a_step * j, bdesc + (2048 >> 4) * j, idesc,
+                                   (ks | j) != 0 ? 1u : 0u);
+                issued_any = true;
+                tc_commit_elect(&empty[stage]);
+                if (++stage == kBStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (failed) break;
+            tc_commit_elect(&tmem_full[buf]);
+            ++acc_iter;
+        }
+        if (failed) {
+            if (lane == 0) set_device_error(job.err, NVFP4_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            if (issued_any) {   // let the issued MMAs finish before TMEM is released
+                tc_commit_elect(drain);
+                mbar_wait_bounded(drain, 0, nullptr, kWaitBudgetCycles);
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue: one row per thread
         const int q = warp & 3;                             // TMEM lane quarter
+        const int half = (warp - 2) >> 2;                   // which half of the tile's columns
         const int r = q * 32 + lane;                        // row of the tile
-        // destination of this row (nullptr: not stored)
-        uint16_t* orow16 = nullptr;
-        float* orow32 = nullptr;
-        if (job.mode == kModeRows) {
-            orow16 = job.out_bf16 + static_cast<int64_t>(m0 + r) * job.N + n0;
-        } else if (job.mode == kModePairs) {
-            const int pair = job.row_pair[m0 + r];
-            if (pair >= 0) orow16 = job.out_bf16 + static_cast<int64_t>(pair) * job.N + n0;
-        } else {
-            orow32 = job.out_f32 + (static_cast<int64_t>(e) * job.M + m0 + r) * job.N + n0;
-        }
-        if (num_ks == 0) {
-            // an expert without routed rows: its weight gradient is zero
-            const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (orow32 != nullptr)
-                for (int c = 0; c < job.BN; c += 8) st_v8(orow32 + c, z);
-        } else {
-            const bool ok = mbar_wait_bounded(tmem_full, 0, abort_flag, kWaitBudgetCycles);
+        const int cols = job.BN / 2;
+        uint32_t acc_iter = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            const BTile T = bgemm_tile(job, s_off, s_end, t);
+            const int c0 = T.n0 + half * cols;
+            // destination of this row (nullptr: not stored)
+            uint16_t* orow16 = nullptr;
+            float* orow32 = nullptr;
+            if (job.mode == kModeRows) {
+                orow16 = job.out_bf16 + static_cast<int64_t>(T.m0 + r) * job.N + c0;
+            } else if (job.mode == kModePairs) {
+                const int pair = job.row_pair[T.m0 + r];
+                if (pair >= 0) orow16 = job.out_bf16 + static_cast<int64_t>(pair) * job.N + c0;
+            } else {
+                orow32 = job.out_f32 + (static_cast<int64_t>(T.e) * job.M + T.m0 + r) * job.N + c0;
+            }
+            if (T.num_ks == 0) {
+                // an expert without routed rows: its weight gradient is zero
+                const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                for (int c = 0; c < cols; c += 8) st_v8(orow32 + c, z);
+                continue;
+            }
+            const uint32_t buf = acc_iter & 1u;
+            const bool ok = mbar_wait_bounded(&tmem_full[buf], (acc_iter >> 1) & 1u, abort_flag, kWaitBudgetCycles);
             if (!__all_sync(0xFFFFFFFFu, ok)) {
                 if (lane == 0) set_device_error(job.err, NVFP4_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
-            } else {
-                tc_fence_after();
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-                for (int c = 0; c < job.BN; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(taddr + c, v);
-                    tmem_ld_wait();
-                    if (orow16 != nullptr) {
-                        uint32_t w[8];
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem + buf * kBMaxN + half * cols + (static_cast<uint32_t>(q * 32) << 16);
+            for (int c = 0; c < cols; c += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(taddr + c, v);
+                tmem_ld_wait();
+                if (orow16 != nullptr) {
+                    uint32_t w[8];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                        st_v8(orow16 + c, w);
-                    } else if (orow32 != nullptr) {
-                        uint32_t w0[8], w1[8];
+                    for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                    st_v8(orow16 + c, w);
+                } else if (orow32 != nullptr) {
+                    uint32_t w0[8], w1[8];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            w0[i] = v[i];
-                            w1[i] = v[8 + i];
-                        }
-                        st_v8(orow32 + c, w0);
-                        st_v8(orow32 + c + 8, w1);
+                    for (int i = 0; i < 8; ++i) {
+                        w0[i] = v[i];
+                        w1[i] = v[8 + i];
                     }
+                    st_v8(orow32 + c, w0);
+                    st_v8(orow32 + c + 8, w1);
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+            ++acc_iter;
         }
     }
 
@@ -307,71 +420,35 @@ __global__ void __launch_bounds__(kBThreads, 1)
 }
 
 // dst[r][0..C) = src[row_pair[r] / k][0..C) for the routed rows r < offsets[E], zeros for a
-// pad row.  One warp per row, 16-byte copies; C % 8 == 0.
+// pad row; one warp per row, 16-byte copies, C % 8 == 0.  With real_end != nullptr the grid
+// has ceil(E/8) more blocks, whose warps (one per expert e) write real_end[e], the end of e's
+// real rows: its rows are real first, then fewer than 128 pad rows (row_pair -1).
 __global__ void __launch_bounds__(256)
     gather_token_rows_kernel(const uint16_t* __restrict__ src, int C, const int32_t* __restrict__ row_pair, int k,
-                             const int32_t* __restrict__ offsets, int E, uint16_t* __restrict__ dst) {
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+                             const int32_t* __restrict__ offsets, int E, int64_t row_blocks, uint16_t* __restrict__ dst,
+                             int32_t* __restrict__ real_end) {
     const int lane = threadIdx.x & 31;
+    if (static_cast<int64_t>(blockIdx.x) >= row_blocks) {
+        const int e = static_cast<int>((blockIdx.x - row_blocks) * 8 + (threadIdx.x >> 5));
+        if (e >= E) return;
+        const int k1 = offsets[e + 1];
+        const int lo = max(offsets[e], k1 - 128);
+        int first = k1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int idx = lo + 4 * lane + j;
+            if (idx < k1 && row_pair[idx] < 0) first = min(first, idx);
+        }
+        first = __reduce_min_sync(0xFFFFFFFFu, first);
+        if (lane == 0) real_end[e] = first;
+        return;
+    }
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (r >= offsets[E]) return;
     const int pair = row_pair[r];
     const uint4* s = pair >= 0 ? reinterpret_cast<const uint4*>(src + static_cast<int64_t>(pair / k) * C) : nullptr;
     uint4* d = reinterpret_cast<uint4*>(dst + r * C);
     for (int i = lane; i < C / 8; i += 32) d[i] = s != nullptr ? s[i] : make_uint4(0u, 0u, 0u, 0u);
-}
-
-enum : int { kSrcPlain = 0, kSrcToken = 1, kSrcRouted = 2 };
-
-// Transpose of one 64 x 64 tile: out[c][r] = S(r)[c] for r in [r0, r0+64), c in [c0, c0+64),
-// where S(r) is, for problem z = blockIdx.z,
-//   kSrcPlain:   row r of in + z*in_batch (stride ld_in)
-//   kSrcToken:   row row_pair[r] / k of in, or zeros if row_pair[r] < 0   (r < offsets[E])
-//   kSrcRouted:  row r of in, or zeros if row_pair[r] < 0                  (r < offsets[E])
-// out row c (stride ld_out) of problem z starts at out + z*out_batch.  Row tiles past
-// offsets[E] are not written in the routed modes.  ld_in, ld_out, in_batch, out_batch,
-// r0 and c0 are multiples of 64 elements (16-byte aligned rows).
-template <int kSrc>
-__global__ void __launch_bounds__(256)
-    transpose_tile_kernel(const uint16_t* __restrict__ in, int64_t ld_in, int64_t in_batch,
-                          const int32_t* __restrict__ row_pair, int k, const int32_t* __restrict__ offsets, int E,
-                          uint16_t* __restrict__ out, int64_t ld_out, int64_t out_batch) {
-    __shared__ __align__(16) uint16_t tile[64][66];   // 33-word rows: the column reads spread over the banks
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 64;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 64;
-    const int64_t z = blockIdx.z;
-    if (kSrc != kSrcPlain && r0 >= offsets[E]) return;
-    const int t = threadIdx.x;
-    {
-        const int rr = t >> 2, cc = (t & 3) * 16;        // 16 elements of source row r0 + rr
-        const int64_t r = r0 + rr;
-        const uint16_t* src = nullptr;
-        if (kSrc == kSrcPlain) {
-            src = in + z * in_batch + r * ld_in;
-        } else {
-            const int pair = row_pair[r];
-            if (pair >= 0) src = in + (kSrc == kSrcToken ? static_cast<int64_t>(pair / k) : r) * ld_in;
-        }
-        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-        if (src != nullptr) {
-            const uint4* s = reinterpret_cast<const uint4*>(src + c0 + cc);
-            v0 = s[0];
-            v1 = s[1];
-        }
-        uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[rr][cc]);
-        dst[0] = v0.x; dst[1] = v0.y; dst[2] = v0.z; dst[3] = v0.w;
-        dst[4] = v1.x; dst[5] = v1.y; dst[6] = v1.z; dst[7] = v1.w;
-    }
-    __syncthreads();
-    {
-        const int cc = t >> 2, rr = (t & 3) * 16;        // 16 elements of output row c0 + cc
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i] = static_cast<uint32_t>(tile[rr + 2 * i][cc]) | (static_cast<uint32_t>(tile[rr + 2 * i + 1][cc]) << 16);
-        uint4* d = reinterpret_cast<uint4*>(out + z * out_batch + (c0 + cc) * ld_out + r0 + rr);
-        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    }
 }
 
 // The SwiGLU x prob derivative, one warp per routed row r < offsets[E]:
@@ -450,13 +527,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Byte-typed 2D map over a K-major BF16 matrix [rows][K]: boxes of box_rows rows x 128 bytes
-// (64 elements of K), 128B swizzle.
-bool make_kmajor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box_rows) {
+// Byte-typed 2D map over a BF16 matrix [rows][cols]: boxes of box_rows rows x 128 bytes
+// (64 consecutive elements of a row), 128B swizzle.  A K-major operand takes 128- or 256-row
+// boxes (64 elements of K per row); an MN-major one 64-row boxes (64 K-rows of 64 elements).
+bool make_box_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * K), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * K)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * cols)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBRowBytes), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -484,7 +562,12 @@ cudaError_t ensure_smem_attr() {
 
 int tile_n(int N) { return N % 256 == 0 ? 256 : 128; }
 
-// Grouped dgrad: out = A (routed rows [rows_cap][K]) x B[e]^T (B [E*N][K]), K % 64 == 0, N % 128 == 0.
+unsigned persistent_grid(int64_t tiles) {
+    return static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count())));
+}
+
+// Grouped dgrad: out = A (routed rows [rows_cap][K], K-major) x B[e] (B [E*K][N], rows e*K..
+// are expert e's), K % 64 == 0, N % 128 == 0.
 cudaError_t launch_dgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap, int K, int N, int E,
                          const int32_t* offsets, const int32_t* row_pair, int mode, uint16_t* out, int* err,
                          cudaStream_t st) {
@@ -496,23 +579,25 @@ cudaError_t launch_dgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap,
     j.N = N;
     j.M = 0;
     j.num_ks = K / kBK;
+    j.K = K;
     j.E = E;
     j.offsets = offsets;
+    j.real_end = nullptr;
     j.row_pair = row_pair;
     j.out_bf16 = out;
     j.out_f32 = nullptr;
     j.err = err;
     CUtensorMap ma, mb;
-    if (!make_kmajor_map(&ma, A, rows_cap, K, kBM) || !make_kmajor_map(&mb, B, static_cast<int64_t>(E) * N, K, j.BN))
+    if (!make_box_map(&ma, A, rows_cap, K, kBM) || !make_box_map(&mb, B, static_cast<int64_t>(E) * K, N, kBK))
         return cudaErrorInvalidValue;
-    const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(j.m_tiles) * j.n_tiles);
-    return launch_pdl(false, bgemm_bf16_kernel, grid, kBThreads, kBSmemBytes, st, ma, mb, j);
+    return launch_pdl(false, bgemm_bf16_kernel, persistent_grid(static_cast<int64_t>(j.m_tiles) * j.n_tiles),
+                      kBThreads, kBSmemBytes, st, ma, mb, j);
 }
 
-// Grouped wgrad: out[e] (FP32 [M][N]) = A[:, rows of e] x B[:, rows of e]^T with A [M][rows_cap],
-// B [N][rows_cap] (K over the routed rows of expert e).
+// Grouped wgrad: out[e] (FP32 [M][N]) = A[rows of e]^T B[rows of e] with A [rows_cap][M],
+// B [rows_cap][N] (K over expert e's real routed rows offsets[e] .. real_end[e]).
 cudaError_t launch_wgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap, int M, int N, int E,
-                         const int32_t* offsets, float* out, int* err, cudaStream_t st) {
+                         const int32_t* offsets, const int32_t* real_end, float* out, int* err, cudaStream_t st) {
     BgemmJob j{};
     j.mode = kModeWgrad;
     j.BN = tile_n(N);
@@ -521,70 +606,56 @@ cudaError_t launch_wgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap,
     j.N = N;
     j.M = M;
     j.num_ks = 0;
+    j.K = 0;
     j.E = E;
     j.offsets = offsets;
+    j.real_end = real_end;
     j.row_pair = nullptr;
     j.out_bf16 = nullptr;
     j.out_f32 = out;
     j.err = err;
     CUtensorMap ma, mb;
-    if (!make_kmajor_map(&ma, A, M, rows_cap, kBM) || !make_kmajor_map(&mb, B, N, rows_cap, j.BN))
+    if (!make_box_map(&ma, A, rows_cap, M, kBK) || !make_box_map(&mb, B, rows_cap, N, kBK))
         return cudaErrorInvalidValue;
-    const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(E) * j.m_tiles * j.n_tiles);
-    return launch_pdl(false, bgemm_bf16_kernel, grid, kBThreads, kBSmemBytes, st, ma, mb, j);
+    return launch_pdl(false, bgemm_bf16_kernel, persistent_grid(static_cast<int64_t>(E) * j.m_tiles * j.n_tiles),
+                      kBThreads, kBSmemBytes, st, ma, mb, j);
 }
 
-template <int kSrc>
-cudaError_t launch_transpose(const uint16_t* in, int64_t ld_in, int64_t in_batch, const int32_t* row_pair, int k,
-                             const int32_t* offsets, int E, int64_t rows, int64_t cols, int64_t batch, uint16_t* out,
-                             int64_t ld_out, int64_t out_batch, cudaStream_t st) {
-    const dim3 grid(static_cast<unsigned>(rows / 64), static_cast<unsigned>(cols / 64), static_cast<unsigned>(batch));
-    return launch_pdl(false, transpose_tile_kernel<kSrc>, grid, 256, 0, st, in, ld_in, in_batch, row_pair, k, offsets,
-                      E, out, ld_out, out_batch);
+cudaError_t launch_gather(const uint16_t* src, int C, const BackwardArgs& a, uint16_t* dst, int32_t* real_end,
+                          cudaStream_t st) {
+    const int64_t row_blocks = a.rows_cap / 8;
+    const int64_t blocks = row_blocks + (real_end != nullptr ? (a.E + 7) / 8 : 0);
+    return launch_pdl(false, gather_token_rows_kernel, static_cast<unsigned>(blocks), 256, 0, st, src, C, a.row_pair,
+                      a.k, a.offsets, a.E, row_blocks, dst, real_end);
 }
 
 }  // namespace
 
-cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t batch, int64_t rows, int64_t cols, uint16_t* out,
-                                  cudaStream_t st) {
-    if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
-    return launch_transpose<kSrcPlain>(in, cols, rows * cols, nullptr, 1, nullptr, 0, rows, cols, batch, out, rows,
-                                       rows * cols, st);
-}
-
 cudaError_t launch_moe_backward_ste(const BackwardArgs& a, cudaStream_t st) {
+    if (a.E > kBMaxE) return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem_attr();
     if (e != cudaSuccess) return e;
     const int64_t rc = a.rows_cap;
-    const unsigned warp_rows_grid = static_cast<unsigned>(rc / 8);
-    // dY rows, FC2 dgrad, SwiGLU x prob derivative
-    e = launch_pdl(false, gather_token_rows_kernel, warp_rows_grid, 256, 0, st, a.dout, a.H, a.row_pair, a.k,
-                   a.offsets, a.E, a.dy_rows);
+    // dY rows (and each expert's end of real rows), FC2 dgrad, SwiGLU x prob derivative
+    e = launch_gather(a.dout, a.H, a, a.dy_rows, a.real_end, st);
     if (e != cudaSuccess) return e;
-    e = launch_dgrad(a.dy_rows, a.w2t, rc, a.H, a.I, a.E, a.offsets, a.row_pair, kModeRows, a.dh, a.err, st);
+    e = launch_dgrad(a.dy_rows, a.w2, rc, a.H, a.I, a.E, a.offsets, a.row_pair, kModeRows, a.dh, a.err, st);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(false, swiglu_bwd_kernel, warp_rows_grid, 256, 0, st, a.dh, a.fc1_pre, a.row_pair, a.row_prob,
-                   a.offsets, a.E, a.I, a.dgu, a.dprob);
+    e = launch_pdl(false, swiglu_bwd_kernel, static_cast<unsigned>(rc / 8), 256, 0, st, a.dh, a.fc1_pre, a.row_pair,
+                   a.row_prob, a.offsets, a.E, a.I, a.dgu, a.dprob);
     if (e != cudaSuccess) return e;
     // FC1 dgrad per (token, slot), then the slot-order sum
-    e = launch_dgrad(a.dgu, a.w1t, rc, 2 * a.I, a.H, a.E, a.offsets, a.row_pair, kModePairs, a.dx_pairs, a.err, st);
+    e = launch_dgrad(a.dgu, a.w1, rc, 2 * a.I, a.H, a.E, a.offsets, a.row_pair, kModePairs, a.dx_pairs, a.err, st);
     if (e != cudaSuccess) return e;
     e = launch_combine(a.dx_pairs, nullptr, a.T, a.k, a.H, a.dx, st, false);
     if (e != cudaSuccess) return e;
-    // FC2 wgrad: dW2[e] = dy^T h over the expert's rows
-    e = launch_transpose<kSrcToken>(a.dout, a.H, 0, a.row_pair, a.k, a.offsets, a.E, rc, a.H, 1, a.dy_t, rc, 0, st);
+    // FC2 wgrad: dW2[e] = dy^T h over the expert's real rows
+    e = launch_wgrad(a.dy_rows, a.h, rc, a.H, a.I, a.E, a.offsets, a.real_end, a.dw2, a.err, st);
     if (e != cudaSuccess) return e;
-    e = launch_transpose<kSrcRouted>(a.h, a.I, 0, a.row_pair, a.k, a.offsets, a.E, rc, a.I, 1, a.h_t, rc, 0, st);
+    // FC1 wgrad: dW1[e] = [da, du]^T x over the expert's real rows
+    e = launch_gather(a.x, a.H, a, a.x_rows, nullptr, st);
     if (e != cudaSuccess) return e;
-    e = launch_wgrad(a.dy_t, a.h_t, rc, a.H, a.I, a.E, a.offsets, a.dw2, a.err, st);
-    if (e != cudaSuccess) return e;
-    // FC1 wgrad: dW1[e] = [da, du]^T x over the expert's rows
-    e = launch_transpose<kSrcRouted>(a.dgu, 2 * a.I, 0, a.row_pair, a.k, a.offsets, a.E, rc, 2 * a.I, 1, a.dgu_t, rc,
-                                     0, st);
-    if (e != cudaSuccess) return e;
-    e = launch_transpose<kSrcToken>(a.x, a.H, 0, a.row_pair, a.k, a.offsets, a.E, rc, a.H, 1, a.x_t, rc, 0, st);
-    if (e != cudaSuccess) return e;
-    return launch_wgrad(a.dgu_t, a.x_t, rc, 2 * a.I, a.H, a.E, a.offsets, a.dw1, a.err, st);
+    return launch_wgrad(a.dgu, a.x_rows, rc, 2 * a.I, a.H, a.E, a.offsets, a.real_end, a.dw1, a.err, st);
 }
 
 }  // namespace nvfp4

@@ -10,8 +10,8 @@ struct BackwardArgs {
     int64_t T;
     int H, I, E, k;
     int64_t rows_cap;          // routed-row capacity of the forward's layout
-    const uint16_t* w1t;       // BF16 [E][H][2I]: W1 transposed per expert
-    const uint16_t* w2t;       // BF16 [E][I][H]: W2 transposed per expert
+    const uint16_t* w1;        // BF16 [E][2I][H]: the original W1 (gate rows, then up rows)
+    const uint16_t* w2;        // BF16 [E][H][I]: the original W2
     const uint16_t* x;         // BF16 [T][H]
     const uint16_t* dout;      // BF16 [T][H]
     const int32_t* offsets;    // [E+1] padded expert row starts
@@ -28,17 +28,11 @@ struct BackwardArgs {
     uint16_t* dh;              // [rows_cap][I]
     uint16_t* dgu;             // [rows_cap][2I]
     uint16_t* dx_pairs;        // [T*k][H]
-    uint16_t* dy_t;            // [H][rows_cap]
-    uint16_t* h_t;             // [I][rows_cap]
-    uint16_t* dgu_t;           // [2I][rows_cap]
-    uint16_t* x_t;             // [H][rows_cap]
+    uint16_t* x_rows;          // [rows_cap][H]: x gathered per routed row
+    int32_t* real_end;         // [E]: end of each expert's real routed rows
     int* err;
 };
 
 cudaError_t launch_moe_backward_ste(const BackwardArgs& a, cudaStream_t st);
-
-// out[b][c][r] = in[b][r][c]; rows % 64 == 0, cols % 64 == 0, 16-byte aligned.
-cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t batch, int64_t rows, int64_t cols, uint16_t* out,
-                                  cudaStream_t st);
 
 }  // namespace nvfp4
