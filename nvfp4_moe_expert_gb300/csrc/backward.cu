@@ -46,7 +46,6 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kBStages = 4;
 constexpr int kBM = 128;                                // output rows per tile
 constexpr int kBK = 64;                                 // BF16 elements of K per stage
 constexpr int kBRowBytes = 2 * kBK;                     // 128 bytes, one swizzle span
@@ -59,9 +58,29 @@ constexpr int kBEpiWarps = 8;
 constexpr int kBThreads = 64 + 32 * kBEpiWarps;         // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t kBTmemCols = 2 * kBMaxN;             // two accumulators
 constexpr int kBMaxE = 1024;
-constexpr int kBBarOff = kBStages * kBStageBytes;
-constexpr int kBOffOff = kBBarOff + 256;                // offsets[0..E] then real_end[0..E)
-constexpr int kBSmemBytes = kBOffOff + 2 * (kBMaxE + 1) * 4 + 1024;
+
+// Shared memory of one instantiation: a ring of kStages operand stages, the barriers, the
+// expert offsets (and ends of real rows), and the epilogue staging.  Each epilogue warp passes
+// its 32 accumulator rows through a tile of 32 rows x kStgWords 32-bit words (FP32 columns, or
+// BF16 column pairs), 16-byte slots swizzled by row so that neither the row-wise writes nor the
+// column-wise reads conflict, and stores it as whole kStgWords*4-byte row segments.  The
+// activation gradients (24-32 K stages per tile) keep four stages; the weight gradients (a few
+// K stages per tile, FP32 output) trade one for wider row segments.
+template <bool kWgrad>
+struct BCfg {
+    static constexpr int kStages = kWgrad ? 3 : 4;
+    static constexpr int kStgWords = kWgrad ? 32 : 16;
+    static constexpr int kStgSlots = kStgWords / 4;              // 16-byte slots per staged row
+    static constexpr int kStgShift = kStgSlots == 8 ? 0 : 1;     // rows sharing a bank group differ here
+    static constexpr int kStgRowsPerSt = 32 / kStgSlots;         // rows one warp-wide 16-byte store covers
+    static constexpr int kStgBytes = 32 * kStgWords * 4;         // per epilogue warp
+    static constexpr int kBarOff = kStages * kBStageBytes;
+    static constexpr int kOffOff = kBarOff + 256;                // offsets[0..E] then real_end[0..E)
+    static constexpr int kStgOff = kOffOff + ((2 * (kBMaxE + 1) * 4 + 127) & ~127);
+    static constexpr int kSmemBytes = kStgOff + kBEpiWarps * kStgBytes + 1024;
+    static_assert(kStgWords == 16 || kStgWords == 32, "staged row chunk");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
 
 enum : int { kModeRows = 0, kModePairs = 1, kModeWgrad = 2 };
 
@@ -140,13 +159,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// 32-byte store; p 32-byte aligned.
-__device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
 // Expert owning routed row `row`: largest e < E with off[e] <= row (off in shared memory).
 __device__ __forceinline__ int bwd_expert_of_row(const int32_t* off, int E, int row) {
     int lo = 0, hi = E;
@@ -194,29 +206,38 @@ __device__ __forceinline__ BTile bgemm_tile(const BgemmJob& job, const int32_t* 
     return T;
 }
 
+// The slot of 16-byte chunk j of staged row `row`.
+template <class C>
+__device__ __forceinline__ int stg_slot(int row, int j) {
+    return j ^ ((row >> C::kStgShift) & (C::kStgSlots - 1));
+}
+
+// kWgrad: FP32 weight gradients (both operands MN-major); else BF16 activation gradients
+// (A K-major, B MN-major), kModeRows or kModePairs.
+template <bool kWgrad>
 __global__ void __launch_bounds__(kBThreads, 1)
     bgemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const BgemmJob job) {
+    using C = BCfg<kWgrad>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBBarOff);
-    uint64_t* empty = full + kBStages;
-    uint64_t* tmem_full = empty + kBStages;           // [2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* tmem_full = empty + C::kStages;           // [2]
     uint64_t* tmem_empty = tmem_full + 2;             // [2]
     uint64_t* drain = tmem_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int32_t* s_off = reinterpret_cast<int32_t*>(smem + kBOffOff);
+    int32_t* s_off = reinterpret_cast<int32_t*>(smem + C::kOffOff);
     int32_t* s_end = s_off + kBMaxE + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool wgrad = job.mode == kModeWgrad;
 
     for (int i = threadIdx.x; i <= job.E; i += kBThreads) {
         s_off[i] = job.offsets[i];
-        if (wgrad && i < job.E) s_end[i] = job.real_end[i];
+        if (kWgrad && i < job.E) s_end[i] = job.real_end[i];
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kBStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -240,7 +261,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int num_tiles = wgrad ? job.E * job.m_tiles * job.n_tiles : (s_off[job.E] / kBM) * job.n_tiles;
+    const int num_tiles = kWgrad ? job.E * job.m_tiles * job.n_tiles : (s_off[job.E] / kBM) * job.n_tiles;
     const int b_boxes = job.BN / 64;
     const uint32_t b_bytes = static_cast<uint32_t>(job.BN) * kBRowBytes;
 
@@ -261,7 +282,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 uint8_t* st = smem + stage * kBStageBytes;
                 const int k = ks * kBK;
                 mbar_arrive_expect_tx_elect(&full[stage], kBABytes + b_bytes);
-                if (wgrad) {
+                if (kWgrad) {
                     tma_load_2d_elect(st, &tmA, &full[stage], T.a_x, T.k0 + k, pol);
                     tma_load_2d_elect(st + kBMnBox, &tmA, &full[stage], T.a_x + 128, T.k0 + k, pol);
                 } else {
@@ -272,7 +293,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
                                       T.b_row + k, pol);
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == kBStages) {
+                if (++stage == C::kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -281,13 +302,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
         if (failed) {
             if (lane == 0) set_device_error(job.err, NVFP4_ERR_DEVICE_TIMEOUT);
             *abort_flag = 1;
-            for (int s = 0; s < kBStages; ++s) {
+            for (int s = 0; s < C::kStages; ++s) {
                 if (issued & (1u << s)) mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, kWaitBudgetCycles);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (warp-uniform)
-        const uint32_t idesc = idesc_bf16(kBM, job.BN, wgrad, true);
+        const uint32_t idesc = idesc_bf16(kBM, job.BN, kWgrad, true);
         int stage = 0;
         uint32_t phase = 0, acc_iter = 0;
         bool failed = false, issued_any = false;
@@ -311,7 +332,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 }
                 tc_fence_after();
                 uint8_t* stp = smem + stage * kBStageBytes;
-                if (ks == T.num_ks - 1 && T.tail < kBK) {
+                if (kWgrad && ks == T.num_ks - 1 && T.tail < kBK) {
                     // rows past the expert's real rows: zero B's K-rows tail..63 in every box
                     const int chunks = (kBK - T.tail) * (kBRowBytes / 16);
                     for (int c = 0; c < b_boxes; ++c) {
@@ -322,16 +343,16 @@ __global__ void __launch_bounds__(kBThreads, 1)
                     __syncwarp();
                 }
                 const uint32_t st = smem_u32(stp);
-                const uint64_t adesc = wgrad ? sdesc_mn_sw128(st) : sdesc_k_swizzled<128>(st);
+                const uint64_t adesc = kWgrad ? sdesc_mn_sw128(st) : sdesc_k_swizzled<128>(st);
                 const uint64_t bdesc = sdesc_mn_sw128(st + kBABytes);
-                const uint64_t a_step = wgrad ? 2048 >> 4 : 32 >> 4;
+                constexpr uint64_t a_step = kWgrad ? 2048 >> 4 : 32 >> 4;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)   // K = 16 BF16 per MMA
                     mma_bf16_elect(d_tmem, adesc + a_step * j, bdesc + (2048 >> 4) * j, idesc,
                                    (ks | j) != 0 ? 1u : 0u);
                 issued_any = true;
                 tc_commit_elect(&empty[stage]);
-                if (++stage == kBStages) {
+                if (++stage == C::kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -349,30 +370,44 @@ __global__ void __launch_bounds__(kBThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue: one row per thread
-        const int q = warp & 3;                             // TMEM lane quarter
-        const int half = (warp - 2) >> 2;                   // which half of the tile's columns
-        const int r = q * 32 + lane;                        // row of the tile
-        const int cols = job.BN / 2;
+        // ------------------------------------------------------------ epilogue
+        // Warp w reads TMEM lane quarter w % 4 (rows q*32..+31 of the tile) and one part of the
+        // columns; lane l owns row q*32 + l while reading the accumulator, and the staged
+        // stores cover C::kStgRowsPerSt rows x C::kStgWords*4 bytes per instruction.
+        constexpr int kColsPerChunk = kWgrad ? C::kStgWords : 2 * C::kStgWords;   // accumulator columns
+        const int q = warp & 3;
+        const int part = (warp - 2) >> 2;
+        const int cols = job.BN / (kBEpiWarps / 4);
+        uint32_t* stg = reinterpret_cast<uint32_t*>(smem + C::kStgOff) + (warp - 2) * (C::kStgBytes / 4);
+        const int srow = lane / C::kStgSlots;                  // this lane's row within a store's rows
+        const int sj = lane % C::kStgSlots;                    // and its 16-byte slot
         uint32_t acc_iter = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const BTile T = bgemm_tile(job, s_off, s_end, t);
-            const int c0 = T.n0 + half * cols;
-            // destination of this row (nullptr: not stored)
-            uint16_t* orow16 = nullptr;
-            float* orow32 = nullptr;
-            if (job.mode == kModeRows) {
-                orow16 = job.out_bf16 + static_cast<int64_t>(T.m0 + r) * job.N + c0;
-            } else if (job.mode == kModePairs) {
-                const int pair = job.row_pair[T.m0 + r];
-                if (pair >= 0) orow16 = job.out_bf16 + static_cast<int64_t>(pair) * job.N + c0;
+            const int c0 = T.n0 + part * cols;
+            const int row = T.m0 + q * 32 + lane;
+            // start of this lane's row segment (nullptr: not stored)
+            uint8_t* dst;
+            if (kWgrad) {
+                dst = reinterpret_cast<uint8_t*>(job.out_f32 + (static_cast<int64_t>(T.e) * job.M + row) * job.N + c0);
+            } else if (job.mode == kModeRows) {
+                dst = reinterpret_cast<uint8_t*>(job.out_bf16 + static_cast<int64_t>(row) * job.N + c0);
             } else {
-                orow32 = job.out_f32 + (static_cast<int64_t>(T.e) * job.M + T.m0 + r) * job.N + c0;
+                const int pair = job.row_pair[row];
+                dst = pair >= 0 ? reinterpret_cast<uint8_t*>(job.out_bf16 + static_cast<int64_t>(pair) * job.N + c0)
+                                : nullptr;
             }
-            if (T.num_ks == 0) {
+            const int chunks = cols / kColsPerChunk;
+            if (kWgrad && T.num_ks == 0) {
                 // an expert without routed rows: its weight gradient is zero
-                const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                for (int c = 0; c < cols; c += 8) st_v8(orow32 + c, z);
+                for (int ch = 0; ch < chunks; ++ch) {
+#pragma unroll
+                    for (int i = 0; i < C::kStgSlots; ++i) {
+                        const int rr = i * C::kStgRowsPerSt + srow;
+                        uint8_t* d = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(dst), rr));
+                        *reinterpret_cast<uint4*>(d + ch * C::kStgWords * 4 + sj * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
                 continue;
             }
             const uint32_t buf = acc_iter & 1u;
@@ -383,26 +418,30 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t taddr = tmem + buf * kBMaxN + half * cols + (static_cast<uint32_t>(q * 32) << 16);
-            for (int c = 0; c < cols; c += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(taddr + c, v);
+            const uint32_t taddr = tmem + buf * kBMaxN + part * cols + (static_cast<uint32_t>(q * 32) << 16);
+            for (int ch = 0; ch < chunks; ++ch) {
+                uint32_t v[kColsPerChunk];
+#pragma unroll
+                for (int l = 0; l < kColsPerChunk / 16; ++l)
+                    tmem_ld_32x32b_x16(taddr + ch * kColsPerChunk + 16 * l, reinterpret_cast<uint32_t(&)[16]>(v[16 * l]));
                 tmem_ld_wait();
-                if (orow16 != nullptr) {
-                    uint32_t w[8];
+                uint32_t w[C::kStgWords];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    st_v8(orow16 + c, w);
-                } else if (orow32 != nullptr) {
-                    uint32_t w0[8], w1[8];
+                for (int i = 0; i < C::kStgWords; ++i)
+                    w[i] = kWgrad ? v[i] : pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        w0[i] = v[i];
-                        w1[i] = v[8 + i];
-                    }
-                    st_v8(orow32 + c, w0);
-                    st_v8(orow32 + c + 8, w1);
+                for (int j = 0; j < C::kStgSlots; ++j)
+                    *reinterpret_cast<uint4*>(stg + lane * C::kStgWords + 4 * stg_slot<C>(lane, j)) =
+                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < C::kStgSlots; ++i) {
+                    const int rr = i * C::kStgRowsPerSt + srow;
+                    const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * C::kStgWords + 4 * stg_slot<C>(rr, sj));
+                    uint8_t* d = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(dst), rr));
+                    if (d != nullptr) *reinterpret_cast<uint4*>(d + ch * C::kStgWords * 4 + sj * 16) = val;
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -553,7 +592,11 @@ cudaError_t ensure_smem_attr() {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_bwd_mutex);
     if (!g_bwd_attr[dev]) {
-        e = cudaFuncSetAttribute(bgemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmemBytes);
+        e = cudaFuncSetAttribute(bgemm_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 BCfg<false>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(bgemm_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 BCfg<true>::kSmemBytes);
         if (e != cudaSuccess) return e;
         g_bwd_attr[dev] = true;
     }
@@ -590,8 +633,8 @@ cudaError_t launch_dgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap,
     CUtensorMap ma, mb;
     if (!make_box_map(&ma, A, rows_cap, K, kBM) || !make_box_map(&mb, B, static_cast<int64_t>(E) * K, N, kBK))
         return cudaErrorInvalidValue;
-    return launch_pdl(false, bgemm_bf16_kernel, persistent_grid(static_cast<int64_t>(j.m_tiles) * j.n_tiles),
-                      kBThreads, kBSmemBytes, st, ma, mb, j);
+    return launch_pdl(false, bgemm_bf16_kernel<false>, persistent_grid(static_cast<int64_t>(j.m_tiles) * j.n_tiles),
+                      kBThreads, BCfg<false>::kSmemBytes, st, ma, mb, j);
 }
 
 // Grouped wgrad: out[e] (FP32 [M][N]) = A[rows of e]^T B[rows of e] with A [rows_cap][M],
@@ -617,8 +660,8 @@ cudaError_t launch_wgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap,
     CUtensorMap ma, mb;
     if (!make_box_map(&ma, A, rows_cap, M, kBK) || !make_box_map(&mb, B, rows_cap, N, kBK))
         return cudaErrorInvalidValue;
-    return launch_pdl(false, bgemm_bf16_kernel, persistent_grid(static_cast<int64_t>(E) * j.m_tiles * j.n_tiles),
-                      kBThreads, kBSmemBytes, st, ma, mb, j);
+    return launch_pdl(false, bgemm_bf16_kernel<true>, persistent_grid(static_cast<int64_t>(E) * j.m_tiles * j.n_tiles),
+                      kBThreads, BCfg<true>::kSmemBytes, st, ma, mb, j);
 }
 
 cudaError_t launch_gather(const uint16_t* src, int C, const BackwardArgs& a, uint16_t* dst, int32_t* real_end,
