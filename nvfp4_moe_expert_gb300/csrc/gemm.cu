@@ -88,8 +88,6 @@ constexpr int kSfaOff = kABytes + kBBytes;            // kMmaPerStage scale tile
 constexpr int kSfbOff = kSfaOff + kMmaPerStage * kSfAtomBytes;   // 2 x kMmaPerStage scale tiles of B
 constexpr int kStageBytes = kSfbOff + 2 * kMmaPerStage * kSfAtomBytes;
 static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
-constexpr int kStagePitch = 144;                      // 128 B of BF16 per row + 16 B pad (no bank conflicts)
-constexpr int kStageWarpBytes = 32 * kStagePitch;     // one warp's 32 rows (FC2 output transpose)
 constexpr int kEpiStageOff = kStages * kStageBytes;
 // SiLU of the BF16 values with 2^-24 <= |a| < 2^7 (bit patterns 0x3380..0x42FF and their
 // negatives): 7936 entries copied from the global table into shared memory per FC1 CTA.
@@ -186,11 +184,8 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
     return r;
 }
 
-// FC1 output: 64 BF16 values (packed[0..31], column pairs) of this lane's row at dst
-// (32-byte aligned) as four 32-byte stores: each lane owns one row, so every store is
-// a whole 32-byte sector and needs no exchange between lanes.  (FC2's rows go to
-// scattered (token, slot) places, where whole 128-byte lines through
-// store_rows_64 write faster.)
+// 64 BF16 values (packed[0..31], column pairs) of this lane's row at dst (32-byte aligned)
+// as four 32-byte stores.
 __device__ __forceinline__ void store_row_64(uint16_t* dst, const uint32_t (&packed)[32]) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -199,34 +194,6 @@ __device__ __forceinline__ void store_row_64(uint16_t* dst, const uint32_t (&pac
                      "r"(packed[8 * k + 4]), "r"(packed[8 * k + 5]), "r"(packed[8 * k + 6]), "r"(packed[8 * k + 7])
                      : "memory");
     }
-}
-
-// FC2 output: the warp's 32 rows x 64 BF16 columns (packed[lane][0..31]) staged through shared
-// memory and written as 8 rows x 128 B per store instruction (32 bytes per lane).  dst_row(r) gives
-// the global address of row r's 64-column chunk, or nullptr to skip the row.
-template <typename RowPtr>
-__device__ __forceinline__ void store_rows_64(uint8_t* stage, const uint32_t (&packed)[32], RowPtr dst_row) {
-    const int lane = threadIdx.x & 31;
-    uint4* mine = reinterpret_cast<uint4*>(stage + lane * kStagePitch);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        mine[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-    }
-    __syncwarp();
-    const int sub = lane & 3;                 // 32-byte quarter of the 128-byte row
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int r = it * 8 + (lane >> 2);
-        const uint4 v0 = *reinterpret_cast<const uint4*>(stage + r * kStagePitch + sub * 32);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(stage + r * kStagePitch + sub * 32 + 16);
-        uint16_t* dst = dst_row(r);
-        if (dst) {
-            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + sub * 16),
-                         "r"(v0.x), "r"(v0.y), "r"(v0.z), "r"(v0.w), "r"(v1.x), "r"(v1.y), "r"(v1.z), "r"(v1.w)
-                         : "memory");
-        }
-    }
-    __syncwarp();
 }
 
 // 32 BF16 values (packed[0..15], column pairs) of this lane's row at dst (32-byte aligned) as
