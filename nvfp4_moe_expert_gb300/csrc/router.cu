@@ -19,8 +19,8 @@
 // warps 2-5 copy the partial logits into shared memory.  After a cluster barrier, CTA c sums
 // rows 32c..32c+31 over the four partials in quarter order, reading the peers' shared memory
 // (distributed shared memory), so a logit is ((q0 + q1) + q2) + q3 whatever T is; one warp per
-// token then picks the top k (k rounds of a warp-wide arg-max) and writes ids and
-// probabilities.  A second cluster barrier keeps every CTA's shared memory alive until its
+// token then picks the top k (k rounds of a 64-bit key maximum over the token's four threads)
+// and writes ids and probabilities.  A second cluster barrier keeps every CTA's shared memory alive until its
 // peers have read it; every thread reaches both barriers on every path.  All pipeline waits
 // are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
 #include <cmath>
@@ -96,11 +96,23 @@ __device__ __forceinline__ void tc_mma_bf16_elect(uint32_t d_tmem, uint64_t ades
         : "memory");
 }
 
-// (va, ia) comes before (vb, ib) in the selection order
-__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
-    return va > vb || (va == vb && ia < ib);
+// Selection key of logit v of expert e: unsigned order = the selection order (a larger logit
+// first, the lower id first on equal logits; -0 and +0 are equal); 0 for a NaN (never picked)
+// and for no expert.  The logit's bits, made order-preserving, above the complemented id.
+__device__ __forceinline__ unsigned long long select_key(float v, int e) {
+    uint32_t b = __float_as_uint(v);
+    if (b == 0x80000000u) b = 0u;
+    if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0ull;
+    const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return (static_cast<unsigned long long>(ord) << 32) | static_cast<uint32_t>(~e);
+}
+__device__ __forceinline__ float key_logit(unsigned long long key) {
+    const uint32_t ord = static_cast<uint32_t>(key >> 32);
+    return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
 }
 
+// kPer: experts per thread (4 threads per token), E <= 4 * kPer
+template <int kPer>
 __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
     router_topk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, int64_t T,
                        int H, int E, int k, int32_t* __restrict__ ids, float* __restrict__ probs,
@@ -246,10 +258,10 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
     if (warp >= 2) {
         // ------------------------------------------------------------ sum, top-k, probabilities
         // This CTA's rows 32*split .. +31 of the tile, four threads per token: thread q of a
-        // token holds the logits of experts q, q + 4, q + 8, ... (each the four quarters'
-        // partials added in quarter order), scans them itself each round and the four
-        // candidates are merged by two shuffles, so every thread knows every pick.
-        constexpr int kPer = kRMaxE / 4;
+        // token holds the selection keys of experts q, q + 4, q + 8, ... (each logit the four
+        // quarters' partials added in quarter order); each round every thread takes its
+        // largest key, two shuffles merge the token's four, and the thread holding the pick
+        // clears it, so every thread knows every pick.
         const int tid = threadIdx.x - 64;                   // 0..127
         const int ti = tid >> 2, q = tid & 3;
         const int r = 32 * static_cast<int>(split) + ti;
@@ -257,18 +269,18 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
         uint32_t peer[kRSplit];
 #pragma unroll
         for (int s = 0; s < kRSplit; ++s) peer[s] = cluster_map(smem_u32(part), static_cast<uint32_t>(s));
-        float v[kPer];
+        unsigned long long key[kPer];
         bool finite = true;
 #pragma unroll
         for (int m = 0; m < kPer; ++m) {
             const int e = q + 4 * m;
-            v[m] = -INFINITY;
+            key[m] = 0ull;
             if (e < E) {
                 const uint32_t off = static_cast<uint32_t>(r * row_stride + e) * 4u;
                 float a = ld_cluster_f32(peer[0] + off);
 #pragma unroll
                 for (int s = 1; s < kRSplit; ++s) a = __fadd_rn(a, ld_cluster_f32(peer[s] + off));
-                v[m] = a;
+                key[m] = select_key(a, e);
                 if (t < T) {
                     finite = finite && (__float_as_uint(a) & 0x7F800000u) != 0x7F800000u;
                     if (logits != nullptr) logits[t * E + e] = a;
@@ -276,54 +288,25 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
             }
         }
         if (!finite) set_device_error(err, NVFP4_ERR_NONFINITE);
-        // k rounds: each takes the first entry, in (logit desc, id asc) order, after the
-        // previous pick; four independent chains per thread, merged, then over the four threads
         float* pick_v = reinterpret_cast<float*>(smem + kRPickOff) + ti * 32;
         int* pick_id = reinterpret_cast<int*>(smem + kRPickOff + 32 * 32 * 4) + ti * 32;
-        float pv = INFINITY;
-        int pid = -1;
         for (int j = 0; j < k; ++j) {
-            float cv[4];
-            int cid[4];
+            unsigned long long best = key[0];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                cv[u] = -INFINITY;
-                cid[u] = -1;
-            }
-#pragma unroll
-            for (int m = 0; m < kPer; ++m) {
-                const int e = q + 4 * m, u = m & 3;
-                if (e < E) {
-                    const bool after = v[m] < pv || (v[m] == pv && e > pid);
-                    if (after && (cid[u] < 0 || before(v[m], e, cv[u], cid[u]))) {
-                        cv[u] = v[m];
-                        cid[u] = e;
-                    }
-                }
-            }
-            float bv = cv[0];
-            int bid = cid[0];
-#pragma unroll
-            for (int u = 1; u < 4; ++u) {
-                if (cid[u] >= 0 && (bid < 0 || before(cv[u], cid[u], bv, bid))) {
-                    bv = cv[u];
-                    bid = cid[u];
-                }
-            }
+            for (int m = 1; m < kPer; ++m) best = key[m] > best ? key[m] : best;
 #pragma unroll
             for (int o = 1; o <= 2; o <<= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-                const int oid = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
-                if (oid >= 0 && (bid < 0 || before(ov, oid, bv, bid))) {
-                    bv = ov;
-                    bid = oid;
-                }
+                const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                best = other > best ? other : best;
             }
-            pv = bv;
-            pid = bid;
+            if (best != 0ull) {
+#pragma unroll
+                for (int m = 0; m < kPer; ++m)
+                    if (key[m] == best) key[m] = 0ull;
+            }
             if (q == 0) {
-                pick_v[j] = bv;
-                pick_id[j] = bid;
+                pick_v[j] = best != 0ull ? key_logit(best) : -INFINITY;
+                pick_id[j] = best != 0ull ? static_cast<int>(~static_cast<uint32_t>(best)) : -1;
             }
         }
         __syncwarp();
@@ -396,7 +379,9 @@ cudaError_t launch_router_topk(const uint16_t* x, int64_t T, int H, const uint16
     {
         std::lock_guard<std::mutex> lock(g_router_mutex);
         if (!g_router_attr[dev]) {
-            e = cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
+            e = cudaFuncSetAttribute(router_topk_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(router_topk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
             if (e != cudaSuccess) return e;
             g_router_attr[dev] = true;
         }
@@ -404,7 +389,10 @@ cudaError_t launch_router_topk(const uint16_t* x, int64_t T, int H, const uint16
     CUtensorMap mx, mw;
     if (!make_bf16_map(&mx, x, T, H, kRBM) || !make_bf16_map(&mw, w, E, H, E)) return cudaErrorInvalidValue;
     const unsigned grid = static_cast<unsigned>((T + kRBM - 1) / kRBM * kRSplit);   // whole clusters
-    return launch_pdl(false, router_topk_kernel, grid, kRThreads, kRSmemBytes, st, mx, mw, T, H, E, k, ids, probs,
+    if (E <= 128)
+        return launch_pdl(false, router_topk_kernel<32>, grid, kRThreads, kRSmemBytes, st, mx, mw, T, H, E, k, ids,
+                          probs, logits, err);
+    return launch_pdl(false, router_topk_kernel<64>, grid, kRThreads, kRSmemBytes, st, mx, mw, T, H, E, k, ids, probs,
                       logits, err);
 }
 
