@@ -47,9 +47,11 @@ constexpr uint32_t kRTmemCols = 256;
 // after the MMAs, the partial logits sit in the idle stage buffers: 128 rows of E floats at a
 // stride of E + 1 (odd: the row-per-thread stores and the column reads are conflict-free)
 static_assert(kRBM * (kRMaxE + 1) * 4 <= kRBarOff, "partial logits fit in the stage buffers");
-// then each token's picks (32 values, 32 ids) for this CTA's 32 tokens
+// then each token's picks (32 values, 32 ids) for this CTA's 32 tokens, then the summed logits
+// of those 32 tokens (stride E + 1)
 constexpr int kRPickOff = kRBM * (kRMaxE + 1) * 4;
-static_assert(kRPickOff + 32 * 32 * 8 <= kRBarOff, "picks fit in the stage buffers");
+constexpr int kRLogitOff = kRPickOff + 32 * 32 * 8;
+static_assert(kRLogitOff + 32 * (kRMaxE + 1) * 4 <= kRBarOff, "picks and logits fit in the stage buffers");
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -67,9 +69,11 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
+// (Not volatile: read only between the two cluster barriers, while no CTA writes the data, so
+// the compiler may batch the loads.)
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 
@@ -257,43 +261,76 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
 
     if (warp >= 2) {
         // ------------------------------------------------------------ sum, top-k, probabilities
-        // This CTA's rows 32*split .. +31 of the tile, four threads per token: thread q of a
-        // token holds the selection keys of experts q, q + 4, q + 8, ... (each logit the four
-        // quarters' partials added in quarter order); each round every thread takes its
+        // This CTA's rows 32*split .. +31 of the tile.  First the sums: warp w of the four adds
+        // rows w, w + 4, ... over the four quarters' partials in quarter order, its lanes over
+        // consecutive experts (each read of a peer's shared memory is 128 contiguous bytes),
+        // into a local copy lg.  Then four threads per token: thread q holds the selection keys
+        // of experts 8q + j + 32i (j < 8; with the row stride E + 1 the 32 lanes of a warp, 8
+        // tokens x 4 threads, read 32 different banks); each round every thread takes its
         // largest key, two shuffles merge the token's four, and the thread holding the pick
         // clears it, so every thread knows every pick.
+        float* lg = reinterpret_cast<float*>(smem + kRLogitOff);
+        {
+            uint32_t peer[kRSplit];
+#pragma unroll
+            for (int s = 0; s < kRSplit; ++s) peer[s] = cluster_map(smem_u32(part), static_cast<uint32_t>(s));
+            bool finite = true;
+            constexpr int kChunks = kPer / 8;               // 32-expert chunks of a row (E <= 4 kPer)
+            for (int ri = warp - 2; ri < 32; ri += 4) {
+                const int r = 32 * static_cast<int>(split) + ri;
+                const int64_t t = m0 + r;
+                float pv[kChunks][kRSplit];                   // all of the row's loads in flight at once
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const int e = 32 * c + lane;
+#pragma unroll
+                    for (int s = 0; s < kRSplit; ++s)
+                        pv[c][s] = e < E ? ld_cluster_f32(peer[s] + static_cast<uint32_t>(r * row_stride + e) * 4u) : 0.0f;
+                }
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const int e = 32 * c + lane;
+                    if (e < E) {
+                        float a = pv[c][0];
+#pragma unroll
+                        for (int s = 1; s < kRSplit; ++s) a = __fadd_rn(a, pv[c][s]);
+                        lg[ri * row_stride + e] = a;
+                        if (t < T) {
+                            finite = finite && (__float_as_uint(a) & 0x7F800000u) != 0x7F800000u;
+                            if (logits != nullptr) logits[t * E + e] = a;
+                        }
+                    }
+                }
+            }
+            if (!finite) set_device_error(err, NVFP4_ERR_NONFINITE);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");    // the four warps' sums are in lg
         const int tid = threadIdx.x - 64;                   // 0..127
         const int ti = tid >> 2, q = tid & 3;
         const int r = 32 * static_cast<int>(split) + ti;
         const int64_t t = m0 + r;
-        uint32_t peer[kRSplit];
-#pragma unroll
-        for (int s = 0; s < kRSplit; ++s) peer[s] = cluster_map(smem_u32(part), static_cast<uint32_t>(s));
         unsigned long long key[kPer];
-        bool finite = true;
 #pragma unroll
-        for (int m = 0; m < kPer; ++m) {
-            const int e = q + 4 * m;
-            key[m] = 0ull;
-            if (e < E) {
-                const uint32_t off = static_cast<uint32_t>(r * row_stride + e) * 4u;
-                float a = ld_cluster_f32(peer[0] + off);
+        for (int i = 0; i < kPer / 8; ++i) {
 #pragma unroll
-                for (int s = 1; s < kRSplit; ++s) a = __fadd_rn(a, ld_cluster_f32(peer[s] + off));
-                key[m] = select_key(a, e);
-                if (t < T) {
-                    finite = finite && (__float_as_uint(a) & 0x7F800000u) != 0x7F800000u;
-                    if (logits != nullptr) logits[t * E + e] = a;
-                }
+            for (int j = 0; j < 8; ++j) {
+                const int e = 8 * q + j + 32 * i;
+                key[8 * i + j] = e < E ? select_key(lg[ti * row_stride + e], e) : 0ull;
             }
         }
-        if (!finite) set_device_error(err, NVFP4_ERR_NONFINITE);
         float* pick_v = reinterpret_cast<float*>(smem + kRPickOff) + ti * 32;
         int* pick_id = reinterpret_cast<int*>(smem + kRPickOff + 32 * 32 * 4) + ti * 32;
         for (int j = 0; j < k; ++j) {
-            unsigned long long best = key[0];
+            // the thread's largest key by a pairwise tree (depth log2 kPer)
+            unsigned long long tr[kPer / 2];
 #pragma unroll
-            for (int m = 1; m < kPer; ++m) best = key[m] > best ? key[m] : best;
+            for (int m = 0; m < kPer / 2; ++m) tr[m] = key[2 * m] > key[2 * m + 1] ? key[2 * m] : key[2 * m + 1];
+#pragma unroll
+            for (int w = kPer / 4; w >= 1; w >>= 1) {
+#pragma unroll
+                for (int m = 0; m < w; ++m) tr[m] = tr[2 * m] > tr[2 * m + 1] ? tr[2 * m] : tr[2 * m + 1];
+            }
+            unsigned long long best = tr[0];
 #pragma unroll
             for (int o = 1; o <= 2; o <<= 1) {
                 const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
