@@ -195,3 +195,68 @@ def test_layer_forward_backward_pipeline():
     for name in ("dx", "dw1", "dprob"):
         assert rel_l2(got[name], ex[name]) <= EXACT_REL_L2[name], (name, rel_l2(got[name], ex[name]))
     assert rel_l2(got["dw2"], ex["dw2"]) <= 1e-3     # h itself comes from the GPU forward here
+
+
+def test_backward_qwen3_30b_a3b_full_size_sampled():
+    """The backward at the size the bench times (4096 tokens, H 2048, I 768, 128 experts, top-8):
+    dW1 and dW2 of three experts over all their pairs, and dX and dprob of six tokens, against the
+    oracle fed with the GPU forward's own saved gate/up and h (so the backward alone is checked).
+    An expert's weight gradients sum over its own pairs only, and a token's dX and dprob over its
+    own k pairs, so each sample is the oracle on that expert's pairs or that token's slots."""
+    cfg = S.CONFIGS["qwen3_30b_a3b"]
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    Lay = S.make_layer(cfg)
+    dout_bits = S.make_grad_out(cfg)
+    w = M.quantize_moe_weights(bf16_to_torch(Lay["w1"]), bf16_to_torch(Lay["w2"]))
+    x = bf16_to_torch(Lay["x"])
+    ws = M.alloc_workspace(T, H, I, E, k)
+    lay = M.moe_workspace_layout_query(T, H, I, E, k)
+    offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    M.moe_route_sort_amax(x, torch.from_numpy(Lay["topk_ids"]).cuda(), torch.from_numpy(Lay["topk_w"]).cuda(), E,
+                          offs, ws)
+    rc = lay.rows_cap
+    fc1_pre = torch.empty((rc, 2 * I), dtype=torch.float32, device="cuda")
+    M.moe_fc1_swiglu_nvfp4(w, T, k, offs, ws, debug=fc1_pre)
+    wt = M.MoEWeightsBF16(bf16_to_torch(Lay["w1"]), bf16_to_torch(Lay["w2"]))
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    dw1 = torch.full((E, 2 * I, H), float("nan"), device="cuda")
+    dw2 = torch.full((E, H, I), float("nan"), device="cuda")
+    dprob = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    bws = M.alloc_backward_workspace(T, H, I, E, k)
+    M.moe_expert_backward_ste(wt, T, k, x, bf16_to_torch(dout_bits), offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws)
+    assert M.nvfp4_get_device_error() == 0
+    # the saved values of every (token, slot): the BF16 gate/up the SwiGLU ran on, and h
+    pair_row = ws[lay.pair_row:lay.pair_row + 4 * T * k].view(torch.int32).cpu().numpy().reshape(T, k)
+    pre = fc1_pre.cpu().numpy()
+    h_rows = ws[lay.h:lay.h + 2 * rc * I].view(torch.int16).cpu().numpy().view(np.uint16).reshape(rc, I)
+
+    def saved(t, s):
+        rows = pair_row[t, s]
+        return F.round_to_bf16_bits(pre[rows]), h_rows[rows]
+
+    ids, p = Lay["topk_ids"], Lay["topk_w"]
+    dw1_g, dw2_g = dw1.cpu().numpy(), dw2.cpu().numpy()
+    for e in (0, 77, 127):
+        t_e, s_e = np.nonzero(ids == e)
+        gu_e, h_e = saved(t_e, s_e)
+        args = (_f(dout_bits[t_e]), _f(Lay["x"][t_e]), np.zeros((len(t_e), 1), np.int32), p[t_e, s_e][:, None],
+                _f(Lay["w1"][e:e + 1]), _f(Lay["w2"][e:e + 1]), _f(gu_e[:, None]), _f(h_e[:, None]))
+        st = OB.moe_backward_ste(*args, bf16_stages=True)
+        ex = OB.moe_backward_ste(*args, bf16_stages=False)
+        assert rel_l2(dw1_g[e], st["dw1"][0]) <= STAGED_REL_L2["dw1"], e
+        assert rel_l2(dw2_g[e], ex["dw2"][0]) <= DW2_REL_L2, e
+    toks = np.sort(np.random.default_rng(1).choice(T, 6, replace=False))
+    dx_g = _f(torch_to_bf16_bits(dx))
+    dprob_g = dprob.cpu().numpy()
+    got_dx, ref_dx, got_p, ref_p = [], [], [], []
+    for t in toks:
+        e_t = ids[t]
+        gu_t, h_t = saved(np.full(k, t), np.arange(k))
+        st = OB.moe_backward_ste(_f(dout_bits[t:t + 1]), _f(Lay["x"][t:t + 1]), np.arange(k, dtype=np.int32)[None],
+                                 p[t:t + 1], _f(Lay["w1"][e_t]), _f(Lay["w2"][e_t]), _f(gu_t[None]), _f(h_t[None]),
+                                 bf16_stages=True)
+        got_dx.append(dx_g[t]), ref_dx.append(st["dx"][0]), got_p.append(dprob_g[t]), ref_p.append(st["dprob"][0])
+    got_dx, ref_dx = np.array(got_dx), np.array(ref_dx)
+    assert np.mean(got_dx == ref_dx) >= STAGED_DX_EQUAL
+    assert rel_l2(got_dx, ref_dx) <= STAGED_REL_L2["dx"]
+    assert rel_l2(np.array(got_p), np.array(ref_p)) <= STAGED_REL_L2["dprob"]
