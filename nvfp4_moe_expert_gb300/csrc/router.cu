@@ -17,12 +17,12 @@
 // per row per stage, 128B swizzle, 4-stage ring) and warp 1 issues tcgen05.mma.kind::f16
 // (M=128, N=E, K=16) into an FP32 TMEM accumulator, walking its quarter in one fixed order;
 // warps 2-5 copy the partial logits into shared memory.  After a cluster barrier, CTA c sums
-// rows 32c..32c+31 over the four partials in quarter order, reading the peers' shared memory
-// (distributed shared memory), so a logit is ((q0 + q1) + q2) + q3 whatever T is; one warp per
-// token then picks the top k (k rounds of a 64-bit key maximum over the token's four threads)
-// and writes ids and probabilities.  A second cluster barrier keeps every CTA's shared memory alive until its
-// peers have read it; every thread reaches both barriers on every path.  All pipeline waits
-// are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
+// rows 32c..32c+31 over the four partials in quarter order on all eight warps, reading the
+// peers' shared memory (distributed shared memory), so a logit is ((q0 + q1) + q2) + q3
+// whatever T is; eight threads per token then pick the top k (k rounds of a 64-bit key
+// maximum) and write ids and probabilities.  A second cluster barrier keeps every CTA's shared
+// memory alive until its peers have read it; every thread reaches both barriers on every
+// path.  All pipeline waits are bounded (NVFP4_ERR_DEVICE_TIMEOUT, then a clean exit).
 #include <cmath>
 #include <mutex>
 
@@ -42,7 +42,8 @@ constexpr int kRBBytes = kRMaxE * kRRowBytes;           // room for 256 expert r
 constexpr int kRStageBytes = kRABytes + kRBBytes;       // 48 KB
 constexpr int kRBarOff = kRStages * kRStageBytes;
 constexpr int kRSmemBytes = kRBarOff + 128 + 1024;
-constexpr int kRThreads = 192;                          // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kRWarps = 8;                              // warp 0 TMA, warp 1 MMA, warps 2-5 partial logits;
+constexpr int kRThreads = 32 * kRWarps;                 // then all eight sum and select
 constexpr uint32_t kRTmemCols = 256;
 // after the MMAs, the partial logits sit in the idle stage buffers: 128 rows of E floats at a
 // stride of E + 1 (odd: the row-per-thread stores and the column reads are conflict-free)
@@ -115,7 +116,7 @@ __device__ __forceinline__ float key_logit(unsigned long long key) {
     return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
 }
 
-// kPer: experts per thread (4 threads per token), E <= 4 * kPer
+// kPer: experts per thread (8 threads per token), E <= 8 * kPer
 template <int kPer>
 __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
     router_topk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, int64_t T,
@@ -230,7 +231,7 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
                 mbar_wait_bounded(tmem_full, 0, nullptr, kWaitBudgetCycles);
             }
         }
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------ partial logits to shared memory
         const int q = warp & 3;                             // TMEM lane quarter
         const int r = q * 32 + lane;                        // row of the tile
@@ -259,24 +260,24 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
     __syncthreads();
     cluster_barrier();                                      // every CTA's partial logits are in place
 
-    if (warp >= 2) {
+    {
         // ------------------------------------------------------------ sum, top-k, probabilities
-        // This CTA's rows 32*split .. +31 of the tile.  First the sums: warp w of the four adds
-        // rows w, w + 4, ... over the four quarters' partials in quarter order, its lanes over
-        // consecutive experts (each read of a peer's shared memory is 128 contiguous bytes),
-        // into a local copy lg.  Then four threads per token: thread q holds the selection keys
-        // of experts 8q + j + 32i (j < 8; with the row stride E + 1 the 32 lanes of a warp, 8
-        // tokens x 4 threads, read 32 different banks); each round every thread takes its
-        // largest key, two shuffles merge the token's four, and the thread holding the pick
-        // clears it, so every thread knows every pick.
+        // This CTA's rows 32*split .. +31 of the tile, on all eight warps.  First the sums: warp w
+        // adds rows w, w + 8, ... over the four quarters' partials in quarter order, its lanes
+        // over consecutive experts (each read of a peer's shared memory is 128 contiguous
+        // bytes), into a local copy lg.  Then eight threads per token: thread q holds the
+        // selection keys of experts 4q + j + 32i (j < 4; with the row stride E + 1 the 32 lanes
+        // of a warp, 4 tokens x 8 threads, read 32 different banks); each round every thread
+        // takes its largest key, three shuffles merge the token's eight, and the thread holding
+        // the pick clears it, so every thread knows every pick.
         float* lg = reinterpret_cast<float*>(smem + kRLogitOff);
         {
             uint32_t peer[kRSplit];
 #pragma unroll
             for (int s = 0; s < kRSplit; ++s) peer[s] = cluster_map(smem_u32(part), static_cast<uint32_t>(s));
             bool finite = true;
-            constexpr int kChunks = kPer / 8;               // 32-expert chunks of a row (E <= 4 kPer)
-            for (int ri = warp - 2; ri < 32; ri += 4) {
+            constexpr int kChunks = kPer / 4;               // 32-expert chunks of a row (E <= 8 kPer)
+            for (int ri = warp; ri < 32; ri += kRWarps) {
                 const int r = 32 * static_cast<int>(split) + ri;
                 const int64_t t = m0 + r;
                 float pv[kChunks][kRSplit];                   // all of the row's loads in flight at once
@@ -304,18 +305,17 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
             }
             if (!finite) set_device_error(err, NVFP4_ERR_NONFINITE);
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");    // the four warps' sums are in lg
-        const int tid = threadIdx.x - 64;                   // 0..127
-        const int ti = tid >> 2, q = tid & 3;
+        __syncthreads();                                    // every row's sums are in lg
+        const int ti = threadIdx.x >> 3, q = threadIdx.x & 7;
         const int r = 32 * static_cast<int>(split) + ti;
         const int64_t t = m0 + r;
         unsigned long long key[kPer];
 #pragma unroll
-        for (int i = 0; i < kPer / 8; ++i) {
+        for (int i = 0; i < kPer / 4; ++i) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = 8 * q + j + 32 * i;
-                key[8 * i + j] = e < E ? select_key(lg[ti * row_stride + e], e) : 0ull;
+            for (int j = 0; j < 4; ++j) {
+                const int e = 4 * q + j + 32 * i;
+                key[4 * i + j] = e < E ? select_key(lg[ti * row_stride + e], e) : 0ull;
             }
         }
         float* pick_v = reinterpret_cast<float*>(smem + kRPickOff) + ti * 32;
@@ -332,7 +332,7 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
             }
             unsigned long long best = tr[0];
 #pragma unroll
-            for (int o = 1; o <= 2; o <<= 1) {
+            for (int o = 1; o <= 4; o <<= 1) {
                 const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
                 best = other > best ? other : best;
             }
@@ -348,12 +348,12 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
         }
         __syncwarp();
         // p_j = exp(l_j - l_1) / sum over the picks in slot order, in FP32 (each of the token's
-        // threads sums the same terms in the same order); thread q writes slots q, q + 4, ...
+        // threads sums the same terms in the same order); thread q writes slots q, q + 8, ...
         const float l1 = pick_id[0] < 0 ? 0.0f : pick_v[0];
         float sum = 0.0f;
         for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, pick_id[j] < 0 ? 0.0f : expf(__fsub_rn(pick_v[j], l1)));
         if (t < T) {
-            for (int j = q; j < k; j += 4) {
+            for (int j = q; j < k; j += 8) {
                 const int id = pick_id[j];
                 ids[t * k + j] = id < 0 ? 0 : id;
                 probs[t * k + j] = id < 0 ? 0.0f : __fdiv_rn(expf(__fsub_rn(pick_v[j], l1)), sum);
@@ -416,9 +416,9 @@ cudaError_t launch_router_topk(const uint16_t* x, int64_t T, int H, const uint16
     {
         std::lock_guard<std::mutex> lock(g_router_mutex);
         if (!g_router_attr[dev]) {
-            e = cudaFuncSetAttribute(router_topk_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
+            e = cudaFuncSetAttribute(router_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
             if (e != cudaSuccess) return e;
-            e = cudaFuncSetAttribute(router_topk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
+            e = cudaFuncSetAttribute(router_topk_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
             if (e != cudaSuccess) return e;
             g_router_attr[dev] = true;
         }
@@ -427,9 +427,9 @@ cudaError_t launch_router_topk(const uint16_t* x, int64_t T, int H, const uint16
     if (!make_bf16_map(&mx, x, T, H, kRBM) || !make_bf16_map(&mw, w, E, H, E)) return cudaErrorInvalidValue;
     const unsigned grid = static_cast<unsigned>((T + kRBM - 1) / kRBM * kRSplit);   // whole clusters
     if (E <= 128)
-        return launch_pdl(false, router_topk_kernel<32>, grid, kRThreads, kRSmemBytes, st, mx, mw, T, H, E, k, ids,
+        return launch_pdl(false, router_topk_kernel<16>, grid, kRThreads, kRSmemBytes, st, mx, mw, T, H, E, k, ids,
                           probs, logits, err);
-    return launch_pdl(false, router_topk_kernel<64>, grid, kRThreads, kRSmemBytes, st, mx, mw, T, H, E, k, ids, probs,
+    return launch_pdl(false, router_topk_kernel<32>, grid, kRThreads, kRSmemBytes, st, mx, mw, T, H, E, k, ids, probs,
                       logits, err);
 }
 
