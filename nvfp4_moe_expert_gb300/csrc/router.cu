@@ -267,9 +267,9 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
         // over consecutive experts (each read of a peer's shared memory is 128 contiguous
         // bytes), into a local copy lg.  Then eight threads per token: thread q holds the
         // selection keys of experts 4q + j + 32i (j < 4; with the row stride E + 1 the 32 lanes
-        // of a warp, 4 tokens x 8 threads, read 32 different banks); each round every thread
-        // takes its largest key, three shuffles merge the token's eight, and the thread holding
-        // the pick clears it, so every thread knows every pick.
+        // of a warp, 4 tokens x 8 threads, read 32 different banks) and sorts them once; each
+        // round three shuffles find the largest head of the token's eight sorted lists, and the
+        // thread holding it moves on, so every thread knows every pick.
         float* lg = reinterpret_cast<float*>(smem + kRLogitOff);
         {
             uint32_t peer[kRSplit];
@@ -320,26 +320,37 @@ __global__ void __cluster_dims__(kRSplit, 1, 1) __launch_bounds__(kRThreads, 1)
         }
         float* pick_v = reinterpret_cast<float*>(smem + kRPickOff) + ti * 32;
         int* pick_id = reinterpret_cast<int*>(smem + kRPickOff + 32 * 32 * 4) + ti * 32;
-        for (int j = 0; j < k; ++j) {
-            // the thread's largest key by a pairwise tree (depth log2 kPer)
-            unsigned long long tr[kPer / 2];
+        // the thread's keys in descending order (bitonic network, compile-time indices)
 #pragma unroll
-            for (int m = 0; m < kPer / 2; ++m) tr[m] = key[2 * m] > key[2 * m + 1] ? key[2 * m] : key[2 * m + 1];
+        for (int size = 2; size <= kPer; size <<= 1) {
 #pragma unroll
-            for (int w = kPer / 4; w >= 1; w >>= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
 #pragma unroll
-                for (int m = 0; m < w; ++m) tr[m] = tr[2 * m] > tr[2 * m + 1] ? tr[2 * m] : tr[2 * m + 1];
+                for (int i = 0; i < kPer; ++i) {
+                    const int l = i ^ stride;
+                    if (l > i) {
+                        const bool desc = (i & size) == 0;   // this pair's direction in the merge
+                        const unsigned long long a = key[i], b = key[l];
+                        const bool swap = desc ? (a < b) : (a > b);
+                        key[i] = swap ? b : a;
+                        key[l] = swap ? a : b;
+                    }
+                }
             }
-            unsigned long long best = tr[0];
+        }
+        // k rounds: the largest head of the token's eight lists is the next pick; its owner
+        // moves on to its next key
+        for (int j = 0; j < k; ++j) {
+            unsigned long long best = key[0];
 #pragma unroll
             for (int o = 1; o <= 4; o <<= 1) {
                 const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
                 best = other > best ? other : best;
             }
-            if (best != 0ull) {
+            if (best != 0ull && key[0] == best) {
 #pragma unroll
-                for (int m = 0; m < kPer; ++m)
-                    if (key[m] == best) key[m] = 0ull;
+                for (int m = 0; m + 1 < kPer; ++m) key[m] = key[m + 1];
+                key[kPer - 1] = 0ull;
             }
             if (q == 0) {
                 pick_v[j] = best != 0ull ? key_logit(best) : -INFINITY;
