@@ -693,13 +693,16 @@ int block_lanes_passes(int I) {
     return P <= kBlockLanesMaxPasses ? P : 0;
 }
 
-template <int P>
+// ICT: the width I compiled in (0: I_rt at run time); with it the index and scale-tile address
+// arithmetic folds to constants (I = 768 and 1536: 8-9% fewer cycles).
+template <int P, int ICT = 0>
 __global__ void __launch_bounds__(256, P <= 3 ? 4 : 2) requant_blocks_kernel(const uint16_t* __restrict__ h,
                                                              const uint32_t* __restrict__ amax2,
                                                              const int32_t* __restrict__ row_pair,
-                                                             const int32_t* __restrict__ offsets, int E, int I,
+                                                             const int32_t* __restrict__ offsets, int E, int I_rt,
                                                              uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                              float* __restrict__ g, int* err) {
+    const int I = ICT ? ICT : I_rt;
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -890,7 +893,12 @@ cudaError_t launch_requant(const uint16_t* h, const uint32_t* amax2, const int32
         switch (P) {
             case 1: return launch_pdl(pdl, requant_blocks_kernel<1>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
             case 2: return launch_pdl(pdl, requant_blocks_kernel<2>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
-            case 3: return launch_pdl(pdl, requant_blocks_kernel<3>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
+            case 3:
+                if (I == 768)
+                    return launch_pdl(pdl, requant_blocks_kernel<3, 768>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
+                if (I == 1536)
+                    return launch_pdl(pdl, requant_blocks_kernel<3, 1536>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
+                return launch_pdl(pdl, requant_blocks_kernel<3>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
             case 4: return launch_pdl(pdl, requant_blocks_kernel<4>, grid, 256, 0, st, h, amax2, row_pair, offsets, E, I, codes, sf, g, err);
             default: break;
         }
