@@ -26,11 +26,12 @@
 // the expert's routed rows) is loaded as 64-row x 128-byte TMA boxes (128B swizzle) and handed
 // to tcgen05.mma.kind::f16 through MN-major shared-memory descriptors; dy and [da, du] in the
 // activation gradients are K-major as stored.  One persistent CTA per SM walks a static tile
-// list: warp 0 issues the TMA loads into a four-stage ring, warp 1 the MMAs (M=128, N=128 or
-// 256) into one of two TMEM accumulators, and warps 2-9 read the other accumulator (two warps
-// per TMEM lane quarter, each half of the columns) and store it, so a tile's stores overlap
-// the next tile's loads and MMAs.  Each tile walks K in one fixed order, so a token's dX and
-// dprob do not depend on the other tokens.
+// list: warp 0 issues the TMA loads into a stage ring (four stages for the activation
+// gradients, three for the weight gradients), warp 1 the MMAs (M=128, N=128 or 256) into one
+// of two TMEM accumulators, and warps 2-9 read the other accumulator (two warps per TMEM lane
+// quarter, each half of the columns) and store it through a small shared-memory tile as whole
+// row segments, so a tile's stores overlap the next tile's loads and MMAs.  Each tile walks K
+// in one fixed order, so a token's dX and dprob do not depend on the other tokens.
 //
 // Pad rows: the forward's h holds whatever was there before in an expert's pad rows (FC1 does
 // not store them), so the weight gradients stop at each expert's last real row (found once per
