@@ -107,10 +107,13 @@ CASES = [
     dict(H=256, I=128, E=9, k=2, T=300, seed=1, unused_experts=1),          # N = 128 tiles, an empty expert
     dict(H=512, I=256, E=16, k=4, T=200, seed=2, routing="zipf"),           # N = 256 tiles, skewed routing
     dict(H=256, I=384, E=4, k=2, T=150, seed=3),                            # I % 256 = 128
+    dict(H=256, I=128, E=300, k=2, T=200, seed=7, unused_experts=40),       # many experts, most with a
+                                                                            # few rows, 40+ empty
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=["h256_i128_e9", "h512_i256_e16_zipf", "h256_i384_e4"])
+@pytest.mark.parametrize("case", CASES, ids=["h256_i128_e9", "h512_i256_e16_zipf", "h256_i384_e4",
+                                             "h256_i128_e300"])
 def test_backward_matches_oracle(case):
     c = make_case(**case)
     g = gpu_backward(c)
