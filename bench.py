@@ -224,12 +224,12 @@ def layer_roofline(cfg, peaks, peak_kind, ms_per_step):
 def backward_work(cfg):
     """Algorithmic FLOPs and bytes of one moe_expert_backward_ste call: four BF16 GEMMs
     (2RHI, 2R(2I)H, 2RHI, 2R(2I)H FLOPs); the BF16 weights read once, the FP32
-    weight gradients written once, x, dOut, the saved h (BF16) and FC1 values (FP32) read,
-    dX and dprob written."""
+    weight gradients written once, x, dOut, the saved h and gate/up (BF16) read, dX and
+    dprob written."""
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
     R = T * k
     flops = 12 * R * H * I
-    nbytes = (E * 3 * I * H * 2 + E * 3 * I * H * 4 + 2 * T * H * 2 + R * I * 2 + R * 2 * I * 4
+    nbytes = (E * 3 * I * H * 2 + E * 3 * I * H * 4 + 2 * T * H * 2 + R * I * 2 + R * 2 * I * 2
               + T * H * 2 + R * 4)
     return {"flops": flops, "bytes": nbytes}
 
@@ -851,7 +851,7 @@ def backward_step(M, torch, cfg, weights, w1, w2, x, ids, pw, ws, offs, flush, s
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
     wt = M.MoEWeightsBF16(w1, w2)
     lay = M.moe_workspace_layout_query(T, H, I, E, k)
-    fc1_pre = torch.empty((lay.rows_cap, 2 * I), dtype=torch.float32, device=dev)
+    gu = torch.empty((lay.rows_cap, 2 * I), dtype=torch.bfloat16, device=dev)
     dout = to_dev(S.make_grad_out(cfg))
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -860,13 +860,13 @@ def backward_step(M, torch, cfg, weights, w1, w2, x, ids, pw, ws, offs, flush, s
     dprob = torch.empty((T, k), dtype=torch.float32, device=dev)
     bws = M.alloc_backward_workspace(T, H, I, E, k, dev)
     M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
-    M.moe_fc1_swiglu_nvfp4(weights, T, k, offs, ws, debug=fc1_pre)
+    M.moe_fc1_swiglu_save_nvfp4(weights, T, k, offs, ws, gu)
     M.moe_requant_nvfp4(weights, T, k, offs, ws)
     M.moe_fc2_nvfp4(weights, T, k, offs, ws)
     M.moe_combine_bf16(weights, T, k, out, ws)
 
     def bwd():
-        M.moe_expert_backward_ste(wt, T, k, x, dout, offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws)
+        M.moe_expert_backward_ste(wt, T, k, x, dout, offs, ws, gu, dx, dw1, dw2, dprob, bws)
 
     for _ in range(3):
         bwd()

@@ -266,6 +266,18 @@ nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int
 nvfp4_status moe_fc1_swiglu_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
                                   const int32_t* expert_offsets_dev, void* ws_dev,
                                   size_t ws_bytes, float* fc1_debug_dev, void* stream);
+/* moe_fc1_swiglu_save_nvfp4 -- moe_fc1_swiglu_nvfp4 for a forward whose backward
+ * will run (moe_expert_backward_ste): the same h and FC2 maxima, and the BF16 gate
+ * and up values that the SwiGLU ran on, which the backward takes its SwiGLU
+ * derivative at ([miniTE/differs]: the backward works on saved BF16
+ * values).  gu_save_dev: BF16 [rows_cap][2I] (gate columns then up columns) of
+ * every real routed row, pad rows not written; device memory owned by the caller,
+ * 4-byte aligned (16-byte for the backward that reads it).  Other arguments and
+ * errors as for moe_fc1_swiglu_nvfp4 (contiguous layout only); NVFP4_ERR_INVALID_ARG
+ * if gu_save_dev is NULL or misaligned. */
+nvfp4_status moe_fc1_swiglu_save_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
+                                       const int32_t* expert_offsets_dev, void* ws_dev,
+                                       size_t ws_bytes, void* gu_save_dev, void* stream);
 nvfp4_status moe_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k,
                                const int32_t* expert_offsets_dev, void* ws_dev,
                                size_t ws_bytes, void* stream);
@@ -392,8 +404,9 @@ size_t moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k);
  *  expert_offsets_dev   as moe_route_sort_amax wrote it for this forward (contiguous layout)
  *  fwd_ws_dev, fwd_ws_bytes  the forward's workspace after the forward (its row map, router
  *                       probabilities and h are read)
- *  fc1_pre_dev          FP32 [rows_cap][2I], what moe_fc1_swiglu_nvfp4 wrote to its
- *                       fc1_debug_dev in this forward; 16-byte aligned
+ *  gu_dev               BF16 [rows_cap][2I], what moe_fc1_swiglu_save_nvfp4 wrote to its
+ *                       gu_save_dev in this forward (the BF16 gate/up of every real routed
+ *                       row); 16-byte aligned
  *  dx_dev               BF16 [T][H] out; 16-byte aligned
  *  dw1_dev, dw2_dev     FP32 [E][2I][H] and [E][H][I] out (overwritten); 32-byte aligned
  *  dprob_dev            FP32 [T][k] out, the gradient of topk_w; 4-byte aligned
@@ -405,7 +418,7 @@ size_t moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k);
  * pipeline wait ran out). */
 nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int k, const void* x_dev,
                                      const void* dout_dev, const int32_t* expert_offsets_dev, const void* fwd_ws_dev,
-                                     size_t fwd_ws_bytes, const float* fc1_pre_dev, void* dx_dev, float* dw1_dev,
+                                     size_t fwd_ws_bytes, const void* gu_dev, void* dx_dev, float* dw1_dev,
                                      float* dw2_dev, float* dprob_dev, void* bwd_ws_dev, size_t bwd_ws_bytes,
                                      void* stream);
 

@@ -5,7 +5,7 @@ CUDA kernels; PyTorch provides device memory and the current stream.  The
 entry points have the names of the C ABI in ``include/nvfp4_moe.h``:
 
     nvfp4_quantize_rows, moe_route_sort_amax, moe_expert_forward_nvfp4,
-    moe_fc1_swiglu_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_fc2_requant_nvfp4, moe_combine_bf16,
+    moe_fc1_swiglu_nvfp4, moe_fc1_swiglu_save_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_fc2_requant_nvfp4, moe_combine_bf16,
     moe_workspace_bytes, moe_workspace_layout_query, nvfp4_sf_bytes,
     nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string, nvfp4_silu_table,
     moe_router_topk, the fixed-capacity moe_*_masked calls, and the
@@ -80,6 +80,7 @@ _SIGNATURES = {
     "moe_route_sort_amax": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_forward_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _P, _SZ, _P]),
     "moe_fc1_swiglu_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
+    "moe_fc1_swiglu_save_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_requant_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
     "moe_fc2_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_combine_bf16": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
@@ -323,6 +324,15 @@ def moe_fc1_swiglu_nvfp4(weights, T, k, expert_offsets, ws, debug=None, stream=N
         weights.ref(), T, k, _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(debug), _stream(stream)))
 
 
+def moe_fc1_swiglu_save_nvfp4(weights, T, k, expert_offsets, ws, gu_save, stream=None):
+    """FC1 + SwiGLU x prob that also saves the BF16 gate/up [rows_cap, 2I] for the backward."""
+    if gu_save.dtype != torch.bfloat16 or gu_save.dim() != 2 or gu_save.shape[1] != 2 * weights.I:
+        raise ValueError("gu_save must be a bfloat16 [rows_cap, 2I] tensor")
+    _need_cuda(expert_offsets, ws, gu_save)
+    _check("moe_fc1_swiglu_save_nvfp4", lib().moe_fc1_swiglu_save_nvfp4(
+        weights.ref(), T, k, _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(gu_save), _stream(stream)))
+
+
 def moe_requant_nvfp4(weights, T, k, expert_offsets, ws, stream=None):
     _need_cuda(expert_offsets, ws)
     _check("moe_requant_nvfp4", lib().moe_requant_nvfp4(
@@ -387,10 +397,11 @@ def alloc_backward_workspace(T, H, I, E, k, device="cuda"):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def moe_expert_backward_ste(wt, T, k, x, dout, expert_offsets, ws, fc1_pre, dx, dw1, dw2, dprob, bws,
+def moe_expert_backward_ste(wt, T, k, x, dout, expert_offsets, ws, gu, dx, dw1, dw2, dprob, bws,
                             stream=None):
     """STE gradients (dx, dw1, dw2, dprob written in place) of the forward whose route
-    sort filled `ws` / `expert_offsets` and whose FC1 stage wrote `fc1_pre`."""
+    sort filled `ws` / `expert_offsets` and whose FC1 stage (moe_fc1_swiglu_save_nvfp4)
+    saved the BF16 gate/up `gu` [rows_cap, 2I]."""
     E, H, I = wt.E, wt.H, wt.I
     want = ((x, torch.bfloat16, (T, H)), (dout, torch.bfloat16, (T, H)), (dx, torch.bfloat16, (T, H)),
             (dw1, torch.float32, (E, 2 * I, H)), (dw2, torch.float32, (E, H, I)), (dprob, torch.float32, (T, k)),
@@ -399,11 +410,13 @@ def moe_expert_backward_ste(wt, T, k, x, dout, expert_offsets, ws, fc1_pre, dx, 
         if T > 0 or t is dw1 or t is dw2:
             if t.dtype != dt or tuple(t.shape) != shape:
                 raise ValueError(f"expected {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
-    if T > 0 and (fc1_pre.dtype != torch.float32 or fc1_pre.numel() < 2 * I * nvfp4_rows_padded(1)):
-        raise ValueError("fc1_pre must be the float32 [rows_cap, 2I] buffer FC1 wrote")
-    _need_cuda(x, dout, expert_offsets, ws, fc1_pre, dx, dw1, dw2, dprob, bws)
+    if T > 0:
+        rows_cap = moe_workspace_layout_query(T, H, I, E, k).rows_cap
+        if gu.dtype != torch.bfloat16 or tuple(gu.shape) != (rows_cap, 2 * I):
+            raise ValueError(f"gu must be the bfloat16 [{rows_cap}, {2 * I}] gate/up FC1 saved")
+    _need_cuda(x, dout, expert_offsets, ws, gu, dx, dw1, dw2, dprob, bws)
     _check("moe_expert_backward_ste", lib().moe_expert_backward_ste(
-        wt.ref(), T, k, _ptr(x), _ptr(dout), _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(fc1_pre),
+        wt.ref(), T, k, _ptr(x), _ptr(dout), _ptr(expert_offsets), _ptr(ws), ws.numel(), _ptr(gu),
         _ptr(dx), _ptr(dw1), _ptr(dw2), _ptr(dprob), _ptr(bws), bws.numel(), _stream(stream)))
 
 
@@ -472,12 +485,12 @@ class MoELayer:
             moe_expert_forward_nvfp4(self.weights, T, k, offs, out, ws, stream=stream)
             return out
         L = moe_workspace_layout_query(T, self.H, self.I, self.E, k)
-        fc1_pre = torch.empty((L.rows_cap, 2 * self.I), dtype=torch.float32, device=x.device)
-        moe_fc1_swiglu_nvfp4(self.weights, T, k, offs, ws, debug=fc1_pre, stream=stream)
+        gu = torch.empty((L.rows_cap, 2 * self.I), dtype=torch.bfloat16, device=x.device)
+        moe_fc1_swiglu_save_nvfp4(self.weights, T, k, offs, ws, gu, stream=stream)
         moe_requant_nvfp4(self.weights, T, k, offs, ws, stream=stream)
         moe_fc2_nvfp4(self.weights, T, k, offs, ws, stream=stream)
         moe_combine_bf16(self.weights, T, k, out, ws, stream=stream)
-        self._saved = (x, offs, ws, fc1_pre, T, k, (self._wver, self._gen))
+        self._saved = (x, offs, ws, gu, T, k, (self._wver, self._gen))
         return out
 
     def backward(self, dout, stream=None):
@@ -485,7 +498,7 @@ class MoELayer:
         last forward run with save_for_backward=True."""
         if self._saved is None:
             raise RuntimeError("backward needs a forward with save_for_backward=True")
-        x, offs, ws, fc1_pre, T, k, (wver, gen) = self._saved
+        x, offs, ws, gu, T, k, (wver, gen) = self._saved
         if self._weight_version() != wver or self._gen != gen:
             raise RuntimeError("the weights changed after the forward this backward belongs to")
         wt = MoEWeightsBF16(*self._w_bf16)
@@ -495,7 +508,7 @@ class MoELayer:
         dw2 = torch.empty((self.E, self.H, self.I), dtype=torch.float32, device=dev)
         dprob = torch.empty((T, k), dtype=torch.float32, device=dev)
         bws = alloc_backward_workspace(T, self.H, self.I, self.E, k, dev)
-        moe_expert_backward_ste(wt, T, k, x, dout, offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws,
+        moe_expert_backward_ste(wt, T, k, x, dout, offs, ws, gu, dx, dw1, dw2, dprob, bws,
                                 stream=stream)
         return dx, dw1, dw2, dprob
 

@@ -379,7 +379,8 @@ size_t moe_workspace_bytes_masked(int64_t T, int H, int I, int E, int k, int cap
 }
 
 static nvfp4_status moe_fc1_swiglu_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
-                                  void* ws_dev, size_t ws_bytes, float* fc1_debug_dev, void* stream, bool pdl, int capacity = 0) {
+                                  void* ws_dev, size_t ws_bytes, float* fc1_debug_dev, void* stream, bool pdl, int capacity = 0,
+                                  uint16_t* gu_save = nullptr) {
     moe_workspace_layout L;
     const nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
     if (s != NVFP4_OK) return s;
@@ -387,8 +388,9 @@ static nvfp4_status moe_fc1_swiglu_nvfp4_impl(const moe_nvfp4_weights* w, int64_
     if (T == 0) return NVFP4_OK;
     int* err = device_error_ptr();
     if (!err) return NVFP4_ERR_CUDA;
-    return from_cuda(launch_fc1(fc1_args(w, expert_offsets_dev, ws_dev, L, fc1_debug_dev, err),
-                                static_cast<cudaStream_t>(stream), pdl));
+    GemmArgs a = fc1_args(w, expert_offsets_dev, ws_dev, L, fc1_debug_dev, err);
+    a.gu_save = gu_save;
+    return from_cuda(launch_fc1(a, static_cast<cudaStream_t>(stream), pdl));
 }
 
 static nvfp4_status moe_requant_nvfp4_impl(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
@@ -470,6 +472,13 @@ nvfp4_status moe_fc1_swiglu_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, 
     return moe_fc1_swiglu_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, fc1_debug_dev, stream, false);
 }
 
+nvfp4_status moe_fc1_swiglu_save_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
+                                       void* ws_dev, size_t ws_bytes, void* gu_save_dev, void* stream) {
+    if (!gu_save_dev || !aligned(gu_save_dev, 4)) return NVFP4_ERR_INVALID_ARG;
+    return moe_fc1_swiglu_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, nullptr, stream, false, 0,
+                                     static_cast<uint16_t*>(gu_save_dev));
+}
+
 nvfp4_status moe_requant_nvfp4(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* expert_offsets_dev,
                                void* ws_dev, size_t ws_bytes, void* stream) {
     return moe_requant_nvfp4_impl(w, T, k, expert_offsets_dev, ws_dev, ws_bytes, stream, false);
@@ -547,7 +556,7 @@ size_t moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k) {
 
 nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int k, const void* x_dev,
                                      const void* dout_dev, const int32_t* expert_offsets_dev, const void* fwd_ws_dev,
-                                     size_t fwd_ws_bytes, const float* fc1_pre_dev, void* dx_dev, float* dw1_dev,
+                                     size_t fwd_ws_bytes, const void* gu_dev, void* dx_dev, float* dw1_dev,
                                      float* dw2_dev, float* dprob_dev, void* bwd_ws_dev, size_t bwd_ws_bytes,
                                      void* stream) {
     if (!w) return NVFP4_ERR_INVALID_ARG;
@@ -562,11 +571,11 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
         if (e == cudaSuccess) e = cudaMemsetAsync(dw2_dev, 0, static_cast<size_t>(E) * H * I * 4, st);
         return from_cuda(e);
     }
-    if (!x_dev || !dout_dev || !expert_offsets_dev || !fwd_ws_dev || !fc1_pre_dev || !dx_dev || !dprob_dev ||
+    if (!x_dev || !dout_dev || !expert_offsets_dev || !fwd_ws_dev || !gu_dev || !dx_dev || !dprob_dev ||
         !bwd_ws_dev)
         return NVFP4_ERR_INVALID_ARG;
     if (!aligned(x_dev, 16) || !aligned(dout_dev, 16) || !aligned(expert_offsets_dev, 4) || !aligned(fwd_ws_dev, 256) ||
-        !aligned(fc1_pre_dev, 16) || !aligned(dx_dev, 16) || !aligned(dprob_dev, 4) || !aligned(bwd_ws_dev, 256))
+        !aligned(gu_dev, 16) || !aligned(dx_dev, 16) || !aligned(dprob_dev, 4) || !aligned(bwd_ws_dev, 256))
         return NVFP4_ERR_INVALID_ARG;
     moe_workspace_layout L;
     compute_layout(T, H, I, E, k, &L);
@@ -593,7 +602,7 @@ nvfp4_status moe_expert_backward_ste(const moe_bf16_weights_t* w, int64_t T, int
     a.row_pair = at<int32_t>(fws, L.row_pair);
     a.row_prob = at<float>(fws, L.row_prob);
     a.h = at<uint16_t>(fws, L.h);
-    a.fc1_pre = fc1_pre_dev;
+    a.gu = static_cast<const uint16_t*>(gu_dev);
     a.dx = static_cast<uint16_t*>(dx_dev);
     a.dw1 = dw1_dev;
     a.dw2 = dw2_dev;

@@ -12,7 +12,7 @@
 // token*k + slot, t(r) its token, p(r) its router probability):
 //   dY rows    dy[r] = dOut[t(r)]                                        (gather)
 //   FC2 dgrad  dh[r] = bf16( dy[r] W2[e] )                  BF16 GEMM, FP32 accumulation
-//   SwiGLU     a, u = bf16 of the forward's FC1 values of r (the gate/up the SwiGLU ran on),
+//   SwiGLU     a, u = the forward's BF16 gate/up of r (saved by FC1; the values SwiGLU ran on),
 //              s = 1/(1+exp(-a)):  da = bf16(dh*p*u*s*(1+a*(1-s))),  du = bf16(dh*p*a*s),
 //              dprob[pair(r)] = sum_i dh_i*(a_i*s_i)*u_i               (FP32)
 //   FC1 dgrad  dxs[pair(r)] = bf16( [da, du] W1[e] )        BF16 GEMM
@@ -492,13 +492,13 @@ __global__ void __launch_bounds__(256)
 }
 
 // The SwiGLU x prob derivative, one warp per routed row r < offsets[E]:
-//   a, u = bf16(fc1_pre[r][i]), bf16(fc1_pre[r][I + i]) (the forward's gate and up), s = sigma(a)
+//   a, u = gu[r][i], gu[r][I + i] (the forward's BF16 gate and up), s = sigma(a)
 //   dgu[r][i] = bf16(dh*p*u*s*(1 + a*(1-s))),  dgu[r][I + i] = bf16(dh*p*(a*s))
 //   dprob[row_pair[r]] = sum_i dh_i*(a_i*s_i)*u_i   (FP32; per lane in column order, then a
 //                                                    fixed butterfly over the lanes)
 // A pad row gets zeros.  I % 8 == 0.
 __global__ void __launch_bounds__(256)
-    swiglu_bwd_kernel(const uint16_t* __restrict__ dh, const float* __restrict__ fc1_pre,
+    swiglu_bwd_kernel(const uint16_t* __restrict__ dh, const uint16_t* __restrict__ gu,
                       const int32_t* __restrict__ row_pair, const float* __restrict__ row_prob,
                       const int32_t* __restrict__ offsets, int E, int I, uint16_t* __restrict__ dgu,
                       float* __restrict__ dprob) {
@@ -514,21 +514,20 @@ __global__ void __launch_bounds__(256)
     }
     const float p = row_prob[r];
     const uint4* dhr = reinterpret_cast<const uint4*>(dh + r * I);
-    const float4* gate = reinterpret_cast<const float4*>(fc1_pre + r * 2 * I);
-    const float4* up = gate + I / 4;
+    const uint4* gate = reinterpret_cast<const uint4*>(gu + r * 2 * I);
+    const uint4* up = gate + nvec;
     float acc = 0.0f;
     for (int c = lane; c < nvec; c += 32) {
-        const uint4 d4 = dhr[c];
-        const float4 g0 = gate[2 * c], g1 = gate[2 * c + 1], u0 = up[2 * c], u1 = up[2 * c + 1];
+        const uint4 d4 = dhr[c], g4 = gate[c], u4 = up[c];
         const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
-        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        const float uvr[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+        const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
         float da[8], du[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float dhv = (j & 1) ? bf16_hi(dw[j >> 1]) : bf16_lo(dw[j >> 1]);
-            const uint32_t ab = pack_bf16x2(gv[j], uvr[j]);      // the forward's BF16 gate and up
-            const float a = bf16_lo(ab), u = bf16_hi(ab);
+            const float a = (j & 1) ? bf16_hi(gw[j >> 1]) : bf16_lo(gw[j >> 1]);
+            const float u = (j & 1) ? bf16_hi(uw[j >> 1]) : bf16_lo(uw[j >> 1]);
             const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-a)));
             const float silu = __fmul_rn(a, s);
             const float dsilu = __fmul_rn(s, __fadd_rn(1.0f, __fmul_rn(a, __fsub_rn(1.0f, s))));
@@ -685,7 +684,7 @@ cudaError_t launch_moe_backward_ste(const BackwardArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     e = launch_dgrad(a.dy_rows, a.w2, rc, a.H, a.I, a.E, a.offsets, a.row_pair, kModeRows, a.dh, a.err, st);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(false, swiglu_bwd_kernel, static_cast<unsigned>(rc / 8), 256, 0, st, a.dh, a.fc1_pre, a.row_pair,
+    e = launch_pdl(false, swiglu_bwd_kernel, static_cast<unsigned>(rc / 8), 256, 0, st, a.dh, a.gu, a.row_pair,
                    a.row_prob, a.offsets, a.E, a.I, a.dgu, a.dprob);
     if (e != cudaSuccess) return e;
     // FC1 dgrad per (token, slot), then the slot-order sum

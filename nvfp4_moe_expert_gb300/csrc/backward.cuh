@@ -18,7 +18,7 @@ struct BackwardArgs {
     const int32_t* row_pair;   // [rows_cap] token*k + slot, -1 for a pad row
     const float* row_prob;     // [rows_cap]
     const uint16_t* h;         // BF16 [rows_cap][I], the forward's SwiGLU x prob
-    const float* fc1_pre;      // FP32 [rows_cap][2I], the forward's FC1 values before the BF16 cast
+    const uint16_t* gu;        // BF16 [rows_cap][2I], the forward's gate/up (the values its SwiGLU ran on)
     uint16_t* dx;              // BF16 [T][H]
     float* dw1;                // FP32 [E][2I][H]
     float* dw2;                // FP32 [E][H][I]

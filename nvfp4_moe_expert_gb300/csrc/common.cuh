@@ -122,6 +122,7 @@ struct GemmArgs {
     int H;
     uint16_t* y;              // [rows_cap][H], per routed row
     float* debug;             // optional pre-cast FP32 values
+    uint16_t* gu_save;        // optional FC1 BF16 gate/up [rows_cap][2I] (the values SwiGLU runs on)
     int* err;
 };
 

@@ -212,10 +212,13 @@ __device__ __forceinline__ void store_row_32(uint16_t* dst, const uint32_t (&pac
 // up columns (acc[1]): gate/up = bf16((acc*g^x)*g^w) with the column scales sc[0..31] (gate)
 // and sc[32..63] (up), h = bf16(f32(f32(silu(gate)*up)*p)) into packed[0..15]; returns the
 // running max of |h| as a BF16 pair.  kDbg: also write the FP32 gate/up values to dbg
-// (gate at dbg[j], up at dbg[I + j]).
-template <bool kDbg>
+// (gate at dbg[j], up at dbg[I + j]).  kSave: also write the BF16 gate/up values to sv (gate
+// at sv[j], up at sv[I + j]; one 4-byte store per pair of values: wider stores need registers
+// for the pairs, and the epilogue is at its register limit).
+template <bool kDbg, bool kSave>
 __device__ __forceinline__ uint32_t fc1_rows(const uint32_t (&acc)[2][32], const float* sc, float gr, float p,
-                                             const float* s_silu, float* dbg, int I, uint32_t (&packed)[16]) {
+                                             const float* s_silu, float* dbg, uint16_t* sv, int I,
+                                             uint32_t (&packed)[16]) {
     const uint64_t gr2 = f2(__float_as_uint(gr), __float_as_uint(gr));
     const uint64_t p2 = f2(__float_as_uint(p), __float_as_uint(p));
     uint32_t hmax2 = 0u;
@@ -234,6 +237,10 @@ __device__ __forceinline__ uint32_t fc1_rows(const uint32_t (&acc)[2][32], const
             dbg[I + j + 1] = vu[1];
         }
         const uint32_t gb = bf16x2_rn(vg[0], vg[1]), ub = bf16x2_rn(vu[0], vu[1]);
+        if (kSave) {
+            *reinterpret_cast<uint32_t*>(sv + j) = gb;
+            *reinterpret_cast<uint32_t*>(sv + I + j) = ub;
+        }
         const float sl0 = silu_bf16(gb & 0xFFFFu, s_silu), sl1 = silu_bf16(gb >> 16, s_silu);
         // silu(gate) * up in FP32, then * p, one BF16 rounding
         const uint64_t h2 =
@@ -511,10 +518,12 @@ __global__ void __maxnreg__(96)
             if (kFC1) {
                 const int I = args.I;
                 float* dbg = args.debug && live ? args.debug + row * (2 * I) + nt * 128 + 32 * sub : nullptr;
+                uint16_t* sv = args.gu_save && live ? args.gu_save + row * (2 * I) + nt * 128 + 32 * sub : nullptr;
                 uint32_t packed[16];
                 uint32_t hmax2;
-                if (dbg) hmax2 = fc1_rows<true>(acc, sc, gr, p, s_silu, dbg, I, packed);
-                else hmax2 = fc1_rows<false>(acc, sc, gr, p, s_silu, nullptr, I, packed);
+                if (dbg) hmax2 = fc1_rows<true, false>(acc, sc, gr, p, s_silu, dbg, nullptr, I, packed);
+                else if (sv) hmax2 = fc1_rows<false, true>(acc, sc, gr, p, s_silu, nullptr, sv, I, packed);
+                else hmax2 = fc1_rows<false, false>(acc, sc, gr, p, s_silu, nullptr, nullptr, I, packed);
                 const float hmax = __uint_as_float((bf16x2_max(hmax2, hmax2 >> 16) & 0xFFFFu) << 16);
                 if (live) {
                     atomicMax(args.amax2 + row, __float_as_uint(hmax));

@@ -164,6 +164,10 @@ def test_forward_validation(lib):
         assert stage(ctypes.byref(w), 16, 2, ws, ws, need - 1, None, None) == 3
     assert lib.moe_requant_nvfp4(ctypes.byref(w), 16, 2, ws, ws, need - 1, None) == 3
     assert lib.moe_combine_bf16(ctypes.byref(w), 16, 2, ws, ws, need - 1, None) == 3
+    save = lib.moe_fc1_swiglu_save_nvfp4
+    assert save(ctypes.byref(w), 16, 2, ws, ws, need, None, None) == 1               # no gate/up buffer
+    assert save(ctypes.byref(w), 16, 2, ws, ws, need, ctypes.c_void_p(4098), None) == 1   # misaligned
+    assert save(ctypes.byref(w), 16, 2, ws, ws, need - 1, ws, None) == 3
 
 
 def test_backward_layout(lib):
@@ -223,19 +227,22 @@ def test_backward_binding_checks_tensors(lib):
     bf, f32 = torch.bfloat16, torch.float32
     ok = dict(x=torch.zeros(T, H, dtype=bf), dout=torch.zeros(T, H, dtype=bf),
               offs=torch.zeros(E + 1, dtype=torch.int32), ws=torch.zeros(16, dtype=torch.uint8),
-              pre=torch.zeros(256, 2 * I, dtype=f32), dx=torch.zeros(T, H, dtype=bf),
+              gu=torch.zeros(M.moe_workspace_layout_query(T, H, I, E, k).rows_cap, 2 * I, dtype=bf),
+              dx=torch.zeros(T, H, dtype=bf),
               dw1=torch.zeros(E, 2 * I, H), dw2=torch.zeros(E, H, I), dprob=torch.zeros(T, k))
 
     def call(**kw):
         a = dict(ok, **kw)
-        M.moe_expert_backward_ste(wt, T, k, a["x"], a["dout"], a["offs"], a["ws"], a["pre"], a["dx"], a["dw1"],
+        M.moe_expert_backward_ste(wt, T, k, a["x"], a["dout"], a["offs"], a["ws"], a["gu"], a["dx"], a["dw1"],
                                   a["dw2"], a["dprob"], a["ws"])
     with pytest.raises(ValueError, match="float32"):
         call(dw1=torch.zeros(E, 2 * I, H, dtype=bf))
     with pytest.raises(ValueError, match=r"\(8, 2\)"):
         call(dprob=torch.zeros(T, k + 1))
-    with pytest.raises(ValueError, match="fc1_pre"):
-        call(pre=torch.zeros(4, dtype=f32))
+    with pytest.raises(ValueError, match="gu must be"):
+        call(gu=torch.zeros(256, 2 * I, dtype=f32))                    # the FP32 values: refused
+    with pytest.raises(ValueError, match="gu must be"):
+        call(gu=torch.zeros(4, 2 * I, dtype=bf))                       # fewer rows than rows_cap
     with pytest.raises(ValueError, match="CUDA"):      # right shapes, but host tensors: refused before any call
         call()
 

@@ -60,9 +60,9 @@ def test_backward_roofline_arithmetic():
     w = bench.backward_work(c2)
     assert w["flops"] == 12 * 4096 * 8 * 2048 * 768
     # BF16 weights read (E*3IH*2) and FP32 weight gradients written (E*3IH*4) dominate
-    assert 3.9e9 < w["bytes"] < 4.0e9
+    assert 3.8e9 < w["bytes"] < 3.85e9
     r = bench.backward_roofline(w, 1.6705, peaks, "measured")
-    assert r["bound"] == "hbm" and r["unit"] == "GB/s"           # 0.58 ms of bytes vs 0.32 ms of FLOPs
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"           # 0.56 ms of bytes vs 0.32 ms of FLOPs
     assert r["frac"] == pytest.approx(w["bytes"] / 1.6705e-3 / 6791.7e9, abs=1e-4)
     assert r["bound_ms"] == pytest.approx(1e3 * w["bytes"] / 6791.7e9, abs=1e-3)
     big = bench.backward_roofline(bench.backward_work(S.CONFIGS["large"]), 20.0, peaks, "measured")

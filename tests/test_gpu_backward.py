@@ -83,16 +83,16 @@ def gpu_backward(c):
     h_rows = np.full((rc, I), 0x7FC0, np.uint16)                 # NaN in pad rows
     h_rows[real] = c["h"].reshape(T * k, I)[pair[real]]
     ws[L.h:L.h + rc * I * 2].copy_(torch.from_numpy(h_rows.view(np.uint8).ravel()).cuda())
-    pre = np.full((rc, 2 * I), np.nan, np.float32)
-    pre[real] = F.bf16_bits_to_f32(c["gu"].reshape(T * k, 2 * I)[pair[real]])
-    fc1_pre = torch.from_numpy(pre).cuda()
+    gu_rows = np.full((rc, 2 * I), 0x7FC0, np.uint16)              # NaN in pad rows
+    gu_rows[real] = c["gu"].reshape(T * k, 2 * I)[pair[real]]
+    gu = bf16_to_torch(gu_rows)
     wt = M.MoEWeightsBF16(bf16_to_torch(c["w1"]), bf16_to_torch(c["w2"]))
     dx = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     dw1 = torch.full((E, 2 * I, H), float("nan"), device="cuda")
     dw2 = torch.full((E, H, I), float("nan"), device="cuda")
     dprob = torch.empty((T, k), dtype=torch.float32, device="cuda")
     bws = M.alloc_backward_workspace(T, H, I, E, k)
-    M.moe_expert_backward_ste(wt, T, k, x, bf16_to_torch(c["dout"]), offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws)
+    M.moe_expert_backward_ste(wt, T, k, x, bf16_to_torch(c["dout"]), offs, ws, gu, dx, dw1, dw2, dprob, bws)
     assert M.nvfp4_get_device_error() == 0
     return dict(dx=_f(torch_to_bf16_bits(dx)), dx_bits=torch_to_bf16_bits(dx), dw1=dw1.cpu().numpy(),
                 dw2=dw2.cpu().numpy(), dprob=dprob.cpu().numpy())
@@ -218,24 +218,24 @@ def test_backward_qwen3_30b_a3b_full_size_sampled():
     M.moe_route_sort_amax(x, torch.from_numpy(Lay["topk_ids"]).cuda(), torch.from_numpy(Lay["topk_w"]).cuda(), E,
                           offs, ws)
     rc = lay.rows_cap
-    fc1_pre = torch.empty((rc, 2 * I), dtype=torch.float32, device="cuda")
-    M.moe_fc1_swiglu_nvfp4(w, T, k, offs, ws, debug=fc1_pre)
+    gu = torch.empty((rc, 2 * I), dtype=torch.bfloat16, device="cuda")
+    M.moe_fc1_swiglu_save_nvfp4(w, T, k, offs, ws, gu)
     wt = M.MoEWeightsBF16(bf16_to_torch(Lay["w1"]), bf16_to_torch(Lay["w2"]))
     dx = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     dw1 = torch.full((E, 2 * I, H), float("nan"), device="cuda")
     dw2 = torch.full((E, H, I), float("nan"), device="cuda")
     dprob = torch.empty((T, k), dtype=torch.float32, device="cuda")
     bws = M.alloc_backward_workspace(T, H, I, E, k)
-    M.moe_expert_backward_ste(wt, T, k, x, bf16_to_torch(dout_bits), offs, ws, fc1_pre, dx, dw1, dw2, dprob, bws)
+    M.moe_expert_backward_ste(wt, T, k, x, bf16_to_torch(dout_bits), offs, ws, gu, dx, dw1, dw2, dprob, bws)
     assert M.nvfp4_get_device_error() == 0
     # the saved values of every (token, slot): the BF16 gate/up the SwiGLU ran on, and h
     pair_row = ws[lay.pair_row:lay.pair_row + 4 * T * k].view(torch.int32).cpu().numpy().reshape(T, k)
-    pre = fc1_pre.cpu().numpy()
+    gu_bits = torch_to_bf16_bits(gu)
     h_rows = ws[lay.h:lay.h + 2 * rc * I].view(torch.int16).cpu().numpy().view(np.uint16).reshape(rc, I)
 
     def saved(t, s):
         rows = pair_row[t, s]
-        return F.round_to_bf16_bits(pre[rows]), h_rows[rows]
+        return gu_bits[rows], h_rows[rows]
 
     ids, p = Lay["topk_ids"], Lay["topk_w"]
     dw1_g, dw2_g = dw1.cpu().numpy(), dw2.cpu().numpy()

@@ -119,6 +119,29 @@ def test_fc1_stage(run):
     assert np.array_equal(amax2, hmax.view(np.uint32))
 
 
+def test_fc1_save_matches_debug(run):
+    # the training forward's FC1 saves the BF16 gate/up its SwiGLU ran on: bitwise the BF16
+    # rounding of the FP32 epilogue values, with h and the FC2 maxima unchanged; pad rows and
+    # rows past expert_offsets[E] keep what they held
+    c = run.cfg
+    rc = run.lay.rows_cap
+    dbg = torch.zeros((rc, 2 * c.I), dtype=torch.float32, device="cuda")
+    M.moe_fc1_swiglu_nvfp4(run.w, c.T, c.k, run.offs, run.ws, debug=dbg)
+    h0 = run.view("h", rc * c.I, torch.int16).cpu().numpy()[:run.off_np[-1] * c.I].copy()
+    a0 = run.view("amax2", rc, torch.int32).cpu().numpy()[run.real].copy()
+    gu = torch.full((rc, 2 * c.I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    M.moe_fc1_swiglu_save_nvfp4(run.w, c.T, c.k, run.offs, run.ws, gu)
+    assert M.nvfp4_get_device_error() == 0
+    gu_bits = torch_to_bf16_bits(gu)
+    assert np.array_equal(gu_bits[run.real], F.round_to_bf16_bits(dbg.cpu().numpy()[run.real]))
+    untouched = np.ones(rc, bool)
+    untouched[run.real] = False
+    assert np.array_equal(gu_bits[untouched], np.full((untouched.sum(), 2 * c.I), 0x7FC0, np.uint16))
+    h1 = run.view("h", rc * c.I, torch.int16).cpu().numpy()[:run.off_np[-1] * c.I]
+    assert np.array_equal(h0, h1)
+    assert np.array_equal(a0, run.view("amax2", rc, torch.int32).cpu().numpy()[run.real])
+
+
 def _synthetic_h(run, seed):
     c = run.cfg
     rng = np.random.default_rng(seed)
