@@ -1,10 +1,11 @@
 #!/usr/bin/env python
 """NVFP4 MoE expert-forward throughput on GB300.
 
-One step = the whole hot path on one batch: moe_route_sort_amax (route sort +
-per-token amax + pad + NVFP4 quantise) and moe_expert_forward_nvfp4 (FC1 +
-SwiGLU x prob, requant, FC2, fixed-order combine), through the C ABI, with the
-quantised weights resident.  Default workload: the Qwen3-30B-A3B-shaped layer
+One step = the whole hot path on one batch through the C ABI's one-call layer
+entry, moe_layer_forward_nvfp4: the route sort (+ per-token amax + pad + NVFP4
+quantise, as moe_route_sort_amax) and the expert forward (FC1 + SwiGLU x prob,
+requant, FC2, fixed-order combine, as moe_expert_forward_nvfp4), with the
+quantised weights resident.  The per-stage attribution times the stage calls.  Default workload: the Qwen3-30B-A3B-shaped layer
 (hidden 2048, expert intermediate 768, 128 experts, top-8, 4096 tokens,
 balanced routing), seeded synthetic data.
 
@@ -516,13 +517,12 @@ def fused_fc2_timing(M, torch, cfg, weights, x, ids, pw, offs, ws, flush, stream
 
 
 def time_steps(M, torch, weights, cfg, x, ids, pw, offs, ws, out, flush, stream, K, W):
-    """CUDA-event time (ms) of each of K steps (route sort + expert forward), after W warm-up
+    """CUDA-event time (ms) of each of K steps (moe_layer_forward_nvfp4), after W warm-up
     steps, L2 flushed between steps outside the events."""
     T, E, k = cfg.T, cfg.E, cfg.k
 
     def step():
-        M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
-        M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+        M.moe_layer_forward_nvfp4(weights, x, ids, pw, offs, out, ws)
 
     for _ in range(W):
         step()
@@ -622,8 +622,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
-        M.moe_route_sort_amax(x, ids, pw, E, offs, ws)
-        M.moe_expert_forward_nvfp4(weights, T, k, offs, out, ws)
+        M.moe_layer_forward_nvfp4(weights, x, ids, pw, offs, out, ws)
 
     for _ in range(args.warmup):
         step()
@@ -772,8 +771,7 @@ def run_ours(args, cfg, rank, world, local_rank):
             h2d_done[b].record(h2d_s)
         stream.wait_event(h2d_done[b])
         stream.wait_event(d2h_done[b])                # step i-2's output has been copied out
-        M.moe_route_sort_amax(x_d[b], ids_d[b], pw_d[b], E, offs, ws)
-        M.moe_expert_forward_nvfp4(weights, T, k, offs, out_d[b], ws)
+        M.moe_layer_forward_nvfp4(weights, x_d[b], ids_d[b], pw_d[b], offs, out_d[b], ws)
         comp_done[b].record(stream)
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(comp_done[b])

@@ -256,6 +256,25 @@ nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int
                                       const int32_t* expert_offsets_dev, void* out_dev,
                                       void* ws_dev, size_t ws_bytes, void* stream);
 
+/*
+ * moe_layer_forward_nvfp4 -- the whole hot path in one call: moe_route_sort_amax
+ * followed by moe_expert_forward_nvfp4, with the same results bit for bit
+ * (out, expert_offsets and the workspace).  One call lets the FC1 kernel be
+ * launched as a programmatic dependent of the route sort's last kernel: its
+ * set-up (barriers, TMEM, the SiLU range) overlaps that kernel's tail, and it
+ * reads the routed rows only once the route sort has completed.
+ *
+ *  w, T, k, out_dev, ws_dev, ws_bytes   as for moe_expert_forward_nvfp4
+ *  x_dev, topk_ids_dev, topk_w_dev      as for moe_route_sort_amax (H and E from w)
+ *  expert_offsets_dev                   int32 [E+1], written as moe_route_sort_amax writes it
+ * Every argument is checked before anything is launched; errors and device
+ * errors as for the two calls.
+ */
+nvfp4_status moe_layer_forward_nvfp4(const moe_nvfp4_weights* w, const void* x_dev, int64_t T, int k,
+                                     const int32_t* topk_ids_dev, const float* topk_w_dev,
+                                     int32_t* expert_offsets_dev, void* out_dev, void* ws_dev,
+                                     size_t ws_bytes, void* stream);
+
 /* The four stages of moe_expert_forward_nvfp4, callable one by one (the
  * "unfused API").  fc1_debug_dev / fc2_debug_dev may be NULL; if given they
  * receive the FP32 pre-cast epilogue values v of every real routed row:

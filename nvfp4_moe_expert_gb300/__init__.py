@@ -4,7 +4,7 @@ Argument marshalling only: every step of the layer runs in the library's
 CUDA kernels; PyTorch provides device memory and the current stream.  The
 entry points have the names of the C ABI in ``include/nvfp4_moe.h``:
 
-    nvfp4_quantize_rows, moe_route_sort_amax, moe_expert_forward_nvfp4,
+    nvfp4_quantize_rows, moe_route_sort_amax, moe_expert_forward_nvfp4, moe_layer_forward_nvfp4,
     moe_fc1_swiglu_nvfp4, moe_fc1_swiglu_save_nvfp4, moe_requant_nvfp4, moe_fc2_nvfp4, moe_fc2_requant_nvfp4, moe_combine_bf16,
     moe_workspace_bytes, moe_workspace_layout_query, nvfp4_sf_bytes,
     nvfp4_rows_padded, nvfp4_get_device_error, nvfp4_status_string, nvfp4_silu_table,
@@ -81,6 +81,8 @@ _SIGNATURES = {
     "moe_expert_forward_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _P, _SZ, _P]),
     "moe_fc1_swiglu_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_fc1_swiglu_save_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
+    "moe_layer_forward_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _P, _I64, _I32, _P, _P, _P, _P, _P, _SZ,
+                                       _P]),
     "moe_requant_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
     "moe_fc2_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_combine_bf16": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
@@ -318,6 +320,20 @@ def moe_expert_forward_nvfp4(weights, T, k, expert_offsets, out, ws, stream=None
         weights.ref(), T, k, _ptr(expert_offsets), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
 
 
+def moe_layer_forward_nvfp4(weights, x, topk_ids, topk_w, expert_offsets, out, ws, stream=None):
+    """moe_route_sort_amax + moe_expert_forward_nvfp4 in one call (FC1 chained to the route
+    sort by programmatic launch); the same results bit for bit."""
+    _need_cuda(x, topk_ids, topk_w, expert_offsets, out, ws)
+    if x.dtype != torch.bfloat16 or topk_ids.dtype != torch.int32 or topk_w.dtype != torch.float32:
+        raise ValueError("x bf16, topk_ids int32, topk_w float32 expected")
+    T, H = x.shape
+    if H != weights.H or out.dtype != torch.bfloat16 or tuple(out.shape) != (T, H):
+        raise ValueError(f"x and out must be bfloat16 [T, {weights.H}]")
+    _check("moe_layer_forward_nvfp4", lib().moe_layer_forward_nvfp4(
+        weights.ref(), _ptr(x), T, topk_ids.shape[1], _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets),
+        _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def moe_fc1_swiglu_nvfp4(weights, T, k, expert_offsets, ws, debug=None, stream=None):
     _need_cuda(expert_offsets, ws, debug)
     _check("moe_fc1_swiglu_nvfp4", lib().moe_fc1_swiglu_nvfp4(
@@ -479,11 +495,11 @@ class MoELayer:
         offs = torch.empty(self.E + 1, dtype=torch.int32, device=x.device)
         if out is None:
             out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
-        moe_route_sort_amax(x, topk_ids, topk_w, self.E, offs, ws, stream=stream)
         if not save_for_backward:
             self._saved = None
-            moe_expert_forward_nvfp4(self.weights, T, k, offs, out, ws, stream=stream)
+            moe_layer_forward_nvfp4(self.weights, x, topk_ids, topk_w, offs, out, ws, stream=stream)
             return out
+        moe_route_sort_amax(x, topk_ids, topk_w, self.E, offs, ws, stream=stream)
         L = moe_workspace_layout_query(T, self.H, self.I, self.E, k)
         gu = torch.empty((L.rows_cap, 2 * self.I), dtype=torch.bfloat16, device=x.device)
         moe_fc1_swiglu_save_nvfp4(self.weights, T, k, offs, ws, gu, stream=stream)

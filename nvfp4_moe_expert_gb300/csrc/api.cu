@@ -456,8 +456,8 @@ static nvfp4_status moe_combine_bf16_impl(const moe_nvfp4_weights* w, int64_t T,
 // moe_fc2_requant_nvfp4 (same bits), whose in-kernel quantisation is issue-bound on the few
 // warps the FC2 kernel's registers and shared memory leave for it.
 static nvfp4_status forward_stages(const moe_nvfp4_weights* w, int64_t T, int k, const int32_t* offs, void* out_dev,
-                                   void* ws_dev, size_t ws_bytes, void* stream, int capacity) {
-    nvfp4_status s = moe_fc1_swiglu_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, false, capacity);
+                                   void* ws_dev, size_t ws_bytes, void* stream, int capacity, bool pdl_fc1 = false) {
+    nvfp4_status s = moe_fc1_swiglu_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, nullptr, stream, pdl_fc1, capacity);
     if (s != NVFP4_OK) return s;
     s = moe_requant_nvfp4_impl(w, T, k, offs, ws_dev, ws_bytes, stream, true, capacity);
     if (s != NVFP4_OK) return s;
@@ -509,6 +509,24 @@ nvfp4_status moe_expert_forward_nvfp4(const moe_nvfp4_weights* w, int64_t T, int
     if (T == 0) return NVFP4_OK;
     if (!expert_offsets_dev || !out_dev || !aligned(out_dev, 16)) return NVFP4_ERR_INVALID_ARG;
     return forward_stages(w, T, k, expert_offsets_dev, out_dev, ws_dev, ws_bytes, stream, 0);
+}
+
+// Route sort + quantise and the expert forward in one call: every argument of both is checked
+// before anything is launched, and FC1 is launched as a programmatic dependent of the route's
+// last kernel (its set-up overlaps that kernel's tail; its reads of the routed rows wait for
+// the route to complete), which the two separate calls cannot do.
+nvfp4_status moe_layer_forward_nvfp4(const moe_nvfp4_weights* w, const void* x_dev, int64_t T, int k,
+                                     const int32_t* topk_ids_dev, const float* topk_w_dev,
+                                     int32_t* expert_offsets_dev, void* out_dev, void* ws_dev, size_t ws_bytes,
+                                     void* stream) {
+    moe_workspace_layout L;
+    nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L);
+    if (s != NVFP4_OK) return s;
+    if (T > 0 && (!out_dev || !aligned(out_dev, 16))) return NVFP4_ERR_INVALID_ARG;
+    s = route_impl(x_dev, T, w->H, w->E, k, topk_ids_dev, topk_w_dev, expert_offsets_dev, ws_dev, ws_bytes, 0,
+                   stream);
+    if (s != NVFP4_OK || T == 0) return s;
+    return forward_stages(w, T, k, expert_offsets_dev, out_dev, ws_dev, ws_bytes, stream, 0, true);
 }
 
 nvfp4_status moe_router_topk(const void* x_dev, int64_t T, int H, const void* w_router_dev, int E, int k,

@@ -311,12 +311,13 @@ __global__ void __maxnreg__(96)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    // everything above touches only this CTA's shared memory and TMEM, so it overlaps the
-    // previous kernel's tail; global memory is read only after the wait
+    // everything above touches only this CTA's shared memory and TMEM, and the SiLU table is
+    // constant data of the library's image, so all of it overlaps the previous kernel's tail;
+    // what earlier kernels write is read only after the wait
+    if (kFC1) load_silu_range(s_silu);
     pdl_wait();
     pdl_launch_dependents();
     for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
-    if (kFC1) load_silu_range(s_silu);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -164,6 +164,14 @@ def test_forward_validation(lib):
         assert stage(ctypes.byref(w), 16, 2, ws, ws, need - 1, None, None) == 3
     assert lib.moe_requant_nvfp4(ctypes.byref(w), 16, 2, ws, ws, need - 1, None) == 3
     assert lib.moe_combine_bf16(ctypes.byref(w), 16, 2, ws, ws, need - 1, None) == 3
+    # the one-call layer checks the forward's and the route sort's arguments before launching
+    layer = lib.moe_layer_forward_nvfp4
+    assert layer(None, ws, 16, 2, ws, ws, ws, ws, ws, need, None) == 1
+    assert layer(ctypes.byref(w), ws, 16, 2, ws, ws, ws, ws, ws, need - 1, None) == 3
+    assert layer(ctypes.byref(w), ws, 16, 2, ws, ws, ws, ctypes.c_void_p(4104), ws, need, None) == 1  # out
+    assert layer(ctypes.byref(w), ws, 16, 2, None, ws, ws, ws, ws, need, None) == 1                   # ids
+    assert layer(ctypes.byref(w), ctypes.c_void_p(4100), 16, 2, ws, ws, ws, ws, ws, need, None) == 1  # x
+    assert layer(ctypes.byref(w), ws, 16, 9, ws, ws, ws, ws, ws, need, None) == 2
     save = lib.moe_fc1_swiglu_save_nvfp4
     assert save(ctypes.byref(w), 16, 2, ws, ws, need, None, None) == 1               # no gate/up buffer
     assert save(ctypes.byref(w), 16, 2, ws, ws, need, ctypes.c_void_p(4098), None) == 1   # misaligned

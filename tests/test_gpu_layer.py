@@ -1,6 +1,7 @@
 """End-to-end parity of the GPU layer (moe_route_sort_amax + moe_expert_forward_nvfp4)
 with the oracle: output relative L2 <= 1e-2, FC2 requantisation code flips
-<= 0.1%, the forward identical to the four stages called one by one, and FC2
+<= 0.1%, the forward identical to the four stages called one by one and the
+one-call layer (moe_layer_forward_nvfp4) identical to the two calls, and FC2
 with the requantisation fused in (moe_fc2_requant_nvfp4) identical to the two
 stages it replaces.
 At the full 2048/768/128/top-8 size with 4096 tokens the oracle checks a
@@ -137,6 +138,37 @@ def test_fused_fc2_rejects_wide_intermediate():
     offs = torch.zeros(cfg.E + 1, dtype=torch.int32, device="cuda")
     with pytest.raises(M.NVFP4Error, match="UNSUPPORTED_SHAPE"):
         M.moe_fc2_requant_nvfp4(w, cfg.T, cfg.k, offs, ws)
+
+
+@pytest.mark.parametrize("cfg", [
+    S.LayerConfig("one_block_sort", H=256, I=128, E=8, k=2, T=300, seed=11),                 # <= 8192 pairs
+    S.LayerConfig("chunked_sort", H=2048, I=768, E=128, k=8, T=1500, seed=12, routing="zipf"),
+    S.LayerConfig("empty", H=256, I=128, E=8, k=2, T=0, seed=13),
+], ids=lambda c: c.name)
+def test_layer_call_equals_route_then_forward(cfg):
+    # the one-call layer (FC1 chained to the route sort by programmatic launch) gives the two
+    # calls' output, offsets and routed rows bit for bit
+    L = S.make_layer(cfg)
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+    out2, ws2, offs2, lay = gpu_layer(L, E)
+    w = M.quantize_moe_weights(bf16_to_torch(L["w1"]), bf16_to_torch(L["w2"]))
+    ws = M.alloc_workspace(T, H, cfg.I, E, k)
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    M.moe_layer_forward_nvfp4(w, bf16_to_torch(L["x"]), torch.from_numpy(L["topk_ids"]).cuda(),
+                              torch.from_numpy(L["topk_w"]).cuda(), offs, out, ws)
+    assert M.nvfp4_get_device_error() == 0
+    assert torch.equal(offs, offs2)
+    assert np.array_equal(torch_to_bf16_bits(out), torch_to_bf16_bits(out2))
+    if T:
+        rows = int(offs[-1].item())
+        pair = ws[lay.row_pair:lay.row_pair + 4 * rows].view(torch.int32)
+        assert torch.equal(pair, ws2[lay.row_pair:lay.row_pair + 4 * rows].view(torch.int32))
+        real = pair >= 0                              # pad rows of h are never written
+        for name, width in (("a_codes", H // 2), ("h", 2 * cfg.I)):
+            a = ws[getattr(lay, name):getattr(lay, name) + rows * width].view(rows, width)
+            b = ws2[getattr(lay, name):getattr(lay, name) + rows * width].view(rows, width)
+            assert torch.equal(a[real], b[real]), name
 
 
 def test_run_to_run_deterministic():
