@@ -233,10 +233,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
     int32_t* s_end = s_off + kBMaxE + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    for (int i = threadIdx.x; i <= job.E; i += kBThreads) {
-        s_off[i] = job.offsets[i];
-        if (kWgrad && i < job.E) s_end[i] = job.real_end[i];
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -257,6 +253,15 @@ __global__ void __launch_bounds__(kBThreads, 1)
     if (warp == 1) {
         tmem_alloc(tmem_slot, kBTmemCols);
         tmem_relinquish();
+    }
+    // the set-up above touches only this CTA's shared memory and TMEM (and the tensor maps,
+    // kernel parameters), so it overlaps the previous kernel's tail; every global read and
+    // write follows the wait
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i <= job.E; i += kBThreads) {
+        s_off[i] = job.offsets[i];
+        if (kWgrad && i < job.E) s_end[i] = job.real_end[i];
     }
     tc_fence_before();
     __syncthreads();
@@ -467,6 +472,8 @@ __global__ void __launch_bounds__(256)
     gather_token_rows_kernel(const uint16_t* __restrict__ src, int C, const int32_t* __restrict__ row_pair, int k,
                              const int32_t* __restrict__ offsets, int E, int64_t row_blocks, uint16_t* __restrict__ dst,
                              int32_t* __restrict__ real_end) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     if (static_cast<int64_t>(blockIdx.x) >= row_blocks) {
         const int e = static_cast<int>((blockIdx.x - row_blocks) * 8 + (threadIdx.x >> 5));
@@ -502,6 +509,8 @@ __global__ void __launch_bounds__(256)
                       const int32_t* __restrict__ row_pair, const float* __restrict__ row_prob,
                       const int32_t* __restrict__ offsets, int E, int I, uint16_t* __restrict__ dgu,
                       float* __restrict__ dprob) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= offsets[E]) return;
@@ -613,7 +622,7 @@ unsigned persistent_grid(int64_t tiles) {
 // are expert e's), K % 64 == 0, N % 128 == 0.
 cudaError_t launch_dgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap, int K, int N, int E,
                          const int32_t* offsets, const int32_t* row_pair, int mode, uint16_t* out, int* err,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool pdl) {
     BgemmJob j{};
     j.mode = mode;
     j.BN = tile_n(N);
@@ -633,14 +642,15 @@ cudaError_t launch_dgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap,
     CUtensorMap ma, mb;
     if (!make_box_map(&ma, A, rows_cap, K, kBM) || !make_box_map(&mb, B, static_cast<int64_t>(E) * K, N, kBK))
         return cudaErrorInvalidValue;
-    return launch_pdl(false, bgemm_bf16_kernel<false>, persistent_grid(static_cast<int64_t>(j.m_tiles) * j.n_tiles),
+    return launch_pdl(pdl, bgemm_bf16_kernel<false>, persistent_grid(static_cast<int64_t>(j.m_tiles) * j.n_tiles),
                       kBThreads, BCfg<false>::kSmemBytes, st, ma, mb, j);
 }
 
 // Grouped wgrad: out[e] (FP32 [M][N]) = A[rows of e]^T B[rows of e] with A [rows_cap][M],
 // B [rows_cap][N] (K over expert e's real routed rows offsets[e] .. real_end[e]).
 cudaError_t launch_wgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap, int M, int N, int E,
-                         const int32_t* offsets, const int32_t* real_end, float* out, int* err, cudaStream_t st) {
+                         const int32_t* offsets, const int32_t* real_end, float* out, int* err, cudaStream_t st,
+                         bool pdl) {
     BgemmJob j{};
     j.mode = kModeWgrad;
     j.BN = tile_n(N);
@@ -660,15 +670,15 @@ cudaError_t launch_wgrad(const uint16_t* A, const uint16_t* B, int64_t rows_cap,
     CUtensorMap ma, mb;
     if (!make_box_map(&ma, A, rows_cap, M, kBK) || !make_box_map(&mb, B, rows_cap, N, kBK))
         return cudaErrorInvalidValue;
-    return launch_pdl(false, bgemm_bf16_kernel<true>, persistent_grid(static_cast<int64_t>(E) * j.m_tiles * j.n_tiles),
+    return launch_pdl(pdl, bgemm_bf16_kernel<true>, persistent_grid(static_cast<int64_t>(E) * j.m_tiles * j.n_tiles),
                       kBThreads, BCfg<true>::kSmemBytes, st, ma, mb, j);
 }
 
 cudaError_t launch_gather(const uint16_t* src, int C, const BackwardArgs& a, uint16_t* dst, int32_t* real_end,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool pdl) {
     const int64_t row_blocks = a.rows_cap / 8;
     const int64_t blocks = row_blocks + (real_end != nullptr ? (a.E + 7) / 8 : 0);
-    return launch_pdl(false, gather_token_rows_kernel, static_cast<unsigned>(blocks), 256, 0, st, src, C, a.row_pair,
+    return launch_pdl(pdl, gather_token_rows_kernel, static_cast<unsigned>(blocks), 256, 0, st, src, C, a.row_pair,
                       a.k, a.offsets, a.E, row_blocks, dst, real_end);
 }
 
@@ -679,26 +689,30 @@ cudaError_t launch_moe_backward_ste(const BackwardArgs& a, cudaStream_t st) {
     cudaError_t e = ensure_smem_attr();
     if (e != cudaSuccess) return e;
     const int64_t rc = a.rows_cap;
+    // The first kernel is launched normally (ordered after whatever the caller queued); each
+    // later one as a programmatic dependent of the one before it: its CTAs are scheduled while
+    // that kernel finishes and wait (griddepcontrol.wait) before their first global access.
     // dY rows (and each expert's end of real rows), FC2 dgrad, SwiGLU x prob derivative
-    e = launch_gather(a.dout, a.H, a, a.dy_rows, a.real_end, st);
+    e = launch_gather(a.dout, a.H, a, a.dy_rows, a.real_end, st, false);
     if (e != cudaSuccess) return e;
-    e = launch_dgrad(a.dy_rows, a.w2, rc, a.H, a.I, a.E, a.offsets, a.row_pair, kModeRows, a.dh, a.err, st);
+    e = launch_dgrad(a.dy_rows, a.w2, rc, a.H, a.I, a.E, a.offsets, a.row_pair, kModeRows, a.dh, a.err, st, true);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(false, swiglu_bwd_kernel, static_cast<unsigned>(rc / 8), 256, 0, st, a.dh, a.gu, a.row_pair,
+    e = launch_pdl(true, swiglu_bwd_kernel, static_cast<unsigned>(rc / 8), 256, 0, st, a.dh, a.gu, a.row_pair,
                    a.row_prob, a.offsets, a.E, a.I, a.dgu, a.dprob);
     if (e != cudaSuccess) return e;
     // FC1 dgrad per (token, slot), then the slot-order sum
-    e = launch_dgrad(a.dgu, a.w1, rc, 2 * a.I, a.H, a.E, a.offsets, a.row_pair, kModePairs, a.dx_pairs, a.err, st);
+    e = launch_dgrad(a.dgu, a.w1, rc, 2 * a.I, a.H, a.E, a.offsets, a.row_pair, kModePairs, a.dx_pairs, a.err, st,
+                     true);
     if (e != cudaSuccess) return e;
-    e = launch_combine(a.dx_pairs, nullptr, a.T, a.k, a.H, a.dx, st, false);
+    e = launch_combine(a.dx_pairs, nullptr, a.T, a.k, a.H, a.dx, st, true);
     if (e != cudaSuccess) return e;
     // FC2 wgrad: dW2[e] = dy^T h over the expert's real rows
-    e = launch_wgrad(a.dy_rows, a.h, rc, a.H, a.I, a.E, a.offsets, a.real_end, a.dw2, a.err, st);
+    e = launch_wgrad(a.dy_rows, a.h, rc, a.H, a.I, a.E, a.offsets, a.real_end, a.dw2, a.err, st, true);
     if (e != cudaSuccess) return e;
     // FC1 wgrad: dW1[e] = [da, du]^T x over the expert's real rows
-    e = launch_gather(a.x, a.H, a, a.x_rows, nullptr, st);
+    e = launch_gather(a.x, a.H, a, a.x_rows, nullptr, st, true);
     if (e != cudaSuccess) return e;
-    return launch_wgrad(a.dgu, a.x_rows, rc, 2 * a.I, a.H, a.E, a.offsets, a.real_end, a.dw1, a.err, st);
+    return launch_wgrad(a.dgu, a.x_rows, rc, 2 * a.I, a.H, a.E, a.offsets, a.real_end, a.dw1, a.err, st, true);
 }
 
 }  // namespace nvfp4
