@@ -349,6 +349,14 @@ nvfp4_status moe_route_sort_amax_masked(const void* x_dev, int64_t T, int H, int
 nvfp4_status moe_expert_forward_nvfp4_masked(const moe_nvfp4_weights* w, int64_t T, int k, int capacity,
                                              const int32_t* expert_offsets_dev, void* out_dev, void* ws_dev,
                                              size_t ws_bytes, void* stream);
+/* moe_route_sort_amax_masked followed by moe_expert_forward_nvfp4_masked in one call, as
+ * moe_layer_forward_nvfp4 is for the contiguous layout (FC1 launched as a programmatic
+ * dependent of the route sort; every argument checked before anything is launched); the
+ * same results bit for bit. */
+nvfp4_status moe_layer_forward_nvfp4_masked(const moe_nvfp4_weights* w, const void* x_dev, int64_t T, int k,
+                                            const int32_t* topk_ids_dev, const float* topk_w_dev, int capacity,
+                                            int32_t* expert_offsets_dev, void* out_dev, void* ws_dev,
+                                            size_t ws_bytes, void* stream);
 
 /* moe_router_topk -- the router step that produces the inputs of
  * moe_route_sort_amax: logits[t, e] = sum_h x[t, h] * W_r[e, h] (BF16 inputs, FP32

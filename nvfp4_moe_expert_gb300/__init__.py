@@ -83,6 +83,8 @@ _SIGNATURES = {
     "moe_fc1_swiglu_save_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_layer_forward_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _P, _I64, _I32, _P, _P, _P, _P, _P, _SZ,
                                        _P]),
+    "moe_layer_forward_nvfp4_masked": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _P, _I64, _I32, _P, _P, _I32, _P,
+                                              _P, _P, _SZ, _P]),
     "moe_requant_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
     "moe_fc2_nvfp4": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P, _P]),
     "moe_combine_bf16": (_I32, [ctypes.POINTER(moe_nvfp4_weights), _I64, _I32, _P, _P, _SZ, _P]),
@@ -332,6 +334,19 @@ def moe_layer_forward_nvfp4(weights, x, topk_ids, topk_w, expert_offsets, out, w
     _check("moe_layer_forward_nvfp4", lib().moe_layer_forward_nvfp4(
         weights.ref(), _ptr(x), T, topk_ids.shape[1], _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets),
         _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_layer_forward_nvfp4_masked(weights, x, topk_ids, topk_w, capacity, expert_offsets, out, ws, stream=None):
+    """moe_route_sort_amax_masked + moe_expert_forward_nvfp4_masked in one call."""
+    _need_cuda(x, topk_ids, topk_w, expert_offsets, out, ws)
+    if x.dtype != torch.bfloat16 or topk_ids.dtype != torch.int32 or topk_w.dtype != torch.float32:
+        raise ValueError("x bf16, topk_ids int32, topk_w float32 expected")
+    T, H = x.shape
+    if H != weights.H or out.dtype != torch.bfloat16 or tuple(out.shape) != (T, H):
+        raise ValueError(f"x and out must be bfloat16 [T, {weights.H}]")
+    _check("moe_layer_forward_nvfp4_masked", lib().moe_layer_forward_nvfp4_masked(
+        weights.ref(), _ptr(x), T, topk_ids.shape[1], _ptr(topk_ids), _ptr(topk_w), capacity,
+        _ptr(expert_offsets), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_fc1_swiglu_nvfp4(weights, T, k, expert_offsets, ws, debug=None, stream=None):

@@ -558,6 +558,21 @@ nvfp4_status moe_expert_forward_nvfp4_masked(const moe_nvfp4_weights* w, int64_t
     return forward_stages(w, T, k, expert_offsets_dev, out_dev, ws_dev, ws_bytes, stream, capacity);
 }
 
+nvfp4_status moe_layer_forward_nvfp4_masked(const moe_nvfp4_weights* w, const void* x_dev, int64_t T, int k,
+                                            const int32_t* topk_ids_dev, const float* topk_w_dev, int capacity,
+                                            int32_t* expert_offsets_dev, void* out_dev, void* ws_dev,
+                                            size_t ws_bytes, void* stream) {
+    if (capacity == 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    moe_workspace_layout L;
+    nvfp4_status s = check_forward_args(w, T, k, ws_dev, ws_bytes, &L, capacity);
+    if (s != NVFP4_OK) return s;
+    if (T > 0 && (!out_dev || !aligned(out_dev, 16))) return NVFP4_ERR_INVALID_ARG;
+    s = route_impl(x_dev, T, w->H, w->E, k, topk_ids_dev, topk_w_dev, expert_offsets_dev, ws_dev, ws_bytes,
+                   capacity, stream);
+    if (s != NVFP4_OK || T == 0) return s;
+    return forward_stages(w, T, k, expert_offsets_dev, out_dev, ws_dev, ws_bytes, stream, capacity, true);
+}
+
 nvfp4_status moe_backward_layout_query(int64_t T, int H, int I, int E, int k, moe_backward_layout* out) {
     if (!out) return NVFP4_ERR_INVALID_ARG;
     if (!moe_shape_ok(T, H, I, E, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;

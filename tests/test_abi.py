@@ -172,6 +172,12 @@ def test_forward_validation(lib):
     assert layer(ctypes.byref(w), ws, 16, 2, None, ws, ws, ws, ws, need, None) == 1                   # ids
     assert layer(ctypes.byref(w), ctypes.c_void_p(4100), 16, 2, ws, ws, ws, ws, ws, need, None) == 1  # x
     assert layer(ctypes.byref(w), ws, 16, 9, ws, ws, ws, ws, ws, need, None) == 2
+    lm = lib.moe_layer_forward_nvfp4_masked
+    need_m = lib.moe_workspace_bytes_masked(16, 256, 128, 8, 2, 128)
+    assert lm(ctypes.byref(w), ws, 16, 2, ws, ws, 0, ws, ws, ws, need_m, None) == 2          # capacity 0
+    assert lm(ctypes.byref(w), ws, 16, 2, ws, ws, 100, ws, ws, ws, need_m, None) == 2        # not a multiple of 128
+    assert lm(ctypes.byref(w), ws, 16, 2, ws, ws, 128, ws, ws, ws, need_m - 1, None) == 3
+    assert lm(ctypes.byref(w), ws, 16, 2, None, ws, 128, ws, ws, ws, need_m, None) == 1      # ids
     save = lib.moe_fc1_swiglu_save_nvfp4
     assert save(ctypes.byref(w), 16, 2, ws, ws, need, None, None) == 1               # no gate/up buffer
     assert save(ctypes.byref(w), 16, 2, ws, ws, need, ctypes.c_void_p(4098), None) == 1   # misaligned

@@ -78,6 +78,13 @@ def test_masked_equals_contiguous(name, T):
         assert np.array_equal(sf_m[rm], sf_c[rc])
         assert np.array_equal(g_m[rm], g_c[rc])
         assert not sf_m[e * C + n:(e + 1) * C].any() and not g_m[e * C + n:(e + 1) * C].any()   # pad rows
+    # the one-call masked layer: the same offsets and output bits
+    ws_1 = M.alloc_workspace_masked(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, C)
+    off_1 = torch.full((cfg.E + 1,), -7, dtype=torch.int32, device=dev)
+    out_1 = torch.empty_like(out_m)
+    M.moe_layer_forward_nvfp4_masked(w, x, ids, pw, C, off_1, out_1, ws_1)
+    assert M.nvfp4_get_device_error() == 0
+    assert torch.equal(off_1, off_m) and torch.equal(out_1.view(torch.int16), out_m.view(torch.int16))
 
 
 @pytest.mark.parametrize("T", [64, 4096])     # one-block sort and chunked sort
